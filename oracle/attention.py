@@ -1,0 +1,183 @@
+"""Sparse attention, split-KV partials, the LSE combine and sparse decode in
+fp64 (test infrastructure; see the package header).
+
+Sources:
+* "Sparge Attention (Composable Kernel)" README, intro: the sparse FMHA stage
+  visits only the kv blocks listed in each q block's LUT row.
+* "Incremental_FlashAttention updating_log.md", Stage 1: reference attention
+  returns (O, LSE) with a natural-log LSE; partials over disjoint key sets are
+  merged with the lse_max trick, in any order, and an empty partial
+  (LSE = -inf) is the identity.  Stage 3: an empty block list writes O = 0 and
+  LSE = -inf.
+* ROCm/aiter pull 6841: the exported LSE is the logsumexp of the scores that
+  were actually computed (the selected blocks), -inf for an empty LUT row.
+* ROCm/aiter pull 4919: sparse MLA decode - each query lists top-k token
+  positions, resolved through a page table into rows of a paged cache; a K row
+  is 512 latent + 64 rotary values and V is its latent plane; the key list is
+  split into chunks whose partials (O_s, LSE_s) an LSE reduce merges.
+"""
+from __future__ import annotations
+
+from typing import Iterable, Optional
+
+import numpy as np
+
+from synth import bits_to_f64
+
+
+def row_keys(lut_row: Iterable[int], blkk: int, s_k: int) -> np.ndarray:
+    """Key positions covered by a list of kv blocks, in list order."""
+    parts = [np.arange(j * blkk, min((j + 1) * blkk, s_k)) for j in lut_row]
+    if not parts:
+        return np.zeros(0, dtype=np.int64)
+    return np.concatenate(parts)
+
+
+def _softmax_attend(scores: np.ndarray, vals: np.ndarray):
+    """O = softmax(scores) @ vals and LSE = logsumexp(scores) per row, with
+    rows whose scores are all -inf giving O = 0, LSE = -inf."""
+    rows, dv = scores.shape[0], vals.shape[1]
+    out = np.zeros((rows, dv), dtype=np.float64)
+    lse = np.full(rows, -np.inf, dtype=np.float64)
+    if scores.shape[1] == 0:
+        return out, lse
+    m = scores.max(axis=1)
+    live = np.isfinite(m)
+    if not live.any():
+        return out, lse
+    p = np.exp(scores[live] - m[live, None])
+    l = p.sum(axis=1)
+    out[live] = (p @ vals) / l[:, None]
+    lse[live] = m[live] + np.log(l)
+    return out, lse
+
+
+def attention_unit(q: np.ndarray, k: np.ndarray, v: np.ndarray, lut_row: Iterable[int],
+                   i: int, blkq: int, blkk: int, scale: float, causal: bool):
+    """Attention of the rows of q block ``i`` over the keys of the listed kv
+    blocks.  q [s_q, d], k [s_k, d], v [s_k, dv] are one head's float64
+    values.  Under ``causal`` (s_q == s_k) a key at position u is visible to
+    the query at position t only when u <= t.  Returns (O [rows, dv], LSE
+    [rows])."""
+    s_q, s_k = q.shape[0], k.shape[0]
+    t = np.arange(i * blkq, min((i + 1) * blkq, s_q))
+    keys = row_keys(lut_row, blkk, s_k)
+    scores = scale * (q[t] @ k[keys].T)
+    if causal:
+        scores = np.where(keys[None, :] <= t[:, None], scores, -np.inf)
+    return _softmax_attend(scores, v[keys])
+
+
+def _head(x: np.ndarray, bi: int, h: int, dtype: Optional[str]) -> np.ndarray:
+    if dtype is None:
+        return np.asarray(x[bi, h], dtype=np.float64)
+    return bits_to_f64(x[bi, h], dtype)
+
+
+def sparse_fmha(q: np.ndarray, k: np.ndarray, v: np.ndarray, lut: np.ndarray,
+                count: np.ndarray, scale: float, causal: bool, units: Optional[list] = None,
+                blkq: int = 64, blkk: int = 64, dtype: Optional[str] = None) -> dict:
+    """Block-sparse attention of q [b, hq, s_q, d] over k, v [b, hk, s_k, *]
+    with LUT [b, hq, nq, nk] / count [b, hq, nq] (values, or bit patterns when
+    ``dtype`` is given).  Query head h reads KV head h // (hq // hk).
+    ``units`` lists (b, h, i) q blocks to compute (default: all).  Returns
+    {(b, h, i): (O, LSE)}."""
+    b, hq, s_q, _ = q.shape
+    hk = k.shape[1]
+    ratio = hq // hk
+    nq = (s_q + blkq - 1) // blkq
+    if units is None:
+        units = [(bi, h, i) for bi in range(b) for h in range(hq) for i in range(nq)]
+    res = {}
+    cache = {}
+    for bi, h, i in units:
+        key = (bi, h)
+        if key not in cache:
+            cache.clear()
+            cache[key] = (_head(q, bi, h, dtype), _head(k, bi, h // ratio, dtype),
+                          _head(v, bi, h // ratio, dtype))
+        qh, kg, vg = cache[key]
+        row = lut[bi, h, i, :count[bi, h, i]]
+        res[(bi, h, i)] = attention_unit(qh, kg, vg, row, i, blkq, blkk, scale, causal)
+    return res
+
+
+def split_bounds(n: int, num_splits: int) -> list:
+    """Contiguous chunks of an n-entry list: the first n mod S chunks hold
+    ceil(n/S) entries, the others floor(n/S) (some may be empty)."""
+    base, extra = divmod(n, num_splits)
+    out, start = [], 0
+    for s in range(num_splits):
+        size = base + (1 if s < extra else 0)
+        out.append((start, start + size))
+        start += size
+    return out
+
+
+def split_partials_unit(qh: np.ndarray, kg: np.ndarray, vg: np.ndarray, lut_row,
+                        i: int, num_splits: int, blkq: int, blkk: int, scale: float,
+                        causal: bool):
+    """Split-KV partials of one q block: attention over each contiguous chunk
+    of its LUT row.  Returns (O_parts [S, rows, dv], LSE_parts [S, rows])."""
+    lut_row = list(lut_row)
+    outs, lses = [], []
+    for lo, hi in split_bounds(len(lut_row), num_splits):
+        o, l = attention_unit(qh, kg, vg, lut_row[lo:hi], i, blkq, blkk, scale, causal)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
+
+
+def combine(o_parts: np.ndarray, lse_parts: np.ndarray):
+    """Merge partials over disjoint key sets (the lse_max trick of the
+    updating_log's Stage 1): m = max_s LSE_s, w_s = exp(LSE_s - m),
+    O = sum_s w_s O_s / sum_s w_s, LSE = m + ln(sum_s w_s).  Rows whose
+    partials are all empty (LSE = -inf) give O = 0, LSE = -inf.
+    o_parts [S, rows, dv], lse_parts [S, rows]."""
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    m = lse_parts.max(axis=0)
+    rows, dv = o_parts.shape[1], o_parts.shape[2]
+    out = np.zeros((rows, dv), dtype=np.float64)
+    lse = np.full(rows, -np.inf, dtype=np.float64)
+    live = np.isfinite(m)
+    if live.any():
+        w = np.exp(lse_parts[:, live] - m[None, live])
+        wsum = w.sum(axis=0)
+        out[live] = (w[:, :, None] * o_parts[:, live]).sum(axis=0) / wsum[:, None]
+        lse[live] = m[live] + np.log(wsum)
+    return out, lse
+
+
+# ----------------------------------------------------------------------------
+# Sparse decode (paged cache, token index lists)
+# ----------------------------------------------------------------------------
+
+
+def decode_rows(page_table: np.ndarray, idx: np.ndarray, page: int) -> np.ndarray:
+    """Physical cache row of every listed token position: the row sits at
+    offset pos mod page inside page page_table[c, pos div page] (paged KV
+    addressing of ROCm/aiter pull 4919)."""
+    pt = np.asarray(page_table, dtype=np.int64)
+    pos = np.asarray(idx, dtype=np.int64)
+    c = np.arange(pos.shape[0])[:, None]
+    return pt[c, pos // page] * page + pos % page
+
+
+def decode_attention(q: np.ndarray, kv: np.ndarray, dv: int, scale: float):
+    """One query token per row of q [H, d] attending to the gathered rows kv
+    [T, d]: K = kv, V = kv[:, :dv] (the latent plane).  Returns (O [H, dv],
+    LSE [H])."""
+    scores = scale * (q @ kv.T)
+    return _softmax_attend(scores, kv[:, :dv])
+
+
+def decode_partials(q: np.ndarray, kv: np.ndarray, dv: int, scale: float, num_splits: int):
+    """Split-KV partials of one query: attention over each contiguous chunk of
+    its gathered key list.  Returns (O_parts [S, H, dv], LSE_parts [S, H])."""
+    outs, lses = [], []
+    for lo, hi in split_bounds(kv.shape[0], num_splits):
+        o, l = decode_attention(q, kv[lo:hi], dv, scale)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)

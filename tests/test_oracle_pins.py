@@ -1,0 +1,490 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Nothing here compares the oracle with itself: each check is a closed form, a
+brute-force enumeration on tiny inputs, a textbook / library routine
+(torch scaled_dot_product_attention and logsumexp in float64), or an identity
+the pages state (the combine identity of the Incremental_FlashAttention
+updating_log, Stage 1).  The last tests plant mistakes in copies of oracle
+functions and check that a pin catches each one.
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import attention as oatt
+from oracle import block_map as obm
+
+RNG = np.random.default_rng(12345)
+
+
+# ----------------------------------------------------------------------------
+# self-similarity and pooling
+# ----------------------------------------------------------------------------
+
+
+def brute_similarity(block):
+    """Mean of cos(x_a, x_b) over all ordered pairs, in plain Python."""
+    rows = [list(map(float, r)) for r in block]
+    n = len(rows)
+    norms = [math.sqrt(sum(v * v for v in r)) for r in rows]
+    tot = 0.0
+    for a in range(n):
+        for b in range(n):
+            if norms[a] == 0.0 or norms[b] == 0.0:
+                continue
+            tot += sum(x * y for x, y in zip(rows[a], rows[b])) / (norms[a] * norms[b])
+    return tot / (n * n)
+
+
+@pytest.mark.parametrize("n,d", [(64, 8), (5, 3), (17, 33)])
+def test_self_similarity_matches_pairwise_cosines(n, d):
+    for _ in range(3):
+        blk = RNG.standard_normal((n, d)) + RNG.standard_normal(d)
+        assert obm.self_similarity(blk) == pytest.approx(brute_similarity(blk), abs=1e-12)
+
+
+def test_self_similarity_special_cases():
+    row = RNG.standard_normal(16)
+    same = np.tile(row, (64, 1))
+    assert obm.self_similarity(same) == pytest.approx(1.0, abs=1e-14)
+    half = RNG.standard_normal((32, 16))
+    anti = np.empty((64, 16))
+    anti[0::2], anti[1::2] = half, -half
+    assert obm.self_similarity(anti) == pytest.approx(0.0, abs=1e-14)
+    # a zero row contributes a zero unit vector: (n-1)^2 / n^2
+    z = same.copy()
+    z[3] = 0.0
+    assert obm.self_similarity(z) == pytest.approx((63 / 64) ** 2, abs=1e-14)
+    # independent noise averages out: E[sim] = 1/n for isotropic rows
+    noise = RNG.standard_normal((64, 2048))
+    assert obm.self_similarity(noise) == pytest.approx(1 / 64, abs=3e-3)
+
+
+def test_pool_blocks_exact_means_with_partial_block():
+    x = np.arange(7 * 2, dtype=np.float64).reshape(7, 2)  # 7 rows, blk = 3
+    got = obm.pool_blocks(x, 3)
+    want = []
+    for j in range(3):
+        rows = [list(map(Fraction, r)) for r in x[3 * j:3 * j + 3].astype(int)]
+        want.append([sum(c) / len(rows) for c in zip(*rows)])
+    assert got.shape == (3, 2)
+    assert [[Fraction(v) for v in r] for r in got] == want
+
+
+# ----------------------------------------------------------------------------
+# eligibility, counts and selection
+# ----------------------------------------------------------------------------
+
+
+def test_eligibility_causal_is_lower_triangle():
+    e = obm.eligible_mask(8, 8, 64, 64, True)
+    assert (e == np.tril(np.ones((8, 8), dtype=bool))).all()
+    assert (e.sum(axis=1) == np.arange(1, 9)).all()
+    assert obm.eligible_mask(3, 5, 64, 64, False).all()
+    # unequal blocks: q blocks of 128 see kv blocks of 64 up to 2i+1
+    e2 = obm.eligible_mask(2, 4, 128, 64, True)
+    assert e2.tolist() == [[True, True, False, False], [True, True, True, True]]
+
+
+@pytest.mark.parametrize("topk,n,want", [(0.5, 8, 4), (0.1, 256, 26), (0.2, 256, 52),
+                                         (0.4, 256, 103), (0.6, 256, 154), (1.0, 256, 256),
+                                         (0.2, 5, 1), (0.2, 512, 103), (1e-6, 9, 1)])
+def test_topk_count_table(topk, n, want):
+    assert obm.topk_count(topk, n) == want
+
+
+def _softmax(sc):
+    fin = np.isfinite(sc)
+    p = np.zeros_like(sc)
+    e = np.exp(sc[fin] - sc[fin].max())
+    p[fin] = e / e.sum()
+    return p
+
+
+def check_topk_bruteforce(select, sc, topk):
+    """The chosen set is the lexicographically-first maximiser of total pooled
+    probability among all sets of min(K, #finite) finite entries."""
+    nk = sc.shape[0]
+    fin = [j for j in range(nk) if np.isfinite(sc[j])]
+    kk = min(obm.topk_count(topk, nk), len(fin))
+    p = _softmax(sc)
+    best, best_set = -1.0, None
+    for comb in itertools.combinations(fin, kk):  # lexicographic order
+        tot = sum(p[j] for j in comb)
+        if tot > best + 1e-15:
+            best, best_set = tot, comb
+    got = tuple(np.nonzero(select(sc, topk, None, nk))[0])
+    assert got == tuple(best_set), (got, best_set)
+
+
+def check_cdf_bruteforce(select, sc, tau):
+    """The chosen set has the smallest size m for which some m-subset of
+    finite entries reaches mass tau, and is the top-m by probability (lower
+    index on ties); everything finite when nothing reaches tau."""
+    nk = sc.shape[0]
+    fin = [j for j in range(nk) if np.isfinite(sc[j])]
+    p = _softmax(sc)
+    got = tuple(np.nonzero(select(sc, None, tau, nk))[0])
+    want = tuple(fin)
+    for m in range(1, len(fin) + 1):
+        cands = [c for c in itertools.combinations(fin, m) if sum(p[j] for j in c) >= tau]
+        if cands:
+            bestmass = max(sum(p[j] for j in c) for c in cands)
+            want = min(c for c in cands if sum(p[j] for j in c) >= bestmass - 1e-15)
+            break
+    assert got == tuple(sorted(want)), (got, want)
+
+
+def _tiny_rows(seed):
+    rng = np.random.default_rng(seed)
+    rows = []
+    for _ in range(40):
+        nk = int(rng.integers(1, 9))
+        sc = rng.standard_normal(nk) * 2.0
+        if nk > 2:
+            sc[rng.integers(0, nk)] = -np.inf
+        if nk > 3 and rng.random() < 0.5:  # an exact tie
+            a, b = rng.choice(nk, 2, replace=False)
+            sc[b] = sc[a]
+        rows.append(sc)
+    return rows
+
+
+@pytest.mark.parametrize("topk", [0.1, 0.25, 0.5, 0.75, 1.0])
+def test_topk_selection_bruteforce(topk):
+    for sc in _tiny_rows(1):
+        check_topk_bruteforce(obm.select_row, sc, topk)
+
+
+@pytest.mark.parametrize("tau", [0.3, 0.5, 0.8, 0.9, 0.99])
+def test_cdf_selection_bruteforce(tau):
+    for sc in _tiny_rows(2):
+        check_cdf_bruteforce(obm.select_row, sc, tau)
+
+
+def test_selection_special_cases():
+    sc = np.array([0.3, 1.7, -np.inf, 1.7, -0.2])
+    assert np.nonzero(obm.select_row(sc, 1e-6, None, 5))[0].tolist() == [1]  # argmax, low index
+    assert np.nonzero(obm.select_row(sc, None, 1.0, 5))[0].tolist() == [0, 1, 3, 4]
+    assert not obm.select_row(np.full(4, -np.inf), 0.5, None, 4).any()
+    assert np.nonzero(obm.select_row(sc, 1.0, None, 5))[0].tolist() == [0, 1, 3, 4]
+
+
+def test_block_map_hand_example():
+    """A tiny worked example with exact rational pooled scores.
+
+    blk = 2, d = 2.  q blocks pool to (1,0) and (0,1); k blocks pool to
+    (2,0), (0,3), (1,1), (-1,0).  Scores (scale 1): row 0 = [2,0,1,-1],
+    row 1 = [0,3,1,0].  topk 0.5 of 4 -> 2 per row: row 0 {0,2}, row 1 {1,2}.
+    Every block is 'similar' (rows of a block are parallel, sim = 1 > 0.5).
+    """
+    q = np.array([[1, 0], [1, 0], [0, 1], [0, 1]], dtype=np.float64)
+    k = np.array([[2, 0], [2, 0], [0, 3], [0, 3], [1, 1], [1, 1], [-1, 0], [-1, 0]],
+                 dtype=np.float64)
+    r = obm.block_map_head(q, k, 0.5, 0.5, None, 1.0, False, False, 2, 2)
+    assert r["raw"].tolist() == [[2, 0, 1, -1], [0, 3, 1, 0]]
+    assert r["lut"].tolist() == [[0, 2, -1, -1], [1, 2, -1, -1]]
+    assert r["count"].tolist() == [2, 2]
+    # causal + sink on the same data (q blocks and k blocks of equal size 2):
+    # row 0 sees only kv block 0; row 1 sees 0,1 -> K = ceil(0.5*2) = 1 -> {1}, plus sink 0
+    k2 = k[:4]
+    r = obm.block_map_head(q, k2, 0.5, 0.5, None, 1.0, True, True, 2, 2)
+    assert r["lut"].tolist() == [[0, -1], [0, 1]]
+    # kv block 1 made dissimilar (antithetic rows): its column is forced on
+    k3 = k2.copy()
+    k3[2], k3[3] = [1.0, 0.0], [-1.0, 0.0]
+    r = obm.block_map_head(q, k3, 0.5, 0.5, None, 1.0, False, False, 2, 2)
+    assert r["simk"].tolist() == [1.0, 0.0]
+    assert r["lut"].tolist() == [[0, 1], [0, 1]]
+    # a dissimilar q block keeps every eligible column
+    q3 = q.copy()
+    q3[0], q3[1] = [0.0, 2.0], [0.0, -2.0]
+    r = obm.block_map_head(q3, k, 0.5, 0.25, None, 1.0, False, False, 2, 2)
+    assert r["lut"][0].tolist() == [0, 1, 2, 3]
+    assert r["count"][1] == 1 and r["lut"][1, 0] == 1
+
+
+def test_all_dissimilar_gives_dense_map():
+    cfg = synth.C1
+    x = synth.prefill(cfg)
+    r = oracle.sparge_block_map(x["q"], x["k"], synth.per_head(cfg, 0.1), None,
+                                synth.per_head(cfg, 2.0), cfg.scale, False, False,
+                                dtype="f16")
+    assert r["block_map"].all()
+    assert (r["count"] == cfg.nq).all()
+
+
+def test_generated_blocks_clear_the_threshold():
+    """The centroid-plus-noise blocks (diffuse ones included) sit far above
+    simthreshd1 = 0.001, so nothing is forced at the configured threshold;
+    the antithetic variant drives diffuse blocks to exactly zero."""
+    cfg = synth.C1
+    x = synth.prefill(cfg)
+    q = synth.bits_to_f64(x["q"], "f16")
+    sims = [obm.self_similarity(q[0, 0, i * 64:(i + 1) * 64]) for i in range(cfg.nq)]
+    assert min(sims) > 0.1
+    xa = synth.prefill(cfg.replace(antithetic_diffuse=True))
+    qa = synth.bits_to_f64(xa["q"], "f16")
+    sa = sorted(obm.self_similarity(qa[0, 0, i * 64:(i + 1) * 64]) for i in range(cfg.nq))
+    assert sa[0] == 0.0 and sa[1] == 0.0 and sa[2] > 0.5
+
+
+# ----------------------------------------------------------------------------
+# attention
+# ----------------------------------------------------------------------------
+
+
+def _sdpa(q, k, v, scale, causal=False):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))[None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), scale=scale,
+                                                         is_causal=causal)
+    return o[0, 0].numpy()
+
+
+def _loop_row(qrow, k, v, scale, upto=None):
+    """One query row, written as plain loops with math.exp."""
+    n = k.shape[0] if upto is None else upto
+    sc = [scale * float(qrow @ k[u]) for u in range(n)]
+    m = max(sc)
+    w = [math.exp(x - m) for x in sc]
+    l = sum(w)
+    o = sum(w[u] * v[u] for u in range(n)) / l
+    return o, m + math.log(l)
+
+
+def test_topk_one_is_dense_attention():
+    cfg = synth.C1
+    x = synth.prefill(cfg)
+    q, k, v = (synth.bits_to_f64(x[t], "f16") for t in ("q", "k", "v"))
+    bm = oracle.sparge_block_map(x["q"], x["k"], synth.per_head(cfg, 1.0), None,
+                                 synth.per_head(cfg, cfg.simthreshd1), cfg.scale, False,
+                                 False, dtype="f16")
+    assert (bm["count"] == cfg.nq).all()
+    res = oracle.sparse_fmha(q, k, v, bm["lut"], bm["count"], cfg.scale, False)
+    for h in range(cfg.hq):
+        o_full = np.concatenate([res[(0, h, i)][0] for i in range(cfg.nq)])
+        lse_full = np.concatenate([res[(0, h, i)][1] for i in range(cfg.nq)])
+        ref = _sdpa(q[0, h], k[0, h], v[0, h], cfg.scale)
+        assert np.abs(o_full - ref).max() < 1e-12
+        for t in (0, 77, 511):
+            o_t, lse_t = _loop_row(q[0, h, t], k[0, h], v[0, h], cfg.scale)
+            assert np.abs(o_full[t] - o_t).max() < 1e-12
+            assert abs(lse_full[t] - lse_t) < 1e-12
+        sc = torch.from_numpy(q[0, h] @ k[0, h].T * cfg.scale)
+        assert np.abs(lse_full - torch.logsumexp(sc, dim=-1).numpy()).max() < 1e-12
+
+
+def test_causal_topk_one_is_causal_attention_with_sink():
+    cfg = synth.C1.replace(causal=True, attention_sink=True, topk=1.0, hq=4, hk=2)
+    x = synth.prefill(cfg)
+    q, k, v = (synth.bits_to_f64(x[t], "f16") for t in ("q", "k", "v"))
+    bm = oracle.sparge_block_map(x["q"], x["k"], synth.per_head(cfg, 1.0), None,
+                                 synth.per_head(cfg, cfg.simthreshd1), cfg.scale, True,
+                                 True, dtype="f16")
+    nq = cfg.nq
+    assert (bm["count"] == np.arange(1, nq + 1)[None, None, :]).all()
+    assert (bm["lut"][..., 0] == 0).all()
+    res = oracle.sparse_fmha(q, k, v, bm["lut"], bm["count"], cfg.scale, True)
+    for h in range(cfg.hq):
+        g = h // 2
+        o_full = np.concatenate([res[(0, h, i)][0] for i in range(nq)])
+        ref = _sdpa(q[0, h], k[0, g], v[0, g], cfg.scale, causal=True)
+        assert np.abs(o_full - ref).max() < 1e-12
+        o_t, lse_t = _loop_row(q[0, h, 130], k[0, g], v[0, g], cfg.scale, upto=131)
+        assert np.abs(o_full[130] - o_t).max() < 1e-12
+        assert abs(res[(0, h, 2)][1][2] - lse_t) < 1e-12
+
+
+def test_sink_column_under_small_topk():
+    cfg = synth.C1.replace(causal=True, attention_sink=True, topk=0.1)
+    x = synth.prefill(cfg)
+    bm = oracle.sparge_block_map(x["q"], x["k"], synth.per_head(cfg, 0.1), None,
+                                 synth.per_head(cfg, cfg.simthreshd1), cfg.scale, True,
+                                 True, dtype="f16")
+    assert (bm["lut"][..., 0] == 0).all()
+    for i in range(cfg.nq):
+        row = bm["lut"][0, 0, i, :bm["count"][0, 0, i]]
+        assert (row <= i).all() and (np.diff(row) > 0).all()
+
+
+def test_sparse_lse_is_logsumexp_of_selected_scores():
+    cfg = synth.C1
+    x = synth.prefill(cfg)
+    q, k, v = (synth.bits_to_f64(x[t], "f16") for t in ("q", "k", "v"))
+    lut_row = [1, 4, 6]
+    o, lse = oatt.attention_unit(q[0, 1], k[0, 1], v[0, 1], lut_row, 3, 64, 64, cfg.scale,
+                                 False)
+    keys = np.concatenate([np.arange(j * 64, j * 64 + 64) for j in lut_row])
+    sc = torch.from_numpy(cfg.scale * q[0, 1, 192:256] @ k[0, 1, keys].T)
+    assert np.abs(lse - torch.logsumexp(sc, -1).numpy()).max() < 1e-12
+    ref = _sdpa(q[0, 1, 192:256], k[0, 1, keys], v[0, 1, keys], cfg.scale)
+    assert np.abs(o - ref).max() < 1e-12
+
+
+def test_empty_row_gives_zero_and_minus_inf():
+    q = RNG.standard_normal((128, 8))
+    o, lse = oatt.attention_unit(q, q, q, [], 1, 64, 64, 0.3, False)
+    assert o.shape == (64, 8) and (o == 0).all() and np.isneginf(lse).all()
+
+
+# ----------------------------------------------------------------------------
+# split-KV and the combine identity
+# ----------------------------------------------------------------------------
+
+
+def _splits(nb):
+    allb = list(range(nb))
+    return {
+        "interleaved": (allb[0::2], allb[1::2]),
+        "spec_heavy": (allb[: nb - 2], allb[nb - 2:]),
+        "miss_heavy": (allb[:2], allb[2:]),
+        "contiguous_miss": ([b for b in allb if not 2 <= b < 5], [2, 3, 4]),
+    }
+
+
+@pytest.mark.parametrize("seqlen_q", [1, 4, 16])
+@pytest.mark.parametrize("block_size", [32, 64, 128])
+@pytest.mark.parametrize("split", ["interleaved", "spec_heavy", "miss_heavy",
+                                   "contiguous_miss"])
+def test_combine_identity(seqlen_q, block_size, split):
+    """FA(A u B) == Combine(FA(A), FA(B)) to 1e-10 in fp64, on the grid of the
+    updating_log's Stage 1 (seqlen_q x block_size x four splits)."""
+    rng = np.random.default_rng(seqlen_q * 1000 + block_size)
+    nb, d = 8, 32
+    q = rng.standard_normal((seqlen_q, d))
+    k = rng.standard_normal((nb * block_size, d))
+    v = rng.standard_normal((nb * block_size, d))
+    a, b = _splits(nb)[split]
+    full = oatt.attention_unit(q, k, v, sorted(a + b), 0, seqlen_q, block_size, 0.2, False)
+    pa = oatt.attention_unit(q, k, v, a, 0, seqlen_q, block_size, 0.2, False)
+    pb = oatt.attention_unit(q, k, v, b, 0, seqlen_q, block_size, 0.2, False)
+    o, lse = oracle.combine(np.stack([pa[0], pb[0]]), np.stack([pa[1], pb[1]]))
+    assert np.abs(o - full[0]).max() < 1e-10
+    assert np.abs(lse - full[1]).max() < 1e-10
+    o2, lse2 = oracle.combine(np.stack([pb[0], pa[0]]), np.stack([pb[1], pa[1]]))
+    assert np.abs(o2 - o).max() < 1e-10 and np.abs(lse2 - lse).max() < 1e-10
+
+
+def test_combine_empty_partials():
+    rng = np.random.default_rng(5)
+    o1 = rng.standard_normal((4, 8))
+    l1 = rng.standard_normal(4)
+    empty_o, empty_l = np.zeros((4, 8)), np.full(4, -np.inf)
+    o, l = oracle.combine(np.stack([o1, empty_o]), np.stack([l1, empty_l]))
+    assert np.abs(o - o1).max() < 1e-15 and np.abs(l - l1).max() < 1e-15
+    o, l = oracle.combine(np.stack([empty_o, empty_o]), np.stack([empty_l, empty_l]))
+    assert (o == 0).all() and np.isneginf(l).all()
+    # a row empty in one partial only
+    l1b = l1.copy()
+    l1b[2] = -np.inf
+    o, l = oracle.combine(np.stack([o1, empty_o]), np.stack([l1b, empty_l]))
+    assert (o[2] == 0).all() and np.isneginf(l[2])
+
+
+def test_combine_closed_form_two_partials():
+    """Two partials with LSE a, b: weights e^a/(e^a+e^b), LSE = ln(e^a+e^b)."""
+    o1, o2 = np.array([[1.0, 0.0]]), np.array([[0.0, 1.0]])
+    a, b = math.log(3.0), math.log(1.0)
+    o, l = oracle.combine(np.stack([o1, o2]), np.array([[a], [b]]))
+    assert np.abs(o[0] - [0.75, 0.25]).max() < 1e-15
+    assert abs(l[0] - math.log(4.0)) < 1e-15
+
+
+@pytest.mark.parametrize("n,S,sizes", [(10, 4, [3, 3, 2, 2]), (3, 8, [1, 1, 1, 0, 0, 0, 0, 0]),
+                                       (12, 3, [4, 4, 4]), (0, 2, [0, 0]), (7, 1, [7])])
+def test_split_bounds_table(n, S, sizes):
+    b = oracle.split_bounds(n, S)
+    assert [hi - lo for lo, hi in b] == sizes
+    assert b[0][0] == 0 and b[-1][1] == n
+    assert all(b[s][1] == b[s + 1][0] for s in range(S - 1))
+
+
+@pytest.mark.parametrize("S", [2, 3, 4, 8])
+def test_split_partials_combine_to_the_full_row(S):
+    rng = np.random.default_rng(S)
+    q = rng.standard_normal((256, 32))
+    k = rng.standard_normal((512, 32))
+    v = rng.standard_normal((512, 16))
+    row = [0, 2, 3, 5, 7]
+    parts = oatt.split_partials_unit(q, k, v, row, 2, S, 64, 64, 0.25, True)
+    o, l = oracle.combine(*parts)
+    ref = oatt.attention_unit(q, k, v, row, 2, 64, 64, 0.25, True)
+    assert np.abs(o - ref[0]).max() < 1e-10 and np.abs(l - ref[1]).max() < 1e-10
+
+
+# ----------------------------------------------------------------------------
+# decode
+# ----------------------------------------------------------------------------
+
+
+def test_decode_rows_hand_example():
+    rows = oatt.decode_rows(np.array([[3, 1]]), np.array([[0, 5, 7]]), 4)
+    assert rows.tolist() == [[12, 5, 7]]
+
+
+SMALL_DEC = synth.C5.replace(n_queries=4, pages_per_query=8, topk=96)
+
+
+@pytest.mark.parametrize("S", [2, 3, 4, 5, 8])
+def test_decode_split_invariance(S):
+    cfg = SMALL_DEC
+    inp = synth.decode(cfg)
+    q = synth.bits_to_f64(inp["q"], "bf16")
+    rows = oatt.decode_rows(inp["page_table"], inp["idx"], cfg.page)
+    for c in range(cfg.n_queries):
+        kv = synth.bits_to_f64(synth.cache_rows(cfg, rows[c]), "bf16")
+        full = oatt.decode_attention(q[c], kv, cfg.dv, cfg.sm_scale)
+        o, l = oracle.combine(*oatt.decode_partials(q[c], kv, cfg.dv, cfg.sm_scale, S))
+        assert np.abs(o - full[0]).max() < 1e-10 and np.abs(l - full[1]).max() < 1e-10
+        ref = _sdpa(q[c], kv, kv[:, :cfg.dv], cfg.sm_scale)
+        assert np.abs(full[0] - ref).max() < 1e-12
+
+
+# ----------------------------------------------------------------------------
+# planted mistakes: each must be caught by one of the pins above
+# ----------------------------------------------------------------------------
+
+
+def _select_high_index_ties(score, topk, cdf, n_elig):
+    sel = np.zeros(score.shape[0], dtype=bool)
+    fin = np.nonzero(np.isfinite(score))[0]
+    order = fin[np.lexsort((-fin, -score[fin]))]  # planted: higher index first
+    kk = min(obm.topk_count(topk, n_elig), fin.size)
+    sel[order[:kk]] = True
+    return sel
+
+
+def _select_cdf_exclusive(score, topk, cdf, n_elig):
+    sel = np.zeros(score.shape[0], dtype=bool)
+    fin = np.nonzero(np.isfinite(score))[0]
+    p = _softmax(score)[fin]
+    order = np.lexsort((fin, -p))
+    cum = np.cumsum(p[order])
+    take = int((cum < cdf).sum())  # planted: crossing entry left out
+    sel[fin[order[:take]]] = True
+    return sel
+
+
+def test_planted_mistakes_are_caught():
+    rows = _tiny_rows(1)
+    with pytest.raises(AssertionError):
+        for sc in rows:
+            check_topk_bruteforce(_select_high_index_ties, sc, 0.5)
+    with pytest.raises(AssertionError):
+        for sc in rows:
+            check_cdf_bruteforce(_select_cdf_exclusive, sc, 0.8)
+
+    def bad_combine(o_parts, lse_parts):  # planted: weights not renormalised
+        m = lse_parts.max(axis=0)
+        w = np.exp(lse_parts - m)
+        return (w[:, :, None] * o_parts).sum(axis=0), m + np.log(w.sum(axis=0))
+
+    o1, o2 = np.array([[1.0, 0.0]]), np.array([[0.0, 1.0]])
+    o, _ = bad_combine(np.stack([o1, o2]), np.array([[math.log(3.0)], [0.0]]))
+    assert np.abs(o[0] - [0.75, 0.25]).max() > 1e-3
