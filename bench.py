@@ -1,0 +1,387 @@
+#!/usr/bin/env python3
+"""Throughput of LUT-driven block-sparse attention forward on GB300.
+
+One step = the whole hot path over one batch of the headline workload
+(b=2, h=32, s=16384, d=128, fp16, non-causal, BLKQ=BLKK=64, simthreshd1=0.001):
+sparge_block_map (pool + similarity + pooled-score top-k -> LUT) followed by
+sparse_fmha_fwd over the selected tiles.  Inputs (Q, K, V: 805 MB) are larger
+than the 129 MB L2, so no flush is needed between steps.
+
+Metric: effective TFLOP/s = (selected tiles x 4 * 64 * 64 * d) / step time,
+plus the speedup over this library's own dense FMHA (the same kernel with no
+LUT) at the same shape.  `--topk` picks the step's topk (default 0.4); the
+sweep over {0.1, 0.2, 0.4, 0.6, 1.0} is reported alongside.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own batch on its own GPU (no
+collective on the data path); value = all ranks' work / the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective TFLOP/s & speedup vs own dense FMHA, b2 h32 s16k d128 per topk"
+FLOP_PER_TILE = 4 * 64 * 64 * 128  # QK^T and PV of one selected 64x64 tile at d = 128
+TOPKS = (0.1, 0.2, 0.4, 0.6, 1.0)
+
+# DRAM bytes per launch of the sparse FMHA kernel from one ncu capture (see
+# profiles/), keyed by the sha256 of the kernel source it was taken on; a
+# kernel edited since then reports traffic = null.
+NCU_TRAFFIC = {}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--topk", type=float, default=0.4)
+    p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash():
+    path = os.path.join(ROOT, "fmha_block_map_gb300", "csrc", "fmha_tc.cu")
+    try:
+        return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import fmha_block_map_gb300 as fbm
+    import synth
+    from fmha_block_map_gb300 import build as fbuild
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    fbuild.build()
+    fbm.lib()
+    cfg = synth.C3.replace(topk=args.topk)
+    x = synth.prefill(cfg)
+    dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.float16).cuda()
+    q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
+    stream = torch.cuda.current_stream()
+    ws = torch.empty(fbm.block_map_workspace_bytes(cfg.b, cfg.hq, cfg.hk, cfg.s, cfg.d),
+                     dtype=torch.uint8, device="cuda")
+    nq = cfg.nq
+    lut = torch.empty((cfg.b, cfg.hq, nq, nq), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((cfg.b, cfg.hq, nq), dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def block_map(topk):
+        fbm.sparge_block_map(q, k, topk=topk, simthreshd1=cfg.simthreshd1, scale=cfg.scale,
+                             lut=lut, lut_count=cnt, workspace=ws)
+
+    def attn(dense=False):
+        fbm.sparse_fmha_fwd(q, k, v, None if dense else lut, None if dense else cnt,
+                            scale=cfg.scale, out=out)
+
+    def timed(fn, steps, warm):
+        for _ in range(warm):
+            fn()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        barrier()
+        return e0.elapsed_time(e1) / steps
+
+    # ---- the timed step: block map + sparse attention, per-kernel events
+    for _ in range(args.warmup):
+        block_map(args.topk)
+        attn()
+    barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t0.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        block_map(args.topk)
+        ev[s][1].record(stream)
+        attn()
+        ev[s][2].record(stream)
+    t1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    step_ms = t0.elapsed_time(t1) / args.steps
+    bm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    at_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    tiles = int(cnt.sum().item())
+    assert fbm.get_error() == 0
+    flops = tiles * FLOP_PER_TILE
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([step_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = flops * world / (step_ms * 1e-3) / 1e12
+
+    # ---- dense reference FMHA and the topk sweep
+    dense_ms = timed(lambda: attn(dense=True), max(2, args.steps // 2), 1)
+    sweep = []
+    if not args.no_sweep:
+        for tk in TOPKS:
+            block_map(tk)
+            torch.cuda.synchronize()
+            tl = int(cnt.sum().item())
+            bm = timed(lambda: block_map(tk), 5, 1)
+            a = timed(lambda: attn(), max(2, args.steps // 2), 1)
+            sweep.append({"topk": tk, "selected_tiles": tl, "block_map_ms": round(bm, 4),
+                          "attn_ms": round(a, 4),
+                          "eff_tflops_attn": round(tl * FLOP_PER_TILE / (a * 1e-3) / 1e12, 1),
+                          "eff_tflops_step": round(tl * FLOP_PER_TILE / ((a + bm) * 1e-3) / 1e12, 1),
+                          "speedup_vs_dense_attn": round(dense_ms / a, 3),
+                          "speedup_vs_dense_step": round(dense_ms / (a + bm), 3)})
+        block_map(args.topk)
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq_, hk_, hv_ = (t.cpu().pin_memory() for t in (q, k, v))
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq, dk, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            dq.copy_(hq_, non_blocking=True)
+            dk.copy_(hk_, non_blocking=True)
+            dv_.copy_(hv_, non_blocking=True)
+            fbm.sparge_block_map(dq, dk, topk=args.topk, simthreshd1=cfg.simthreshd1,
+                                 scale=cfg.scale, lut=lut, lut_count=cnt, workspace=ws)
+            fbm.sparse_fmha_fwd(dq, dk, dv_, lut, cnt, scale=cfg.scale, out=out)
+            ho.copy_(out, non_blocking=True)
+
+        e2e_ms = timed(e2e_step, max(3, args.steps // 2), 2)
+        h2d = 3 * q.numel() * q.element_size()
+        d2h = out.numel() * out.element_size()
+        e2e = {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    peaks, peak_kind = load_peaks()
+    peak = peaks.get("bf16_tflops_sustained", 1700.0)
+    achieved = flops / (at_ms * 1e-3) / 1e12
+    kind = fbm.fmha_kernel_kind(torch.float16, 128, 128, 1, cfg.s, cfg.s)
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get(src_hash)
+    # block map algorithmic bytes: Q and K read once, pooled means + sims written
+    # and read back once, the -1-padded LUT rows and the counts written
+    pooled = (cfg.b * cfg.hq * nq + cfg.b * cfg.hk * nq) * (cfg.d + 1) * 4
+    bm_bytes = (q.numel() + k.numel()) * 2 + 2 * pooled + lut.numel() * 4 + cnt.numel() * 4
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded centroid-plus-noise blocks, 25% diffuse)",
+        "config": {"workload": "b2 h32 s16384 d128 fp16 non-causal, BLKQ=BLKK=64, "
+                               f"topk={args.topk}, simthreshd1=0.001",
+                   "b": 2, "h": 32, "s": 16384, "d": 128, "topk": args.topk,
+                   "l2": "inputs (805 MB) larger than L2; no flush"},
+        "speedup_vs_dense": {"dense_attn_ms": round(dense_ms, 4),
+                             "vs_attn": round(dense_ms / at_ms, 3),
+                             "vs_step": round(dense_ms / step_ms, 3)},
+        "block_map": {"ms": round(bm_ms, 4), "algorithmic_bytes": bm_bytes,
+                      "GB_s": round(bm_bytes / (bm_ms * 1e-3) / 1e9, 1),
+                      "frac_hbm": round(bm_bytes / (bm_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
+                      "share_of_step": round(bm_ms / step_ms, 3)},
+        "roofline": {"kernel": "sparse_fmha_fwd (" + ("tcgen05" if kind == 1 else "mma.sync") +
+                     ")", "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} bf16 sustained (fp16 tensor rate = bf16)",
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "frac_of_burst": round(achieved / peaks.get("bf16_tflops", peak), 4),
+                     "traffic": traffic, "selected_tiles": tiles,
+                     "flop_per_tile": FLOP_PER_TILE, "attn_ms": round(at_ms, 4)},
+        "sweep": sweep,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": 3 * args.steps,
+    }
+    if rank == 0 and os.environ.get("FBM_BENCH_NO_CPU") != "1":
+        res["cpu_baseline"] = cpu_baseline(cfg, x, args.topk)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return res if rank == 0 else None
+
+
+# ----------------------------------------------------------------------------
+# the fp64 oracle on the host cores (cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+
+
+def cpu_baseline(cfg, x, topk, qblocks=24, heads=1):
+    """The oracle as it stands on a bounded sample of the same workload: the
+    block map of `heads` (batch, head) pairs, then sparse attention of
+    `qblocks` q blocks of each; effective TFLOP/s over the selected tiles of
+    the sample, charging the block map in proportion to the q blocks done."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    units = [(0, h) for h in range(heads)]
+    t0 = time.perf_counter()
+    r = oracle.sparge_block_map(x["q"], x["k"], synth.per_head(cfg, topk), None,
+                                synth.per_head(cfg, cfg.simthreshd1), cfg.scale, False, False,
+                                dtype=cfg.dtype, heads=units)
+    t_bm = time.perf_counter() - t0
+    rng = np.random.default_rng(0)
+    todo = [(b, h, int(i)) for b, h in units for i in rng.choice(cfg.nq, qblocks, replace=False)]
+    t0 = time.perf_counter()
+    oracle.sparse_fmha(x["q"], x["k"], x["v"], r["lut"], r["count"], cfg.scale, False,
+                       units=todo, dtype=cfg.dtype)
+    t_at = time.perf_counter() - t0
+    tiles = sum(int(r["count"][b, h, i]) for b, h, i in todo)
+    t = t_at + t_bm * qblocks / cfg.nq
+    return {"value": round(tiles * FLOP_PER_TILE / t / 1e12, 6), "unit": "TFLOP/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"block map of {heads} (batch, head), attention of {len(todo)} q blocks "
+                      f"({tiles} selected tiles) at topk={topk}; {t:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import synth
+
+    cfg = synth.C3.replace(topk=args.topk)
+    x = synth.prefill(cfg.replace(b=1, hq=1, hk=1))
+    for _ in range(args.warmup):
+        cpu_baseline(cfg, x, args.topk, qblocks=4)
+    vals, t_all = [], time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(cfg, x, args.topk, qblocks=8))
+    t_all = time.perf_counter() - t_all
+    v = statistics.mean(r["value"] for r in vals)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t_all / args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded centroid-plus-noise blocks, 25% diffuse)",
+            "config": {"workload": "b2 h32 s16384 d128 fp16 non-causal, BLKQ=BLKK=64, "
+                                   f"topk={args.topk}, simthreshd1=0.001"},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": vals[0]["sample"]},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,359 @@
+// Block-map prediction kernels ("Sparge Attention (Composable Kernel)" README:
+// mean-pool -> cosine sim -> pooled QK -> top-k / cdfthreshd LUT).
+//
+//  k_pool_sim     one warp per 64-token block of Q or K: 128-bit loads, fp32
+//                 compensated row sums (the pooled mean) and the sum of unit
+//                 rows (self-similarity = ||sum u||^2 / n^2).  HBM-bound: it
+//                 reads Q and K once and writes (d + 1) floats per block.
+//  k_score_select one CTA per 16 q blocks of one (batch, head): pooled scores
+//                 by an fp32 register-tiled dot product (K-block means staged
+//                 through shared memory, shared by the 16 rows), then one warp
+//                 per row for the pooled softmax, a radix (bitwise) threshold
+//                 search for top-k / cdf, and ballot-scan emission of the
+//                 ascending LUT row.  No atomics take part in slot assignment.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fbm {
+
+// ---------------------------------------------------------------------------
+// k_pool_sim
+// ---------------------------------------------------------------------------
+
+struct PoolSide {
+  const uint16_t *x;  // [bh, s, D] bit patterns
+  float *pooled;      // [bh * nb, D]
+  float *sim;         // [bh * nb]
+  int s;              // rows per (batch, head)
+  int nb;             // blocks per (batch, head)
+  int nunits;         // bh * nb
+};
+
+template <class E, int D>
+__global__ void __launch_bounds__(256) k_pool_sim(PoolSide qs, PoolSide ks) {
+  constexpr int LPR = D / 8;      // lanes per row (16 B = 8 elements per lane)
+  constexpr int RPI = 32 / LPR;   // rows per warp-wide load
+  constexpr int ITERS = kBlk / RPI;
+  constexpr int UNR = 8;
+  const int lane = threadIdx.x & 31;
+  const int unit_all = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (unit_all >= qs.nunits + ks.nunits) return;
+  const PoolSide &side = unit_all < qs.nunits ? qs : ks;
+  const int unit = unit_all < qs.nunits ? unit_all : unit_all - qs.nunits;
+  const int bh = unit / side.nb;
+  const int j = unit - bh * side.nb;
+  const int row0 = j * kBlk;
+  const int n = min(kBlk, side.s - row0);
+  const uint16_t *base = side.x + ((size_t)bh * side.s + row0) * D;
+  const int sub = lane % LPR;
+  const int rgrp = lane / LPR;
+
+  float msum[8], mcomp[8], usum[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) msum[e] = mcomp[e] = usum[e] = 0.f;
+
+#pragma unroll
+  for (int it0 = 0; it0 < ITERS; it0 += UNR) {
+    uint4 raw[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int r = (it0 + u) * RPI + rgrp;
+      if (r < n)
+        raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + (size_t)r * D) + sub);
+      else
+        raw[u] = make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      float x[8];
+      const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        float2 f = E::to_f2(w[p]);
+        x[2 * p] = f.x;
+        x[2 * p + 1] = f.y;
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+      for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float inv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        usum[e] = fmaf(x[e], inv, usum[e]);
+        // Kahan-compensated running sum of the raw values (pooled mean)
+        const float y = x[e] - mcomp[e];
+        const float t = msum[e] + y;
+        mcomp[e] = (t - msum[e]) - y;
+        msum[e] = t;
+      }
+    }
+  }
+  float tot[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) tot[e] = msum[e] - mcomp[e];
+#pragma unroll
+  for (int o = 16; o >= LPR; o >>= 1) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      tot[e] += __shfl_xor_sync(0xffffffffu, tot[e], o);
+      usum[e] += __shfl_xor_sync(0xffffffffu, usum[e], o);
+    }
+  }
+  float su = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) su = fmaf(usum[e], usum[e], su);
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
+  if (rgrp == 0) {
+    const float fn = (float)n;
+    float4 *dst = reinterpret_cast<float4 *>(side.pooled + (size_t)unit * D) + sub * 2;
+    dst[0] = make_float4(tot[0] / fn, tot[1] / fn, tot[2] / fn, tot[3] / fn);
+    dst[1] = make_float4(tot[4] / fn, tot[5] / fn, tot[6] / fn, tot[7] / fn);
+    if (sub == 0) side.sim[unit] = su / (fn * fn);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// k_score_select
+// ---------------------------------------------------------------------------
+
+constexpr int kSelRows = 16;   // q blocks per CTA
+constexpr int kSelCols = 64;   // kv blocks per staged tile
+
+FBM_DEVICE uint32_t order_key(float f) {
+  // order-preserving map of a finite float onto uint32 (finite values > 0x7FFFFF)
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
+  extern __shared__ __align__(16) float smem[];
+  constexpr int LD = D + 4;
+  float *q_s = smem;                          // [16][LD]
+  float *k_s = q_s + kSelRows * LD;           // [64][LD]
+  float *S_s = k_s + kSelCols * LD;           // [16][NT * 32]
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y, bi = blockIdx.z;
+  const int ratio = a.hq / a.hk;
+  const int g = h / ratio;
+  const int i0 = blockIdx.x * kSelRows;
+  const float *qbar = a.qbar + ((size_t)(bi * a.hq + h) * a.nq) * D;
+  const float *kbar = a.kbar + ((size_t)(bi * a.hk + g) * a.nk) * D;
+  const float *qsim = a.qsim + (size_t)(bi * a.hq + h) * a.nq;
+  const float *ksim = a.ksim + (size_t)(bi * a.hk + g) * a.nk;
+
+  // stage the 16 pooled q rows
+  for (int idx = tid; idx < kSelRows * (D / 4); idx += blockDim.x) {
+    const int r = idx / (D / 4), c = idx % (D / 4);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i0 + r < a.nq) v = reinterpret_cast<const float4 *>(qbar + (size_t)(i0 + r) * D)[c];
+    *reinterpret_cast<float4 *>(q_s + r * LD + c * 4) = v;
+  }
+  const int tr = tid / 16, tc = tid % 16;
+  for (int c0 = 0; c0 < a.nk; c0 += kSelCols) {
+    __syncthreads();
+    for (int idx = tid; idx < kSelCols * (D / 4); idx += blockDim.x) {
+      const int r = idx / (D / 4), c = idx % (D / 4);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c0 + r < a.nk) v = reinterpret_cast<const float4 *>(kbar + (size_t)(c0 + r) * D)[c];
+      *reinterpret_cast<float4 *>(k_s + r * LD + c * 4) = v;
+    }
+    __syncthreads();
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int kk = 0; kk < D; kk += 4) {
+      const float4 qv = *reinterpret_cast<const float4 *>(q_s + tr * LD + kk);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 kv = *reinterpret_cast<const float4 *>(k_s + (tc + 16 * c) * LD + kk);
+        acc[c] = fmaf(qv.x, kv.x, acc[c]);
+        acc[c] = fmaf(qv.y, kv.y, acc[c]);
+        acc[c] = fmaf(qv.z, kv.z, acc[c]);
+        acc[c] = fmaf(qv.w, kv.w, acc[c]);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = c0 + tc + 16 * c;
+      if (j < a.nk) S_s[tr * (NT * 32) + j] = a.scale * acc[c];
+    }
+  }
+  __syncthreads();
+
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int rr = warp; rr < kSelRows; rr += 8) {
+    const int i = i0 + rr;
+    if (i >= a.nq) break;
+    const float theta = hp.theta[h];
+    const bool q_similar = qsim[i] > theta;
+    const int last_q = (i + 1) * a.blkq - 1;
+    const int n_elig = a.causal ? min(a.nk, last_q / a.blkk + 1) : a.nk;
+    float sc[NT];
+    uint32_t key[NT];
+    bool elig[NT], ksim_ok[NT];
+    float mloc = -INFINITY;
+    int nfin = 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int j = lane + 32 * t;
+      const bool valid = j < a.nk;
+      elig[t] = valid && (!a.causal || j * a.blkk <= last_q);
+      ksim_ok[t] = valid && ksim[j] > theta;
+      const bool fin = elig[t] && ksim_ok[t];
+      sc[t] = valid ? S_s[rr * (NT * 32) + j] : 0.f;
+      key[t] = fin ? order_key(sc[t]) : 0u;
+      if (fin) mloc = fmaxf(mloc, sc[t]);
+      nfin += fin ? 1 : 0;
+    }
+    nfin = __reduce_add_sync(0xffffffffu, nfin);
+    bool sel[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) sel[t] = false;
+    if (nfin > 0) {
+      const float m = warp_max(mloc);
+      if (!a.mode_cdf) {
+        const float prod = __fmul_rn(hp.sel[h], (float)n_elig);
+        const int kcount = min((int)ceilf(prod), nfin);
+        // largest T with #(key >= T) >= kcount: the kcount-th largest key
+        uint32_t T = 0;
+        for (int bit = 31; bit >= 0; --bit) {
+          const uint32_t cand = T | (1u << bit);
+          int c = 0;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) c += key[t] >= cand ? 1 : 0;
+          if (__reduce_add_sync(0xffffffffu, c) >= kcount) T = cand;
+        }
+        int cgt = 0;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) cgt += key[t] > T ? 1 : 0;
+        const int need = kcount - __reduce_add_sync(0xffffffffu, cgt);
+        int run = 0;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const bool tie = key[t] == T && key[t] != 0u;
+          const unsigned bal = __ballot_sync(0xffffffffu, tie);
+          sel[t] = key[t] > T || (tie && run + __popc(bal & lt_mask) < need);
+          run += __popc(bal);
+        }
+      } else {
+        float p[NT];
+        float ps = 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          p[t] = key[t] ? expf(sc[t] - m) : 0.f;
+          ps += p[t];
+        }
+        const float inv = 1.0f / warp_sum(ps);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) p[t] *= inv;
+        const float tau = hp.sel[h];
+        float mass_all = 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) mass_all += p[t];
+        mass_all = warp_sum(mass_all);
+        if (mass_all < tau) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) sel[t] = key[t] != 0u;
+        } else {
+          // largest T with mass(key >= T) >= tau
+          uint32_t T = 0;
+          for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = T | (1u << bit);
+            float ms = 0.f;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) ms += key[t] >= cand ? p[t] : 0.f;
+            if (warp_sum(ms) >= tau) T = cand;
+          }
+          float mgt = 0.f;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) mgt += key[t] > T ? p[t] : 0.f;
+          float carry = warp_sum(mgt);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const bool tie = key[t] == T && key[t] != 0u;
+            float v = tie ? p[t] : 0.f;
+            float incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const float up = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += up;
+            }
+            sel[t] = key[t] > T || (tie && carry + (incl - v) < tau);
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+          }
+        }
+      }
+    }
+    // forced columns / rows, sink, causal; ascending emission by ballot scan
+    const size_t row = ((size_t)(bi * a.hq + h) * a.nq + i);
+    int32_t *lut = a.lut + row * a.nk;
+    int run = 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int j = lane + 32 * t;
+      const bool forced = elig[t] && (!ksim_ok[t] || !q_similar || (a.sink && j == 0));
+      const bool keep = elig[t] && (sel[t] || forced);
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (keep) lut[run + __popc(bal & lt_mask)] = j;
+      if (a.bmap && j < a.nk) a.bmap[row * a.nk + j] = keep ? 1 : 0;
+      run += __popc(bal);
+    }
+    for (int p = run + lane; p < a.nk; p += 32) lut[p] = -1;
+    if (lane == 0) a.cnt[row] = run;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+// ---------------------------------------------------------------------------
+
+size_t block_map_smem_bytes(int d, int nt) {
+  return sizeof(float) * ((size_t)(kSelRows + kSelCols) * (d + 4) + (size_t)kSelRows * nt * 32);
+}
+
+template <int D, int NT>
+static cudaError_t launch_select(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {
+  const size_t smem = block_map_smem_bytes(D, NT);
+  cudaError_t e = cudaFuncSetAttribute(k_score_select<D, NT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.nq + kSelRows - 1) / kSelRows, a.hq, a.b);
+  k_score_select<D, NT><<<grid, 256, smem, st>>>(a, hp);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_select_nt(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {
+  if (a.nk <= 256) return launch_select<D, 8>(a, hp, st);
+  if (a.nk <= 512) return launch_select<D, 16>(a, hp, st);
+  return launch_select<D, 32>(a, hp, st);
+}
+
+cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
+  PoolSide qs{static_cast<const uint16_t *>(L.q), L.qbar, L.qsim, L.s, L.nq, L.b * L.hq * L.nq};
+  PoolSide ks{static_cast<const uint16_t *>(L.k), L.kbar, L.ksim, L.s, L.nk, L.b * L.hk * L.nk};
+  const int units = qs.nunits + ks.nunits;
+  const int grid = (units + 7) / 8;
+  if (L.d == 128) {
+    if (L.bf16) k_pool_sim<BF16, 128><<<grid, 256, 0, st>>>(qs, ks);
+    else k_pool_sim<F16, 128><<<grid, 256, 0, st>>>(qs, ks);
+  } else {
+    if (L.bf16) k_pool_sim<BF16, 64><<<grid, 256, 0, st>>>(qs, ks);
+    else k_pool_sim<F16, 64><<<grid, 256, 0, st>>>(qs, ks);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  SelectArgs a{};
+  a.qbar = L.qbar; a.qsim = L.qsim; a.kbar = L.kbar; a.ksim = L.ksim;
+  a.b = L.b; a.hq = L.hq; a.hk = L.hk; a.nq = L.nq; a.nk = L.nk;
+  a.blkq = kBlk; a.blkk = kBlk;
+  a.scale = L.scale; a.causal = L.causal; a.sink = L.sink; a.mode_cdf = L.mode_cdf;
+  a.lut = L.lut; a.cnt = L.cnt; a.bmap = L.bmap;
+  return L.d == 128 ? launch_select_nt<128>(a, L.hp, st) : launch_select_nt<64>(a, L.hp, st);
+}
+
+}  // namespace fbm

@@ -1,0 +1,72 @@
+// LSE combine of split-KV partials (Incremental_FlashAttention updating_log,
+// Stage 1: the lse_max trick; ROCm/aiter pull 4919: the split-KV reduce).
+//
+// One warp per output row: lanes first read the S partial LSEs, form
+// m = max_s LSE_s and the weights w_s = exp(LSE_s - m), then stream the S
+// partial rows with 128-bit loads and write sum_s w_s O_s / sum_s w_s.  A row
+// whose partials are all -inf (empty) writes O = 0 and LSE = -inf.  The kernel
+// is bandwidth-bound: it reads S * (dv + 1) * 4 bytes and writes dv elements
+// (+ 4 bytes of LSE) per row.
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fbm {
+namespace {
+
+constexpr int kMaxSplits = 64;
+
+template <int OUT>  // 0 = f16, 1 = bf16, 2 = f32
+__global__ void __launch_bounds__(256) k_attn_combine(const CombineLaunch L) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (row >= L.rows) return;
+  // weights: lane s holds split s (and s + 32)
+  float l0 = -INFINITY, l1 = -INFINITY;
+  if (lane < L.num_splits) l0 = L.lse_part[(int64_t)lane * L.rows + row];
+  if (lane + 32 < L.num_splits) l1 = L.lse_part[(int64_t)(lane + 32) * L.rows + row];
+  const float m = warp_max(fmaxf(l0, l1));
+  const bool live = m != -INFINITY;
+  const float w0 = live ? expf(l0 - m) : 0.f;
+  const float w1 = live ? expf(l1 - m) : 0.f;
+  const float wsum = warp_sum(w0 + w1);
+  const float inv = live ? 1.0f / wsum : 0.f;
+  for (int c = lane * 4; c < L.dv; c += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) {
+      for (int s = 0; s < L.num_splits; ++s) {
+        const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
+        if (w == 0.f) continue;  // an empty partial (weight 0) is skipped
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(
+            L.o_part + ((int64_t)s * L.rows + row) * L.dv + c));
+        acc.x = fmaf(w, x.x, acc.x);
+        acc.y = fmaf(w, x.y, acc.y);
+        acc.z = fmaf(w, x.z, acc.z);
+        acc.w = fmaf(w, x.w, acc.w);
+      }
+    }
+    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    if constexpr (OUT == 2) {
+      *reinterpret_cast<float4 *>(static_cast<float *>(L.out) + row * L.dv + c) = acc;
+    } else {
+      using E = typename std::conditional<OUT == 1, BF16, F16>::type;
+      uint2 pk = make_uint2(E::from_f2(acc.x, acc.y), E::from_f2(acc.z, acc.w));
+      *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(L.out) + row * L.dv + c) = pk;
+    }
+  }
+  if (L.lse_out && lane == 0) L.lse_out[row] = live ? m + logf(wsum) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineLaunch &L, cudaStream_t st) {
+  const int64_t threads = L.rows * 32;
+  const unsigned grid = (unsigned)((threads + 255) / 256);
+  if (L.out_dtype == FBM_F32) k_attn_combine<2><<<grid, 256, 0, st>>>(L);
+  else if (L.out_dtype == FBM_BF16) k_attn_combine<1><<<grid, 256, 0, st>>>(L);
+  else k_attn_combine<0><<<grid, 256, 0, st>>>(L);
+  return cudaGetLastError();
+}
+
+}  // namespace fbm

@@ -1,0 +1,76 @@
+// Internal launch interfaces between the C ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fbm.h"
+
+namespace fbm {
+
+struct HeadParams {
+  float theta[FBM_MAX_HEADS];  // simthreshd1 per query head
+  float sel[FBM_MAX_HEADS];    // topk or cdfthreshd per query head
+};
+
+struct SelectArgs {
+  const float *qbar, *qsim, *kbar, *ksim;
+  int b, hq, hk, nq, nk, blkq, blkk;
+  float scale;
+  int causal, sink, mode_cdf;
+  int32_t *lut, *cnt;
+  uint8_t *bmap;
+};
+
+struct BlockMapLaunch {
+  const void *q, *k;
+  int bf16, b, hq, hk, s, d, nq, nk;
+  float scale;
+  int causal, sink, mode_cdf;
+  HeadParams hp;
+  float *qbar, *qsim, *kbar, *ksim;  // workspace carve-out
+  int32_t *lut, *cnt;
+  uint8_t *bmap;
+};
+cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st);
+size_t block_map_smem_bytes(int d, int nt);
+
+struct FmhaLaunch {
+  const void *q, *k, *v;
+  int bf16, b, hq, hk, s_q, s_k, d, nq, nk;
+  const int32_t *lut, *cnt;  // lut == nullptr: dense
+  int lut_stride, num_splits, causal;
+  float scale;
+  void *out;
+  float *lse, *o_part, *lse_part;
+  uint32_t *err;
+};
+cudaError_t launch_fmha_mma(const FmhaLaunch &L, cudaStream_t st);
+cudaError_t launch_fmha_tc(const FmhaLaunch &L, cudaStream_t st);
+bool fmha_tc_supported(int d, int dv, int num_splits, int s_q, int s_k);
+
+struct CombineLaunch {
+  const float *o_part, *lse_part;
+  int num_splits;
+  int64_t rows;
+  int dv, out_dtype;
+  void *out;
+  float *lse_out;
+};
+cudaError_t launch_combine(const CombineLaunch &L, cudaStream_t st);
+
+struct DecodeLaunch {
+  const void *q, *cache;
+  int bf16, n_q, hq, d, dv, page;
+  int64_t n_pages;
+  const int32_t *page_table;
+  int pages_per_query;
+  const int32_t *idx;
+  int topk, num_splits;
+  float scale;
+  float *o_part, *lse_part;
+  uint32_t *err;
+};
+cudaError_t launch_decode(const DecodeLaunch &L, cudaStream_t st);
+
+}  // namespace fbm

@@ -1,0 +1,208 @@
+/*
+ * fbm.h - C ABI of libfbm: LUT-driven block-sparse attention forward on one
+ * GB300 GPU (sm_103a).
+ *
+ * The method (web pages, cited by title and section):
+ *  - "Sparge Attention (Composable Kernel)" README, intro and 'Status vs
+ *    Upstream': a block-map pipeline (per-block mean-pool -> cosine
+ *    similarity -> pooled QK -> top-k / cdfthreshd block selection -> LUT)
+ *    followed by a sparse FMHA stage that visits only the selected K/V tiles;
+ *    per-head topk / simthreshd1 / cdfthreshd; 'Not yet ported': causal mask in
+ *    the pooled score, attention sink (kv-block column 0 forced on).
+ *  - "Incremental_FlashAttention updating_log.md", Stage 1 (combine identity,
+ *    lse_max trick, empty partial = identity) and Stage 3 (an empty block list
+ *    writes O = 0 and LSE = -inf).
+ *  - ROCm/aiter pull 6841: LSE export of the computed scores, -inf for an
+ *    empty LUT row; the GQA mapping query head j -> KV head j / (hq / hk).
+ *  - ROCm/aiter pull 4919: sparse MLA decode over per-query token index lists
+ *    through a page table, split-KV partials and an LSE reduce; a caller
+ *    provided output buffer.
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument marked "device" is caller-owned device memory; the
+ *    library allocates nothing per call and keeps no pointer after returning.
+ *    "host" arrays are read before the call returns.
+ *  - All work is enqueued on `stream` (a cudaStream_t passed as void*, NULL =
+ *    the legacy default stream) and runs asynchronously; outputs are valid
+ *    once the stream reaches that point.
+ *  - Argument checks run on the host before any launch.  A failed check
+ *    returns FBM_ERR_INVALID_ARG or FBM_ERR_UNSUPPORTED and launches nothing;
+ *    fbm_last_error_message() then describes it (per thread).
+ *  - A launch failure returns FBM_ERR_CUDA.
+ *  - Conditions detected on the device (a LUT entry out of range, a bounded
+ *    wait that expired) set bits of a device error word; fbm_get_error()
+ *    synchronises the stream and reads (and clears) it.
+ *  - Tensors are contiguous, row-major, with the shapes given below; base
+ *    pointers must be 16-byte aligned.
+ *  - Head layout is BHSD: Q/O [b, hq, s_q, d], K/V [b, hk, s_k, d].
+ */
+#ifndef FBM_H_
+#define FBM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FBM_OK = 0,
+  FBM_ERR_INVALID_ARG = 1, /* a null pointer, a bad size or an inconsistent argument */
+  FBM_ERR_UNSUPPORTED = 2, /* valid, but outside what the kernels implement */
+  FBM_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
+  FBM_ERR_DEVICE = 4       /* fbm_get_error found device error bits set */
+} fbm_status;
+
+typedef enum { FBM_F16 = 0, FBM_BF16 = 1, FBM_F32 = 2 } fbm_dtype;
+
+/* Bits of the device error word. */
+#define FBM_DEVERR_LUT_RANGE 0x1u /* a LUT / index entry outside [0, n) or a count > n */
+#define FBM_DEVERR_TIMEOUT 0x2u   /* a bounded wait on an mbarrier expired */
+
+/* Largest number of query heads a call may pass per-head parameters for. */
+#define FBM_MAX_HEADS 256
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+int fbm_version(void);
+
+/* Description of the last failed argument check of the calling thread. */
+const char *fbm_last_error_message(void);
+
+/* Synchronises `stream`, then reads and clears the device error word into
+ * *detail (FBM_DEVERR_* bits; may be NULL).  Returns FBM_ERR_DEVICE when any
+ * bit was set, FBM_ERR_CUDA when the synchronisation failed, else FBM_OK. */
+fbm_status fbm_get_error(void *stream, uint32_t *detail);
+
+/*
+ * Workspace (bytes) that sparge_block_map needs for the given shape: pooled
+ * means (fp32) and self-similarities (fp32) of every Q and K block.
+ */
+size_t fbm_block_map_workspace_bytes(int b, int hq, int hk, int s, int d, int blkq,
+                                     int blkk);
+
+/*
+ * sparge_block_map - block-map prediction ("Sparge Attention (Composable
+ * Kernel)" README: mean-pool -> cosine sim -> pooled QK -> top-k LUT).
+ *
+ * For every (batch, query head h, q block i), with KV head g = h / (hq / hk):
+ *   1. qbar_i, kbar_j = means of the rows of each block (a partial last block
+ *      averages the rows it has);
+ *   2. sim(X) = || sum_t x_t / ||x_t|| ||^2 / n^2 of every block; a block is
+ *      similar when sim > simthreshd1[h] (K blocks of head g are compared with
+ *      the threshold of query head h);
+ *   3. eligible(i, j) = causal ? j * blkk <= (i + 1) * blkq - 1 : true;
+ *   4. S_ij = scale * qbar_i . kbar_j, -inf where kv block j is not similar or
+ *      (i, j) is not eligible; P_i = softmax_j S_i;
+ *   5. entries ordered by P descending, lower j first on ties; topk mode keeps
+ *      ceil(topk[h] * n_eligible_i) of them (product in fp32), cdf mode the
+ *      shortest prefix whose mass reaches cdfthreshd[h] (crossing entry
+ *      included; everything finite when the mass never reaches it);
+ *   6. forced on where eligible: non-similar kv columns, every column of a
+ *      non-similar q row, column 0 when attention_sink;
+ *   7. lut[b][h][i][0 .. count) = the kept kv blocks in ascending order,
+ *      lut[b][h][i][count .. nk) = -1, lut_count[b][h][i] = count.
+ *
+ * q: device [b, hq, s, d], k: device [b, hk, s, d], dtype FBM_F16 / FBM_BF16.
+ * d in {64, 128}; blkq = blkk = 64; nk = ceil(s / 64) <= 1024; hq % hk == 0;
+ * hq <= FBM_MAX_HEADS.
+ * topk, cdfthreshd, simthreshd1: host float[hq]; exactly one of topk /
+ *   cdfthreshd is non-NULL; topk and cdfthreshd values in (0, 1].
+ * lut: device int32 [b, hq, nq, nk]; lut_count: device int32 [b, hq, nq];
+ * block_map: device uint8 [b, hq, nq, nk] (1 = kept) or NULL.
+ * workspace: device, >= fbm_block_map_workspace_bytes(...) bytes, 16-byte
+ *   aligned; its contents are scratch between calls.
+ */
+fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int hq, int hk,
+                            int s, int d, int blkq, int blkk, const float *topk,
+                            const float *cdfthreshd, const float *simthreshd1, float scale,
+                            int causal, int attention_sink, int32_t *lut, int32_t *lut_count,
+                            uint8_t *block_map, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
+/*
+ * sparse_fmha_fwd - flash attention over the LUT-selected K/V tiles
+ * ("Sparge Attention (Composable Kernel)" README: the sparse FMHA stage;
+ * updating_log Stage 3 for the per-row-block loop over a block list).
+ *
+ * For each query row t of q block i (head h, KV head g = h / (hq / hk)), the
+ * keys are the union of kv blocks lut[b][h][i][0 .. lut_count[b][h][i]); under
+ * causal (s_q == s_k) only keys at positions <= t.  With s = scale * q_t . k_u,
+ * O_t = sum_u e^(s_u - m) v_u / sum_u e^(s_u - m) and LSE_t = m + ln sum_u
+ * e^(s_u - m) (natural log).  An empty key set gives O_t = 0, LSE_t = -inf.
+ *
+ * q: device [b, hq, s_q, d]; k: device [b, hk, s_k, d]; v: device [b, hk, s_k, dv];
+ * dtype FBM_F16 / FBM_BF16; d = dv in {64, 128}; blkq = blkk = 64.
+ * lut: device int32 [b, hq, nq, lut_stride] with nq = ceil(s_q / 64), entries in
+ *   [0, ceil(s_k / 64)), ascending (an out-of-range entry is skipped and sets
+ *   FBM_DEVERR_LUT_RANGE); lut_count: device int32 [b, hq, nq].
+ *   lut == NULL (and lut_count == NULL) selects dense attention: every kv
+ *   block (every causally visible one under causal).
+ * num_splits == 1: out = device [b, hq, s_q, dv] in dtype; lse = device fp32
+ *   [b, hq, s_q] or NULL (return_lse off); o_partial / lse_partial unused.
+ * num_splits > 1 (split-KV): the LUT row of each q block is cut into
+ *   num_splits contiguous chunks (the first n mod S chunks hold ceil(n/S)
+ *   entries, the rest floor(n/S)); chunk s writes its normalised partial to
+ *   o_partial = device fp32 [S, b, hq, s_q, dv] and its LSE to lse_partial =
+ *   device fp32 [S, b, hq, s_q] (empty chunk: 0 and -inf); out / lse unused.
+ *   attn_combine merges them.
+ */
+fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtype, int b,
+                           int hq, int hk, int s_q, int s_k, int d, int dv, int blkq, int blkk,
+                           const int32_t *lut, const int32_t *lut_count, int lut_stride,
+                           int num_splits, float scale, int causal, void *out, float *lse,
+                           float *o_partial, float *lse_partial, void *stream);
+
+/*
+ * attn_combine - merge split-KV partials over disjoint key sets
+ * (updating_log Stage 1, the lse_max trick): per row, m = max_s LSE_s,
+ * w_s = e^(LSE_s - m), O = sum_s w_s O_s / sum_s w_s, LSE = m + ln sum_s w_s;
+ * rows whose partials are all empty (LSE = -inf) give O = 0, LSE = -inf.
+ *
+ * o_part: device fp32 [num_splits, rows, dv]; lse_part: device fp32
+ * [num_splits, rows]; out: device [rows, dv] in out_dtype (FBM_F16, FBM_BF16 or
+ * FBM_F32); lse_out: device fp32 [rows] or NULL.  dv % 4 == 0, dv <= 1024,
+ * 1 <= num_splits <= 64.
+ */
+fbm_status attn_combine(const float *o_part, const float *lse_part, int num_splits,
+                        int64_t rows, int dv, int out_dtype, void *out, float *lse_out,
+                        void *stream);
+
+/*
+ * sparse_decode_fwd - sparse decode over per-query token index lists through a
+ * page table (ROCm/aiter pull 4919: sparse MLA decode with split-KV partials).
+ *
+ * Query c (one token, hq heads sharing one KV head) attends to the tokens
+ * listed in indices[c][0 .. topk); token position p lives in cache row
+ * page_table[c][p / page_size] * page_size + p % page_size; K = that row
+ * (d values), V = its first dv values.  A negative index is a sentinel and is
+ * skipped.  The list is cut into num_splits contiguous chunks (sizes as in
+ * sparse_fmha_fwd); chunk s writes the normalised partial o_partial[s][c][h][:]
+ * and its LSE lse_partial[s][c][h] (empty chunk: 0 and -inf).  attn_combine
+ * over rows = n_q * hq merges them.
+ *
+ * q: device [n_q, hq, d] in dtype; kv_cache: device [n_pages, page_size, d];
+ * dtype FBM_BF16 or FBM_F16; implemented shape: hq == 16, d == 576, dv == 512,
+ * page_size == 64 (other shapes return FBM_ERR_UNSUPPORTED);
+ * ceil(topk / num_splits) <= 16384;
+ * page_table: device int32 [n_q, pages_per_query], entries in [0, n_pages);
+ * indices: device int32 [n_q, topk], entries < pages_per_query * page_size;
+ * o_partial: device fp32 [num_splits, n_q, hq, dv]; lse_partial: device fp32
+ * [num_splits, n_q, hq]; 1 <= num_splits <= 64.
+ */
+fbm_status sparse_decode_fwd(const void *q, const void *kv_cache, int dtype, int n_q, int hq,
+                             int d, int dv, int page_size, int64_t n_pages,
+                             const int32_t *page_table, int pages_per_query,
+                             const int32_t *indices, int topk, int num_splits, float scale,
+                             float *o_partial, float *lse_partial, void *stream);
+
+/* Which sparse-FMHA kernel sparse_fmha_fwd launches for these arguments:
+ * 1 = tcgen05 / TMA kernel, 2 = mma.sync kernel, 0 = none (the arguments
+ * would be rejected).  Host-only; launches nothing. */
+int fbm_fmha_kernel_kind(int dtype, int d, int dv, int num_splits, int s_q, int s_k);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FBM_H_ */

@@ -1,0 +1,135 @@
+"""The C ABI library loads, exports every entry point include/fbm.h declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fmha_block_map_gb300 as fbm
+from fmha_block_map_gb300 import build as fbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "fbm.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    fbuild.build()
+    return fbm.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) -
+                  {"defined", "sizeof", "extern"})
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("sparge_block_map", "sparse_fmha_fwd", "attn_combine", "sparse_decode_fwd",
+              "fbm_get_error", "fbm_block_map_workspace_bytes", "fbm_last_error_message",
+              "fbm_version", "fbm_fmha_kernel_kind"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), f"libfbm.so does not export {n}"
+    assert L.fbm_version() == 100
+
+
+def test_workspace_size(L):
+    n = fbm.block_map_workspace_bytes(2, 32, 32, 16384, 128)
+    # pooled means (fp32) and sims (fp32) of 2*32*256 q and k blocks, 256-B aligned pieces
+    assert n >= 2 * (2 * 32 * 256 * 128 * 4 + 2 * 32 * 256 * 4)
+    assert L.fbm_block_map_workspace_bytes(1, 1, 1, 64, 64, 32, 64) == 0
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: checks fail before any launch
+
+
+def _bm(L, **kw):
+    a = dict(q=FAKE, k=FAKE, dtype=0, b=1, hq=2, hk=2, s=512, d=64, blkq=64, blkk=64,
+             topk=(ctypes.c_float * 2)(0.5, 0.5), cdf=None,
+             sim=(ctypes.c_float * 2)(0.001, 0.001), scale=0.125, causal=0, sink=0,
+             lut=FAKE, cnt=FAKE, bmap=None, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    return L.sparge_block_map(a["q"], a["k"], a["dtype"], a["b"], a["hq"], a["hk"], a["s"],
+                              a["d"], a["blkq"], a["blkk"], a["topk"], a["cdf"], a["sim"],
+                              a["scale"], a["causal"], a["sink"], a["lut"], a["cnt"], a["bmap"],
+                              a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fbm.FBM_ERR_INVALID_ARG),
+    (dict(hq=3, topk=(ctypes.c_float * 3)(.5, .5, .5), sim=(ctypes.c_float * 3)(0, 0, 0)),
+     fbm.FBM_ERR_INVALID_ARG),
+    (dict(d=96), fbm.FBM_ERR_UNSUPPORTED),
+    (dict(blkq=128), fbm.FBM_ERR_UNSUPPORTED),
+    (dict(cdf=(ctypes.c_float * 2)(0.9, 0.9)), fbm.FBM_ERR_INVALID_ARG),  # both modes
+    (dict(topk=None), fbm.FBM_ERR_INVALID_ARG),                            # neither
+    (dict(topk=(ctypes.c_float * 2)(0.0, 0.5)), fbm.FBM_ERR_INVALID_ARG),
+    (dict(topk=(ctypes.c_float * 2)(1.5, 0.5)), fbm.FBM_ERR_INVALID_ARG),
+    (dict(wsb=16), fbm.FBM_ERR_INVALID_ARG),
+    (dict(q=ctypes.c_void_p((1 << 20) + 4)), fbm.FBM_ERR_INVALID_ARG),
+    (dict(dtype=7), fbm.FBM_ERR_INVALID_ARG),
+    (dict(s=70000), fbm.FBM_ERR_UNSUPPORTED),
+    (dict(scale=0.0), fbm.FBM_ERR_INVALID_ARG),
+])
+def test_block_map_rejects(L, kw, code):
+    assert _bm(L, **kw) == code
+    assert L.fbm_last_error_message()
+
+
+def _fm(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=1, b=1, hq=4, hk=2, s_q=256, s_k=256, d=128, dv=128,
+             blkq=64, blkk=64, lut=FAKE, cnt=FAKE, stride=4, S=1, scale=0.1, causal=0,
+             out=FAKE, lse=None, op=None, lp=None)
+    a.update(kw)
+    return L.sparse_fmha_fwd(a["q"], a["k"], a["v"], a["dtype"], a["b"], a["hq"], a["hk"],
+                             a["s_q"], a["s_k"], a["d"], a["dv"], a["blkq"], a["blkk"],
+                             a["lut"], a["cnt"], a["stride"], a["S"], a["scale"], a["causal"],
+                             a["out"], a["lse"], a["op"], a["lp"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(v=None), fbm.FBM_ERR_INVALID_ARG),
+    (dict(cnt=None), fbm.FBM_ERR_INVALID_ARG),
+    (dict(hk=3), fbm.FBM_ERR_INVALID_ARG),
+    (dict(d=96, dv=96), fbm.FBM_ERR_UNSUPPORTED),
+    (dict(dv=64), fbm.FBM_ERR_UNSUPPORTED),
+    (dict(causal=1, s_k=512), fbm.FBM_ERR_UNSUPPORTED),
+    (dict(S=2), fbm.FBM_ERR_INVALID_ARG),      # split without partial buffers
+    (dict(S=0), fbm.FBM_ERR_INVALID_ARG),
+    (dict(out=None), fbm.FBM_ERR_INVALID_ARG),
+    (dict(stride=0), fbm.FBM_ERR_INVALID_ARG),
+    (dict(blkk=128), fbm.FBM_ERR_UNSUPPORTED),
+    (dict(k=ctypes.c_void_p((1 << 20) + 2)), fbm.FBM_ERR_INVALID_ARG),
+])
+def test_fmha_rejects(L, kw, code):
+    assert _fm(L, **kw) == code
+
+
+def test_combine_and_decode_reject(L):
+    assert L.attn_combine(FAKE, FAKE, 0, 10, 128, 2, FAKE, None, None) == fbm.FBM_ERR_INVALID_ARG
+    assert L.attn_combine(FAKE, FAKE, 2, 10, 130, 2, FAKE, None, None) == fbm.FBM_ERR_UNSUPPORTED
+    assert L.attn_combine(FAKE, None, 2, 10, 128, 2, FAKE, None, None) == fbm.FBM_ERR_INVALID_ARG
+    args = [FAKE, FAKE, 1, 64, 16, 576, 512, 64, 65536, FAKE, 1024, FAKE, 2048, 4, 0.12,
+            FAKE, FAKE, None]
+    bad = list(args)
+    bad[4] = 8  # hq
+    assert L.sparse_decode_fwd(*bad) == fbm.FBM_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[13] = 0  # splits
+    assert L.sparse_decode_fwd(*bad) == fbm.FBM_ERR_INVALID_ARG
+    bad = list(args)
+    bad[9] = None  # page table
+    assert L.sparse_decode_fwd(*bad) == fbm.FBM_ERR_INVALID_ARG
+
+
+def test_kernel_kind_is_host_only(L):
+    assert L.fbm_fmha_kernel_kind(0, 96, 96, 1, 128, 128) == 0
+    assert L.fbm_fmha_kernel_kind(1, 64, 64, 2, 128, 128) == 2
+    assert L.fbm_fmha_kernel_kind(1, 128, 128, 1, 16384, 16384) in (1, 2)

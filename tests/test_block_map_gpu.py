@@ -1,0 +1,117 @@
+"""GPU block map (sparge_block_map) against the fp64 oracle on the same seeded
+inputs: LUT bit-exact except counted near-ties, ascending rows, -1 padding,
+deterministic relaunches."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _util import SIM_MARGIN, cached_prefill, compare_lut_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(fbm, cfg, mode, param, heads=None, check_sim_margin=True):
+    x = cached_prefill(cfg)
+    q, k = to_dev(x["q"], cfg.dtype), to_dev(x["k"], cfg.dtype)
+    kw = {"topk": param} if mode == "topk" else {"cdfthreshd": param}
+    lut, cnt, bmap = fbm.sparge_block_map(q, k, simthreshd1=cfg.simthreshd1, scale=cfg.scale,
+                                          causal=cfg.causal, attention_sink=cfg.attention_sink,
+                                          return_block_map=True, **kw)
+    assert fbm.get_error() == 0
+    lut, cnt, bmap = lut.cpu().numpy(), cnt.cpu().numpy(), bmap.cpu().numpy()
+    ph = synth.per_head(cfg, param)
+    ora = oracle.sparge_block_map(x["q"], x["k"], ph if mode == "topk" else None,
+                                  ph if mode == "cdf" else None,
+                                  synth.per_head(cfg, cfg.simthreshd1), cfg.scale, cfg.causal,
+                                  cfg.attention_sink, keep_aux=True, dtype=cfg.dtype, heads=heads)
+    todo = heads or [(b, h) for b in range(cfg.b) for h in range(cfg.hq)]
+    exact = near = 0
+    for b, h in todo:
+        aux = ora["aux"][(b, h)]
+        if check_sim_margin:
+            for v in (aux["simq"], aux["simk"]):
+                assert np.all(np.abs(v - cfg.simthreshd1) > SIM_MARGIN), "sim too close to theta"
+        e, n = compare_lut_rows(lut[b, h], cnt[b, h], ora["lut"][b, h], ora["count"][b, h], aux,
+                                mode, param, cfg.causal, cfg.attention_sink)
+        exact += e
+        near += n
+        for i in range(lut.shape[2]):
+            row = np.zeros(lut.shape[3], dtype=bool)
+            row[lut[b, h, i, :cnt[b, h, i]]] = True
+            assert (row == bmap[b, h, i].astype(bool)).all()
+    print(f"{cfg.name} {mode}={param}: {exact} rows exact, {near} near-tie rows")
+    return lut, cnt, exact, near
+
+
+def test_c1_tiny(fbm_gpu):
+    run_case(fbm_gpu, synth.C1, "topk", 0.5)
+
+
+def test_c1_antithetic_forces_dense_rows_and_columns(fbm_gpu):
+    cfg = synth.C1.replace(antithetic_diffuse=True)
+    lut, cnt, _, _ = run_case(fbm_gpu, cfg, "topk", 0.5)
+    assert (cnt == cfg.nq).any()          # dissimilar q blocks keep every column
+
+
+def test_c1_theta_half_splits_populations(fbm_gpu):
+    cfg = synth.C1.replace(simthreshd1=0.5)
+    run_case(fbm_gpu, cfg, "topk", 0.5)
+
+
+@pytest.mark.parametrize("topk", [0.1, 1e-6, 1.0])
+def test_c1_topk_extremes(fbm_gpu, topk):
+    lut, cnt, _, _ = run_case(fbm_gpu, synth.C1, "topk", topk)
+    if topk == 1.0:
+        assert (cnt == synth.C1.nq).all()
+
+
+def test_c1_causal_sink_gqa(fbm_gpu):
+    cfg = synth.C1.replace(hq=4, hk=2, causal=True, attention_sink=True, topk=0.3)
+    lut, cnt, _, _ = run_case(fbm_gpu, cfg, "topk", 0.3)
+    assert (lut[..., 0] == 0).all()
+
+
+def test_ragged_sequence(fbm_gpu):
+    cfg = synth.C2.replace(b=2, hq=2, hk=1, s=1000, cs_range=None, dtype="f16")
+    run_case(fbm_gpu, cfg, "topk", 0.25)
+    run_case(fbm_gpu, cfg.replace(causal=True, attention_sink=True), "cdf", 0.8)
+
+
+def test_c2_cdf(fbm_gpu):
+    run_case(fbm_gpu, synth.C2, "cdf", 0.9)
+
+
+@pytest.mark.parametrize("tau", [0.5, 1.0])
+def test_c2_cdf_extremes(fbm_gpu, tau):
+    cfg = synth.C2.replace(hq=2, hk=2)
+    run_case(fbm_gpu, cfg, "cdf", tau)
+
+
+def test_c3_full_lut_topk04(fbm_gpu):
+    run_case(fbm_gpu, synth.C3, "topk", 0.4)
+
+
+@pytest.mark.parametrize("topk", [0.1, 0.2, 0.6, 1.0])
+def test_c3_sampled_heads(fbm_gpu, topk):
+    heads = [(0, 0), (0, 17), (1, 5), (1, 31)]
+    run_case(fbm_gpu, synth.C3, "topk", topk, heads=heads)
+
+
+def test_c4_causal_gqa_sink(fbm_gpu):
+    lut, cnt, _, _ = run_case(fbm_gpu, synth.C4, "topk", 0.2)
+    assert (lut[..., 0] == 0).all()
+
+
+def test_block_map_is_deterministic(fbm_gpu):
+    cfg = synth.C2.replace(hq=4, hk=2)
+    x = synth.prefill(cfg)
+    q, k = to_dev(x["q"], cfg.dtype), to_dev(x["k"], cfg.dtype)
+    ref = None
+    for _ in range(20):
+        lut, cnt, _ = fbm_gpu.sparge_block_map(q, k, cdfthreshd=0.9, scale=cfg.scale)
+        cur = (lut.cpu(), cnt.cpu())
+        if ref is None:
+            ref = cur
+        assert torch.equal(cur[0], ref[0]) and torch.equal(cur[1], ref[1])

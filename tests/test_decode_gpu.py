@@ -1,0 +1,77 @@
+"""GPU sparse decode (sparse_decode_fwd + attn_combine) against the fp64 oracle:
+paged gathers of top-k token rows, V = latent plane, split-KV partials."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _util import assert_close_lse, assert_close_o
+from oracle.attention import decode_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_cache(cfg, device="cuda"):
+    n_rows = cfg.n_pages * cfg.page
+    cache = torch.empty((n_rows, cfg.d), dtype=torch.bfloat16, device=device)
+    step = 1 << 18
+    for r0 in range(0, n_rows, step):
+        r1 = min(n_rows, r0 + step)
+        cache[r0:r1] = synth.cache_rows_torch(cfg, r0, r1, device)
+    return cache.view(cfg.n_pages, cfg.page, cfg.d)
+
+
+def run(fbm, cfg, S, inp=None, cache=None, queries=None, idx_override=None):
+    inp = inp or synth.decode(cfg)
+    cache = cache if cache is not None else gpu_cache(cfg)
+    idx = inp["idx"] if idx_override is None else idx_override
+    q_bits = inp["q"]
+    q = torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    pt = torch.from_numpy(inp["page_table"]).cuda()
+    ix = torch.from_numpy(np.ascontiguousarray(idx)).cuda()
+    op, lp = fbm.sparse_decode_fwd(q, cache, pt, ix, dv=cfg.dv, scale=cfg.sm_scale, num_splits=S)
+    out, lse = fbm.attn_combine(op, lp, out_dtype=torch.bfloat16)
+    assert fbm.get_error() == 0
+    op, lp = op.double().cpu().numpy(), lp.double().cpu().numpy()
+    out, lse = out.double().cpu().numpy(), lse.double().cpu().numpy()
+    qf = synth.bits_to_f64(q_bits, "bf16")
+    rows = decode_rows(inp["page_table"], np.maximum(idx, 0), cfg.page)
+    for c in (queries if queries is not None else range(cfg.n_queries)):
+        keep = idx[c] >= 0
+        kv = synth.bits_to_f64(synth.cache_rows(cfg, rows[c][keep]), "bf16")
+        # partials follow the chunks of the full list (sentinels included)
+        bounds = oracle.split_bounds(idx.shape[1], S)
+        for s, (lo, hi) in enumerate(bounds):
+            sel = keep[lo:hi]
+            kv_s = synth.bits_to_f64(synth.cache_rows(cfg, rows[c][lo:hi][sel]), "bf16")
+            po, pl = oracle.decode_attention(qf[c], kv_s, cfg.dv, cfg.sm_scale)
+            assert_close_o(op[s, c], po, f"Opart q{c} s{s}")
+            assert_close_lse(lp[s, c], pl, f"LSEpart q{c} s{s}")
+        ro, rl = oracle.decode_attention(qf[c], kv, cfg.dv, cfg.sm_scale)
+        assert_close_o(out[c], ro, f"O q{c}")
+        assert_close_lse(lse[c], rl, f"LSE q{c}")
+
+
+SMALL = synth.C5.replace(n_queries=8, pages_per_query=32, topk=300)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 8])
+def test_small_decode(fbm_gpu, S):
+    run(fbm_gpu, SMALL, S)
+
+
+def test_sentinels_are_skipped(fbm_gpu):
+    inp = synth.decode(SMALL)
+    idx = inp["idx"].copy()
+    idx[:, ::7] = -1
+    idx[0, :] = -1  # a query with nothing to attend: O = 0, LSE = -inf
+    run(fbm_gpu, SMALL, 3, inp=inp, idx_override=idx)
+
+
+def test_full_decode_sampled(fbm_gpu):
+    cfg = synth.C5
+    inp = synth.decode(cfg)
+    cache = gpu_cache(cfg)
+    for S in (2, 4, 8):
+        run(fbm_gpu, cfg, S, inp=inp, cache=cache, queries=[0, 13, 37, 63])

@@ -1,0 +1,189 @@
+"""GPU sparse FMHA (sparse_fmha_fwd, attn_combine) against the fp64 oracle on
+the same seeded inputs and the oracle's own LUTs: O within atol 4e-2 / rtol
+1e-2, LSE within 1e-3 nats, empty rows exactly (0, -inf)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _util import (assert_close_lse, assert_close_o, cached_prefill, prefill_on_gpu, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_lut(cfg, mode="topk", param=None):
+    x = cached_prefill(cfg)
+    param = cfg.topk if param is None else param
+    ph = synth.per_head(cfg, param)
+    r = oracle.sparge_block_map(x["q"], x["k"], ph if mode == "topk" else None,
+                                ph if mode == "cdf" else None,
+                                synth.per_head(cfg, cfg.simthreshd1), cfg.scale, cfg.causal,
+                                cfg.attention_sink, dtype=cfg.dtype)
+    return r["lut"], r["count"]
+
+
+def check(fbm, cfg, lut, cnt, units=None, num_splits=1, dense=False):
+    x, (q, k, v) = prefill_on_gpu(cfg)
+    lut_d = None if dense else torch.from_numpy(lut).cuda()
+    cnt_d = None if dense else torch.from_numpy(cnt).cuda()
+    if num_splits == 1:
+        out, lse = fbm.sparse_fmha_fwd(q, k, v, lut_d, cnt_d, scale=cfg.scale, causal=cfg.causal,
+                                       return_lse=True)
+    else:
+        op, lp = fbm.sparse_fmha_fwd(q, k, v, lut_d, cnt_d, scale=cfg.scale, causal=cfg.causal,
+                                     num_splits=num_splits)
+        out, lse = fbm.attn_combine(op, lp, out_dtype=q.dtype)
+    assert fbm.get_error() == 0
+    o_np = out.double().cpu().numpy()
+    l_np = lse.cpu().numpy().astype(np.float64)
+    res = oracle.sparse_fmha(x["q"], x["k"], x["v"], lut, cnt, cfg.scale, cfg.causal, units=units,
+                             dtype=cfg.dtype)
+    worst_o = worst_l = 0.0
+    for (b, h, i), (o_ref, lse_ref) in res.items():
+        rows = slice(i * 64, i * 64 + o_ref.shape[0])
+        worst_o = max(worst_o, assert_close_o(o_np[b, h, rows], o_ref, f"O{(b, h, i)}"))
+        worst_l = max(worst_l, assert_close_lse(l_np[b, h, rows], lse_ref, f"LSE{(b, h, i)}"))
+        if (cnt[b, h, i] == 0) if not dense else False:
+            assert (o_np[b, h, rows] == 0).all() and np.isneginf(l_np[b, h, rows]).all()
+    print(f"{cfg.name}: {len(res)} q blocks, max |dO| {worst_o:.2e}, max |dLSE| {worst_l:.2e}")
+    return out, lse
+
+
+def hand_lut(cfg, seed=0):
+    """Empty, single, discontinuous, full and random rows."""
+    nq = cfg.nq
+    nk = nq
+    rng = np.random.default_rng(seed)
+    lut = np.full((cfg.b, cfg.hq, nq, nk), -1, dtype=np.int32)
+    cnt = np.zeros((cfg.b, cfg.hq, nq), dtype=np.int32)
+    for b in range(cfg.b):
+        for h in range(cfg.hq):
+            for i in range(nq):
+                hi = i + 1 if cfg.causal else nk
+                kind = (b * 7 + h * 3 + i) % 5
+                if kind == 0:
+                    row = []
+                elif kind == 1:
+                    row = [int(rng.integers(0, hi))]
+                elif kind == 2:
+                    row = sorted({0, hi - 1, (hi - 1) // 2})
+                elif kind == 3:
+                    row = list(range(hi))
+                else:
+                    row = sorted(rng.choice(hi, size=max(1, hi // 3), replace=False).tolist())
+                lut[b, h, i, :len(row)] = row
+                cnt[b, h, i] = len(row)
+    return lut, cnt
+
+
+def test_c1_oracle_lut(fbm_gpu):
+    lut, cnt = oracle_lut(synth.C1)
+    check(fbm_gpu, synth.C1, lut, cnt)
+
+
+@pytest.mark.parametrize("hk", [4, 2, 1])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_hand_luts_gqa(fbm_gpu, hk, dtype, d):
+    cfg = synth.C1.replace(b=2, hq=4, hk=hk, s=640, d=d, dtype=dtype)
+    lut, cnt = hand_lut(cfg)
+    check(fbm_gpu, cfg, lut, cnt)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_hand_luts_causal_and_ragged(fbm_gpu, causal):
+    cfg = synth.C1.replace(b=1, hq=2, hk=1, s=1000, d=128, dtype="bf16", causal=causal)
+    lut, cnt = hand_lut(cfg, seed=3)
+    check(fbm_gpu, cfg, lut, cnt)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_mode_matches_full_lut(fbm_gpu, causal):
+    cfg = synth.C1.replace(b=1, hq=2, hk=2, s=768, d=128, dtype="f16", causal=causal)
+    nq = cfg.nq
+    lut = np.full((1, 2, nq, nq), -1, dtype=np.int32)
+    cnt = np.zeros((1, 2, nq), dtype=np.int32)
+    for i in range(nq):
+        n = i + 1 if causal else nq
+        lut[:, :, i, :n] = np.arange(n)
+        cnt[:, :, i] = n
+    o_dense, l_dense = check(fbm_gpu, cfg, lut, cnt, dense=True)
+    o_full, l_full = check(fbm_gpu, cfg, lut, cnt)
+    # same kernel, same visit order: bit-identical
+    assert torch.equal(o_dense, o_full) and torch.equal(l_dense, l_full)
+
+
+@pytest.mark.parametrize("S", [2, 3, 5])
+def test_split_kv_partials_and_combine(fbm_gpu, S):
+    cfg = synth.C1.replace(b=1, hq=4, hk=2, s=640, d=128, dtype="bf16")
+    lut, cnt = hand_lut(cfg, seed=S)
+    x, (q, k, v) = prefill_on_gpu(cfg)
+    op, lp = fbm_gpu.sparse_fmha_fwd(q, k, v, torch.from_numpy(lut).cuda(),
+                                     torch.from_numpy(cnt).cuda(), scale=cfg.scale, num_splits=S)
+    op, lp = op.double().cpu().numpy(), lp.double().cpu().numpy()
+    qf, kf, vf = (synth.bits_to_f64(x[t], "bf16") for t in ("q", "k", "v"))
+    for h in range(cfg.hq):
+        for i in range(cfg.nq):
+            row = lut[0, h, i, :cnt[0, h, i]]
+            parts = oracle.split_partials_unit(qf[0, h], kf[0, h // 2], vf[0, h // 2], row, i, S,
+                                               64, 64, cfg.scale, False)
+            for s in range(S):
+                assert_close_o(op[s, 0, h, i * 64:(i + 1) * 64], parts[0][s], f"Opart{s}")
+                assert_close_lse(lp[s, 0, h, i * 64:(i + 1) * 64], parts[1][s], f"LSEpart{s}")
+    check(fbm_gpu, cfg, lut, cnt, num_splits=S)
+
+
+def test_c2_cdf_attention(fbm_gpu):
+    lut, cnt = oracle_lut(synth.C2, "cdf", 0.9)
+    check(fbm_gpu, synth.C2, lut, cnt)
+
+
+@pytest.mark.parametrize("topk", [0.1, 0.4])
+def test_c3_sampled(fbm_gpu, topk):
+    cfg = synth.C3
+    lut, cnt = oracle_lut(cfg, "topk", topk)
+    units = [u for u in synth.sample_qblocks(cfg, 8) if u[1] % 8 == 0]
+    check(fbm_gpu, cfg, lut, cnt, units=units)
+
+
+def test_c4_sampled_with_lse(fbm_gpu):
+    cfg = synth.C4
+    lut, cnt = oracle_lut(cfg)
+    units = [u for u in synth.sample_qblocks(cfg, 6) if u[1] % 5 == 0]
+    check(fbm_gpu, cfg, lut, cnt, units=units)
+
+
+def test_relaunch_is_bitwise_deterministic(fbm_gpu):
+    cfg = synth.C1.replace(b=1, hq=4, hk=2, s=1024, d=128, dtype="bf16")
+    lut, cnt = hand_lut(cfg, seed=9)
+    x, (q, k, v) = prefill_on_gpu(cfg)
+    lut_d, cnt_d = torch.from_numpy(lut).cuda(), torch.from_numpy(cnt).cuda()
+    ref = None
+    for _ in range(50):
+        o, l = fbm_gpu.sparse_fmha_fwd(q, k, v, lut_d, cnt_d, scale=cfg.scale, return_lse=True)
+        if ref is None:
+            ref = (o.clone(), l.clone())
+        assert torch.equal(o, ref[0]) and torch.equal(l, ref[1])
+
+
+def test_out_of_range_entry_is_skipped_and_flagged(fbm_gpu):
+    cfg = synth.C1.replace(b=1, hq=2, hk=2, s=512, d=128, dtype="f16")
+    nq = cfg.nq
+    lut = np.full((1, 2, nq, nq), -1, dtype=np.int32)
+    cnt = np.full((1, 2, nq), 2, dtype=np.int32)
+    lut[..., 0] = 1
+    lut[..., 1] = nq + 5  # out of range: skipped, error bit set
+    x, (q, k, v) = prefill_on_gpu(cfg)
+    out, lse = fbm_gpu.sparse_fmha_fwd(q, k, v, torch.from_numpy(lut).cuda(),
+                                       torch.from_numpy(cnt).cuda(), scale=cfg.scale,
+                                       return_lse=True)
+    assert fbm_gpu.get_error() == fbm_gpu.FBM_DEVERR_LUT_RANGE
+    assert fbm_gpu.get_error() == 0  # read clears
+    good = lut.copy()
+    good[..., 1] = -1
+    res = oracle.sparse_fmha(x["q"], x["k"], x["v"], good, np.ones_like(cnt), cfg.scale, False,
+                             dtype="f16")
+    o_np = out.double().cpu().numpy()
+    for (b, h, i), (o_ref, _) in res.items():
+        assert_close_o(o_np[b, h, i * 64:(i + 1) * 64], o_ref)
