@@ -45,7 +45,7 @@ NCU_TRAFFIC = {}
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--topk", type=float, default=0.4)
@@ -85,7 +85,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except OSError:
@@ -226,7 +226,7 @@ def run_ours(args):
     value = flops * world / (step_ms * 1e-3) / 1e12
 
     # ---- dense reference FMHA and the topk sweep
-    dense_ms = timed(lambda: attn(dense=True), max(2, args.steps // 2), 1)
+    dense_ms = timed(lambda: attn(dense=True), max(2, args.steps // 10), 1)
     sweep = []
     if not args.no_sweep:
         for tk in TOPKS:
@@ -234,7 +234,7 @@ def run_ours(args):
             torch.cuda.synchronize()
             tl = int(cnt.sum().item())
             bm = timed(lambda: block_map(tk), 5, 1)
-            a = timed(lambda: attn(), max(2, args.steps // 2), 1)
+            a = timed(lambda: attn(), max(2, args.steps // 10), 1)
             sweep.append({"topk": tk, "selected_tiles": tl, "block_map_ms": round(bm, 4),
                           "attn_ms": round(a, 4),
                           "eff_tflops_attn": round(tl * FLOP_PER_TILE / (a * 1e-3) / 1e12, 1),
@@ -259,7 +259,7 @@ def run_ours(args):
             fbm.sparse_fmha_fwd(dq, dk, dv_, lut, cnt, scale=cfg.scale, out=out)
             ho.copy_(out, non_blocking=True)
 
-        e2e_ms = timed(e2e_step, max(3, args.steps // 2), 2)
+        e2e_ms = timed(e2e_step, max(3, args.steps // 10), 2)
         h2d = 3 * q.numel() * q.element_size()
         d2h = out.numel() * out.element_size()
         e2e = {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",

@@ -32,12 +32,15 @@ __global__ void __launch_bounds__(256) k_attn_combine(const CombineLaunch L) {
   const float w1 = live ? expf(l1 - m) : 0.f;
   const float wsum = warp_sum(w0 + w1);
   const float inv = live ? 1.0f / wsum : 0.f;
-  for (int c = lane * 4; c < L.dv; c += 128) {
+  // every lane runs the same trip counts: the weight shuffles need the full warp
+  for (int c0 = 0; c0 < L.dv; c0 += 128) {
+    const int c = c0 + lane * 4;
+    const bool act = c < L.dv;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) {
       for (int s = 0; s < L.num_splits; ++s) {
         const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-        if (w == 0.f) continue;  // an empty partial (weight 0) is skipped
+        if (w == 0.f || !act) continue;  // an empty partial (weight 0) is skipped
         const float4 x = __ldg(reinterpret_cast<const float4 *>(
             L.o_part + ((int64_t)s * L.rows + row) * L.dv + c));
         acc.x = fmaf(w, x.x, acc.x);
@@ -46,6 +49,7 @@ __global__ void __launch_bounds__(256) k_attn_combine(const CombineLaunch L) {
         acc.w = fmaf(w, x.w, acc.w);
       }
     }
+    if (!act) continue;
     acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
     if constexpr (OUT == 2) {
       *reinterpret_cast<float4 *>(static_cast<float *>(L.out) + row * L.dv + c) = acc;

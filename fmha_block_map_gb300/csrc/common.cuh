@@ -27,6 +27,7 @@ struct F16 {
     return *reinterpret_cast<uint32_t *>(&h);
   }
   static FBM_DEVICE T from_f(float a) { return __float2half_rn(a); }
+  static FBM_DEVICE uint16_t bits(float a) { return __half_as_ushort(__float2half_rn(a)); }
   static constexpr bool kIsBf16 = false;
 };
 struct BF16 {
@@ -41,6 +42,7 @@ struct BF16 {
     return *reinterpret_cast<uint32_t *>(&h);
   }
   static FBM_DEVICE T from_f(float a) { return __float2bfloat16_rn(a); }
+  static FBM_DEVICE uint16_t bits(float a) { return __bfloat16_as_ushort(__float2bfloat16_rn(a)); }
   static constexpr bool kIsBf16 = true;
 };
 

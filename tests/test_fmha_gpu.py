@@ -187,3 +187,12 @@ def test_out_of_range_entry_is_skipped_and_flagged(fbm_gpu):
     o_np = out.double().cpu().numpy()
     for (b, h, i), (o_ref, _) in res.items():
         assert_close_o(o_np[b, h, i * 64:(i + 1) * 64], o_ref)
+
+
+def test_d128_runs_on_the_tcgen05_kernel(fbm_gpu):
+    """The hot shape must not fall back to the mma.sync kernel."""
+    for dt in (torch.float16, torch.bfloat16):
+        assert fbm_gpu.fmha_kernel_kind(dt, 128, 128, 1, 16384, 16384) == 1
+        assert fbm_gpu.fmha_kernel_kind(dt, 128, 128, 1, 1000, 1000) == 1
+    assert fbm_gpu.fmha_kernel_kind(torch.float16, 64, 64, 1, 512, 512) == 2
+    assert fbm_gpu.fmha_kernel_kind(torch.float16, 128, 128, 4, 512, 512) == 2
