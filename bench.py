@@ -51,6 +51,7 @@ def parse():
     p.add_argument("--topk", type=float, default=0.4)
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     return p.parse_args()
 
 
@@ -304,7 +305,7 @@ def run_ours(args):
         "clocks": clocks,
         "gpu_launches": 3 * args.steps,
     }
-    if rank == 0 and os.environ.get("FBM_BENCH_NO_CPU") != "1":
+    if rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(cfg, x, args.topk)
     if world > 1:
         import torch.distributed as dist
