@@ -18,10 +18,11 @@
 // exceeds it by more than 2^8), so the cross-lane column maximum is needed only
 // on those rare pairs.
 //
-// Roles (one persistent CTA per SM, 6 warps):
+// Roles (one persistent CTA per SM, 10 warps):
 //   warp 0    TMA producer: Q (double buffer), K and V pairs (2-slot rings)
 //   warp 1    TMEM owner and single-thread MMA issuer
-//   warps 2-5 softmax + epilogue (TMEM lane quadrants 2, 3, 0, 1)
+//   warps 2-5 softmax + epilogue of queries 0-31, warps 6-9 of queries 32-63
+//             (each group covers TMEM lane quadrants 2, 3, 0, 1: all 128 keys)
 // Pipeline per q block, pairs p = 0..: S(0); then S(p+1) before PV(p), so the
 // softmax of pair p+1 overlaps the PV MMA of pair p.  Every wait is bounded:
 // on expiry the kernel raises FBM_DEVERR_TIMEOUT, every role leaves its loop,
@@ -55,11 +56,12 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + 2 * kQBytes;
 constexpr int OFF_V = OFF_K + 2 * kPairBytes;
 constexpr int OFF_P = OFF_V + 2 * kPairBytes;
-constexpr int OFF_RED = OFF_P + 2 * kPBytes;      // float [4][64]
-constexpr int OFF_ALPHA = OFF_RED + 4 * 64 * 4;   // float [64]
-constexpr int OFF_INVL = OFF_ALPHA + 64 * 4;      // float [64]
-constexpr int OFF_M = OFF_INVL + 64 * 4;          // float [64]
-constexpr int OFF_BAR = OFF_M + 64 * 4;
+constexpr int OFF_STAGE = OFF_P + 2 * kPBytes;   // 16 KB: output staging [64 q][128 d]
+constexpr int OFF_RED = OFF_STAGE + kQBytes;      // float [2 groups][4][32]
+constexpr int OFF_ALPHA = OFF_RED + 2 * 4 * 32 * 4;  // float [2][32]
+constexpr int OFF_INVL = OFF_ALPHA + 2 * 32 * 4;  // float [2][32]
+constexpr int OFF_M = OFF_INVL + 2 * 32 * 4;      // float [2][32]
+constexpr int OFF_BAR = OFF_M + 2 * 32 * 4;
 enum {
   B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_SE = 14,
   B_PF = 16, B_PV = 18, B_OF = 20, B_DRAIN = 21, NBAR = 22
@@ -69,8 +71,9 @@ constexpr int SMEM_BYTES = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
 constexpr uint32_t kTmemCols = 256;                // S0 @0, S1 @64, O @128
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
-constexpr int kSoftmaxThreads = 128;
-constexpr int kBarSoftmax = 1;                     // named barrier id of warps 2-5
+constexpr int kGroupThreads = 128;                 // one softmax warpgroup
+constexpr int kSoftmaxThreads = 2 * kGroupThreads; // two groups: queries 0-31 and 32-63
+constexpr int kThreads = 64 + kSoftmaxThreads;     // + producer warp + MMA warp
 
 struct TcParams {
   CUtensorMap tq, tk, tv;
@@ -107,7 +110,7 @@ FBM_DEVICE Unit unit_of(const TcParams &P, int u) {
 FBM_DEVICE int entry_of(const Unit &U, int t) { return U.row ? __ldg(U.row + t) : t; }
 
 template <bool kBf16>
-__global__ void __launch_bounds__(192, 1) k_fmha_tc(const __grid_constant__ TcParams P) {
+__global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__ TcParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(192, 1) k_fmha_tc(const __grid_constant__ TcPa
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
       if (k == B_SE || k == B_SE + 1 || k == B_PF || k == B_PF + 1 || k == B_OF)
-        cnt = kSoftmaxThreads;
+        cnt = kSoftmaxThreads;  // both query groups arrive
       mbar_init(bar(k), cnt);
     }
     misc[1] = 0;
@@ -263,140 +266,136 @@ __global__ void __launch_bounds__(192, 1) k_fmha_tc(const __grid_constant__ TcPa
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    const int wg = (warp - 2) >> 2;          // query group: columns 32*wg .. 32*wg+31
+    const int cb = wg * 32;
     const int qd = warp & 3;
     const int key = qd * 32 + lane;          // TMEM lane: key of the pair (S^T) / d (O^T)
-    const int t128 = threadIdx.x - 64;       // 0..127
+    const int tg = (threadIdx.x - 64) & 127; // 0..127 within the group
+    const int barid = 1 + wg;                // named barrier of this group
     const uint32_t tl = tbase + ((uint32_t)(qd * 32) << 16);
-    float *red = reinterpret_cast<float *>(smem + OFF_RED);
-    float *alpha_s = reinterpret_cast<float *>(smem + OFF_ALPHA);
-    float *invl_s = reinterpret_cast<float *>(smem + OFF_INVL);
-    float *m_s = reinterpret_cast<float *>(smem + OFF_M);
+    float *red = reinterpret_cast<float *>(smem + OFF_RED) + wg * 128;   // [4][32]
+    float *alpha_s = reinterpret_cast<float *>(smem + OFF_ALPHA) + wg * 32;
+    float *invl_s = reinterpret_cast<float *>(smem + OFF_INVL) + wg * 32;
+    float *m_s = reinterpret_cast<float *>(smem + OFF_M) + wg * 32;
     using E = typename std::conditional<kBf16, BF16, F16>::type;
-    // Every softmax thread runs the same loop trip counts and named barriers
-    // whatever happens: a failed (timed-out) wait only clears `ok`, and later
-    // waits return at once, so no thread is left behind at a named barrier.
-    int pc = 0, uc = 0;
+    // Every softmax thread of a group runs the same loop trip counts and named
+    // barriers whatever happens: a failed (timed-out) wait only clears `ok`,
+    // and later waits return at once, so no thread is left behind at a barrier.
+    int pc = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
       const Unit U = unit_of(P, u);
       const int q0 = U.i * 64;
       const int rows = min(64, P.s_q - q0);
-      uint16_t *orow = static_cast<uint16_t *>(P.out) + ((size_t)U.bh_q * P.s_q + q0) * kD;
-      float *lrow = P.lse ? P.lse + (size_t)U.bh_q * P.s_q + q0 : nullptr;
+      const int my_rows = max(0, min(32, rows - cb));  // this group's valid query rows
+      uint16_t *orow = static_cast<uint16_t *>(P.out) + ((size_t)U.bh_q * P.s_q + q0 + cb) * kD;
+      float *lrow = P.lse ? P.lse + (size_t)U.bh_q * P.s_q + q0 + cb : nullptr;
       if (U.n == 0) {
-        for (int e = t128 * 8; e < rows * kD; e += kSoftmaxThreads * 8)
+        for (int e = tg * 8; e < my_rows * kD; e += kGroupThreads * 8)
           *reinterpret_cast<uint4 *>(orow + e) = make_uint4(0, 0, 0, 0);
-        if (lrow && t128 < rows) lrow[t128] = -INFINITY;
+        if (lrow && tg < my_rows) lrow[tg] = -INFINITY;
         continue;
       }
       const int npairs = (U.n + 1) >> 1;
       // running max per query (log2 domain) lives in m_s; l is this key's share
-      float l[64];
+      float l[32];
 #pragma unroll
-      for (int q = 0; q < 64; ++q) l[q] = 0.f;
-      if (t128 < 64) m_s[t128] = -INFINITY;
-      named_sync(kBarSoftmax, kSoftmaxThreads);
+      for (int q = 0; q < 32; ++q) l[q] = 0.f;
+      if (tg < 32) m_s[tg] = -INFINITY;
+      named_sync(barid, kGroupThreads);
       for (int p = 0; p < npairs; ++p) {
         const int g = pc + p, slot = g & 1;
         // this thread's key: block t of the row, offset key & 63
         const int t = 2 * p + (key >> 6);
-        int j = t < U.n ? entry_of(U, t) : -1;
+        const int j = t < U.n ? entry_of(U, t) : -1;
         const bool jvalid = j >= 0 && j < P.nk;
         const int kpos = (jvalid ? j : 0) * 64 + (key & 63);
         const bool kvalid = jvalid && kpos < P.s_k;
-        const int qmin = P.causal ? kpos - q0 : -1;  // queries q < qmin cannot see this key
+        // queries cb + q with q < qmin cannot see this key (causal)
+        const int qmin = P.causal ? kpos - q0 - cb : -1;
+        const bool plain = kvalid && qmin <= 0;  // the whole column range is visible
         ok = ok && mbar_wait(bar(B_SF + slot), (g >> 1) & 1, abort_flag, kWaitNs);
         tc_fence_after();
-        float s[64];
+        float s[32];
         {
           uint32_t r[32];
-          tmem_ld32(tl + slot * 64, r);
+          tmem_ld32(tl + slot * 64 + cb, r);
           tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < 32; ++q) s[q] = __uint_as_float(r[q]);
-          tmem_ld32(tl + slot * 64 + 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 32; ++q) s[32 + q] = __uint_as_float(r[q]);
         }
         float mx = -INFINITY;
+        if (plain) {
 #pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4) {
-          const float4 mv = reinterpret_cast<const float4 *>(m_s)[q4];
-          const float mq[4] = {mv.x, mv.y, mv.z, mv.w};
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 mv = reinterpret_cast<const float4 *>(m_s)[q4];
+            const float mq[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
-          for (int z = 0; z < 4; ++z) {
-            const int q = 4 * q4 + z;
-            const bool vis = kvalid && q >= qmin;
-            const float x = vis ? fmaf(s[q], P.sl2, -mq[z]) : -INFINITY;
+            for (int z = 0; z < 4; ++z) {
+              const float x = fmaf(s[4 * q4 + z], P.sl2, -mq[z]);
+              mx = fmaxf(mx, x);
+              s[4 * q4 + z] = x;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const float x = (kvalid && q >= qmin) ? fmaf(s[q], P.sl2, -m_s[q]) : -INFINITY;
             mx = fmaxf(mx, x);
             s[q] = x;
           }
         }
-        if (named_or(kBarSoftmax, kSoftmaxThreads, mx > 8.0f)) {
+        if (named_or(barid, kGroupThreads, mx > 8.0f)) {
           // rare: some score exceeds the running max by > 2^8 (always on the
           // first pair): exact column max over the 128 keys, then rescale
           uint32_t r[32];
-          tmem_ld32(tl + slot * 64, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 32; ++q) s[q] = (kvalid && q >= qmin) ? __uint_as_float(r[q]) * P.sl2 : -INFINITY;
-          tmem_ld32(tl + slot * 64 + 32, r);
+          tmem_ld32(tl + slot * 64 + cb, r);
           tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            s[32 + q] = (kvalid && 32 + q >= qmin) ? __uint_as_float(r[q]) * P.sl2 : -INFINITY;
-          // transpose-reduce within the warp: lane ends with columns 2*lane, 2*lane+1
+            s[q] = (kvalid && q >= qmin) ? __uint_as_float(r[q]) * P.sl2 : -INFINITY;
+          // transpose-reduce within the warp: lane ends with column `lane`
 #pragma unroll
-          for (int o = 16, w = 32; o >= 1; o >>= 1, w >>= 1) {
+          for (int o = 16; o >= 1; o >>= 1) {
             const bool hi = (lane & o) != 0;
 #pragma unroll
-            for (int x = 0; x < w; ++x) {
-              const float send = hi ? s[x] : s[x + w];
-              const float keep = hi ? s[x + w] : s[x];
+            for (int x = 0; x < o; ++x) {
+              const float send = hi ? s[x] : s[x + o];
+              const float keep = hi ? s[x + o] : s[x];
               s[x] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
             }
           }
-          red[qd * 64 + 2 * lane] = s[0];
-          red[qd * 64 + 2 * lane + 1] = s[1];
-          named_sync(kBarSoftmax, kSoftmaxThreads);
-          if (t128 < 64) {
-            const int q = t128;
-            const float cm = fmaxf(fmaxf(red[q], red[64 + q]), fmaxf(red[128 + q], red[192 + q]));
+          red[qd * 32 + lane] = s[0];
+          named_sync(barid, kGroupThreads);
+          if (tg < 32) {
+            const int q = tg;
+            const float cm = fmaxf(fmaxf(red[q], red[32 + q]), fmaxf(red[64 + q], red[96 + q]));
             const float mo = m_s[q];
             const float mn = fmaxf(mo, cm);
-            alpha_s[q] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+            alpha_s[q] = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
             m_s[q] = mn;
           }
-          named_sync(kBarSoftmax, kSoftmaxThreads);
+          named_sync(barid, kGroupThreads);
 #pragma unroll
-          for (int q = 0; q < 64; ++q) l[q] *= alpha_s[q];
+          for (int q = 0; q < 32; ++q) l[q] *= alpha_s[q];
           if (p > 0) {
             // O^T holds PV(0 .. p-1): wait for the last of them, then scale
             const int gp = g - 1;
             ok = ok && mbar_wait(bar(B_PV + (gp & 1)), (gp >> 1) & 1, abort_flag, kWaitNs);
             tc_fence_after();
-            for (int half = 0; half < 2; ++half) {
-              tmem_ld32(tl + 128 + half * 32, r);
-              tmem_wait_ld();
+            tmem_ld32(tl + 128 + cb, r);
+            tmem_wait_ld();
 #pragma unroll
-              for (int q = 0; q < 32; ++q)
-                r[q] = __float_as_uint(__uint_as_float(r[q]) * alpha_s[half * 32 + q]);
-              tmem_st32(tl + 128 + half * 32, r);
-            }
+            for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * alpha_s[q]);
+            tmem_st32(tl + 128 + cb, r);
             tmem_wait_st();
             tc_fence_before();
           }
-          tmem_ld32(tl + slot * 64, r);
+          tmem_ld32(tl + slot * 64 + cb, r);
           tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < 32; ++q)
             s[q] = (kvalid && q >= qmin) ? fmaf(__uint_as_float(r[q]), P.sl2, -m_s[q]) : -INFINITY;
-          tmem_ld32(tl + slot * 64 + 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            s[32 + q] = (kvalid && 32 + q >= qmin) ? fmaf(__uint_as_float(r[q]), P.sl2, -m_s[32 + q]) : -INFINITY;
         }
         // P(p) goes to buffer `slot`, last read by PV(g - 2)
         if (p >= 2) {
@@ -405,77 +404,74 @@ __global__ void __launch_bounds__(192, 1) k_fmha_tc(const __grid_constant__ TcPa
         }
         uint8_t *prow = smem + OFF_P + slot * kPBytes + key * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
           float e[8];
 #pragma unroll
           for (int z = 0; z < 8; ++z) {
-            e[z] = exp2f(s[8 * c + z]);
+            e[z] = fast_exp2(s[8 * c + z]);
             l[8 * c + z] += e[z];
           }
           uint4 pk = make_uint4(E::from_f2(e[0], e[1]), E::from_f2(e[2], e[3]),
                                 E::from_f2(e[4], e[5]), E::from_f2(e[6], e[7]));
-          *reinterpret_cast<uint4 *>(prow + ((c ^ (key & 7)) << 4)) = pk;
+          const int chunk = wg * 4 + c;
+          *reinterpret_cast<uint4 *>(prow + ((chunk ^ (key & 7)) << 4)) = pk;
         }
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(bar(B_PF + slot));
         mbar_arrive(bar(B_SE + slot));
       }
-      // ---- epilogue: O = O^T / l, LSE = m ln2 + ln l
+      // ---- epilogue: O = O^T / l, LSE = m ln2 + ln l (this group's 32 queries)
       {
         const int gl = pc + npairs - 1;
         ok = ok && mbar_wait(bar(B_PV + (gl & 1)), (gl >> 1) & 1, abort_flag, kWaitNs);
         tc_fence_after();
         // sum l over the 128 keys
 #pragma unroll
-        for (int o = 16, w = 32; o >= 1; o >>= 1, w >>= 1) {
+        for (int o = 16; o >= 1; o >>= 1) {
           const bool hi = (lane & o) != 0;
 #pragma unroll
-          for (int x = 0; x < w; ++x) {
-            const float send = hi ? l[x] : l[x + w];
-            const float keep = hi ? l[x + w] : l[x];
+          for (int x = 0; x < o; ++x) {
+            const float send = hi ? l[x] : l[x + o];
+            const float keep = hi ? l[x + o] : l[x];
             l[x] = keep + __shfl_xor_sync(0xffffffffu, send, o);
           }
         }
-        red[qd * 64 + 2 * lane] = l[0];
-        red[qd * 64 + 2 * lane + 1] = l[1];
-        named_sync(kBarSoftmax, kSoftmaxThreads);
-        if (t128 < 64) {
-          const int q = t128;
-          const float lt = (red[q] + red[64 + q]) + (red[128 + q] + red[192 + q]);
+        red[qd * 32 + lane] = l[0];
+        named_sync(barid, kGroupThreads);
+        if (tg < 32) {
+          const int q = tg;
+          const float lt = (red[q] + red[32 + q]) + (red[64 + q] + red[96 + q]);
           invl_s[q] = lt > 0.f ? 1.0f / lt : 0.f;
-          if (lrow && q < rows)
+          if (lrow && q < my_rows)
             lrow[q] = lt > 0.f ? m_s[q] * 0.6931471805599453f + logf(lt) : -INFINITY;
         }
-        named_sync(kBarSoftmax, kSoftmaxThreads);
-        // O^T row `key` (= d) -> staging tile [64 q][128 d] in P buffer 0
-        uint16_t *stage = reinterpret_cast<uint16_t *>(smem + OFF_P);
-        for (int half = 0; half < 2; ++half) {
+        named_sync(barid, kGroupThreads);
+        // O^T row `key` (= d), columns cb.. -> staging rows cb.. of [64 q][128 d]
+        uint16_t *stage = reinterpret_cast<uint16_t *>(smem + OFF_STAGE);
+        {
           uint32_t r[32];
-          tmem_ld32(tl + 128 + half * 32, r);
+          tmem_ld32(tl + 128 + cb, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int qq = half * 32 + q;
-            stage[qq * kD + key] = E::bits(__uint_as_float(r[q]) * invl_s[qq]);
-          }
+          for (int q = 0; q < 32; ++q)
+            stage[(cb + q) * kD + key] = E::bits(__uint_as_float(r[q]) * invl_s[q]);
         }
         tc_fence_before();
         mbar_arrive(bar(B_OF));
         fence_proxy_async();
-        named_sync(kBarSoftmax, kSoftmaxThreads);
-        if (t128 == 0) {
-          bulk_store(orow, sbase + OFF_P, (uint32_t)(rows * kD * 2));
+        named_sync(barid, kGroupThreads);
+        if (tg == 0 && my_rows > 0) {
+          bulk_store(orow, sbase + OFF_STAGE + cb * kD * 2, (uint32_t)(my_rows * kD * 2));
           bulk_commit();
           bulk_wait_read0();
         }
-        named_sync(kBarSoftmax, kSoftmaxThreads);
+        named_sync(barid, kGroupThreads);
       }
       pc += npairs;
-      uc += 1;
     }
     if (!ok) fail(FBM_DEVERR_TIMEOUT);
-    if (t128 == 0) bulk_wait0();
+    if (tg == 0) bulk_wait0();
   }
 
   tc_fence_before();
@@ -553,7 +549,7 @@ cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   P.units = L.b * L.hq * L.nq;
   P.sl2 = L.scale * 1.4426950408889634f;
   const int grid = std::min(P.units, sm_count());
-  k_fmha_tc<BF16><<<grid, 192, SMEM_ALLOC, st>>>(P);
+  k_fmha_tc<BF16><<<grid, kThreads, SMEM_ALLOC, st>>>(P);
   return cudaGetLastError();
 }
 

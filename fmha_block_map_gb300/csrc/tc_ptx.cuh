@@ -175,6 +175,13 @@ FBM_DEVICE void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
 FBM_DEVICE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 FBM_DEVICE void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
+// 2^x by the MUFU ex2 instruction (approximate, subnormal results flushed to 0)
+FBM_DEVICE float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // UMMA shared-memory descriptor, 128-byte swizzle, 1024-byte aligned atoms.
 //   bits [0,14) start >> 4, [16,30) LBO >> 4, [32,46) SBO >> 4,
 //   [46,48) = 1 (descriptor version), [61,64) layout (2 = 128B swizzle)
