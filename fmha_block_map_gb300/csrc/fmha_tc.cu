@@ -297,17 +297,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         continue;
       }
       const int npairs = (U.n + 1) >> 1;
-      // running max per query (log2 domain) lives in m_s; l is this key's share
-      float l[32];
+      // running max per query (log2 domain) lives in m_s; l holds this key's
+      // share of the row sums, as packed fp32 pairs (queries 2i, 2i+1)
+      uint64_t l2[16];
 #pragma unroll
-      for (int q = 0; q < 32; ++q) l[q] = 0.f;
+      for (int i = 0; i < 16; ++i) l2[i] = 0ull;
       if (tg < 32) m_s[tg] = -INFINITY;
       named_sync(barid, kGroupThreads);
+      const uint64_t sl2x2 = f2_pack(P.sl2, P.sl2);
+      int j_next = (key >> 6) < U.n ? entry_of(U, key >> 6) : -1;
       for (int p = 0; p < npairs; ++p) {
         const int g = pc + p, slot = g & 1;
         // this thread's key: block t of the row, offset key & 63
-        const int t = 2 * p + (key >> 6);
-        const int j = t < U.n ? entry_of(U, t) : -1;
+        const int j = j_next;
+        {
+          const int tn = 2 * (p + 1) + (key >> 6);
+          j_next = (p + 1 < npairs && tn < U.n) ? entry_of(U, tn) : -1;
+        }
         const bool jvalid = j >= 0 && j < P.nk;
         const int kpos = (jvalid ? j : 0) * 64 + (key & 63);
         const bool kvalid = jvalid && kpos < P.s_k;
@@ -316,56 +322,57 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         const bool plain = kvalid && qmin <= 0;  // the whole column range is visible
         ok = ok && mbar_wait(bar(B_SF + slot), (g >> 1) & 1, abort_flag, kWaitNs);
         tc_fence_after();
-        float s[32];
-        {
-          uint32_t r[32];
-          tmem_ld32(tl + slot * 64 + cb, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 32; ++q) s[q] = __uint_as_float(r[q]);
-        }
-        float mx = -INFINITY;
+        uint32_t r[32];
+        tmem_ld32(tl + slot * 64 + cb, r);
+        tmem_wait_ld();
+        uint64_t x2[16];
+        float mx;
         if (plain) {
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 mv = reinterpret_cast<const float4 *>(m_s)[q4];
-            const float mq[4] = {mv.x, mv.y, mv.z, mv.w};
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-              const float x = fmaf(s[4 * q4 + z], P.sl2, -mq[z]);
-              mx = fmaxf(mx, x);
-              s[4 * q4 + z] = x;
-            }
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 mv = reinterpret_cast<const float4 *>(m_s)[i4];
+            x2[2 * i4] = f2_fma(f2_pack(__uint_as_float(r[4 * i4]), __uint_as_float(r[4 * i4 + 1])),
+                                sl2x2, f2_pack(-mv.x, -mv.y));
+            x2[2 * i4 + 1] = f2_fma(f2_pack(__uint_as_float(r[4 * i4 + 2]), __uint_as_float(r[4 * i4 + 3])),
+                                    sl2x2, f2_pack(-mv.z, -mv.w));
           }
         } else {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const float x = (kvalid && q >= qmin) ? fmaf(s[q], P.sl2, -m_s[q]) : -INFINITY;
-            mx = fmaxf(mx, x);
-            s[q] = x;
+          for (int i = 0; i < 16; ++i) {
+            const int q = 2 * i;
+            const float a = (kvalid && q >= qmin) ? fmaf(__uint_as_float(r[q]), P.sl2, -m_s[q]) : -INFINITY;
+            const float b = (kvalid && q + 1 >= qmin) ? fmaf(__uint_as_float(r[q + 1]), P.sl2, -m_s[q + 1]) : -INFINITY;
+            x2[i] = f2_pack(a, b);
           }
+        }
+        {
+          float t[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float2 a = f2_unpack(x2[2 * i]), b = f2_unpack(x2[2 * i + 1]);
+            t[i] = fmax3(a.x, a.y, fmaxf(b.x, b.y));
+          }
+          mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
         }
         if (named_or(barid, kGroupThreads, mx > 8.0f)) {
           // rare: some score exceeds the running max by > 2^8 (always on the
           // first pair): exact column max over the 128 keys, then rescale
-          uint32_t r[32];
-          tmem_ld32(tl + slot * 64 + cb, r);
-          tmem_wait_ld();
+          float v[32];
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            s[q] = (kvalid && q >= qmin) ? __uint_as_float(r[q]) * P.sl2 : -INFINITY;
+            v[q] = (kvalid && q >= qmin) ? __uint_as_float(r[q]) * P.sl2 : -INFINITY;
           // transpose-reduce within the warp: lane ends with column `lane`
 #pragma unroll
           for (int o = 16; o >= 1; o >>= 1) {
             const bool hi = (lane & o) != 0;
 #pragma unroll
             for (int x = 0; x < o; ++x) {
-              const float send = hi ? s[x] : s[x + o];
-              const float keep = hi ? s[x + o] : s[x];
-              s[x] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+              const float send = hi ? v[x] : v[x + o];
+              const float keep = hi ? v[x + o] : v[x];
+              v[x] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
             }
           }
-          red[qd * 32 + lane] = s[0];
+          red[qd * 32 + lane] = v[0];
           named_sync(barid, kGroupThreads);
           if (tg < 32) {
             const int q = tg;
@@ -377,25 +384,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           }
           named_sync(barid, kGroupThreads);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) l[q] *= alpha_s[q];
+          for (int i = 0; i < 16; ++i)
+            l2[i] = f2_mul(l2[i], f2_pack(alpha_s[2 * i], alpha_s[2 * i + 1]));
           if (p > 0) {
             // O^T holds PV(0 .. p-1): wait for the last of them, then scale
             const int gp = g - 1;
             ok = ok && mbar_wait(bar(B_PV + (gp & 1)), (gp >> 1) & 1, abort_flag, kWaitNs);
             tc_fence_after();
-            tmem_ld32(tl + 128 + cb, r);
+            uint32_t o[32];
+            tmem_ld32(tl + 128 + cb, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * alpha_s[q]);
-            tmem_st32(tl + 128 + cb, r);
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha_s[q]);
+            tmem_st32(tl + 128 + cb, o);
             tmem_wait_st();
             tc_fence_before();
           }
-          tmem_ld32(tl + slot * 64 + cb, r);
-          tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            s[q] = (kvalid && q >= qmin) ? fmaf(__uint_as_float(r[q]), P.sl2, -m_s[q]) : -INFINITY;
+          for (int i = 0; i < 16; ++i) {
+            const int q = 2 * i;
+            const float a = (kvalid && q >= qmin) ? fmaf(__uint_as_float(r[q]), P.sl2, -m_s[q]) : -INFINITY;
+            const float b = (kvalid && q + 1 >= qmin) ? fmaf(__uint_as_float(r[q + 1]), P.sl2, -m_s[q + 1]) : -INFINITY;
+            x2[i] = f2_pack(a, b);
+          }
         }
         // P(p) goes to buffer `slot`, last read by PV(g - 2)
         if (p >= 2) {
@@ -405,16 +416,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         uint8_t *prow = smem + OFF_P + slot * kPBytes + key * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          float e[8];
+          uint32_t pk[4];
 #pragma unroll
-          for (int z = 0; z < 8; ++z) {
-            e[z] = fast_exp2(s[8 * c + z]);
-            l[8 * c + z] += e[z];
+          for (int z = 0; z < 4; ++z) {
+            const float2 xv = f2_unpack(x2[4 * c + z]);
+            const float e0 = fast_exp2(xv.x), e1 = fast_exp2(xv.y);
+            l2[4 * c + z] = f2_add(l2[4 * c + z], f2_pack(e0, e1));
+            pk[z] = E::from_f2(e0, e1);
           }
-          uint4 pk = make_uint4(E::from_f2(e[0], e[1]), E::from_f2(e[2], e[3]),
-                                E::from_f2(e[4], e[5]), E::from_f2(e[6], e[7]));
           const int chunk = wg * 4 + c;
-          *reinterpret_cast<uint4 *>(prow + ((chunk ^ (key & 7)) << 4)) = pk;
+          *reinterpret_cast<uint4 *>(prow + ((chunk ^ (key & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
         fence_proxy_async();
         tc_fence_before();
@@ -427,6 +439,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         ok = ok && mbar_wait(bar(B_PV + (gl & 1)), (gl >> 1) & 1, abort_flag, kWaitNs);
         tc_fence_after();
         // sum l over the 128 keys
+        float l[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 v = f2_unpack(l2[i]);
+          l[2 * i] = v.x;
+          l[2 * i + 1] = v.y;
+        }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
           const bool hi = (lane & o) != 0;
