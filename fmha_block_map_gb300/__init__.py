@@ -23,6 +23,7 @@ FBM_OK, FBM_ERR_INVALID_ARG, FBM_ERR_UNSUPPORTED, FBM_ERR_CUDA, FBM_ERR_DEVICE =
 FBM_F16, FBM_BF16, FBM_F32 = 0, 1, 2
 FBM_DEVERR_LUT_RANGE, FBM_DEVERR_TIMEOUT = 0x1, 0x2
 FBM_MAX_HEADS = 256
+FBM_STATIC_SCRATCH_BYTES = 24 << 20
 
 _lib = None
 
@@ -49,6 +50,8 @@ def lib() -> ctypes.CDLL:
         L.fbm_block_map_workspace_bytes.restype = sz
         L.sparge_block_map.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
                                         f32, i32, i32, vp, vp, vp, vp, sz, vp])
+        L.sparge_block_map_static.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp,
+                                               vp, f32, i32, i32, vp, vp, vp, vp])
         L.sparse_fmha_fwd.argtypes = ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                        vp, vp, i32, i32, f32, i32, vp, vp, vp, vp, vp])
         L.attn_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
@@ -56,8 +59,8 @@ def lib() -> ctypes.CDLL:
                                          i32, i32, f32, vp, vp, vp])
         L.fbm_fmha_kernel_kind.argtypes = [i32] * 6
         L.fbm_fmha_kernel_kind.restype = i32
-        for name in ("fbm_get_error", "sparge_block_map", "sparse_fmha_fwd", "attn_combine",
-                     "sparse_decode_fwd"):
+        for name in ("fbm_get_error", "sparge_block_map", "sparge_block_map_static",
+                     "sparse_fmha_fwd", "attn_combine", "sparse_decode_fwd"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -153,6 +156,35 @@ def sparge_block_map(q: torch.Tensor, k: torch.Tensor, *, topk=None, cdfthreshd=
         _per_head(simthreshd1, hq, "simthreshd1"), float(scale), int(causal),
         int(attention_sink), _ptr(lut), _ptr(lut_count), _ptr(bmap), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return lut, lut_count, bmap
+
+
+def sparge_block_map_static(q: torch.Tensor, k: torch.Tensor, *, topk=None, cdfthreshd=None,
+                            simthreshd1: Union[float, Sequence[float]] = 0.001,
+                            scale: Optional[float] = None, causal: bool = False,
+                            attention_sink: bool = False, return_block_map: bool = False,
+                            lut: Optional[torch.Tensor] = None,
+                            lut_count: Optional[torch.Tensor] = None, stream=None):
+    """sparge_block_map with the library's static scratch array instead of a
+    workspace, for callers that cannot allocate device scratch (the outputs
+    are still the caller's: pass lut / lut_count to allocate nothing here)."""
+    _cuda(q, "q"), _cuda(k, "k")
+    b, hq, s, d = q.shape
+    hk = k.shape[1]
+    nq = (s + 63) // 64
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = q.device
+    if lut is None:
+        lut = torch.empty((b, hq, nq, nq), dtype=torch.int32, device=dev)
+    if lut_count is None:
+        lut_count = torch.empty((b, hq, nq), dtype=torch.int32, device=dev)
+    bmap = torch.empty((b, hq, nq, nq), dtype=torch.uint8, device=dev) if return_block_map else None
+    _check(lib().sparge_block_map_static(
+        _ptr(q), _ptr(k), _dt(q), b, hq, hk, s, d, 64, 64,
+        _per_head(topk, hq, "topk"), _per_head(cdfthreshd, hq, "cdfthreshd"),
+        _per_head(simthreshd1, hq, "simthreshd1"), float(scale), int(causal),
+        int(attention_sink), _ptr(lut), _ptr(lut_count), _ptr(bmap), _stream(stream)))
     return lut, lut_count, bmap
 
 

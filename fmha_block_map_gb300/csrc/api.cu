@@ -73,6 +73,15 @@ WsLayout ws_layout(int b, int hq, int hk, int s, int d) {
 
 }  // namespace
 
+namespace fbm {
+// Records the calling thread's failure message (for entry points defined in
+// other files of the library).
+fbm_status set_message(fbm_status st, const char *msg) {
+  snprintf(g_msg, sizeof(g_msg), "%s", msg);
+  return st;
+}
+}  // namespace fbm
+
 extern "C" {
 
 int fbm_version(void) { return 100; }

@@ -121,6 +121,31 @@ fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int 
                             void *stream);
 
 /*
+ * sparge_block_map_static - sparge_block_map for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that cannot give the library a workspace, such as a runtime that plans
+ * every device buffer before it starts and passes each operation only its
+ * inputs and outputs, or a hot path that must never call cudaMalloc (which
+ * can synchronise the device and take unbounded time).
+ *
+ * Same arguments, results and checks as sparge_block_map, without workspace
+ * and workspace_bytes: the scratch lives in a static device array of
+ * FBM_STATIC_SCRATCH_BYTES that every GPU loading the library holds until the
+ * process exits.  A shape whose scratch (fbm_block_map_workspace_bytes) is
+ * larger returns FBM_ERR_UNSUPPORTED and launches nothing.  The first call on
+ * a device looks the array's address up (make it before any stream capture).
+ * All calls share the array, so calls that overlap on the GPU race; nothing
+ * in it needs to start at zero.  The library allocates nothing.
+ */
+#define FBM_STATIC_SCRATCH_BYTES (24u << 20)
+fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int b, int hq, int hk,
+                                   int s, int d, int blkq, int blkk, const float *topk,
+                                   const float *cdfthreshd, const float *simthreshd1, float scale,
+                                   int causal, int attention_sink, int32_t *lut,
+                                   int32_t *lut_count, uint8_t *block_map, void *stream);
+
+/*
  * sparse_fmha_fwd - flash attention over the LUT-selected K/V tiles
  * ("Sparge Attention (Composable Kernel)" README: the sparse FMHA stage;
  * updating_log Stage 3 for the per-row-block loop over a block list).

@@ -133,3 +133,14 @@ def test_kernel_kind_is_host_only(L):
     assert L.fbm_fmha_kernel_kind(0, 96, 96, 1, 128, 128) == 0
     assert L.fbm_fmha_kernel_kind(1, 64, 64, 2, 128, 128) == 2
     assert L.fbm_fmha_kernel_kind(1, 128, 128, 1, 16384, 16384) in (1, 2)
+
+
+def test_static_block_map_rejects_oversized_shapes_on_the_host(L):
+    # b2 hq64 s32768 d128 needs more scratch than the static array holds
+    need = fbm.block_map_workspace_bytes(2, 64, 64, 32768, 128)
+    assert need > fbm.FBM_STATIC_SCRATCH_BYTES
+    arr = (ctypes.c_float * 64)(*([0.1] * 64))
+    st = L.sparge_block_map_static(FAKE, FAKE, 0, 2, 64, 64, 32768, 128, 64, 64, arr, None, arr,
+                                   0.08, 0, 0, FAKE, FAKE, None, None)
+    assert st == fbm.FBM_ERR_UNSUPPORTED
+    assert b"static array" in L.fbm_last_error_message()
