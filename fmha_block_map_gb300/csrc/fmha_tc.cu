@@ -19,12 +19,15 @@
 // on those rare pairs.
 //
 // Roles (one persistent CTA per SM, 10 warps):
-//   warp 0    TMA producer: Q (double buffer), K and V pairs (2-slot rings)
+//   warp 0    TMA producer: Q (double buffer), K pairs (3-slot ring), V pairs
+//             (2-slot ring)
 //   warp 1    TMEM owner and single-thread MMA issuer
 //   warps 2-5 softmax + epilogue of queries 0-31, warps 6-9 of queries 32-63
 //             (each group covers TMEM lane quadrants 2, 3, 0, 1: all 128 keys)
-// Pipeline per q block, pairs p = 0..: S(0); then S(p+1) before PV(p), so the
-// softmax of pair p+1 overlaps the PV MMA of pair p.  Every wait is bounded:
+// Pipeline per q block, pairs p = 0..: S(0), S(1); then S(p+2) before PV(p)
+// (three S^T accumulators in TMEM), so the softmax of a pair overlaps the MMAs
+// of the two pairs around it and the single MMA-issuing thread never waits for
+// P in steady state.  Every wait is bounded:
 // on expiry the kernel raises FBM_DEVERR_TIMEOUT, every role leaves its loop,
 // in-flight copies and MMAs are drained with bounded waits and TMEM is freed.
 //
@@ -53,23 +56,25 @@ constexpr int kPairChunk = 128 * 128;     // 16 KB: one 64-wide d chunk of a 128
 constexpr int kPBytes = 128 * 128;        // 16 KB: P^T, 128 keys x 64 queries (MN-major)
 
 constexpr int OFF_Q = 0;
+constexpr int kKSlots = 3;                        // K pairs in flight (S runs 2 pairs ahead)
+constexpr int kSSlots = 3;                        // S^T accumulators in TMEM
 constexpr int OFF_K = OFF_Q + 2 * kQBytes;
-constexpr int OFF_V = OFF_K + 2 * kPairBytes;
+constexpr int OFF_V = OFF_K + kKSlots * kPairBytes;
 constexpr int OFF_P = OFF_V + 2 * kPairBytes;
-constexpr int OFF_STAGE = OFF_P + 2 * kPBytes;   // 16 KB: output staging [64 q][128 d]
-constexpr int OFF_RED = OFF_STAGE + kQBytes;      // float [2 groups][4][32]
+constexpr int OFF_RED = OFF_P + 2 * kPBytes;      // float [2 groups][4][32]
 constexpr int OFF_ALPHA = OFF_RED + 2 * 4 * 32 * 4;  // float [2][32]
 constexpr int OFF_INVL = OFF_ALPHA + 2 * 32 * 4;  // float [2][32]
 constexpr int OFF_M = OFF_INVL + 2 * 32 * 4;      // float [2][32]
 constexpr int OFF_BAR = OFF_M + 2 * 32 * 4;
 enum {
-  B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_SE = 14,
-  B_PF = 16, B_PV = 18, B_OF = 20, B_DRAIN = 21, NBAR = 22
+  B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 7, B_VF = 10, B_VE = 12, B_SF = 14, B_SE = 17,
+  B_PF = 20, B_PV = 22, B_OF = 24, B_DRAIN = 25, NBAR = 26
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // [0] tmem base, [1] abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
-constexpr uint32_t kTmemCols = 256;                // S0 @0, S1 @64, O @128
+constexpr uint32_t kTmemCols = 256;                // S0 @0, S1 @64, S2 @128, O @192
+constexpr uint32_t kOCol = 192;
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
 constexpr int kGroupThreads = 128;                 // one softmax warpgroup
 constexpr int kSoftmaxThreads = 2 * kGroupThreads; // two groups: queries 0-31 and 32-63
@@ -123,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
   if (threadIdx.x == 0) {
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
-      if (k == B_SE || k == B_SE + 1 || k == B_PF || k == B_PF + 1 || k == B_OF)
+      if ((k >= B_SE && k < B_SE + kSSlots) || k == B_PF || k == B_PF + 1 || k == B_OF)
         cnt = kSoftmaxThreads;  // both query groups arrive
       mbar_init(bar(k), cnt);
     }
@@ -163,9 +168,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           tma_load_3d(sbase + OFF_Q + qb * kQBytes + c * kQChunk, &P.tq, c * 64, U.i * 64,
                       U.bh_q, bar(B_QF + qb));
         auto load_pair = [&](int p, bool is_v) -> bool {
-          const int g = pc + p, slot = g & 1;
+          const int g = pc + p;
+          const int slot = is_v ? (g & 1) : (g % kKSlots);
+          const int ph = is_v ? ((g >> 1) & 1) : ((g / kKSlots) & 1);
           const int fb = (is_v ? B_VF : B_KF) + slot, eb = (is_v ? B_VE : B_KE) + slot;
-          if (!mbar_wait(bar(eb), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs)) return false;
+          if (!mbar_wait(bar(eb), ph ^ 1, abort_flag, kWaitNs)) return false;
           int js[2] = {-1, -1};
           uint32_t bytes = 0;
           for (int hf = 0; hf < 2; ++hf) {
@@ -191,9 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           }
           return true;
         };
+        // the MMA order is S(0), S(1), then S(p + 2) before PV(p): K leads V by two
         if (!(ok = load_pair(0, false))) break;
+        if (npairs > 1 && !(ok = load_pair(1, false))) break;
         for (int p = 0; p < npairs && ok; ++p) {
-          if (p + 1 < npairs) ok = load_pair(p + 1, false);
+          if (p + 2 < npairs) ok = load_pair(p + 2, false);
           if (ok) ok = load_pair(p, true);
         }
         pc += npairs;
@@ -206,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(kBf16, false, false, 128, 64);
       constexpr uint32_t idO = idesc_f16(kBf16, true, true, 128, 64);
-      const uint32_t tO = tbase + 128;
+      const uint32_t tO = tbase + kOCol;
       int pc = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
@@ -218,9 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         tc_fence_after();
         const uint32_t qaddr = sbase + OFF_Q + qb * kQBytes;
         auto issue_S = [&](int p) -> bool {
-          const int g = pc + p, slot = g & 1;
-          if (!mbar_wait(bar(B_KF + slot), (g >> 1) & 1, abort_flag, kWaitNs)) return false;
-          if (!mbar_wait(bar(B_SE + slot), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs)) return false;
+          const int g = pc + p, slot = g % kKSlots, ph = (g / kKSlots) & 1;
+          if (!mbar_wait(bar(B_KF + slot), ph, abort_flag, kWaitNs)) return false;
+          if (!mbar_wait(bar(B_SE + slot), ph ^ 1, abort_flag, kWaitNs)) return false;
           tc_fence_after();
           const uint32_t kaddr = sbase + OFF_K + slot * kPairBytes;
 #pragma unroll
@@ -233,13 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           mma_commit(bar(B_KE + slot));
           return true;
         };
-        if (!(ok = issue_S(0))) break;
+        int s_next = 0;  // next pair whose S^T is issued (runs two pairs ahead of PV)
+        auto issue_next_S = [&]() -> bool {
+          if (!issue_S(s_next)) return false;
+          if (++s_next == npairs) mma_commit(bar(B_QE + qb));  // Q free once every S^T is done
+          return true;
+        };
+        while (ok && s_next < npairs && s_next < 2) ok = issue_next_S();
         for (int p = 0; p < npairs && ok; ++p) {
-          if (p + 1 < npairs) {
-            if (!(ok = issue_S(p + 1))) break;
-          } else {
-            mma_commit(bar(B_QE + qb));
-          }
+          if (s_next < npairs && !(ok = issue_next_S())) break;
           const int g = pc + p, slot = g & 1;
           if (!(ok = mbar_wait(bar(B_PF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
           if (!(ok = mbar_wait(bar(B_VF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
@@ -320,10 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         // queries cb + q with q < qmin cannot see this key (causal)
         const int qmin = P.causal ? kpos - q0 - cb : -1;
         const bool plain = kvalid && qmin <= 0;  // the whole column range is visible
-        ok = ok && mbar_wait(bar(B_SF + slot), (g >> 1) & 1, abort_flag, kWaitNs);
+        const int ss = g % kSSlots, sph = (g / kSSlots) & 1;
+        ok = ok && mbar_wait(bar(B_SF + ss), sph, abort_flag, kWaitNs);
         tc_fence_after();
         uint32_t r[32];
-        tmem_ld32(tl + slot * 64 + cb, r);
+        tmem_ld32(tl + ss * 64 + cb, r);
         tmem_wait_ld();
         uint64_t x2[16];
         float mx;
@@ -392,11 +404,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             ok = ok && mbar_wait(bar(B_PV + (gp & 1)), (gp >> 1) & 1, abort_flag, kWaitNs);
             tc_fence_after();
             uint32_t o[32];
-            tmem_ld32(tl + 128 + cb, o);
+            tmem_ld32(tl + kOCol + cb, o);
             tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha_s[q]);
-            tmem_st32(tl + 128 + cb, o);
+            tmem_st32(tl + kOCol + cb, o);
             tmem_wait_st();
             tc_fence_before();
           }
@@ -431,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(bar(B_PF + slot));
-        mbar_arrive(bar(B_SE + slot));
+        mbar_arrive(bar(B_SE + ss));
       }
       // ---- epilogue: O = O^T / l, LSE = m ln2 + ln l (this group's 32 queries)
       {
@@ -466,31 +478,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             lrow[q] = lt > 0.f ? m_s[q] * 0.6931471805599453f + logf(lt) : -INFINITY;
         }
         named_sync(barid, kGroupThreads);
-        // O^T row `key` (= d), columns cb.. -> staging rows cb.. of [64 q][128 d]
-        uint16_t *stage = reinterpret_cast<uint16_t *>(smem + OFF_STAGE);
+        // O^T row `key` (= d), columns cb..cb+31 -> O[q][key]: for every query the
+        // warp writes 32 consecutive d values (64 contiguous bytes)
         {
           uint32_t r[32];
-          tmem_ld32(tl + 128 + cb, r);
+          tmem_ld32(tl + kOCol + cb, r);
           tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(B_OF));
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            stage[(cb + q) * kD + key] = E::bits(__uint_as_float(r[q]) * invl_s[q]);
-        }
-        tc_fence_before();
-        mbar_arrive(bar(B_OF));
-        fence_proxy_async();
-        named_sync(barid, kGroupThreads);
-        if (tg == 0 && my_rows > 0) {
-          bulk_store(orow, sbase + OFF_STAGE + cb * kD * 2, (uint32_t)(my_rows * kD * 2));
-          bulk_commit();
-          bulk_wait_read0();
+            if (q < my_rows) orow[(size_t)q * kD + key] = E::bits(__uint_as_float(r[q]) * invl_s[q]);
         }
         named_sync(barid, kGroupThreads);
       }
       pc += npairs;
     }
     if (!ok) fail(FBM_DEVERR_TIMEOUT);
-    if (tg == 0) bulk_wait0();
   }
 
   tc_fence_before();
