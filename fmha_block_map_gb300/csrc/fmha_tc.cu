@@ -19,8 +19,7 @@
 // on those rare pairs.
 //
 // Roles (one persistent CTA per SM, 10 warps):
-//   warp 0    TMA producer: Q (double buffer), K pairs (3-slot ring), V pairs
-//             (2-slot ring)
+//   warp 0    TMA producer: Q (double buffer), K and V pairs (2-slot rings)
 //   warp 1    TMEM owner and single-thread MMA issuer
 //   warps 2-5 softmax + epilogue of queries 0-31, warps 6-9 of queries 32-63
 //             (each group covers TMEM lane quadrants 2, 3, 0, 1: all 128 keys)
@@ -56,19 +55,20 @@ constexpr int kPairChunk = 128 * 128;     // 16 KB: one 64-wide d chunk of a 128
 constexpr int kPBytes = 128 * 128;        // 16 KB: P^T, 128 keys x 64 queries (MN-major)
 
 constexpr int OFF_Q = 0;
-constexpr int kKSlots = 3;                        // K pairs in flight (S runs 2 pairs ahead)
-constexpr int kSSlots = 3;                        // S^T accumulators in TMEM
+constexpr int kKSlots = 2;                        // K pairs in flight
+constexpr int kSSlots = 3;                        // S^T accumulators in TMEM (S runs 2 pairs ahead)
+constexpr int kPSlots = 3;                        // P^T buffers (PV(g) trails S(g) by two pairs)
 constexpr int OFF_K = OFF_Q + 2 * kQBytes;
 constexpr int OFF_V = OFF_K + kKSlots * kPairBytes;
 constexpr int OFF_P = OFF_V + 2 * kPairBytes;
-constexpr int OFF_RED = OFF_P + 2 * kPBytes;      // float [2 groups][4][32]
+constexpr int OFF_RED = OFF_P + kPSlots * kPBytes;  // float [2 groups][4][32]
 constexpr int OFF_ALPHA = OFF_RED + 2 * 4 * 32 * 4;  // float [2][32]
 constexpr int OFF_INVL = OFF_ALPHA + 2 * 32 * 4;  // float [2][32]
 constexpr int OFF_M = OFF_INVL + 2 * 32 * 4;      // float [2][32]
 constexpr int OFF_BAR = OFF_M + 2 * 32 * 4;
 enum {
-  B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 7, B_VF = 10, B_VE = 12, B_SF = 14, B_SE = 17,
-  B_PF = 20, B_PV = 22, B_OF = 24, B_DRAIN = 25, NBAR = 26
+  B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_SE = 15,
+  B_PF = 18, B_PV = 21, B_OF = 24, B_DRAIN = 25, NBAR = 26
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // [0] tmem base, [1] abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 16;
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
   if (threadIdx.x == 0) {
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
-      if ((k >= B_SE && k < B_SE + kSSlots) || k == B_PF || k == B_PF + 1 || k == B_OF)
+      if ((k >= B_SE && k < B_SE + kSSlots) || (k >= B_PF && k < B_PF + kPSlots) || k == B_OF)
         cnt = kSoftmaxThreads;  // both query groups arrive
       mbar_init(bar(k), cnt);
     }
@@ -251,20 +251,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         while (ok && s_next < npairs && s_next < 2) ok = issue_next_S();
         for (int p = 0; p < npairs && ok; ++p) {
           if (s_next < npairs && !(ok = issue_next_S())) break;
-          const int g = pc + p, slot = g & 1;
-          if (!(ok = mbar_wait(bar(B_PF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
+          const int g = pc + p, slot = g & 1, ps = g % kPSlots;
+          if (!(ok = mbar_wait(bar(B_PF + ps), (g / kPSlots) & 1, abort_flag, kWaitNs))) break;
           if (!(ok = mbar_wait(bar(B_VF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
           if (p == 0 && !(ok = mbar_wait(bar(B_OF), (uc & 1) ^ 1, abort_flag, kWaitNs))) break;
           tc_fence_after();
           const uint32_t vaddr = sbase + OFF_V + slot * kPairBytes;
-          const uint32_t paddr = sbase + OFF_P + slot * kPBytes;
+          const uint32_t paddr = sbase + OFF_P + ps * kPBytes;
           const int ksteps = (2 * p + 1 < U.n) ? 8 : 4;  // a half pair has 64 keys
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint64_t ad = sdesc_sw128(vaddr + kk * 2048, kPairChunk, 1024);
             const uint64_t bd = sdesc_sw128(paddr + kk * 2048, kPairChunk, 1024);
             mma_f16(tO, ad, bd, idO, (p > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(B_PV + slot));
+          mma_commit(bar(B_PV + ps));
           mma_commit(bar(B_VE + slot));
         }
         pc += npairs;
@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           if (p > 0) {
             // O^T holds PV(0 .. p-1): wait for the last of them, then scale
             const int gp = g - 1;
-            ok = ok && mbar_wait(bar(B_PV + (gp & 1)), (gp >> 1) & 1, abort_flag, kWaitNs);
+            ok = ok && mbar_wait(bar(B_PV + gp % kPSlots), (gp / kPSlots) & 1, abort_flag, kWaitNs);
             tc_fence_after();
             uint32_t o[32];
             tmem_ld32(tl + kOCol + cb, o);
@@ -420,12 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             x2[i] = f2_pack(a, b);
           }
         }
-        // P(p) goes to buffer `slot`, last read by PV(g - 2)
-        if (p >= 2) {
-          const int gp = g - 2;
-          ok = ok && mbar_wait(bar(B_PV + slot), (gp >> 1) & 1, abort_flag, kWaitNs);
+        // P(p) goes to buffer g % kPSlots, last read by PV(g - kPSlots)
+        const int ps = g % kPSlots;
+        if (p >= kPSlots) {
+          const int gp = g - kPSlots;
+          ok = ok && mbar_wait(bar(B_PV + ps), (gp / kPSlots) & 1, abort_flag, kWaitNs);
         }
-        uint8_t *prow = smem + OFF_P + slot * kPBytes + key * 128;
+        uint8_t *prow = smem + OFF_P + ps * kPBytes + key * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[4];
@@ -442,13 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         }
         fence_proxy_async();
         tc_fence_before();
-        mbar_arrive(bar(B_PF + slot));
+        mbar_arrive(bar(B_PF + ps));
         mbar_arrive(bar(B_SE + ss));
       }
       // ---- epilogue: O = O^T / l, LSE = m ln2 + ln l (this group's 32 queries)
       {
         const int gl = pc + npairs - 1;
-        ok = ok && mbar_wait(bar(B_PV + (gl & 1)), (gl >> 1) & 1, abort_flag, kWaitNs);
+        ok = ok && mbar_wait(bar(B_PV + gl % kPSlots), (gl / kPSlots) & 1, abort_flag, kWaitNs);
         tc_fence_after();
         // sum l over the 128 keys
         float l[32];
