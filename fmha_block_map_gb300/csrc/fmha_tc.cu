@@ -227,19 +227,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         tc_fence_after();
         const uint32_t qaddr = sbase + OFF_Q + qb * kQBytes;
         auto issue_S = [&](int p) -> bool {
-          const int g = pc + p, slot = g % kKSlots, ph = (g / kKSlots) & 1;
-          if (!mbar_wait(bar(B_KF + slot), ph, abort_flag, kWaitNs)) return false;
-          if (!mbar_wait(bar(B_SE + slot), ph ^ 1, abort_flag, kWaitNs)) return false;
+          const int g = pc + p;
+          const int ks = g % kKSlots, kph = (g / kKSlots) & 1;  // K pair ring
+          const int ss = g % kSSlots, sph = (g / kSSlots) & 1;  // S^T accumulator ring
+          if (!mbar_wait(bar(B_KF + ks), kph, abort_flag, kWaitNs)) return false;
+          if (!mbar_wait(bar(B_SE + ss), sph ^ 1, abort_flag, kWaitNs)) return false;
           tc_fence_after();
-          const uint32_t kaddr = sbase + OFF_K + slot * kPairBytes;
+          const uint32_t kaddr = sbase + OFF_K + ks * kPairBytes;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint64_t ad = sdesc_sw128(kaddr + (kk >> 2) * kPairChunk + (kk & 3) * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(qaddr + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
-            mma_f16(tbase + slot * 64, ad, bd, idS, kk > 0 ? 1u : 0u);
+            mma_f16(tbase + ss * 64, ad, bd, idS, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(B_SF + slot));
-          mma_commit(bar(B_KE + slot));
+          mma_commit(bar(B_SF + ss));
+          mma_commit(bar(B_KE + ks));
           return true;
         };
         int s_next = 0;  // next pair whose S^T is issued (runs two pairs ahead of PV)
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       const uint64_t sl2x2 = f2_pack(P.sl2, P.sl2);
       int j_next = (key >> 6) < U.n ? entry_of(U, key >> 6) : -1;
       for (int p = 0; p < npairs; ++p) {
-        const int g = pc + p, slot = g & 1;
+        const int g = pc + p;
         // this thread's key: block t of the row, offset key & 63
         const int j = j_next;
         {
