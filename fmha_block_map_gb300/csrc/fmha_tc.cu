@@ -55,11 +55,10 @@ constexpr int kPairChunk = 128 * 128;     // 16 KB: one 64-wide d chunk of a 128
 constexpr int kPBytes = 128 * 128;        // 16 KB: P^T, 128 keys x 64 queries (MN-major)
 
 constexpr int OFF_Q = 0;
-constexpr int kKSlots = 2;                        // K pairs in flight
 constexpr int kSSlots = 3;                        // S^T accumulators in TMEM (S runs 2 pairs ahead)
 constexpr int kPSlots = 3;                        // P^T buffers (PV(g) trails S(g) by two pairs)
 constexpr int OFF_K = OFF_Q + 2 * kQBytes;
-constexpr int OFF_V = OFF_K + kKSlots * kPairBytes;
+constexpr int OFF_V = OFF_K + 2 * kPairBytes;
 constexpr int OFF_P = OFF_V + 2 * kPairBytes;
 constexpr int OFF_RED = OFF_P + kPSlots * kPBytes;  // float [2 groups][4][32]
 constexpr int OFF_ALPHA = OFF_RED + 2 * 4 * 32 * 4;  // float [2][32]
@@ -67,8 +66,8 @@ constexpr int OFF_INVL = OFF_ALPHA + 2 * 32 * 4;  // float [2][32]
 constexpr int OFF_M = OFF_INVL + 2 * 32 * 4;      // float [2][32]
 constexpr int OFF_BAR = OFF_M + 2 * 32 * 4;
 enum {
-  B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_SE = 15,
-  B_PF = 18, B_PV = 21, B_OF = 24, B_DRAIN = 25, NBAR = 26
+  B_QF = 0, B_QE = 2, B_KF = 4, B_VF = 6, B_SF = 8, B_SE = 11, B_PF = 14, B_PV = 17, B_OF = 20,
+  B_DRAIN = 21, NBAR = 22
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // [0] tmem base, [1] abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 16;
@@ -169,10 +168,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
                       U.bh_q, bar(B_QF + qb));
         auto load_pair = [&](int p, bool is_v) -> bool {
           const int g = pc + p;
-          const int slot = is_v ? (g & 1) : (g % kKSlots);
-          const int ph = is_v ? ((g >> 1) & 1) : ((g / kKSlots) & 1);
-          const int fb = (is_v ? B_VF : B_KF) + slot, eb = (is_v ? B_VE : B_KE) + slot;
-          if (!mbar_wait(bar(eb), ph ^ 1, abort_flag, kWaitNs)) return false;
+          const int slot = g & 1;  // K and V rings of two pair slots
+          const int fb = (is_v ? B_VF : B_KF) + slot;
+          // the slot was last read by S^T(g - 2) (K) or PV(g - 2) (V): wait for
+          // that MMA's completion barrier
+          if (g >= 2) {
+            const int gp = g - 2;
+            const uint32_t done = is_v ? bar(B_PV + gp % kPSlots) : bar(B_SF + gp % kSSlots);
+            const int par = is_v ? ((gp / kPSlots) & 1) : ((gp / kSSlots) & 1);
+            if (!mbar_wait(done, par, abort_flag, kWaitNs)) return false;
+          }
           int js[2] = {-1, -1};
           uint32_t bytes = 0;
           for (int hf = 0; hf < 2; ++hf) {
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         const uint32_t qaddr = sbase + OFF_Q + qb * kQBytes;
         auto issue_S = [&](int p) -> bool {
           const int g = pc + p;
-          const int ks = g % kKSlots, kph = (g / kKSlots) & 1;  // K pair ring
+          const int ks = g & 1, kph = (g >> 1) & 1;           // K pair ring
           const int ss = g % kSSlots, sph = (g / kSSlots) & 1;  // S^T accumulator ring
           if (!mbar_wait(bar(B_KF + ks), kph, abort_flag, kWaitNs)) return false;
           if (!mbar_wait(bar(B_SE + ss), sph ^ 1, abort_flag, kWaitNs)) return false;
@@ -240,8 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             const uint64_t bd = sdesc_sw128(qaddr + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
             mma_f16(tbase + ss * 64, ad, bd, idS, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(B_SF + ss));
-          mma_commit(bar(B_KE + ks));
+          mma_commit(bar(B_SF + ss));  // S^T ready; also frees K slot ks
           return true;
         };
         int s_next = 0;  // next pair whose S^T is issued (runs two pairs ahead of PV)
@@ -266,8 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             const uint64_t bd = sdesc_sw128(paddr + kk * 2048, kPairChunk, 1024);
             mma_f16(tO, ad, bd, idO, (p > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(B_PV + ps));
-          mma_commit(bar(B_VE + slot));
+          mma_commit(bar(B_PV + ps));  // O^T updated; frees P slot ps and V slot
         }
         pc += npairs;
         uc += 1;
