@@ -23,10 +23,8 @@
 //   warp 1    TMEM owner and single-thread MMA issuer
 //   warps 2-5 softmax + epilogue of queries 0-31, warps 6-9 of queries 32-63
 //             (each group covers TMEM lane quadrants 2, 3, 0, 1: all 128 keys)
-// Pipeline per q block, pairs p = 0..: S(0), S(1); then S(p+2) before PV(p)
-// (three S^T accumulators in TMEM), so the softmax of a pair overlaps the MMAs
-// of the two pairs around it and the single MMA-issuing thread never waits for
-// P in steady state.  Every wait is bounded:
+// Pipeline per q block, pairs p = 0..: S(0); then S(p+1) before PV(p), so the
+// softmax of pair p+1 overlaps the PV MMA of pair p.  Every wait is bounded:
 // on expiry the kernel raises FBM_DEVERR_TIMEOUT, every role leaves its loop,
 // in-flight copies and MMAs are drained with bounded waits and TMEM is freed.
 //
@@ -55,25 +53,23 @@ constexpr int kPairChunk = 128 * 128;     // 16 KB: one 64-wide d chunk of a 128
 constexpr int kPBytes = 128 * 128;        // 16 KB: P^T, 128 keys x 64 queries (MN-major)
 
 constexpr int OFF_Q = 0;
-constexpr int kSSlots = 3;                        // S^T accumulators in TMEM (S runs 2 pairs ahead)
-constexpr int kPSlots = 3;                        // P^T buffers (PV(g) trails S(g) by two pairs)
 constexpr int OFF_K = OFF_Q + 2 * kQBytes;
 constexpr int OFF_V = OFF_K + 2 * kPairBytes;
 constexpr int OFF_P = OFF_V + 2 * kPairBytes;
-constexpr int OFF_RED = OFF_P + kPSlots * kPBytes;  // float [2 groups][4][32]
+constexpr int OFF_STAGE = OFF_P + 2 * kPBytes;   // 16 KB: output staging [64 q][128 d]
+constexpr int OFF_RED = OFF_STAGE + kQBytes;      // float [2 groups][4][32]
 constexpr int OFF_ALPHA = OFF_RED + 2 * 4 * 32 * 4;  // float [2][32]
 constexpr int OFF_INVL = OFF_ALPHA + 2 * 32 * 4;  // float [2][32]
 constexpr int OFF_M = OFF_INVL + 2 * 32 * 4;      // float [2][32]
 constexpr int OFF_BAR = OFF_M + 2 * 32 * 4;
 enum {
-  B_QF = 0, B_QE = 2, B_KF = 4, B_VF = 6, B_SF = 8, B_SE = 11, B_PF = 14, B_PV = 17, B_OF = 20,
-  B_DRAIN = 21, NBAR = 22
+  B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_SE = 14,
+  B_PF = 16, B_PV = 18, B_OF = 20, B_DRAIN = 21, NBAR = 22
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // [0] tmem base, [1] abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
-constexpr uint32_t kTmemCols = 256;                // S0 @0, S1 @64, S2 @128, O @192
-constexpr uint32_t kOCol = 192;
+constexpr uint32_t kTmemCols = 256;                // S0 @0, S1 @64, O @128
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
 constexpr int kGroupThreads = 128;                 // one softmax warpgroup
 constexpr int kSoftmaxThreads = 2 * kGroupThreads; // two groups: queries 0-31 and 32-63
@@ -127,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
   if (threadIdx.x == 0) {
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
-      if ((k >= B_SE && k < B_SE + kSSlots) || (k >= B_PF && k < B_PF + kPSlots) || k == B_OF)
+      if (k == B_SE || k == B_SE + 1 || k == B_PF || k == B_PF + 1 || k == B_OF)
         cnt = kSoftmaxThreads;  // both query groups arrive
       mbar_init(bar(k), cnt);
     }
@@ -167,17 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           tma_load_3d(sbase + OFF_Q + qb * kQBytes + c * kQChunk, &P.tq, c * 64, U.i * 64,
                       U.bh_q, bar(B_QF + qb));
         auto load_pair = [&](int p, bool is_v) -> bool {
-          const int g = pc + p;
-          const int slot = g & 1;  // K and V rings of two pair slots
-          const int fb = (is_v ? B_VF : B_KF) + slot;
-          // the slot was last read by S^T(g - 2) (K) or PV(g - 2) (V): wait for
-          // that MMA's completion barrier
-          if (g >= 2) {
-            const int gp = g - 2;
-            const uint32_t done = is_v ? bar(B_PV + gp % kPSlots) : bar(B_SF + gp % kSSlots);
-            const int par = is_v ? ((gp / kPSlots) & 1) : ((gp / kSSlots) & 1);
-            if (!mbar_wait(done, par, abort_flag, kWaitNs)) return false;
-          }
+          const int g = pc + p, slot = g & 1;
+          const int fb = (is_v ? B_VF : B_KF) + slot, eb = (is_v ? B_VE : B_KE) + slot;
+          if (!mbar_wait(bar(eb), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs)) return false;
           int js[2] = {-1, -1};
           uint32_t bytes = 0;
           for (int hf = 0; hf < 2; ++hf) {
@@ -203,11 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           }
           return true;
         };
-        // the MMA order is S(0), S(1), then S(p + 2) before PV(p): K leads V by two
         if (!(ok = load_pair(0, false))) break;
-        if (npairs > 1 && !(ok = load_pair(1, false))) break;
         for (int p = 0; p < npairs && ok; ++p) {
-          if (p + 2 < npairs) ok = load_pair(p + 2, false);
+          if (p + 1 < npairs) ok = load_pair(p + 1, false);
           if (ok) ok = load_pair(p, true);
         }
         pc += npairs;
@@ -220,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(kBf16, false, false, 128, 64);
       constexpr uint32_t idO = idesc_f16(kBf16, true, true, 128, 64);
-      const uint32_t tO = tbase + kOCol;
+      const uint32_t tO = tbase + 128;
       int pc = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
@@ -232,45 +218,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         tc_fence_after();
         const uint32_t qaddr = sbase + OFF_Q + qb * kQBytes;
         auto issue_S = [&](int p) -> bool {
-          const int g = pc + p;
-          const int ks = g & 1, kph = (g >> 1) & 1;           // K pair ring
-          const int ss = g % kSSlots, sph = (g / kSSlots) & 1;  // S^T accumulator ring
-          if (!mbar_wait(bar(B_KF + ks), kph, abort_flag, kWaitNs)) return false;
-          if (!mbar_wait(bar(B_SE + ss), sph ^ 1, abort_flag, kWaitNs)) return false;
+          const int g = pc + p, slot = g & 1;
+          if (!mbar_wait(bar(B_KF + slot), (g >> 1) & 1, abort_flag, kWaitNs)) return false;
+          if (!mbar_wait(bar(B_SE + slot), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs)) return false;
           tc_fence_after();
-          const uint32_t kaddr = sbase + OFF_K + ks * kPairBytes;
+          const uint32_t kaddr = sbase + OFF_K + slot * kPairBytes;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint64_t ad = sdesc_sw128(kaddr + (kk >> 2) * kPairChunk + (kk & 3) * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(qaddr + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
-            mma_f16(tbase + ss * 64, ad, bd, idS, kk > 0 ? 1u : 0u);
+            mma_f16(tbase + slot * 64, ad, bd, idS, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar(B_SF + ss));  // S^T ready; also frees K slot ks
+          mma_commit(bar(B_SF + slot));
+          mma_commit(bar(B_KE + slot));
           return true;
         };
-        int s_next = 0;  // next pair whose S^T is issued (runs two pairs ahead of PV)
-        auto issue_next_S = [&]() -> bool {
-          if (!issue_S(s_next)) return false;
-          if (++s_next == npairs) mma_commit(bar(B_QE + qb));  // Q free once every S^T is done
-          return true;
-        };
-        while (ok && s_next < npairs && s_next < 2) ok = issue_next_S();
+        if (!(ok = issue_S(0))) break;
         for (int p = 0; p < npairs && ok; ++p) {
-          if (s_next < npairs && !(ok = issue_next_S())) break;
-          const int g = pc + p, slot = g & 1, ps = g % kPSlots;
-          if (!(ok = mbar_wait(bar(B_PF + ps), (g / kPSlots) & 1, abort_flag, kWaitNs))) break;
+          if (p + 1 < npairs) {
+            if (!(ok = issue_S(p + 1))) break;
+          } else {
+            mma_commit(bar(B_QE + qb));
+          }
+          const int g = pc + p, slot = g & 1;
+          if (!(ok = mbar_wait(bar(B_PF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
           if (!(ok = mbar_wait(bar(B_VF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
           if (p == 0 && !(ok = mbar_wait(bar(B_OF), (uc & 1) ^ 1, abort_flag, kWaitNs))) break;
           tc_fence_after();
           const uint32_t vaddr = sbase + OFF_V + slot * kPairBytes;
-          const uint32_t paddr = sbase + OFF_P + ps * kPBytes;
+          const uint32_t paddr = sbase + OFF_P + slot * kPBytes;
           const int ksteps = (2 * p + 1 < U.n) ? 8 : 4;  // a half pair has 64 keys
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint64_t ad = sdesc_sw128(vaddr + kk * 2048, kPairChunk, 1024);
             const uint64_t bd = sdesc_sw128(paddr + kk * 2048, kPairChunk, 1024);
             mma_f16(tO, ad, bd, idO, (p > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(B_PV + ps));  // O^T updated; frees P slot ps and V slot
+          mma_commit(bar(B_PV + slot));
+          mma_commit(bar(B_VE + slot));
         }
         pc += npairs;
         uc += 1;
@@ -323,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       const uint64_t sl2x2 = f2_pack(P.sl2, P.sl2);
       int j_next = (key >> 6) < U.n ? entry_of(U, key >> 6) : -1;
       for (int p = 0; p < npairs; ++p) {
-        const int g = pc + p;
+        const int g = pc + p, slot = g & 1;
         // this thread's key: block t of the row, offset key & 63
         const int j = j_next;
         {
@@ -336,11 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         // queries cb + q with q < qmin cannot see this key (causal)
         const int qmin = P.causal ? kpos - q0 - cb : -1;
         const bool plain = kvalid && qmin <= 0;  // the whole column range is visible
-        const int ss = g % kSSlots, sph = (g / kSSlots) & 1;
-        ok = ok && mbar_wait(bar(B_SF + ss), sph, abort_flag, kWaitNs);
+        ok = ok && mbar_wait(bar(B_SF + slot), (g >> 1) & 1, abort_flag, kWaitNs);
         tc_fence_after();
         uint32_t r[32];
-        tmem_ld32(tl + ss * 64 + cb, r);
+        tmem_ld32(tl + slot * 64 + cb, r);
         tmem_wait_ld();
         uint64_t x2[16];
         float mx;
@@ -406,14 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           if (p > 0) {
             // O^T holds PV(0 .. p-1): wait for the last of them, then scale
             const int gp = g - 1;
-            ok = ok && mbar_wait(bar(B_PV + gp % kPSlots), (gp / kPSlots) & 1, abort_flag, kWaitNs);
+            ok = ok && mbar_wait(bar(B_PV + (gp & 1)), (gp >> 1) & 1, abort_flag, kWaitNs);
             tc_fence_after();
             uint32_t o[32];
-            tmem_ld32(tl + kOCol + cb, o);
+            tmem_ld32(tl + 128 + cb, o);
             tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha_s[q]);
-            tmem_st32(tl + kOCol + cb, o);
+            tmem_st32(tl + 128 + cb, o);
             tmem_wait_st();
             tc_fence_before();
           }
@@ -425,13 +408,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             x2[i] = f2_pack(a, b);
           }
         }
-        // P(p) goes to buffer g % kPSlots, last read by PV(g - kPSlots)
-        const int ps = g % kPSlots;
-        if (p >= kPSlots) {
-          const int gp = g - kPSlots;
-          ok = ok && mbar_wait(bar(B_PV + ps), (gp / kPSlots) & 1, abort_flag, kWaitNs);
+        // P(p) goes to buffer `slot`, last read by PV(g - 2)
+        if (p >= 2) {
+          const int gp = g - 2;
+          ok = ok && mbar_wait(bar(B_PV + slot), (gp >> 1) & 1, abort_flag, kWaitNs);
         }
-        uint8_t *prow = smem + OFF_P + ps * kPBytes + key * 128;
+        uint8_t *prow = smem + OFF_P + slot * kPBytes + key * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[4];
@@ -448,13 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         }
         fence_proxy_async();
         tc_fence_before();
-        mbar_arrive(bar(B_PF + ps));
-        mbar_arrive(bar(B_SE + ss));
+        mbar_arrive(bar(B_PF + slot));
+        mbar_arrive(bar(B_SE + slot));
       }
       // ---- epilogue: O = O^T / l, LSE = m ln2 + ln l (this group's 32 queries)
       {
         const int gl = pc + npairs - 1;
-        ok = ok && mbar_wait(bar(B_PV + gl % kPSlots), (gl / kPSlots) & 1, abort_flag, kWaitNs);
+        ok = ok && mbar_wait(bar(B_PV + (gl & 1)), (gl >> 1) & 1, abort_flag, kWaitNs);
         tc_fence_after();
         // sum l over the 128 keys
         float l[32];
@@ -484,23 +466,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             lrow[q] = lt > 0.f ? m_s[q] * 0.6931471805599453f + logf(lt) : -INFINITY;
         }
         named_sync(barid, kGroupThreads);
-        // O^T row `key` (= d), columns cb..cb+31 -> O[q][key]: for every query the
-        // warp writes 32 consecutive d values (64 contiguous bytes)
+        // O^T row `key` (= d), columns cb.. -> staging rows cb.. of [64 q][128 d]
+        uint16_t *stage = reinterpret_cast<uint16_t *>(smem + OFF_STAGE);
         {
           uint32_t r[32];
-          tmem_ld32(tl + kOCol + cb, r);
+          tmem_ld32(tl + 128 + cb, r);
           tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(bar(B_OF));
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            if (q < my_rows) orow[(size_t)q * kD + key] = E::bits(__uint_as_float(r[q]) * invl_s[q]);
+            stage[(cb + q) * kD + key] = E::bits(__uint_as_float(r[q]) * invl_s[q]);
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_OF));
+        fence_proxy_async();
+        named_sync(barid, kGroupThreads);
+        if (tg == 0 && my_rows > 0) {
+          bulk_store(orow, sbase + OFF_STAGE + cb * kD * 2, (uint32_t)(my_rows * kD * 2));
+          bulk_commit();
+          bulk_wait_read0();
         }
         named_sync(barid, kGroupThreads);
       }
       pc += npairs;
     }
     if (!ok) fail(FBM_DEVERR_TIMEOUT);
+    if (tg == 0) bulk_wait0();
   }
 
   tc_fence_before();
