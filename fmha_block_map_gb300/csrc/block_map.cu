@@ -1,16 +1,20 @@
 // Block-map prediction kernels ("Sparge Attention (Composable Kernel)" README:
 // mean-pool -> cosine sim -> pooled QK -> top-k / cdfthreshd LUT).
 //
-//  k_pool_sim     one warp per 64-token block of Q or K: 128-bit loads, fp32
-//                 compensated row sums (the pooled mean) and the sum of unit
-//                 rows (self-similarity = ||sum u||^2 / n^2).  HBM-bound: it
-//                 reads Q and K once and writes (d + 1) floats per block.
-//  k_score_select one CTA per 16 q blocks of one (batch, head): pooled scores
-//                 by an fp32 register-tiled dot product (K-block means staged
-//                 through shared memory, shared by the 16 rows), then one warp
-//                 per row for the pooled softmax, a radix (bitwise) threshold
-//                 search for top-k / cdf, and ballot-scan emission of the
-//                 ascending LUT row.  No atomics take part in slot assignment.
+//  k_pool_sim     one warp per 64-token block of Q or K: each lane streams 32
+//                 bytes of a row per step (128-bit loads, 8 in flight per
+//                 lane), row norms by a 3-level shuffle, fp32 row sums (the
+//                 pooled mean, two interleaved partial sums per element) and the
+//                 sum of unit rows (self-similarity = ||sum u||^2 / n^2).
+//                 HBM-bound: it reads Q and K once and writes (d + 1) floats
+//                 per block.
+//  k_score_select one CTA per 32 q blocks of one (batch, head): pooled scores
+//                 by an fp32 4x4 register-tiled product (K-block means streamed
+//                 through double-buffered shared memory in 32-dimension chunks
+//                 by cp.async, shared by the 32 rows), then one warp per row for
+//                 the pooled softmax, a radix (bitwise) threshold search for
+//                 top-k / cdf, and ballot-scan emission of the ascending LUT
+//                 row.  No atomics take part in slot assignment.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,11 +34,13 @@ struct PoolSide {
 };
 
 template <class E, int D>
-__global__ void __launch_bounds__(256) k_pool_sim(PoolSide qs, PoolSide ks) {
-  constexpr int LPR = D / 8;      // lanes per row (16 B = 8 elements per lane)
-  constexpr int RPI = 32 / LPR;   // rows per warp-wide load
-  constexpr int ITERS = kBlk / RPI;
-  constexpr int UNR = 8;
+__global__ void __launch_bounds__(256, 3) k_pool_sim(PoolSide qs, PoolSide ks) {
+  // a lane owns 16 consecutive elements (32 bytes) of a row; a row spans LPR
+  // lanes and one warp-wide step covers RPI rows
+  constexpr int LPR = D / 16;
+  constexpr int RPI = 32 / LPR;
+  constexpr int STEPS = kBlk / RPI;
+  constexpr int UNR = 4;
   const int lane = threadIdx.x & 31;
   const int unit_all = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (unit_all >= qs.nunits + ks.nunits) return;
@@ -48,69 +54,72 @@ __global__ void __launch_bounds__(256) k_pool_sim(PoolSide qs, PoolSide ks) {
   const int sub = lane % LPR;
   const int rgrp = lane / LPR;
 
-  float msum[8], mcomp[8], usum[8];
+  // two interleaved partial sums per element keep the fp32 sums short
+  float msum[2][16], usum[16];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) msum[e] = mcomp[e] = usum[e] = 0.f;
+  for (int e = 0; e < 16; ++e) msum[0][e] = msum[1][e] = usum[e] = 0.f;
 
 #pragma unroll
-  for (int it0 = 0; it0 < ITERS; it0 += UNR) {
-    uint4 raw[UNR];
+  for (int s0 = 0; s0 < STEPS; s0 += UNR) {
+    uint4 raw[UNR][2];
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
-      const int r = (it0 + u) * RPI + rgrp;
-      if (r < n)
-        raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + (size_t)r * D) + sub);
-      else
-        raw[u] = make_uint4(0, 0, 0, 0);
+      const int r = (s0 + u) * RPI + rgrp;
+      if (r < n) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(base + (size_t)r * D) + sub * 2;
+        raw[u][0] = __ldg(src);
+        raw[u][1] = __ldg(src + 1);
+      } else {
+        raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
+      }
     }
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
-      float x[8];
-      const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+      float x[16];
+      const uint32_t w[8] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
+                             raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        float2 f = E::to_f2(w[p]);
+      for (int p = 0; p < 8; ++p) {
+        const float2 f = E::to_f2(w[p]);
         x[2 * p] = f.x;
         x[2 * p + 1] = f.y;
       }
       float ss = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+      for (int e = 0; e < 16; ++e) ss = fmaf(x[e], x[e], ss);
 #pragma unroll
       for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float inv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+      const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
+      for (int e = 0; e < 16; ++e) {
         usum[e] = fmaf(x[e], inv, usum[e]);
-        // Kahan-compensated running sum of the raw values (pooled mean)
-        const float y = x[e] - mcomp[e];
-        const float t = msum[e] + y;
-        mcomp[e] = (t - msum[e]) - y;
-        msum[e] = t;
+        msum[u & 1][e] += x[e];
       }
     }
   }
-  float tot[8];
+  float tot[16];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) tot[e] = msum[e] - mcomp[e];
+  for (int e = 0; e < 16; ++e) tot[e] = msum[0][e] + msum[1][e];
 #pragma unroll
   for (int o = 16; o >= LPR; o >>= 1) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int e = 0; e < 16; ++e) {
       tot[e] += __shfl_xor_sync(0xffffffffu, tot[e], o);
       usum[e] += __shfl_xor_sync(0xffffffffu, usum[e], o);
     }
   }
   float su = 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) su = fmaf(usum[e], usum[e], su);
+  for (int e = 0; e < 16; ++e) su = fmaf(usum[e], usum[e], su);
 #pragma unroll
   for (int o = LPR / 2; o > 0; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
   if (rgrp == 0) {
     const float fn = (float)n;
-    float4 *dst = reinterpret_cast<float4 *>(side.pooled + (size_t)unit * D) + sub * 2;
-    dst[0] = make_float4(tot[0] / fn, tot[1] / fn, tot[2] / fn, tot[3] / fn);
-    dst[1] = make_float4(tot[4] / fn, tot[5] / fn, tot[6] / fn, tot[7] / fn);
+    float4 *dst = reinterpret_cast<float4 *>(side.pooled + (size_t)unit * D) + sub * 4;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      dst[c] = make_float4(tot[4 * c] / fn, tot[4 * c + 1] / fn, tot[4 * c + 2] / fn,
+                           tot[4 * c + 3] / fn);
     if (sub == 0) side.sim[unit] = su / (fn * fn);
   }
 }
@@ -119,8 +128,10 @@ __global__ void __launch_bounds__(256) k_pool_sim(PoolSide qs, PoolSide ks) {
 // k_score_select
 // ---------------------------------------------------------------------------
 
-constexpr int kSelRows = 16;   // q blocks per CTA
-constexpr int kSelCols = 64;   // kv blocks per staged tile
+constexpr int kSelRows = 32;   // q blocks per CTA
+constexpr int kSelCols = 128;  // kv blocks per column tile
+constexpr int kSelDC = 32;     // dimensions per staged chunk
+constexpr int kSelLDK = kSelDC + 4;
 
 FBM_DEVICE uint32_t order_key(float f) {
   // order-preserving map of a finite float onto uint32 (finite values > 0x7FFFFF)
@@ -131,10 +142,11 @@ FBM_DEVICE uint32_t order_key(float f) {
 template <int D, int NT>
 __global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
   extern __shared__ __align__(16) float smem[];
-  constexpr int LD = D + 4;
-  float *q_s = smem;                          // [16][LD]
-  float *k_s = q_s + kSelRows * LD;           // [64][LD]
-  float *S_s = k_s + kSelCols * LD;           // [16][NT * 32]
+  constexpr int LDQ = D + 4;
+  constexpr int NCH = D / kSelDC;                    // d chunks per column tile
+  float *q_s = smem;                                 // [32][LDQ]
+  float *k_s = q_s + kSelRows * LDQ;                 // [2][128][kSelLDK]
+  float *S_s = k_s + 2 * kSelCols * kSelLDK;         // [32][NT * 32]
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.y, bi = blockIdx.z;
@@ -146,41 +158,78 @@ __global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid
   const float *qsim = a.qsim + (size_t)(bi * a.hq + h) * a.nq;
   const float *ksim = a.ksim + (size_t)(bi * a.hk + g) * a.nk;
 
-  // stage the 16 pooled q rows
-  for (int idx = tid; idx < kSelRows * (D / 4); idx += blockDim.x) {
-    const int r = idx / (D / 4), c = idx % (D / 4);
+  // chunk c of the whole sweep = (column tile c / NCH, d chunk c % NCH)
+  const int ntiles = (a.nk + kSelCols - 1) / kSelCols;
+  const int nchunks = ntiles * NCH;
+  auto stage = [&](int c, int buf) {
+    const int col0 = (c / NCH) * kSelCols, d0 = (c % NCH) * kSelDC;
+    float *dst = k_s + buf * kSelCols * kSelLDK;
+    for (int idx = tid; idx < kSelCols * (kSelDC / 4); idx += 256) {
+      const int r = idx / (kSelDC / 4), c4 = idx % (kSelDC / 4);
+      const bool ok = col0 + r < a.nk;
+      const float *src = kbar + (size_t)(ok ? col0 + r : 0) * D + d0 + c4 * 4;
+      cp_async16(smem_u32(dst + r * kSelLDK + c4 * 4), src, ok);
+    }
+  };
+  stage(0, 0);
+  cp_async_commit();
+  // the 32 pooled q rows
+  for (int idx = tid; idx < kSelRows * (D / 4); idx += 256) {
+    const int r = idx / (D / 4), c4 = idx % (D / 4);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i0 + r < a.nq) v = reinterpret_cast<const float4 *>(qbar + (size_t)(i0 + r) * D)[c];
-    *reinterpret_cast<float4 *>(q_s + r * LD + c * 4) = v;
+    if (i0 + r < a.nq) v = reinterpret_cast<const float4 *>(qbar + (size_t)(i0 + r) * D)[c4];
+    *reinterpret_cast<float4 *>(q_s + r * LDQ + c4 * 4) = v;
   }
-  const int tr = tid / 16, tc = tid % 16;
-  for (int c0 = 0; c0 < a.nk; c0 += kSelCols) {
-    __syncthreads();
-    for (int idx = tid; idx < kSelCols * (D / 4); idx += blockDim.x) {
-      const int r = idx / (D / 4), c = idx % (D / 4);
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (c0 + r < a.nk) v = reinterpret_cast<const float4 *>(kbar + (size_t)(c0 + r) * D)[c];
-      *reinterpret_cast<float4 *>(k_s + r * LD + c * 4) = v;
-    }
-    __syncthreads();
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int kk = 0; kk < D; kk += 4) {
-      const float4 qv = *reinterpret_cast<const float4 *>(q_s + tr * LD + kk);
+  // 4 x 4 register tile: rows tr*4 .. +3, columns tc + 32 m
+  const int tr = tid >> 5, tc = tid & 31;
+  float acc[4][4];
+  for (int c = 0; c < nchunks; ++c) {
+    if (c % NCH == 0) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float4 kv = *reinterpret_cast<const float4 *>(k_s + (tc + 16 * c) * LD + kk);
-        acc[c] = fmaf(qv.x, kv.x, acc[c]);
-        acc[c] = fmaf(qv.y, kv.y, acc[c]);
-        acc[c] = fmaf(qv.z, kv.z, acc[c]);
-        acc[c] = fmaf(qv.w, kv.w, acc[c]);
-      }
-    }
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int j = c0 + tc + 16 * c;
-      if (j < a.nk) S_s[tr * (NT * 32) + j] = a.scale * acc[c];
+        for (int m = 0; m < 4; ++m) acc[r][m] = 0.f;
     }
+    if (c + 1 < nchunks) {
+      stage(c + 1, (c + 1) & 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const float *kc = k_s + (c & 1) * kSelCols * kSelLDK;
+    const int d0 = (c % NCH) * kSelDC;
+#pragma unroll
+    for (int kk = 0; kk < kSelDC; kk += 4) {
+      float4 qv[4], kv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        qv[r] = *reinterpret_cast<const float4 *>(q_s + (tr * 4 + r) * LDQ + d0 + kk);
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        kv[m] = *reinterpret_cast<const float4 *>(kc + (tc + 32 * m) * kSelLDK + kk);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          acc[r][m] = fmaf(qv[r].x, kv[m].x, acc[r][m]);
+          acc[r][m] = fmaf(qv[r].y, kv[m].y, acc[r][m]);
+          acc[r][m] = fmaf(qv[r].z, kv[m].z, acc[r][m]);
+          acc[r][m] = fmaf(qv[r].w, kv[m].w, acc[r][m]);
+        }
+    }
+    if (c % NCH == NCH - 1) {
+      const int col0 = (c / NCH) * kSelCols;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int j = col0 + tc + 32 * m;
+          if (j < a.nk) S_s[(tr * 4 + r) * (NT * 32) + j] = a.scale * acc[r][m];
+        }
+    }
+    __syncthreads();
   }
   __syncthreads();
 
@@ -225,7 +274,9 @@ __global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid
           int c = 0;
 #pragma unroll
           for (int t = 0; t < NT; ++t) c += key[t] >= cand ? 1 : 0;
-          if (__reduce_add_sync(0xffffffffu, c) >= kcount) T = cand;
+          const int tot = __reduce_add_sync(0xffffffffu, c);
+          if (tot >= kcount) T = cand;
+          if (tot == kcount) break;  // exactly kcount keys >= T: no tie left to resolve
         }
         int cgt = 0;
 #pragma unroll
@@ -312,7 +363,8 @@ __global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid
 // ---------------------------------------------------------------------------
 
 size_t block_map_smem_bytes(int d, int nt) {
-  return sizeof(float) * ((size_t)(kSelRows + kSelCols) * (d + 4) + (size_t)kSelRows * nt * 32);
+  return sizeof(float) * ((size_t)kSelRows * (d + 4) + 2 * (size_t)kSelCols * kSelLDK +
+                          (size_t)kSelRows * nt * 32);
 }
 
 template <int D, int NT>
