@@ -62,6 +62,24 @@ def dist_env():
     return rank, world, local
 
 
+def rank_config(cfg, rank: int):
+    """Each rank runs its own independent batch: the same workload shape with
+    a per-rank seed (rank 0 keeps the base seed)."""
+    return cfg.replace(seed=cfg.seed + 7919 * rank)
+
+
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """The slowest rank's time (the job finishes when the last rank does)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
@@ -152,7 +170,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     fbuild.build()
     fbm.lib()
-    cfg = synth.C3.replace(topk=args.topk)
+    cfg = rank_config(synth.C3.replace(topk=args.topk), rank)
     x = synth.prefill(cfg)
     dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.float16).cuda()
     q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
@@ -218,12 +236,7 @@ def run_ours(args):
     tiles = int(cnt.sum().item())
     assert fbm.get_error() == 0
     flops = tiles * FLOP_PER_TILE
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([step_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, world, device="cuda")
     value = flops * world / (step_ms * 1e-3) / 1e12
 
     # ---- dense reference FMHA and the topk sweep

@@ -2,7 +2,7 @@
 // mean-pool -> cosine sim -> pooled QK -> top-k / cdfthreshd LUT).
 //
 //  k_pool_sim     one warp per 64-token block of Q or K: each lane streams 32
-//                 bytes of a row per step (128-bit loads, 8 in flight per
+//                 bytes of a row per step (128-bit loads, 16 in flight per
 //                 lane), row norms by a 3-level shuffle, fp32 row sums (the
 //                 pooled mean, two interleaved partial sums per element) and the
 //                 sum of unit rows (self-similarity = ||sum u||^2 / n^2).
@@ -34,13 +34,13 @@ struct PoolSide {
 };
 
 template <class E, int D>
-__global__ void __launch_bounds__(256, 3) k_pool_sim(PoolSide qs, PoolSide ks) {
+__global__ void __launch_bounds__(256, 2) k_pool_sim(PoolSide qs, PoolSide ks) {
   // a lane owns 16 consecutive elements (32 bytes) of a row; a row spans LPR
   // lanes and one warp-wide step covers RPI rows
   constexpr int LPR = D / 16;
   constexpr int RPI = 32 / LPR;
   constexpr int STEPS = kBlk / RPI;
-  constexpr int UNR = 4;
+  constexpr int UNR = 8;  // 16 loads (256 B) in flight per lane
   const int lane = threadIdx.x & 31;
   const int unit_all = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (unit_all >= qs.nunits + ks.nunits) return;

@@ -29,8 +29,8 @@ Sources (web pages; cited by title and section):
   through a page table, a 576-wide K row (512 latent + 64 rotary) whose latent
   plane is V, split-KV partials merged by an LSE reduce.
 
-Block map, as computed here (the pages only name the steps; every reading the
-pages leave open is listed in the design doc):
+Block map, as computed here (the pages only name the steps; where they leave a
+step open, the plainest reading is taken):
 
 1. pool: qbar_i, kbar_j = mean of the rows of each 64-token block (a partial
    last block averages the rows it has);

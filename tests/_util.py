@@ -10,7 +10,9 @@ import synth
 
 TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16}
 
-# spec tolerances: output atol 4e-2 / rtol 1e-2 (fp16 / bf16), LSE 1e-3 nats,
+# tolerances: output atol 4e-2 / rtol 1e-2 (fp16 / bf16, the dense-FMHA tolerance of the
+# Sparge Attention (Composable Kernel) validation), LSE 1e-3 nats (the bf16 LSE error the
+# ROCm/aiter sparse MHA pull reports is 0.0009 nats),
 # LUT bit-exact except near-ties with pooled-score gap < 1e-6 (counted)
 O_ATOL, O_RTOL, LSE_TOL = 4e-2, 1e-2, 1e-3
 SCORE_GAP = 1e-6

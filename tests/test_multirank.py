@@ -1,0 +1,63 @@
+"""The multi-rank host logic of bench.py on two gloo ranks (CPU): every rank
+gets its own seeded batch of the same shape, the work is the same per rank
+(weak scaling), and the step time is the maximum over ranks."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out_dir):
+    import sys
+
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    import oracle
+    import synth
+
+    cfg = bench.rank_config(synth.C1.replace(hq=2, hk=2, s=256), rank)
+    x = synth.prefill(cfg)
+    r = oracle.sparge_block_map(x["q"], x["k"], synth.per_head(cfg, 0.5), None,
+                                synth.per_head(cfg, cfg.simthreshd1), cfg.scale, False, False,
+                                dtype="f16")
+    tiles = torch.tensor([int(r["count"].sum())], dtype=torch.int64)
+    gathered = [torch.zeros_like(tiles) for _ in range(world)]
+    dist.all_gather(gathered, tiles)
+    slowest = bench.max_over_ranks(1.0 + rank, world)
+    np.save(os.path.join(out_dir, f"r{rank}.npy"),
+            np.array([cfg.seed, int(x["q"].astype(np.int64).sum()), slowest] +
+                     [int(g.item()) for g in gathered]))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks(tmp_path):
+    world = 2
+    mp.start_processes(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       start_method="spawn", join=True)
+    r0, r1 = (np.load(tmp_path / f"r{r}.npy") for r in range(world))
+    import synth
+    import bench
+
+    assert r0[0] == synth.C1.seed and r1[0] != r0[0]          # own batch per rank
+    assert r0[1] != r1[1]                                      # different data
+    assert r0[2] == 2.0 and r1[2] == 2.0                       # max over ranks
+    assert (r0[3:] == r1[3:]).all()                            # same gathered view
+    assert r0[3] == r0[3 + 0] and r0[3] > 0 and r0[4] > 0      # work on both ranks
+    assert bench.max_over_ranks(3.5, 1) == 3.5
