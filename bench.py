@@ -39,7 +39,10 @@ TOPKS = (0.1, 0.2, 0.4, 0.6, 1.0)
 # DRAM bytes per launch of the sparse FMHA kernel from one ncu capture (see
 # profiles/), keyed by the sha256 of the kernel source it was taken on; a
 # kernel edited since then reports traffic = null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/sparse_fmha_tc_b2h32s16384d128_topk04.md: 813.92 MB read + 256.37 MB written
+    "3f8b180bf0ae6cd4": 1070294528,
+}
 
 
 def parse():
