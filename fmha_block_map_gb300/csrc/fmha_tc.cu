@@ -18,11 +18,12 @@
 // exceeds it by more than 2^8), so the cross-lane column maximum is needed only
 // on those rare pairs.
 //
-// Roles (one persistent CTA per SM, 10 warps):
+// Roles (one persistent CTA per SM, 18 warps):
 //   warp 0    TMA producer: Q (double buffer), K and V pairs (2-slot rings)
 //   warp 1    TMEM owner and single-thread MMA issuer
-//   warps 2-5 softmax + epilogue of queries 0-31, warps 6-9 of queries 32-63
-//             (each group covers TMEM lane quadrants 2, 3, 0, 1: all 128 keys)
+//   warps 2-17 four softmax + epilogue warpgroups, each owning 16 of the 64
+//             query columns (each group covers TMEM lane quadrants 2, 3, 0, 1:
+//             all 128 keys)
 // Pipeline per q block, pairs p = 0..: S(0); then S(p+1) before PV(p), so the
 // softmax of pair p+1 overlaps the PV MMA of pair p.  Every wait is bounded:
 // on expiry the kernel raises FBM_DEVERR_TIMEOUT, every role leaves its loop,
@@ -57,11 +58,13 @@ constexpr int OFF_K = OFF_Q + 2 * kQBytes;
 constexpr int OFF_V = OFF_K + 2 * kPairBytes;
 constexpr int OFF_P = OFF_V + 2 * kPairBytes;
 constexpr int OFF_STAGE = OFF_P + 2 * kPBytes;   // 16 KB: output staging [64 q][128 d]
-constexpr int OFF_RED = OFF_STAGE + kQBytes;      // float [2 groups][4][32]
-constexpr int OFF_ALPHA = OFF_RED + 2 * 4 * 32 * 4;  // float [2][32]
-constexpr int OFF_INVL = OFF_ALPHA + 2 * 32 * 4;  // float [2][32]
-constexpr int OFF_M = OFF_INVL + 2 * 32 * 4;      // float [2][32]
-constexpr int OFF_BAR = OFF_M + 2 * 32 * 4;
+constexpr int kGroups = 4;                         // softmax warpgroups per CTA
+constexpr int kCW = 64 / kGroups;                  // query columns per group
+constexpr int OFF_RED = OFF_STAGE + kQBytes;       // float [groups][4 quadrants][kCW]
+constexpr int OFF_ALPHA = OFF_RED + kGroups * 4 * kCW * 4;  // float [groups][kCW]
+constexpr int OFF_INVL = OFF_ALPHA + kGroups * kCW * 4;     // float [groups][kCW]
+constexpr int OFF_M = OFF_INVL + kGroups * kCW * 4;         // float [groups][kCW]
+constexpr int OFF_BAR = OFF_M + kGroups * kCW * 4;
 enum {
   B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_SE = 14,
   B_PF = 16, B_PV = 18, B_OF = 20, B_DRAIN = 21, NBAR = 22
@@ -72,7 +75,7 @@ constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
 constexpr uint32_t kTmemCols = 256;                // S0 @0, S1 @64, O @128
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
 constexpr int kGroupThreads = 128;                 // one softmax warpgroup
-constexpr int kSoftmaxThreads = 2 * kGroupThreads; // two groups: queries 0-31 and 32-63
+constexpr int kSoftmaxThreads = kGroups * kGroupThreads;
 constexpr int kThreads = 64 + kSoftmaxThreads;     // + producer warp + MMA warp
 
 struct TcParams {
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
       if (k == B_SE || k == B_SE + 1 || k == B_PF || k == B_PF + 1 || k == B_OF)
-        cnt = kSoftmaxThreads;  // both query groups arrive
+        cnt = kSoftmaxThreads;  // every query group arrives
       mbar_init(bar(k), cnt);
     }
     misc[1] = 0;
@@ -266,17 +269,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int wg = (warp - 2) >> 2;          // query group: columns 32*wg .. 32*wg+31
-    const int cb = wg * 32;
+    const int wg = (warp - 2) >> 2;          // query group: columns kCW*wg .. kCW*wg+kCW-1
+    const int cb = wg * kCW;
     const int qd = warp & 3;
     const int key = qd * 32 + lane;          // TMEM lane: key of the pair (S^T) / d (O^T)
     const int tg = (threadIdx.x - 64) & 127; // 0..127 within the group
     const int barid = 1 + wg;                // named barrier of this group
     const uint32_t tl = tbase + ((uint32_t)(qd * 32) << 16);
-    float *red = reinterpret_cast<float *>(smem + OFF_RED) + wg * 128;   // [4][32]
-    float *alpha_s = reinterpret_cast<float *>(smem + OFF_ALPHA) + wg * 32;
-    float *invl_s = reinterpret_cast<float *>(smem + OFF_INVL) + wg * 32;
-    float *m_s = reinterpret_cast<float *>(smem + OFF_M) + wg * 32;
+    float *red = reinterpret_cast<float *>(smem + OFF_RED) + wg * 4 * kCW;   // [4][kCW]
+    float *alpha_s = reinterpret_cast<float *>(smem + OFF_ALPHA) + wg * kCW;
+    float *invl_s = reinterpret_cast<float *>(smem + OFF_INVL) + wg * kCW;
+    float *m_s = reinterpret_cast<float *>(smem + OFF_M) + wg * kCW;
     using E = typename std::conditional<kBf16, BF16, F16>::type;
     // Every softmax thread of a group runs the same loop trip counts and named
     // barriers whatever happens: a failed (timed-out) wait only clears `ok`,
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       const Unit U = unit_of(P, u);
       const int q0 = U.i * 64;
       const int rows = min(64, P.s_q - q0);
-      const int my_rows = max(0, min(32, rows - cb));  // this group's valid query rows
+      const int my_rows = max(0, min(kCW, rows - cb));  // this group's valid query rows
       uint16_t *orow = static_cast<uint16_t *>(P.out) + ((size_t)U.bh_q * P.s_q + q0 + cb) * kD;
       float *lrow = P.lse ? P.lse + (size_t)U.bh_q * P.s_q + q0 + cb : nullptr;
       if (U.n == 0) {
@@ -299,10 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       const int npairs = (U.n + 1) >> 1;
       // running max per query (log2 domain) lives in m_s; l holds this key's
       // share of the row sums, as packed fp32 pairs (queries 2i, 2i+1)
-      uint64_t l2[16];
+      uint64_t l2[kCW / 2];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) l2[i] = 0ull;
-      if (tg < 32) m_s[tg] = -INFINITY;
+      for (int i = 0; i < kCW / 2; ++i) l2[i] = 0ull;
+      if (tg < kCW) m_s[tg] = -INFINITY;
       named_sync(barid, kGroupThreads);
       const uint64_t sl2x2 = f2_pack(P.sl2, P.sl2);
       int j_next = (key >> 6) < U.n ? entry_of(U, key >> 6) : -1;
@@ -322,14 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         const bool plain = kvalid && qmin <= 0;  // the whole column range is visible
         ok = ok && mbar_wait(bar(B_SF + slot), (g >> 1) & 1, abort_flag, kWaitNs);
         tc_fence_after();
-        uint32_t r[32];
-        tmem_ld32(tl + slot * 64 + cb, r);
+        uint32_t r[kCW];
+        tmem_ld16(tl + slot * 64 + cb, r);
         tmem_wait_ld();
-        uint64_t x2[16];
+        uint64_t x2[kCW / 2];
         float mx;
         if (plain) {
 #pragma unroll
-          for (int i4 = 0; i4 < 8; ++i4) {
+          for (int i4 = 0; i4 < kCW / 4; ++i4) {
             const float4 mv = reinterpret_cast<const float4 *>(m_s)[i4];
             x2[2 * i4] = f2_fma(f2_pack(__uint_as_float(r[4 * i4]), __uint_as_float(r[4 * i4 + 1])),
                                 sl2x2, f2_pack(-mv.x, -mv.y));
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+          for (int i = 0; i < kCW / 2; ++i) {
             const int q = 2 * i;
             const float a = (kvalid && q >= qmin) ? fmaf(__uint_as_float(r[q]), P.sl2, -m_s[q]) : -INFINITY;
             const float b = (kvalid && q + 1 >= qmin) ? fmaf(__uint_as_float(r[q + 1]), P.sl2, -m_s[q + 1]) : -INFINITY;
@@ -346,24 +349,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           }
         }
         {
-          float t[16];
+          float t[kCW / 4];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
+          for (int i = 0; i < kCW / 4; ++i) {
             const float2 a = f2_unpack(x2[2 * i]), b = f2_unpack(x2[2 * i + 1]);
             t[i] = fmax3(a.x, a.y, fmaxf(b.x, b.y));
           }
-          mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+          mx = fmax3(t[0], t[1], fmaxf(t[2], t[3]));
         }
         if (named_or(barid, kGroupThreads, mx > 8.0f)) {
           // rare: some score exceeds the running max by > 2^8 (always on the
           // first pair): exact column max over the 128 keys, then rescale
-          float v[32];
+          float v[kCW];
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
+          for (int q = 0; q < kCW; ++q)
             v[q] = (kvalid && q >= qmin) ? __uint_as_float(r[q]) * P.sl2 : -INFINITY;
-          // transpose-reduce within the warp: lane ends with column `lane`
+          // transpose-reduce within the warp: lanes l and l + 16 end with column l & 15
 #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) {
+          for (int o = kCW / 2; o >= 1; o >>= 1) {
             const bool hi = (lane & o) != 0;
 #pragma unroll
             for (int x = 0; x < o; ++x) {
@@ -372,11 +375,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
               v[x] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
             }
           }
-          red[qd * 32 + lane] = v[0];
+          v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 16));
+          if (lane < kCW) red[qd * kCW + lane] = v[0];
           named_sync(barid, kGroupThreads);
-          if (tg < 32) {
+          if (tg < kCW) {
             const int q = tg;
-            const float cm = fmaxf(fmaxf(red[q], red[32 + q]), fmaxf(red[64 + q], red[96 + q]));
+            const float cm = fmaxf(fmaxf(red[q], red[kCW + q]), fmaxf(red[2 * kCW + q], red[3 * kCW + q]));
             const float mo = m_s[q];
             const float mn = fmaxf(mo, cm);
             alpha_s[q] = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
@@ -384,24 +388,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           }
           named_sync(barid, kGroupThreads);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
+          for (int i = 0; i < kCW / 2; ++i)
             l2[i] = f2_mul(l2[i], f2_pack(alpha_s[2 * i], alpha_s[2 * i + 1]));
           if (p > 0) {
             // O^T holds PV(0 .. p-1): wait for the last of them, then scale
             const int gp = g - 1;
             ok = ok && mbar_wait(bar(B_PV + (gp & 1)), (gp >> 1) & 1, abort_flag, kWaitNs);
             tc_fence_after();
-            uint32_t o[32];
-            tmem_ld32(tl + 128 + cb, o);
+            uint32_t o[kCW];
+            tmem_ld16(tl + 128 + cb, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha_s[q]);
-            tmem_st32(tl + 128 + cb, o);
+            for (int q = 0; q < kCW; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha_s[q]);
+            tmem_st16(tl + 128 + cb, o);
             tmem_wait_st();
             tc_fence_before();
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+          for (int i = 0; i < kCW / 2; ++i) {
             const int q = 2 * i;
             const float a = (kvalid && q >= qmin) ? fmaf(__uint_as_float(r[q]), P.sl2, -m_s[q]) : -INFINITY;
             const float b = (kvalid && q + 1 >= qmin) ? fmaf(__uint_as_float(r[q + 1]), P.sl2, -m_s[q + 1]) : -INFINITY;
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         }
         uint8_t *prow = smem + OFF_P + slot * kPBytes + key * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kCW / 8; ++c) {
           uint32_t pk[4];
 #pragma unroll
           for (int z = 0; z < 4; ++z) {
@@ -424,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             l2[4 * c + z] = f2_add(l2[4 * c + z], f2_pack(e0, e1));
             pk[z] = E::from_f2(e0, e1);
           }
-          const int chunk = wg * 4 + c;
+          const int chunk = wg * (kCW / 8) + c;
           *reinterpret_cast<uint4 *>(prow + ((chunk ^ (key & 7)) << 4)) =
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
@@ -433,21 +437,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         mbar_arrive(bar(B_PF + slot));
         mbar_arrive(bar(B_SE + slot));
       }
-      // ---- epilogue: O = O^T / l, LSE = m ln2 + ln l (this group's 32 queries)
+      // ---- epilogue: O = O^T / l, LSE = m ln2 + ln l (this group's kCW queries)
       {
         const int gl = pc + npairs - 1;
         ok = ok && mbar_wait(bar(B_PV + (gl & 1)), (gl >> 1) & 1, abort_flag, kWaitNs);
         tc_fence_after();
         // sum l over the 128 keys
-        float l[32];
+        float l[kCW];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < kCW / 2; ++i) {
           const float2 v = f2_unpack(l2[i]);
           l[2 * i] = v.x;
           l[2 * i + 1] = v.y;
         }
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
+        for (int o = kCW / 2; o >= 1; o >>= 1) {
           const bool hi = (lane & o) != 0;
 #pragma unroll
           for (int x = 0; x < o; ++x) {
@@ -456,11 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             l[x] = keep + __shfl_xor_sync(0xffffffffu, send, o);
           }
         }
-        red[qd * 32 + lane] = l[0];
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], 16);
+        if (lane < kCW) red[qd * kCW + lane] = l[0];
         named_sync(barid, kGroupThreads);
-        if (tg < 32) {
+        if (tg < kCW) {
           const int q = tg;
-          const float lt = (red[q] + red[32 + q]) + (red[64 + q] + red[96 + q]);
+          const float lt = (red[q] + red[kCW + q]) + (red[2 * kCW + q] + red[3 * kCW + q]);
           invl_s[q] = lt > 0.f ? 1.0f / lt : 0.f;
           if (lrow && q < my_rows)
             lrow[q] = lt > 0.f ? m_s[q] * 0.6931471805599453f + logf(lt) : -INFINITY;
@@ -469,11 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         // O^T row `key` (= d), columns cb.. -> staging rows cb.. of [64 q][128 d]
         uint16_t *stage = reinterpret_cast<uint16_t *>(smem + OFF_STAGE);
         {
-          uint32_t r[32];
-          tmem_ld32(tl + 128 + cb, r);
+          uint32_t r[kCW];
+          tmem_ld16(tl + 128 + cb, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
+          for (int q = 0; q < kCW; ++q)
             stage[(cb + q) * kD + key] = E::bits(__uint_as_float(r[q]) * invl_s[q]);
         }
         tc_fence_before();

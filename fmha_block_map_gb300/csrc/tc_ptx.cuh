@@ -170,6 +170,21 @@ FBM_DEVICE void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       FBM_W8(0), FBM_W8(8), FBM_W8(16), FBM_W8(24)
       : "memory");
 }
+// 32 lanes x 16 consecutive 32-bit columns
+FBM_DEVICE void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];\n"
+      : FBM_R8(0), FBM_R8(8)
+      : "r"(taddr));
+}
+FBM_DEVICE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};\n" ::"r"(taddr),
+      FBM_W8(0), FBM_W8(8)
+      : "memory");
+}
 #undef FBM_R8
 #undef FBM_W8
 FBM_DEVICE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
