@@ -18,14 +18,17 @@
 // exceeds it by more than 2^8), so the cross-lane column maximum is needed only
 // on those rare pairs.
 //
-// Roles (one persistent CTA per SM, 18 warps):
+// Roles (one persistent CTA per SM, 19 warps):
 //   warp 0    TMA producer: Q (double buffer), K and V pairs (2-slot rings)
-//   warp 1    TMEM owner and single-thread MMA issuer
+//   warp 1    TMEM owner and single-thread S^T issuer
+//   warp 18   single-thread PV issuer (so S^T never queues behind a PV that
+//             waits for the softmax)
 //   warps 2-17 four softmax + epilogue warpgroups, each owning 16 of the 64
 //             query columns (each group covers TMEM lane quadrants 2, 3, 0, 1:
 //             all 128 keys)
-// Pipeline per q block, pairs p = 0..: S(0); then S(p+1) before PV(p), so the
-// softmax of pair p+1 overlaps the PV MMA of pair p.  Every wait is bounded:
+// Pipeline: S^T(p) is issued once K(p) has landed and its TMEM slot (two
+// slots) is free; PV(p) once P(p) is written.  The softmax of pair p+1
+// overlaps the PV MMA of pair p.  Every wait is bounded:
 // on expiry the kernel raises FBM_DEVERR_TIMEOUT, every role leaves its loop,
 // in-flight copies and MMAs are drained with bounded waits and TMEM is freed.
 //
@@ -67,7 +70,7 @@ constexpr int OFF_M = OFF_INVL + kGroups * kCW * 4;         // float [groups][kC
 constexpr int OFF_BAR = OFF_M + kGroups * kCW * 4;
 enum {
   B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_SE = 14,
-  B_PF = 16, B_PV = 18, B_OF = 20, B_DRAIN = 21, NBAR = 22
+  B_PF = 16, B_PV = 18, B_OF = 20, B_DRAIN = 21, B_DRAIN2 = 22, NBAR = 23
 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // [0] tmem base, [1] abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 16;
@@ -76,7 +79,8 @@ constexpr uint32_t kTmemCols = 256;                // S0 @0, S1 @64, O @128
 constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
 constexpr int kGroupThreads = 128;                 // one softmax warpgroup
 constexpr int kSoftmaxThreads = kGroups * kGroupThreads;
-constexpr int kThreads = 64 + kSoftmaxThreads;     // + producer warp + MMA warp
+constexpr int kPvWarp = 2 + kSoftmaxThreads / 32;  // the PV issuer follows the softmax warps
+constexpr int kThreads = 64 + kSoftmaxThreads + 32; // + producer, S^T issuer, PV issuer
 
 struct TcParams {
   CUtensorMap tq, tk, tv;
@@ -205,14 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       if (!ok) fail(FBM_DEVERR_TIMEOUT);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S^T issuer
+    // S^T(g) runs as soon as its K pair is loaded and its TMEM slot is free;
+    // it never waits for P, so it stays ahead of the softmax.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(kBf16, false, false, 128, 64);
-      constexpr uint32_t idO = idesc_f16(kBf16, true, true, 128, 64);
-      const uint32_t tO = tbase + 128;
       int pc = 0, uc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
+      for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
         const Unit U = unit_of(P, u);
         if (U.n == 0) continue;
         const int npairs = (U.n + 1) >> 1;
@@ -220,10 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         if (!(ok = mbar_wait(bar(B_QF + qb), (uc >> 1) & 1, abort_flag, kWaitNs))) break;
         tc_fence_after();
         const uint32_t qaddr = sbase + OFF_Q + qb * kQBytes;
-        auto issue_S = [&](int p) -> bool {
+        for (int p = 0; p < npairs; ++p) {
           const int g = pc + p, slot = g & 1;
-          if (!mbar_wait(bar(B_KF + slot), (g >> 1) & 1, abort_flag, kWaitNs)) return false;
-          if (!mbar_wait(bar(B_SE + slot), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs)) return false;
+          if (!(ok = mbar_wait(bar(B_KF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
+          if (!(ok = mbar_wait(bar(B_SE + slot), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs))) break;
           tc_fence_after();
           const uint32_t kaddr = sbase + OFF_K + slot * kPairBytes;
 #pragma unroll
@@ -234,15 +238,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           }
           mma_commit(bar(B_SF + slot));
           mma_commit(bar(B_KE + slot));
-          return true;
-        };
-        if (!(ok = issue_S(0))) break;
-        for (int p = 0; p < npairs && ok; ++p) {
-          if (p + 1 < npairs) {
-            if (!(ok = issue_S(p + 1))) break;
-          } else {
-            mma_commit(bar(B_QE + qb));
-          }
+        }
+        if (ok) mma_commit(bar(B_QE + qb));  // Q free once every S^T of the row is done
+        pc += npairs;
+        uc += 1;
+      }
+      if (!ok) fail(FBM_DEVERR_TIMEOUT);
+      // drain: every MMA this thread issued has completed before TMEM is freed
+      mma_commit(bar(B_DRAIN));
+      if (!mbar_wait_for(bar(B_DRAIN), 0, kWaitNs)) set_error(P.err, FBM_DEVERR_TIMEOUT);
+    }
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t idO = idesc_f16(kBf16, true, true, 128, 64);
+      const uint32_t tO = tbase + 128;
+      int pc = 0, uc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+        const Unit U = unit_of(P, u);
+        if (U.n == 0) continue;
+        const int npairs = (U.n + 1) >> 1;
+        for (int p = 0; p < npairs; ++p) {
           const int g = pc + p, slot = g & 1;
           if (!(ok = mbar_wait(bar(B_PF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
           if (!(ok = mbar_wait(bar(B_VF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
@@ -263,9 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         uc += 1;
       }
       if (!ok) fail(FBM_DEVERR_TIMEOUT);
-      // drain: every MMA issued so far has completed before TMEM is freed
-      mma_commit(bar(B_DRAIN));
-      if (!mbar_wait_for(bar(B_DRAIN), 0, kWaitNs)) set_error(P.err, FBM_DEVERR_TIMEOUT);
+      mma_commit(bar(B_DRAIN2));
+      if (!mbar_wait_for(bar(B_DRAIN2), 0, kWaitNs)) set_error(P.err, FBM_DEVERR_TIMEOUT);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
