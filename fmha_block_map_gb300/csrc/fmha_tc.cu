@@ -18,8 +18,9 @@
 // exceeds it by more than 2^8), so the cross-lane column maximum is needed only
 // on those rare pairs.
 //
-// Roles (one persistent CTA per SM, 19 warps):
-//   warp 0    TMA producer: Q (double buffer), K and V pairs (2-slot rings)
+// Roles (one persistent CTA per SM, 20 warps):
+//   warp 0    TMA producer of Q (double buffer) and K pairs (2-slot ring)
+//   warp 19   TMA producer of V pairs (2-slot ring)
 //   warp 1    TMEM owner and single-thread S^T issuer
 //   warp 18   single-thread PV issuer (so S^T never queues behind a PV that
 //             waits for the softmax)
@@ -80,7 +81,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
 constexpr int kGroupThreads = 128;                 // one softmax warpgroup
 constexpr int kSoftmaxThreads = kGroups * kGroupThreads;
 constexpr int kPvWarp = 2 + kSoftmaxThreads / 32;  // the PV issuer follows the softmax warps
-constexpr int kThreads = 64 + kSoftmaxThreads + 32; // + producer, S^T issuer, PV issuer
+constexpr int kVWarp = kPvWarp + 1;                 // then the V producer
+constexpr int kThreads = 64 + kSoftmaxThreads + 64; // + Q/K producer, S^T issuer, PV issuer, V producer
 
 struct TcParams {
   CUtensorMap tq, tk, tv;
@@ -154,12 +156,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     *abort_flag = 1;
   };
 
+  // K or V pair g (= pc + p) of a q block into its ring slot, once the MMA that
+  // last read the slot has completed
+  auto load_pair = [&](const Unit &U, int pc, int p, bool is_v) -> bool {
+    const int g = pc + p, slot = g & 1;
+    const int fb = (is_v ? B_VF : B_KF) + slot, eb = (is_v ? B_VE : B_KE) + slot;
+    if (!mbar_wait(bar(eb), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs)) return false;
+    int js[2] = {-1, -1};
+    uint32_t bytes = 0;
+    for (int hf = 0; hf < 2; ++hf) {
+      const int t = 2 * p + hf;
+      if (t >= U.n) break;
+      int j = entry_of(U, t);
+      if (j < 0 || j >= P.nk) {
+        // out of range: flagged; block 0 is fetched in its place so that the
+        // masked keys (P = 0) meet finite V rows
+        set_error(P.err, FBM_DEVERR_LUT_RANGE);
+        j = 0;
+      }
+      js[hf] = j;
+      bytes += 2 * kQChunk;
+    }
+    mbar_arrive_tx(bar(fb), bytes);
+    const uint32_t dst0 = sbase + (is_v ? OFF_V : OFF_K) + slot * kPairBytes;
+    for (int hf = 0; hf < 2; ++hf) {
+      if (js[hf] < 0) continue;
+      for (int c = 0; c < 2; ++c)
+        tma_load_3d(dst0 + c * kPairChunk + hf * kQChunk, is_v ? &P.tv : &P.tk, c * 64,
+                    js[hf] * 64, U.bh_k, bar(fb));
+    }
+    return true;
+  };
+
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
       int pc = 0, uc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
+      for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
         const Unit U = unit_of(P, u);
         if (U.n == 0) continue;
         const int npairs = (U.n + 1) >> 1;
@@ -169,42 +203,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         for (int c = 0; c < 2; ++c)
           tma_load_3d(sbase + OFF_Q + qb * kQBytes + c * kQChunk, &P.tq, c * 64, U.i * 64,
                       U.bh_q, bar(B_QF + qb));
-        auto load_pair = [&](int p, bool is_v) -> bool {
-          const int g = pc + p, slot = g & 1;
-          const int fb = (is_v ? B_VF : B_KF) + slot, eb = (is_v ? B_VE : B_KE) + slot;
-          if (!mbar_wait(bar(eb), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs)) return false;
-          int js[2] = {-1, -1};
-          uint32_t bytes = 0;
-          for (int hf = 0; hf < 2; ++hf) {
-            const int t = 2 * p + hf;
-            if (t >= U.n) break;
-            int j = entry_of(U, t);
-            if (j < 0 || j >= P.nk) {
-              // out of range: flagged; block 0 is fetched in its place so that the
-              // masked keys (P = 0) meet finite V rows
-              set_error(P.err, FBM_DEVERR_LUT_RANGE);
-              j = 0;
-            }
-            js[hf] = j;
-            bytes += 2 * kQChunk;
-          }
-          mbar_arrive_tx(bar(fb), bytes);
-          const uint32_t dst0 = sbase + (is_v ? OFF_V : OFF_K) + slot * kPairBytes;
-          for (int hf = 0; hf < 2; ++hf) {
-            if (js[hf] < 0) continue;
-            for (int c = 0; c < 2; ++c)
-              tma_load_3d(dst0 + c * kPairChunk + hf * kQChunk, is_v ? &P.tv : &P.tk, c * 64,
-                          js[hf] * 64, U.bh_k, bar(fb));
-          }
-          return true;
-        };
-        if (!(ok = load_pair(0, false))) break;
-        for (int p = 0; p < npairs && ok; ++p) {
-          if (p + 1 < npairs) ok = load_pair(p + 1, false);
-          if (ok) ok = load_pair(p, true);
-        }
+        for (int p = 0; p < npairs && ok; ++p) ok = load_pair(U, pc, p, false);
         pc += npairs;
         uc += 1;
+      }
+      if (!ok) fail(FBM_DEVERR_TIMEOUT);
+    }
+  } else if (warp == kVWarp) {
+    // ------------------------------------------------------------ V producer
+    // (its own thread, so a K load never waits behind a V slot that a late PV
+    // still holds)
+    if (lane == 0) {
+      int pc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+        const Unit U = unit_of(P, u);
+        if (U.n == 0) continue;
+        const int npairs = (U.n + 1) >> 1;
+        for (int p = 0; p < npairs && ok; ++p) ok = load_pair(U, pc, p, true);
+        pc += npairs;
       }
       if (!ok) fail(FBM_DEVERR_TIMEOUT);
     }
