@@ -62,7 +62,7 @@ constexpr int OFF_K = OFF_Q + 2 * kQBytes;
 constexpr int OFF_V = OFF_K + 2 * kPairBytes;
 constexpr int OFF_P = OFF_V + 2 * kPairBytes;
 constexpr int OFF_STAGE = OFF_P + 2 * kPBytes;   // 16 KB: output staging [64 q][128 d]
-constexpr int kGroups = 4;                         // softmax warpgroups per CTA
+constexpr int kGroups = 2;                         // softmax warpgroups per CTA
 constexpr int kCW = 64 / kGroups;                  // query columns per group
 constexpr int OFF_RED = OFF_STAGE + kQBytes;       // float [groups][4 quadrants][kCW]
 constexpr int OFF_ALPHA = OFF_RED + kGroups * 4 * kCW * 4;  // float [groups][kCW]
@@ -83,6 +83,18 @@ constexpr int kSoftmaxThreads = kGroups * kGroupThreads;
 constexpr int kPvWarp = 2 + kSoftmaxThreads / 32;  // the PV issuer follows the softmax warps
 constexpr int kVWarp = kPvWarp + 1;                 // then the V producer
 constexpr int kThreads = 64 + kSoftmaxThreads + 64; // + Q/K producer, S^T issuer, PV issuer, V producer
+
+// N consecutive TMEM columns of 32 lanes (a query group's columns)
+template <int N>
+FBM_DEVICE void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 16) tmem_ld16(taddr, r);
+  else tmem_ld32(taddr, r);
+}
+template <int N>
+FBM_DEVICE void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 16) tmem_st16(taddr, r);
+  else tmem_st32(taddr, r);
+}
 
 struct TcParams {
   CUtensorMap tq, tk, tv;
@@ -359,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         ok = ok && mbar_wait(bar(B_SF + slot), (g >> 1) & 1, abort_flag, kWaitNs);
         tc_fence_after();
         uint32_t r[kCW];
-        tmem_ld16(tl + slot * 64 + cb, r);
+        tmem_ld_cols(tl + slot * 64 + cb, r);
         tmem_wait_ld();
         uint64_t x2[kCW / 2];
         float mx;
@@ -388,7 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             const float2 a = f2_unpack(x2[2 * i]), b = f2_unpack(x2[2 * i + 1]);
             t[i] = fmax3(a.x, a.y, fmaxf(b.x, b.y));
           }
-          mx = fmax3(t[0], t[1], fmaxf(t[2], t[3]));
+          mx = t[0];
+#pragma unroll
+          for (int i = 1; i < kCW / 4; i += 2)
+            mx = (i + 1 < kCW / 4) ? fmax3(mx, t[i], t[i + 1]) : fmaxf(mx, t[i]);
         }
         if (named_or(barid, kGroupThreads, mx > 8.0f)) {
           // rare: some score exceeds the running max by > 2^8 (always on the
@@ -408,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
               v[x] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
             }
           }
-          v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 16));
+          if constexpr (kCW == 16) v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 16));
           if (lane < kCW) red[qd * kCW + lane] = v[0];
           named_sync(barid, kGroupThreads);
           if (tg < kCW) {
@@ -429,11 +444,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             ok = ok && mbar_wait(bar(B_PV + (gp & 1)), (gp >> 1) & 1, abort_flag, kWaitNs);
             tc_fence_after();
             uint32_t o[kCW];
-            tmem_ld16(tl + 128 + cb, o);
+            tmem_ld_cols(tl + 128 + cb, o);
             tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < kCW; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha_s[q]);
-            tmem_st16(tl + 128 + cb, o);
+            tmem_st_cols(tl + 128 + cb, o);
             tmem_wait_st();
             tc_fence_before();
           }
@@ -493,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             l[x] = keep + __shfl_xor_sync(0xffffffffu, send, o);
           }
         }
-        l[0] += __shfl_xor_sync(0xffffffffu, l[0], 16);
+        if constexpr (kCW == 16) l[0] += __shfl_xor_sync(0xffffffffu, l[0], 16);
         if (lane < kCW) red[qd * kCW + lane] = l[0];
         named_sync(barid, kGroupThreads);
         if (tg < kCW) {
@@ -508,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         uint16_t *stage = reinterpret_cast<uint16_t *>(smem + OFF_STAGE);
         {
           uint32_t r[kCW];
-          tmem_ld16(tl + 128 + cb, r);
+          tmem_ld_cols(tl + 128 + cb, r);
           tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < kCW; ++q)
