@@ -62,7 +62,7 @@ constexpr int OFF_K = OFF_Q + 2 * kQBytes;
 constexpr int OFF_V = OFF_K + 2 * kPairBytes;
 constexpr int OFF_P = OFF_V + 2 * kPairBytes;
 constexpr int OFF_STAGE = OFF_P + 2 * kPBytes;   // 16 KB: output staging [64 q][128 d]
-constexpr int kGroups = 2;                         // softmax warpgroups per CTA
+constexpr int kGroups = 4;                         // softmax warpgroups per CTA
 constexpr int kCW = 64 / kGroups;                  // query columns per group
 constexpr int OFF_RED = OFF_STAGE + kQBytes;       // float [groups][4 quadrants][kCW]
 constexpr int OFF_ALPHA = OFF_RED + kGroups * 4 * kCW * 4;  // float [groups][kCW]
