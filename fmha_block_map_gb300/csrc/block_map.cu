@@ -360,16 +360,20 @@ FBM_DEVICE void select_rows(const SelectArgs &a, const HeadParams &hp, int bi, i
 // k_block_map: the two passes fused into one persistent cooperative kernel
 // ---------------------------------------------------------------------------
 //
-// Work items, taken in order by a grid that is resident all at once:
-//   pool items   8 blocks each (a warp per block), ordered by KV head: the K
-//                blocks of KV head (b, g), then the Q blocks of its query heads;
-//   select items one per 32 q blocks of a query head, in the same head order.
+// Work items, taken round-robin in one global order by a grid that is resident
+// all at once (cooperative launch):
+//   pool items   8 blocks each (a warp per block) of one KV group: the K blocks
+//                of KV head (b, g), then the Q blocks of its query heads;
+//   select items one per 32 q blocks of a query head.
+// The order walks the KV groups: step t holds the pool items of group t, then
+// the select items of group t - L, L groups behind (about one wave of the grid).
 // A pool warp publishes each finished block by a release increment of its
 // head's counter; a select item first waits (acquire, bounded) until its query
-// head has nq pooled Q blocks and its KV head nk pooled K blocks.  Every pool
-// item precedes every select item in each CTA's sequence, so no select item
-// waits on work that a waiting CTA still owns; the selection of early heads
-// runs while later heads are still being pooled.
+// head has nq pooled Q blocks and its KV head nk pooled K blocks.  A select
+// item only depends on pool items earlier in the order, so the earliest waiting
+// select item always has its producers running: no deadlock, and the
+// compute-bound selection of early groups overlaps the memory-bound pooling of
+// later ones.
 
 struct FusedArgs {
   PoolSide qs, ks;
@@ -378,8 +382,36 @@ struct FusedArgs {
   int *kdone;   // [b * hk] pooled K blocks per KV head
   int *abort;   // raised when a wait expires
   uint32_t *err;
-  int pool_items, sel_items, sel_groups;  // sel_groups = ceil(nq / 32)
+  int groups;         // b * hk KV groups
+  int pool_per_group; // ceil((nk + ratio * nq) / 8)
+  int sel_per_group;  // ratio * sel_groups
+  int sel_groups;     // ceil(nq / 32)
+  int lag;            // select items trail their pool items by `lag` groups
+  int items;          // groups * (pool_per_group + sel_per_group)
 };
+
+// Item `it` of the global order -> (is_pool, group, index within the group's
+// pool or select items).
+FBM_DEVICE void item_of(const FusedArgs &f, int it, bool &is_pool, int &grp, int &k) {
+  const int Pg = f.pool_per_group, Sg = f.sel_per_group, G = f.groups;
+  const int A = min(f.lag, G);  // leading steps with pool items only
+  if (it < A * Pg) {
+    is_pool = true; grp = it / Pg; k = it - grp * Pg;
+    return;
+  }
+  it -= A * Pg;
+  const int B = G - A;          // steps with pool items of group t and selects of t - lag
+  if (it < B * (Pg + Sg)) {
+    const int t = A + it / (Pg + Sg), r = it % (Pg + Sg);
+    if (r < Pg) { is_pool = true; grp = t; k = r; }
+    else { is_pool = false; grp = t - f.lag; k = r - Pg; }
+    return;
+  }
+  it -= B * (Pg + Sg);          // trailing select items of the last groups
+  is_pool = false;
+  grp = (G - A) + it / Sg;
+  k = it % Sg;
+}
 
 FBM_DEVICE int ld_acquire(const int *p) {
   int v;
@@ -403,13 +435,15 @@ __global__ void __launch_bounds__(256, (NT <= 8 ? 2 : 1)) k_block_map(const __gr
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const SelectArgs &a = f.a;
   const int ratio = a.hq / a.hk;
-  const int seg = a.nk + ratio * a.nq;  // pool blocks per KV head
-  const int pool_blocks = a.b * a.hk * seg;
-  for (int it = blockIdx.x; it < f.pool_items + f.sel_items; it += gridDim.x) {
-    if (it < f.pool_items) {
-      const int blk = it * 8 + warp;
-      if (blk < pool_blocks) {
-        const int bg = blk / seg, off = blk - bg * seg;  // bg = b * hk + g
+  const int seg = a.nk + ratio * a.nq;  // pool blocks per KV group
+  for (int it = blockIdx.x; it < f.items; it += gridDim.x) {
+    bool is_pool;
+    int grp, k;
+    item_of(f, it, is_pool, grp, k);
+    if (is_pool) {
+      const int off = k * 8 + warp;
+      if (off < seg) {
+        const int bg = grp;  // bg = b * hk + g
         if (off < a.nk) {
           pool_block<E, D>(f.ks, bg * a.nk + off, lane);
           __threadfence();  // every lane's pooled values are visible before the count
@@ -426,10 +460,9 @@ __global__ void __launch_bounds__(256, (NT <= 8 ? 2 : 1)) k_block_map(const __gr
         }
       }
     } else {
-      const int sidx = it - f.pool_items;
-      const int bh = sidx / f.sel_groups, ig = sidx - bh * f.sel_groups;
-      const int b = bh / a.hq, h = bh - b * a.hq;
-      const int bg = b * a.hk + h / ratio;
+      const int bg = grp, b = bg / a.hk, g = bg - b * a.hk;
+      const int hr = k / f.sel_groups, ig = k - hr * f.sel_groups;
+      const int h = g * ratio + hr, bh = b * a.hq + h;
       if (threadIdx.x == 0) {
         const uint64_t t0 = gtimer();
         int ok = 1;
@@ -472,8 +505,9 @@ static cudaError_t launch_fused(FusedArgs f, const HeadParams &hp, cudaStream_t 
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem)) != cudaSuccess)
     return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int items = f.pool_items + f.sel_items;
-  const int grid = std::min(items, per_sm * sms);
+  const int grid = std::min(f.items, per_sm * sms);
+  // selects trail their pool items by about one wave of the grid (plus one group)
+  f.lag = std::min(f.groups, (grid + f.pool_per_group - 1) / f.pool_per_group + 1);
   void *args[] = {&f, const_cast<HeadParams *>(&hp)};
   // cooperative: the whole grid is resident, which the head counters rely on
   return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(kern), dim3(grid), dim3(256), args,
@@ -502,10 +536,11 @@ cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
   f.abort = L.sync + L.b * L.hq + L.b * L.hk;
   f.err = L.err;
   const int ratio = L.hq / L.hk;
-  const long long pool_blocks = (long long)L.b * L.hk * (L.nk + ratio * L.nq);
-  f.pool_items = (int)((pool_blocks + 7) / 8);
+  f.groups = L.b * L.hk;
+  f.pool_per_group = (L.nk + ratio * L.nq + 7) / 8;
   f.sel_groups = (L.nq + kSelRows - 1) / kSelRows;
-  f.sel_items = L.b * L.hq * f.sel_groups;
+  f.sel_per_group = ratio * f.sel_groups;
+  f.items = f.groups * (f.pool_per_group + f.sel_per_group);
   cudaError_t e = cudaMemsetAsync(L.sync, 0, sizeof(int) * (L.b * L.hq + L.b * L.hk + 1), st);
   if (e != cudaSuccess) return e;
   if (L.d == 128) return L.bf16 ? launch_nt<BF16, 128>(f, L.hp, st) : launch_nt<F16, 128>(f, L.hp, st);
