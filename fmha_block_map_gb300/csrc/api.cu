@@ -56,7 +56,7 @@ fbm_status cuda_status(cudaError_t e, const char *what) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t qbar, qsim, kbar, ksim, sync, total;
+  size_t qbar, qsim, kbar, ksim, total;
 };
 
 WsLayout ws_layout(int b, int hq, int hk, int s, int d) {
@@ -67,7 +67,6 @@ WsLayout ws_layout(int b, int hq, int hk, int s, int d) {
   w.qsim = off; off = align256(off + sizeof(float) * b * hq * nq);
   w.kbar = off; off = align256(off + sizeof(float) * b * hk * nk * d);
   w.ksim = off; off = align256(off + sizeof(float) * b * hk * nk);
-  w.sync = off; off = align256(off + sizeof(int) * (b * hq + b * hk + 1));
   w.total = off;
   return w;
 }
@@ -163,9 +162,6 @@ fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int 
   L.qsim = reinterpret_cast<float *>(ws + w.qsim);
   L.kbar = reinterpret_cast<float *>(ws + w.kbar);
   L.ksim = reinterpret_cast<float *>(ws + w.ksim);
-  L.sync = reinterpret_cast<int *>(ws + w.sync);
-  L.err = error_word();
-  if (!L.err) return fail(FBM_ERR_CUDA, "sparge_block_map: error word lookup failed");
   L.lut = lut; L.cnt = lut_count; L.bmap = block_map;
   return cuda_status(fbm::launch_block_map(L, static_cast<cudaStream_t>(stream)),
                      "sparge_block_map launch");

@@ -1,22 +1,20 @@
 // Block-map prediction kernels ("Sparge Attention (Composable Kernel)" README:
 // mean-pool -> cosine sim -> pooled QK -> top-k / cdfthreshd LUT).
 //
-//  pool pass      one warp per 64-token block of Q or K: each lane streams 32
+//  k_pool_sim     one warp per 64-token block of Q or K: each lane streams 32
 //                 bytes of a row per step (128-bit loads, 16 in flight per
 //                 lane), row norms by a 3-level shuffle, fp32 row sums (the
 //                 pooled mean, two interleaved partial sums per element) and the
 //                 sum of unit rows (self-similarity = ||sum u||^2 / n^2).
 //                 HBM-bound: it reads Q and K once and writes (d + 1) floats
 //                 per block.
-//  select pass    one CTA per 32 q blocks of one (batch, head): pooled scores
+//  k_score_select one CTA per 32 q blocks of one (batch, head): pooled scores
 //                 by an fp32 4x4 register-tiled product (K-block means streamed
 //                 through double-buffered shared memory in 32-dimension chunks
 //                 by cp.async, shared by the 32 rows), then one warp per row for
 //                 the pooled softmax, a radix (bitwise) threshold search for
 //                 top-k / cdf, and ballot-scan emission of the ascending LUT
 //                 row.  No atomics take part in slot assignment.
-#include <algorithm>
-
 #include "common.cuh"
 #include "kernels.h"
 
@@ -35,16 +33,19 @@ struct PoolSide {
   int nunits;         // bh * nb
 };
 
-// One warp pools block `unit` of `side`: pooled mean (d floats) and
-// self-similarity.
 template <class E, int D>
-FBM_DEVICE void pool_block(const PoolSide &side, int unit, int lane) {
+__global__ void __launch_bounds__(256, 2) k_pool_sim(PoolSide qs, PoolSide ks) {
   // a lane owns 16 consecutive elements (32 bytes) of a row; a row spans LPR
   // lanes and one warp-wide step covers RPI rows
   constexpr int LPR = D / 16;
   constexpr int RPI = 32 / LPR;
   constexpr int STEPS = kBlk / RPI;
   constexpr int UNR = 8;  // 16 loads (256 B) in flight per lane
+  const int lane = threadIdx.x & 31;
+  const int unit_all = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (unit_all >= qs.nunits + ks.nunits) return;
+  const PoolSide &side = unit_all < qs.nunits ? qs : ks;
+  const int unit = unit_all < qs.nunits ? unit_all : unit_all - qs.nunits;
   const int bh = unit / side.nb;
   const int j = unit - bh * side.nb;
   const int row0 = j * kBlk;
@@ -138,10 +139,9 @@ FBM_DEVICE uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One CTA scores and selects the q blocks i0 .. i0+31 of (batch bi, query head h).
 template <int D, int NT>
-FBM_DEVICE void select_rows(const SelectArgs &a, const HeadParams &hp, int bi, int h, int i0,
-                            float *smem) {
+__global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
+  extern __shared__ __align__(16) float smem[];
   constexpr int LDQ = D + 4;
   constexpr int NCH = D / kSelDC;                    // d chunks per column tile
   float *q_s = smem;                                 // [32][LDQ]
@@ -149,8 +149,10 @@ FBM_DEVICE void select_rows(const SelectArgs &a, const HeadParams &hp, int bi, i
   float *S_s = k_s + 2 * kSelCols * kSelLDK;         // [32][NT * 32]
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y, bi = blockIdx.z;
   const int ratio = a.hq / a.hk;
   const int g = h / ratio;
+  const int i0 = blockIdx.x * kSelRows;
   const float *qbar = a.qbar + ((size_t)(bi * a.hq + h) * a.nq) * D;
   const float *kbar = a.kbar + ((size_t)(bi * a.hk + g) * a.nk) * D;
   const float *qsim = a.qsim + (size_t)(bi * a.hq + h) * a.nq;
@@ -175,7 +177,7 @@ FBM_DEVICE void select_rows(const SelectArgs &a, const HeadParams &hp, int bi, i
   for (int idx = tid; idx < kSelRows * (D / 4); idx += 256) {
     const int r = idx / (D / 4), c4 = idx % (D / 4);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i0 + r < a.nq) v = __ldcg(reinterpret_cast<const float4 *>(qbar + (size_t)(i0 + r) * D) + c4);
+    if (i0 + r < a.nq) v = reinterpret_cast<const float4 *>(qbar + (size_t)(i0 + r) * D)[c4];
     *reinterpret_cast<float4 *>(q_s + r * LDQ + c4 * 4) = v;
   }
   // 4 x 4 register tile: rows tr*4 .. +3, columns tc + 32 m
@@ -236,7 +238,7 @@ FBM_DEVICE void select_rows(const SelectArgs &a, const HeadParams &hp, int bi, i
     const int i = i0 + rr;
     if (i >= a.nq) break;
     const float theta = hp.theta[h];
-    const bool q_similar = __ldcg(qsim + i) > theta;
+    const bool q_similar = qsim[i] > theta;
     const int last_q = (i + 1) * a.blkq - 1;
     const int n_elig = a.causal ? min(a.nk, last_q / a.blkk + 1) : a.nk;
     float sc[NT];
@@ -249,7 +251,7 @@ FBM_DEVICE void select_rows(const SelectArgs &a, const HeadParams &hp, int bi, i
       const int j = lane + 32 * t;
       const bool valid = j < a.nk;
       elig[t] = valid && (!a.causal || j * a.blkk <= last_q);
-      ksim_ok[t] = valid && __ldcg(ksim + j) > theta;
+      ksim_ok[t] = valid && ksim[j] > theta;
       const bool fin = elig[t] && ksim_ok[t];
       sc[t] = valid ? S_s[rr * (NT * 32) + j] : 0.f;
       key[t] = fin ? order_key(sc[t]) : 0u;
@@ -357,135 +359,7 @@ FBM_DEVICE void select_rows(const SelectArgs &a, const HeadParams &hp, int bi, i
 }
 
 // ---------------------------------------------------------------------------
-// k_block_map: the two passes fused into one persistent cooperative kernel
-// ---------------------------------------------------------------------------
-//
-// Work items, taken round-robin in one global order by a grid that is resident
-// all at once (cooperative launch):
-//   pool items   8 blocks each (a warp per block) of one KV group: the K blocks
-//                of KV head (b, g), then the Q blocks of its query heads;
-//   select items one per 32 q blocks of a query head.
-// The order walks the KV groups: step t holds the pool items of group t, then
-// the select items of group t - L, L groups behind (about one wave of the grid).
-// A pool warp publishes each finished block by a release increment of its
-// head's counter; a select item first waits (acquire, bounded) until its query
-// head has nq pooled Q blocks and its KV head nk pooled K blocks.  A select
-// item only depends on pool items earlier in the order, so the earliest waiting
-// select item always has its producers running: no deadlock, and the
-// compute-bound selection of early groups overlaps the memory-bound pooling of
-// later ones.
-
-struct FusedArgs {
-  PoolSide qs, ks;
-  SelectArgs a;
-  int *qdone;   // [b * hq] pooled Q blocks per query head
-  int *kdone;   // [b * hk] pooled K blocks per KV head
-  int *abort;   // raised when a wait expires
-  uint32_t *err;
-  int groups;         // b * hk KV groups
-  int pool_per_group; // ceil((nk + ratio * nq) / 8)
-  int sel_per_group;  // ratio * sel_groups
-  int sel_groups;     // ceil(nq / 32)
-  int lag;            // select items trail their pool items by `lag` groups
-  int items;          // groups * (pool_per_group + sel_per_group)
-};
-
-// Item `it` of the global order -> (is_pool, group, index within the group's
-// pool or select items).
-FBM_DEVICE void item_of(const FusedArgs &f, int it, bool &is_pool, int &grp, int &k) {
-  const int Pg = f.pool_per_group, Sg = f.sel_per_group, G = f.groups;
-  const int A = min(f.lag, G);  // leading steps with pool items only
-  if (it < A * Pg) {
-    is_pool = true; grp = it / Pg; k = it - grp * Pg;
-    return;
-  }
-  it -= A * Pg;
-  const int B = G - A;          // steps with pool items of group t and selects of t - lag
-  if (it < B * (Pg + Sg)) {
-    const int t = A + it / (Pg + Sg), r = it % (Pg + Sg);
-    if (r < Pg) { is_pool = true; grp = t; k = r; }
-    else { is_pool = false; grp = t - f.lag; k = r - Pg; }
-    return;
-  }
-  it -= B * (Pg + Sg);          // trailing select items of the last groups
-  is_pool = false;
-  grp = (G - A) + it / Sg;
-  k = it % Sg;
-}
-
-FBM_DEVICE int ld_acquire(const int *p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-FBM_DEVICE void red_release_add(int *p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
-}
-FBM_DEVICE uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-  return t;
-}
-
-template <class E, int D, int NT>
-__global__ void __launch_bounds__(256, (NT <= 8 ? 2 : 1)) k_block_map(const __grid_constant__ FusedArgs f,
-                                                  const __grid_constant__ HeadParams hp) {
-  extern __shared__ __align__(16) float smem[];
-  __shared__ int go;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const SelectArgs &a = f.a;
-  const int ratio = a.hq / a.hk;
-  const int seg = a.nk + ratio * a.nq;  // pool blocks per KV group
-  for (int it = blockIdx.x; it < f.items; it += gridDim.x) {
-    bool is_pool;
-    int grp, k;
-    item_of(f, it, is_pool, grp, k);
-    if (is_pool) {
-      const int off = k * 8 + warp;
-      if (off < seg) {
-        const int bg = grp;  // bg = b * hk + g
-        if (off < a.nk) {
-          pool_block<E, D>(f.ks, bg * a.nk + off, lane);
-          __threadfence();  // every lane's pooled values are visible before the count
-          __syncwarp();
-          if (lane == 0) red_release_add(f.kdone + bg, 1);
-        } else {
-          const int b = bg / a.hk, g = bg - b * a.hk;
-          const int r = (off - a.nk) / a.nq, i = (off - a.nk) - r * a.nq;
-          const int bh = b * a.hq + g * ratio + r;
-          pool_block<E, D>(f.qs, bh * a.nq + i, lane);
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) red_release_add(f.qdone + bh, 1);
-        }
-      }
-    } else {
-      const int bg = grp, b = bg / a.hk, g = bg - b * a.hk;
-      const int hr = k / f.sel_groups, ig = k - hr * f.sel_groups;
-      const int h = g * ratio + hr, bh = b * a.hq + h;
-      if (threadIdx.x == 0) {
-        const uint64_t t0 = gtimer();
-        int ok = 1;
-        while (ld_acquire(f.qdone + bh) < a.nq || ld_acquire(f.kdone + bg) < a.nk) {
-          if (ld_acquire(f.abort) || gtimer() - t0 > 2000000000ull) {
-            set_error(f.err, FBM_DEVERR_TIMEOUT);
-            atomicExch(f.abort, 1);
-            ok = 0;
-            break;
-          }
-          __nanosleep(200);
-        }
-        go = ok;
-      }
-      __syncthreads();
-      if (go) select_rows<D, NT>(a, hp, b, h, ig * kSelRows, smem);
-      __syncthreads();
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// host launcher
+// host launchers
 // ---------------------------------------------------------------------------
 
 size_t block_map_smem_bytes(int d, int nt) {
@@ -493,58 +367,45 @@ size_t block_map_smem_bytes(int d, int nt) {
                           (size_t)kSelRows * nt * 32);
 }
 
-template <class E, int D, int NT>
-static cudaError_t launch_fused(FusedArgs f, const HeadParams &hp, cudaStream_t st) {
-  auto kern = k_block_map<E, D, NT>;
+template <int D, int NT>
+static cudaError_t launch_select(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {
   const size_t smem = block_map_smem_bytes(D, NT);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(k_score_select<D, NT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0, per_sm = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem)) != cudaSuccess)
-    return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int grid = std::min(f.items, per_sm * sms);
-  // selects trail their pool items by about one wave of the grid (plus one group)
-  f.lag = std::min(f.groups, (grid + f.pool_per_group - 1) / f.pool_per_group + 1);
-  void *args[] = {&f, const_cast<HeadParams *>(&hp)};
-  // cooperative: the whole grid is resident, which the head counters rely on
-  return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(kern), dim3(grid), dim3(256), args,
-                                     smem, st);
+  dim3 grid((a.nq + kSelRows - 1) / kSelRows, a.hq, a.b);
+  k_score_select<D, NT><<<grid, 256, smem, st>>>(a, hp);
+  return cudaGetLastError();
 }
 
-template <class E, int D>
-static cudaError_t launch_nt(const FusedArgs &f, const HeadParams &hp, cudaStream_t st) {
-  if (f.a.nk <= 256) return launch_fused<E, D, 8>(f, hp, st);
-  if (f.a.nk <= 512) return launch_fused<E, D, 16>(f, hp, st);
-  return launch_fused<E, D, 32>(f, hp, st);
+template <int D>
+static cudaError_t launch_select_nt(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {
+  if (a.nk <= 256) return launch_select<D, 8>(a, hp, st);
+  if (a.nk <= 512) return launch_select<D, 16>(a, hp, st);
+  return launch_select<D, 32>(a, hp, st);
 }
 
 cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
-  FusedArgs f{};
-  f.qs = PoolSide{static_cast<const uint16_t *>(L.q), L.qbar, L.qsim, L.s, L.nq, L.b * L.hq * L.nq};
-  f.ks = PoolSide{static_cast<const uint16_t *>(L.k), L.kbar, L.ksim, L.s, L.nk, L.b * L.hk * L.nk};
-  SelectArgs &a = f.a;
+  PoolSide qs{static_cast<const uint16_t *>(L.q), L.qbar, L.qsim, L.s, L.nq, L.b * L.hq * L.nq};
+  PoolSide ks{static_cast<const uint16_t *>(L.k), L.kbar, L.ksim, L.s, L.nk, L.b * L.hk * L.nk};
+  const int units = qs.nunits + ks.nunits;
+  const int grid = (units + 7) / 8;
+  if (L.d == 128) {
+    if (L.bf16) k_pool_sim<BF16, 128><<<grid, 256, 0, st>>>(qs, ks);
+    else k_pool_sim<F16, 128><<<grid, 256, 0, st>>>(qs, ks);
+  } else {
+    if (L.bf16) k_pool_sim<BF16, 64><<<grid, 256, 0, st>>>(qs, ks);
+    else k_pool_sim<F16, 64><<<grid, 256, 0, st>>>(qs, ks);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  SelectArgs a{};
   a.qbar = L.qbar; a.qsim = L.qsim; a.kbar = L.kbar; a.ksim = L.ksim;
   a.b = L.b; a.hq = L.hq; a.hk = L.hk; a.nq = L.nq; a.nk = L.nk;
   a.blkq = kBlk; a.blkk = kBlk;
   a.scale = L.scale; a.causal = L.causal; a.sink = L.sink; a.mode_cdf = L.mode_cdf;
   a.lut = L.lut; a.cnt = L.cnt; a.bmap = L.bmap;
-  f.qdone = L.sync;
-  f.kdone = L.sync + L.b * L.hq;
-  f.abort = L.sync + L.b * L.hq + L.b * L.hk;
-  f.err = L.err;
-  const int ratio = L.hq / L.hk;
-  f.groups = L.b * L.hk;
-  f.pool_per_group = (L.nk + ratio * L.nq + 7) / 8;
-  f.sel_groups = (L.nq + kSelRows - 1) / kSelRows;
-  f.sel_per_group = ratio * f.sel_groups;
-  f.items = f.groups * (f.pool_per_group + f.sel_per_group);
-  cudaError_t e = cudaMemsetAsync(L.sync, 0, sizeof(int) * (L.b * L.hq + L.b * L.hk + 1), st);
-  if (e != cudaSuccess) return e;
-  if (L.d == 128) return L.bf16 ? launch_nt<BF16, 128>(f, L.hp, st) : launch_nt<F16, 128>(f, L.hp, st);
-  return L.bf16 ? launch_nt<BF16, 64>(f, L.hp, st) : launch_nt<F16, 64>(f, L.hp, st);
+  return L.d == 128 ? launch_select_nt<128>(a, L.hp, st) : launch_select_nt<64>(a, L.hp, st);
 }
 
 }  // namespace fbm

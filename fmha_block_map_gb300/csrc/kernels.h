@@ -29,8 +29,6 @@ struct BlockMapLaunch {
   int causal, sink, mode_cdf;
   HeadParams hp;
   float *qbar, *qsim, *kbar, *ksim;  // workspace carve-out
-  int *sync;                         // workspace: b*hq + b*hk head counters + abort flag
-  uint32_t *err;
   int32_t *lut, *cnt;
   uint8_t *bmap;
 };
