@@ -234,69 +234,10 @@ __global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid
   __syncthreads();
 
   const unsigned lt_mask = (1u << lane) - 1u;
-  const float theta = hp.theta[h];
-  // keys of row rr (masked entries 0) and its eligible count
-  auto row_keys = [&](int rr, uint32_t (&key)[NT], int &n_elig, int &nfin) {
-    const int i = i0 + rr;
-    const int last_q = (i + 1) * a.blkq - 1;
-    n_elig = a.causal ? min(a.nk, last_q / a.blkk + 1) : a.nk;
-    int nf = 0;
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int j = lane + 32 * t;
-      const bool fin = j < a.nk && (!a.causal || j * a.blkk <= last_q) && ksim[j] > theta;
-      key[t] = fin ? order_key(S_s[rr * (NT * 32) + j]) : 0u;
-      nf += fin ? 1 : 0;
-    }
-    nfin = __reduce_add_sync(0xffffffffu, nf);
-  };
-  // top-k thresholds first, RW rows of this warp at a time: the bitwise searches
-  // of the rows interleave, so their dependent warp reductions overlap
-  uint32_t *thr = reinterpret_cast<uint32_t *>(k_s);  // K-mean tiles are no longer needed
-  if (!a.mode_cdf) {
-    constexpr int RW = NT <= 8 ? 4 : (NT <= 16 ? 2 : 1);
-    for (int rb = 0; rb < kSelRows / 8; rb += RW) {
-      uint32_t key[RW][NT], T[RW];
-      int kc[RW];
-      bool live[RW];
-#pragma unroll
-      for (int r = 0; r < RW; ++r) {
-        const int rr = warp + 8 * (rb + r);
-        T[r] = 0u;
-        live[r] = false;
-        kc[r] = 0;
-        if (i0 + rr < a.nq) {
-          int n_elig, nfin;
-          row_keys(rr, key[r], n_elig, nfin);
-          kc[r] = min((int)ceilf(__fmul_rn(hp.sel[h], (float)n_elig)), nfin);
-          live[r] = nfin > 0;
-        }
-      }
-      for (int bit = 31; bit >= 0; --bit) {
-        bool any = false;
-#pragma unroll
-        for (int r = 0; r < RW; ++r) {
-          if (!live[r]) continue;
-          const uint32_t cand = T[r] | (1u << bit);
-          int c = 0;
-#pragma unroll
-          for (int t = 0; t < NT; ++t) c += key[r][t] >= cand ? 1 : 0;
-          const int tot = __reduce_add_sync(0xffffffffu, c);
-          if (tot >= kc[r]) T[r] = cand;
-          if (tot == kc[r]) live[r] = false;  // exactly kc keys >= T: no tie left
-          any |= live[r];
-        }
-        if (!any) break;
-      }
-#pragma unroll
-      for (int r = 0; r < RW; ++r)
-        if (lane == 0) thr[warp + 8 * (rb + r)] = T[r];
-    }
-    __syncwarp();
-  }
   for (int rr = warp; rr < kSelRows; rr += 8) {
     const int i = i0 + rr;
     if (i >= a.nq) break;
+    const float theta = hp.theta[h];
     const bool q_similar = qsim[i] > theta;
     const int last_q = (i + 1) * a.blkq - 1;
     const int n_elig = a.causal ? min(a.nk, last_q / a.blkk + 1) : a.nk;
@@ -326,8 +267,17 @@ __global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid
       if (!a.mode_cdf) {
         const float prod = __fmul_rn(hp.sel[h], (float)n_elig);
         const int kcount = min((int)ceilf(prod), nfin);
-        // T = the largest key value with #(key >= T) >= kcount (found above)
-        const uint32_t T = thr[rr];
+        // largest T with #(key >= T) >= kcount: the kcount-th largest key
+        uint32_t T = 0;
+        for (int bit = 31; bit >= 0; --bit) {
+          const uint32_t cand = T | (1u << bit);
+          int c = 0;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) c += key[t] >= cand ? 1 : 0;
+          const int tot = __reduce_add_sync(0xffffffffu, c);
+          if (tot >= kcount) T = cand;
+          if (tot == kcount) break;  // exactly kcount keys >= T: no tie left to resolve
+        }
         int cgt = 0;
 #pragma unroll
         for (int t = 0; t < NT; ++t) cgt += key[t] > T ? 1 : 0;
