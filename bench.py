@@ -55,6 +55,8 @@ def parse():
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the causal-GQA prefill and sparse-decode measurements")
     return p.parse_args()
 
 
@@ -321,6 +323,9 @@ def run_ours(args):
         "clocks": clocks,
         "gpu_launches": 3 * args.steps,
     }
+    if rank == 0 and not args.no_extra:
+        res["causal_gqa"] = measure_causal_gqa(peaks["hbm_gbs"], peak)
+        res["decode"] = measure_decode(peaks["hbm_gbs"])
     if rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(cfg, x, args.topk)
     if world > 1:
@@ -328,6 +333,114 @@ def run_ours(args):
 
         dist.destroy_process_group()
     return res if rank == 0 else None
+
+
+# ----------------------------------------------------------------------------
+# the other rows of the path, measured on their own workloads (not the step)
+# ----------------------------------------------------------------------------
+
+
+def _events_ms(fn, steps, warm):
+    import torch
+
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def measure_causal_gqa(hbm_gbs, peak):
+    """b=1, 32 query heads on 8 KV heads, s=32768, d=128, bf16, causal, sink,
+    topk=0.2 of the causal-eligible blocks, LSE on."""
+    import numpy as np
+    import torch
+
+    import fmha_block_map_gb300 as fbm
+    import synth
+
+    cfg = synth.C4
+    x = synth.prefill(cfg)
+    dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+    q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
+    nq = cfg.nq
+    ws = torch.empty(fbm.block_map_workspace_bytes(1, 32, 8, cfg.s, 128), dtype=torch.uint8,
+                     device="cuda")
+    lut = torch.empty((1, 32, nq, nq), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((1, 32, nq), dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty((1, 32, cfg.s), dtype=torch.float32, device="cuda")
+    bm = lambda: fbm.sparge_block_map(q, k, topk=cfg.topk, simthreshd1=cfg.simthreshd1,
+                                      scale=cfg.scale, causal=True, attention_sink=True,
+                                      lut=lut, lut_count=cnt, workspace=ws)
+    at = lambda: fbm.sparse_fmha_fwd(q, k, v, lut, cnt, scale=cfg.scale, causal=True, out=out,
+                                     lse=lse, return_lse=True)
+    bm()
+    torch.cuda.synchronize()
+    tiles = int(cnt.sum().item())
+    bm_ms = _events_ms(bm, 10, 2)
+    at_ms = _events_ms(at, 10, 2)
+    bm_bytes = (q.numel() + k.numel()) * 2 + 2 * (32 * nq + 8 * nq) * 129 * 4 + lut.numel() * 4
+    assert fbm.get_error() == 0
+    return {"workload": "b1 hq32 hk8 s32768 d128 bf16 causal + sink, topk=0.2, LSE on",
+            "selected_tiles": tiles, "block_map_ms": round(bm_ms, 4),
+            "block_map_GB_s": round(bm_bytes / (bm_ms * 1e-3) / 1e9, 1),
+            "block_map_frac_hbm": round(bm_bytes / (bm_ms * 1e-3) / 1e9 / hbm_gbs, 3),
+            "attn_ms": round(at_ms, 4),
+            "attn_eff_tflops": round(tiles * FLOP_PER_TILE / (at_ms * 1e-3) / 1e12, 1),
+            "attn_frac_peak": round(tiles * FLOP_PER_TILE / (at_ms * 1e-3) / 1e12 / peak, 4)}
+
+
+def measure_decode(hbm_gbs):
+    """64 queries x 16 heads on one 576-wide KV head, 2048 listed tokens each,
+    65536-page cache (4.8 GB bf16): split-KV decode + LSE combine."""
+    import numpy as np
+    import torch
+
+    import fmha_block_map_gb300 as fbm
+    import synth
+
+    cfg = synth.C5
+    inp = synth.decode(cfg)
+    n_rows = cfg.n_pages * cfg.page
+    cache = torch.empty((n_rows, cfg.d), dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, n_rows, 1 << 18):
+        r1 = min(n_rows, r0 + (1 << 18))
+        cache[r0:r1] = synth.cache_rows_torch(cfg, r0, r1, "cuda")
+    cache = cache.view(cfg.n_pages, cfg.page, cfg.d)
+    q = torch.from_numpy(inp["q"].view(np.int16)).view(torch.bfloat16).cuda()
+    pt = torch.from_numpy(inp["page_table"]).cuda()
+    ix = torch.from_numpy(inp["idx"]).cuda()
+    res = []
+    for S in (2, 4, 8):
+        op = torch.empty((S, cfg.n_queries, cfg.hq, cfg.dv), dtype=torch.float32, device="cuda")
+        lp = torch.empty((S, cfg.n_queries, cfg.hq), dtype=torch.float32, device="cuda")
+        o = torch.empty((cfg.n_queries, cfg.hq, cfg.dv), dtype=torch.bfloat16, device="cuda")
+        dec = lambda: fbm.sparse_decode_fwd(q, cache, pt, ix, dv=cfg.dv, scale=cfg.sm_scale,
+                                            num_splits=S, o_partial=op, lse_partial=lp)
+        comb = lambda: fbm.attn_combine(op, lp, out=o, return_lse=False)
+        d_ms = _events_ms(dec, 20, 3)
+        c_ms = _events_ms(comb, 20, 3)
+        rows_bytes = cfg.n_queries * cfg.topk * cfg.d * 2
+        part_bytes = S * cfg.n_queries * cfg.hq * (cfg.dv + 1) * 4
+        d_bytes = rows_bytes + q.numel() * 2 + ix.numel() * 4 + part_bytes \
+            + cfg.n_queries * cfg.topk * 4  # page-table entries looked up
+        c_bytes = part_bytes + o.numel() * 2
+        res.append({"splits": S, "decode_ms": round(d_ms, 4),
+                    "decode_GB_s": round(d_bytes / (d_ms * 1e-3) / 1e9, 1),
+                    "decode_frac_hbm": round(d_bytes / (d_ms * 1e-3) / 1e9 / hbm_gbs, 3),
+                    "combine_ms": round(c_ms, 4),
+                    "combine_GB_s": round(c_bytes / (c_ms * 1e-3) / 1e9, 1)})
+    assert fbm.get_error() == 0
+    del cache
+    torch.cuda.empty_cache()
+    return {"workload": "64 queries x 16 heads, d=576 (V = first 512), 2048 tokens each, "
+                        "65536 pages of 64 rows, bf16", "by_splits": res}
 
 
 # ----------------------------------------------------------------------------

@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
         L.attn_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
         L.sparse_decode_fwd.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, i32, vp,
                                          i32, i32, f32, vp, vp, vp])
+        L.fbm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.fbm_selftest_wait_timeout.restype = i32
         L.fbm_fmha_kernel_kind.argtypes = [i32] * 6
         L.fbm_fmha_kernel_kind.restype = i32
         for name in ("fbm_get_error", "sparge_block_map", "sparge_block_map_static",
@@ -272,6 +274,11 @@ def sparse_decode_fwd(q: torch.Tensor, kv_cache: torch.Tensor, page_table: torch
         page_table.shape[1], _ptr(indices), indices.shape[1], num_splits, float(scale),
         _ptr(o_partial), _ptr(lse_partial), _stream(stream)))
     return o_partial, lse_partial
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Run the bounded-wait expiry path on the GPU (see include/fbm.h)."""
+    _check(lib().fbm_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def fmha_kernel_kind(dtype: torch.dtype, d: int, dv: int, num_splits: int, s_q: int,

@@ -80,6 +80,8 @@ fbm_status set_message(fbm_status st, const char *msg) {
   snprintf(g_msg, sizeof(g_msg), "%s", msg);
   return st;
 }
+// The device error word of the current device (for other files of the library).
+uint32_t *device_error_word() { return error_word(); }
 }  // namespace fbm
 
 extern "C" {

@@ -221,6 +221,14 @@ fbm_status sparse_decode_fwd(const void *q, const void *kv_cache, int dtype, int
                              const int32_t *indices, int topk, int num_splits, float scale,
                              float *o_partial, float *lse_partial, void *stream);
 
+/* Diagnostic without a counterpart on the pages: launches one CTA that waits,
+ * with the bounded mbarrier wait the tcgen05 kernels use, on a barrier that
+ * nothing arrives on.  After limit_ns (0 < limit_ns <= 1e10) the wait gives up
+ * and sets FBM_DEVERR_TIMEOUT in the device error word (read it with
+ * fbm_get_error); the kernel then returns and the context stays usable.
+ * Asynchronous on `stream`. */
+fbm_status fbm_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
 /* Which sparse-FMHA kernel sparse_fmha_fwd launches for these arguments:
  * 1 = tcgen05 / TMA kernel, 2 = mma.sync kernel, 0 = none (the arguments
  * would be rejected).  Host-only; launches nothing. */

@@ -144,3 +144,8 @@ def test_static_block_map_rejects_oversized_shapes_on_the_host(L):
                                    0.08, 0, 0, FAKE, FAKE, None, None)
     assert st == fbm.FBM_ERR_UNSUPPORTED
     assert b"static array" in L.fbm_last_error_message()
+
+
+def test_selftest_checks_its_limit_on_the_host(L):
+    assert L.fbm_selftest_wait_timeout(0, None) == fbm.FBM_ERR_INVALID_ARG
+    assert L.fbm_selftest_wait_timeout(20_000_000_000, None) == fbm.FBM_ERR_INVALID_ARG
