@@ -1,37 +1,43 @@
 // Sparse FMHA forward for sm_103a on 5th-generation tensor cores (tcgen05,
-// TMEM accumulators, TMA loads), d = 128.
+// TMEM accumulators, TMA loads and stores), d = 128.
 //
 // The per-q-block work of the sparse FMHA stage (the "Sparge Attention
 // (Composable Kernel)" README) visits only the kv blocks of the q block's LUT
-// row.  A q block holds 64 query rows, less than the 128-row tile of a full-rate
-// tcgen05.mma, and neighbouring q blocks select different kv blocks, so the
-// kernel computes the transposed problem: two LUT-selected kv blocks (128 keys)
-// form the M dimension and the 64 queries the N dimension.
+// row, two at a time (a "pair", 128 keys):
 //
-//   S^T [128 keys x 64 q]  = K_pair [128 x d] . Q^T          (A, B K-major)
-//   O^T [d x 64 q]        += V_pair^T [d x 128] . P^T [128 x 64] (A, B MN-major)
+//   S  [64 q x 128 keys]  = Q [64 x d] . K_pair^T        M = 64, N = 128 (A, B in smem)
+//   P  = exp2(S * scale * log2 e - m)                      written to TMEM as fp16 / bf16
+//   O  [64 q x 128 d]    += P . V_pair                    M = 64, N = 128 (A = P in TMEM,
+//                                                          B = V in smem, MN-major)
 //
-// No MMA row is spent on a kv block the q block did not select (an odd count
-// leaves one half-empty pair per row).  The softmax runs along TMEM lanes
-// (keys): each of the 128 softmax threads owns one key and holds that key's 64
-// scores; the running max per query is kept lazily (rescale only when a score
-// exceeds it by more than 2^8), so the cross-lane column maximum is needed only
-// on those rare pairs.
+// Why this orientation: an M = 64 MMA runs at half the rate of an M = 128 one,
+// but the tensor core reads its operands from shared memory at about 128 bytes
+// per cycle, and with P in TMEM a pair costs 48 KB (S) + 32 KB (PV) of operand
+// reads plus 64 KB of TMA writes: about 1100 cycles, close to the 1024 cycles
+// the sixteen M = 64 MMAs take.  (The transposed form, S^T = K . Q^T with M = 128
+// keys, needs P^T in shared memory: 176 KB per pair.)
 //
-// Roles (one persistent CTA per SM, 20 warps):
-//   warp 0    TMA producer of Q (double buffer) and K pairs (2-slot ring)
-//   warp 19   TMA producer of V pairs (2-slot ring)
-//   warp 1    TMEM owner and single-thread S^T issuer
-//   warp 18   single-thread PV issuer (so S^T never queues behind a PV that
-//             waits for the softmax)
-//   warps 2-17 four softmax + epilogue warpgroups, each owning 16 of the 64
-//             query columns (each group covers TMEM lane quadrants 2, 3, 0, 1:
-//             all 128 keys)
-// Pipeline: S^T(p) is issued once K(p) has landed and its TMEM slot (two
-// slots) is free; PV(p) once P(p) is written.  The softmax of pair p+1
-// overlaps the PV MMA of pair p.  Every wait is bounded:
-// on expiry the kernel raises FBM_DEVERR_TIMEOUT, every role leaves its loop,
-// in-flight copies and MMAs are drained with bounded waits and TMEM is freed.
+// TMEM (512 columns): S slots at columns 0 and 128 (fp32), P buffers at 256 and
+// 320 (two 16-bit values per column), O at 384.  An M = 64 accumulator keeps
+// row i in lane (i mod 16) + 32 (i / 16): softmax warp w (subpartition w) owns
+// rows 16w .. 16w + 15, and with the 16x32bx2 load shape thread t holds row
+// 16w + (t mod 16), keys 64 (t / 16) .. + 63 of the pair, i.e. one kv block.
+// The running max of a row is kept lazily (O and l are rescaled only when a
+// score exceeds it by more than 2^8); both threads of a row agree on it through
+// one shuffle.
+//
+// Roles (one persistent CTA per SM, 8 warps):
+//   warp 0   TMA producer of Q (double buffer) and K pairs (3-slot ring)
+//   warp 1   TMA producer of V pairs (2-slot ring)
+//   warp 2   TMEM owner and S issuer
+//   warp 3   PV issuer
+//   warps 4-7 softmax and epilogue (TMEM subpartitions 0-3)
+// Pipeline: S(g) is issued once K(g) has landed and its TMEM slot is free (the
+// softmax releases a slot as soon as it holds the scores in registers), so the
+// S MMA of pair g + 1 runs during the softmax of pair g; PV(g) once P(g) is in
+// TMEM.  Every wait is bounded: on expiry the kernel raises FBM_DEVERR_TIMEOUT,
+// every role leaves its loop, in-flight copies and MMAs are drained with
+// bounded waits and TMEM is freed.
 //
 // Loop shape: the Incremental_FlashAttention updating_log's Stage 3/4 sparse
 // mainloop (listed blocks only, next K prefetched while the current tile is
@@ -51,53 +57,46 @@ namespace {
 using namespace tc;
 
 constexpr int kD = 128;
-constexpr int kQBytes = 64 * kD * 2;      // 16 KB: a 64-row Q tile
+constexpr int kQBytes = 64 * kD * 2;      // 16 KB: a 64-row Q (or output) tile
 constexpr int kPairBytes = 128 * kD * 2;  // 32 KB: two 64-row kv blocks
 constexpr int kQChunk = 64 * 128;         // 8 KB: one 64-wide d chunk of a 64-row tile
 constexpr int kPairChunk = 128 * 128;     // 16 KB: one 64-wide d chunk of a 128-row pair
-constexpr int kPBytes = 128 * 128;        // 16 KB: P^T, 128 keys x 64 queries (MN-major)
+constexpr int kKSlots = 3;                // K ring (S(g) may run ahead of the softmax)
+constexpr int kVSlots = 2;                // V ring
+constexpr int kSSlots = 2;                // S slots in TMEM
+constexpr int kPBufs = 2;                 // P buffers in TMEM
 
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + 2 * kQBytes;
-constexpr int OFF_V = OFF_K + 2 * kPairBytes;
-constexpr int OFF_P = OFF_V + 2 * kPairBytes;
-constexpr int OFF_STAGE = OFF_P + 2 * kPBytes;   // 16 KB: output staging [64 q][128 d]
-constexpr int kGroups = 4;                         // softmax warpgroups per CTA
-constexpr int kCW = 64 / kGroups;                  // query columns per group
-constexpr int OFF_RED = OFF_STAGE + kQBytes;       // float [groups][4 quadrants][kCW]
-constexpr int OFF_ALPHA = OFF_RED + kGroups * 4 * kCW * 4;  // float [groups][kCW]
-constexpr int OFF_INVL = OFF_ALPHA + kGroups * kCW * 4;     // float [groups][kCW]
-constexpr int OFF_M = OFF_INVL + kGroups * kCW * 4;         // float [groups][kCW]
-constexpr int OFF_BAR = OFF_M + kGroups * kCW * 4;
+constexpr int OFF_V = OFF_K + kKSlots * kPairBytes;
+constexpr int OFF_STAGE = OFF_V + kVSlots * kPairBytes;  // output tile, [chunk][64 rows][128 B] SW128
+constexpr int OFF_BAR = OFF_STAGE + kQBytes;
 enum {
-  B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 6, B_VF = 8, B_VE = 10, B_SF = 12, B_SE = 14,
-  B_PF = 16, B_PV = 18, B_OF = 20, B_DRAIN = 21, B_DRAIN2 = 22, NBAR = 23
+  B_QF = 0, B_QE = 2, B_KF = 4, B_KE = B_KF + kKSlots, B_VF = B_KE + kKSlots,
+  B_VE = B_VF + kVSlots, B_SF = B_VE + kVSlots, B_SE = B_SF + kSSlots, B_PF = B_SE + kSSlots,
+  B_PV = B_PF + kPBufs, B_OF = B_PV + kPBufs, B_DRAIN = B_OF + 1, B_DRAIN2 = B_DRAIN + 1,
+  NBAR = B_DRAIN2 + 1
 };
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // [0] tmem base, [1] abort flag
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] tmem base, [1] abort flag
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
-constexpr uint32_t kTmemCols = 256;                // S0 @0, S1 @64, O @128
-constexpr uint64_t kWaitNs = 2000000000ull;        // 2 s per wait
-constexpr int kGroupThreads = 128;                 // one softmax warpgroup
-constexpr int kSoftmaxThreads = kGroups * kGroupThreads;
-constexpr int kPvWarp = 2 + kSoftmaxThreads / 32;  // the PV issuer follows the softmax warps
-constexpr int kVWarp = kPvWarp + 1;                 // then the V producer
-constexpr int kThreads = 64 + kSoftmaxThreads + 64; // + Q/K producer, S^T issuer, PV issuer, V producer
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
-// N consecutive TMEM columns of 32 lanes (a query group's columns)
-template <int N>
-FBM_DEVICE void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
-  if constexpr (N == 16) tmem_ld16(taddr, r);
-  else tmem_ld32(taddr, r);
-}
-template <int N>
-FBM_DEVICE void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
-  if constexpr (N == 16) tmem_st16(taddr, r);
-  else tmem_st32(taddr, r);
-}
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTS = 0;    // S slot s at kTS + 128 s
+constexpr uint32_t kTP = 256;  // P buffer b at kTP + 64 b
+constexpr uint32_t kTO = 384;  // O
+constexpr uint32_t kDescHi = sdesc_hi_sw128(1024);  // every operand: 1024-byte 8-row atoms
+constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
+
+constexpr int kWarpQK = 0, kWarpV = 1, kWarpS = 2, kWarpPV = 3, kWarpSm = 4;
+constexpr int kSoftmaxWarps = 4;
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kThreads = 32 * (kWarpSm + kSoftmaxWarps);
+constexpr int kSoftmaxBar = 1;  // named barrier of the softmax warps
 
 struct TcParams {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const int32_t *lut, *cnt;
   void *out;
   float *lse;
@@ -144,8 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
   if (threadIdx.x == 0) {
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
-      if (k == B_SE || k == B_SE + 1 || k == B_PF || k == B_PF + 1 || k == B_OF)
-        cnt = kSoftmaxThreads;  // every query group arrives
+      if ((k >= B_SE && k < B_SE + kSSlots) || (k >= B_PF && k < B_PF + kPBufs) || k == B_OF)
+        cnt = kSoftmaxWarps;  // one elected arrive per softmax warp
       mbar_init(bar(k), cnt);
     }
     misc[1] = 0;
@@ -153,8 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     prefetch_map(&P.tq);
     prefetch_map(&P.tk);
     prefetch_map(&P.tv);
+    prefetch_map(&P.to);
   }
-  if (warp == 1) {
+  if (warp == kWarpS) {
     tmem_alloc(sbase + OFF_MISC, kTmemCols);
     tmem_relinquish();
   }
@@ -171,9 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
   // K or V pair g (= pc + p) of a q block into its ring slot, once the MMA that
   // last read the slot has completed
   auto load_pair = [&](const Unit &U, int pc, int p, bool is_v) -> bool {
-    const int g = pc + p, slot = g & 1;
+    const int ns = is_v ? kVSlots : kKSlots;
+    const int g = pc + p, slot = g % ns;
     const int fb = (is_v ? B_VF : B_KF) + slot, eb = (is_v ? B_VE : B_KE) + slot;
-    if (!mbar_wait(bar(eb), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs)) return false;
+    if (!mbar_wait(bar(eb), ((g / ns) & 1) ^ 1, abort_flag, kWaitNs)) return false;
     int js[2] = {-1, -1};
     uint32_t bytes = 0;
     for (int hf = 0; hf < 2; ++hf) {
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     return true;
   };
 
-  if (warp == 0) {
+  if (warp == kWarpQK) {
     // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
       int pc = 0, uc = 0;
@@ -221,10 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       }
       if (!ok) fail(FBM_DEVERR_TIMEOUT);
     }
-  } else if (warp == kVWarp) {
+  } else if (warp == kWarpV) {
     // ------------------------------------------------------------ V producer
-    // (its own thread, so a K load never waits behind a V slot that a late PV
-    // still holds)
     if (lane == 0) {
       int pc = 0;
       bool ok = true;
@@ -237,12 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       }
       if (!ok) fail(FBM_DEVERR_TIMEOUT);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ S^T issuer
-    // S^T(g) runs as soon as its K pair is loaded and its TMEM slot is free;
-    // it never waits for P, so it stays ahead of the softmax.
+  } else if (warp == kWarpS) {
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_f16(kBf16, false, false, 128, 64);
+      constexpr uint32_t idS = idesc_f16(kBf16, false, false, 64, 128);
       int pc = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
@@ -252,23 +249,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         const int qb = uc & 1;
         if (!(ok = mbar_wait(bar(B_QF + qb), (uc >> 1) & 1, abort_flag, kWaitNs))) break;
         tc_fence_after();
-        const uint32_t qaddr = sbase + OFF_Q + qb * kQBytes;
+        const uint32_t q_lo = sdesc_lo(sbase + OFF_Q + qb * kQBytes, 16);
         for (int p = 0; p < npairs; ++p) {
-          const int g = pc + p, slot = g & 1;
-          if (!(ok = mbar_wait(bar(B_KF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
-          if (!(ok = mbar_wait(bar(B_SE + slot), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs))) break;
+          const int g = pc + p, slot = g % kKSlots, ss = g % kSSlots;
+          if (!(ok = mbar_wait(bar(B_KF + slot), (g / kKSlots) & 1, abort_flag, kWaitNs))) break;
+          if (!(ok = mbar_wait(bar(B_SE + ss), ((g / kSSlots) & 1) ^ 1, abort_flag, kWaitNs))) break;
           tc_fence_after();
-          const uint32_t kaddr = sbase + OFF_K + slot * kPairBytes;
+          const uint32_t k_lo = sdesc_lo(sbase + OFF_K + slot * kPairBytes, 16);
+          const uint32_t dS = tbase + kTS + ss * 128;
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(kaddr + (kk >> 2) * kPairChunk + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(qaddr + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
-            mma_f16(tbase + slot * 64, ad, bd, idS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(B_SF + slot));
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_f16_lo(dS, q_lo + (((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4),
+                       k_lo + (((kk >> 2) * kPairChunk + (kk & 3) * 32) >> 4), kDescHi, idS,
+                       kk > 0 ? 1u : 0u);
+          mma_commit(bar(B_SF + ss));
           mma_commit(bar(B_KE + slot));
         }
-        if (ok) mma_commit(bar(B_QE + qb));  // Q free once every S^T of the row is done
+        if (ok) mma_commit(bar(B_QE + qb));  // Q free once every S of the row is done
         pc += npairs;
         uc += 1;
       }
@@ -277,11 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       mma_commit(bar(B_DRAIN));
       if (!mbar_wait_for(bar(B_DRAIN), 0, kWaitNs)) set_error(P.err, FBM_DEVERR_TIMEOUT);
     }
-  } else if (warp == kPvWarp) {
+  } else if (warp == kWarpPV) {
     // ------------------------------------------------------------ PV issuer
     if (lane == 0) {
-      constexpr uint32_t idO = idesc_f16(kBf16, true, true, 128, 64);
-      const uint32_t tO = tbase + 128;
+      // A = P (TMEM, K-major), B = V pair (MN-major: d contiguous)
+      constexpr uint32_t idO = idesc_f16(kBf16, false, true, 64, 128);
+      const uint32_t tO = tbase + kTO;
       int pc = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
@@ -289,20 +287,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         if (U.n == 0) continue;
         const int npairs = (U.n + 1) >> 1;
         for (int p = 0; p < npairs; ++p) {
-          const int g = pc + p, slot = g & 1;
-          if (!(ok = mbar_wait(bar(B_PF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
-          if (!(ok = mbar_wait(bar(B_VF + slot), (g >> 1) & 1, abort_flag, kWaitNs))) break;
+          const int g = pc + p, slot = g % kVSlots, pb = g % kPBufs;
+          if (!(ok = mbar_wait(bar(B_PF + pb), (g / kPBufs) & 1, abort_flag, kWaitNs))) break;
+          if (!(ok = mbar_wait(bar(B_VF + slot), (g / kVSlots) & 1, abort_flag, kWaitNs))) break;
           if (p == 0 && !(ok = mbar_wait(bar(B_OF), (uc & 1) ^ 1, abort_flag, kWaitNs))) break;
           tc_fence_after();
-          const uint32_t vaddr = sbase + OFF_V + slot * kPairBytes;
-          const uint32_t paddr = sbase + OFF_P + slot * kPBytes;
-          const int ksteps = (2 * p + 1 < U.n) ? 8 : 4;  // a half pair has 64 keys
-          for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t ad = sdesc_sw128(vaddr + kk * 2048, kPairChunk, 1024);
-            const uint64_t bd = sdesc_sw128(paddr + kk * 2048, kPairChunk, 1024);
-            mma_f16(tO, ad, bd, idO, (p > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(B_PV + slot));
+          const uint32_t v_lo = sdesc_lo(sbase + OFF_V + slot * kPairBytes, kPairChunk);
+          const uint32_t tP = tbase + kTP + pb * 64;
+          const bool half = 2 * p + 1 >= U.n;  // a half pair has 64 keys: 4 steps
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            if (kk < 4 || !half)
+              mma_f16_ta(tO, tP + kk * 8, v_lo + kk * 128, kDescHi, idO,
+                         (p > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(B_PV + pb));
           mma_commit(bar(B_VE + slot));
         }
         pc += npairs;
@@ -314,242 +312,183 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int wg = (warp - 2) >> 2;          // query group: columns kCW*wg .. kCW*wg+kCW-1
-    const int cb = wg * kCW;
-    const int qd = warp & 3;
-    const int key = qd * 32 + lane;          // TMEM lane: key of the pair (S^T) / d (O^T)
-    const int tg = (threadIdx.x - 64) & 127; // 0..127 within the group
-    const int barid = 1 + wg;                // named barrier of this group
-    const uint32_t tl = tbase + ((uint32_t)(qd * 32) << 16);
-    float *red = reinterpret_cast<float *>(smem + OFF_RED) + wg * 4 * kCW;   // [4][kCW]
-    float *alpha_s = reinterpret_cast<float *>(smem + OFF_ALPHA) + wg * kCW;
-    float *invl_s = reinterpret_cast<float *>(smem + OFF_INVL) + wg * kCW;
-    float *m_s = reinterpret_cast<float *>(smem + OFF_M) + wg * kCW;
     using E = typename std::conditional<kBf16, BF16, F16>::type;
-    // Every softmax thread of a group runs the same loop trip counts and named
-    // barriers whatever happens: a failed (timed-out) wait only clears `ok`,
-    // and later waits return at once, so no thread is left behind at a barrier.
+    const int sw = warp - kWarpSm;            // == warp % 4: TMEM subpartition
+    const int half = lane >> 4;               // block of the pair / d half of O
+    const int row = sw * 16 + (lane & 15);    // query row within the q block
+    const int tid = threadIdx.x - kWarpSm * 32;
+    const uint32_t tl = tbase + ((uint32_t)(sw * 32) << 16);
+    const uint64_t sl2x2 = f2_pack(P.sl2, P.sl2);
+    // Every softmax thread runs the same loop trip counts and barriers whatever
+    // happens: a failed (timed-out) wait only clears `ok`, and later waits
+    // return at once.
     int pc = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
       const Unit U = unit_of(P, u);
       const int q0 = U.i * 64;
       const int rows = min(64, P.s_q - q0);
-      const int my_rows = max(0, min(kCW, rows - cb));  // this group's valid query rows
-      uint16_t *orow = static_cast<uint16_t *>(P.out) + ((size_t)U.bh_q * P.s_q + q0 + cb) * kD;
-      float *lrow = P.lse ? P.lse + (size_t)U.bh_q * P.s_q + q0 + cb : nullptr;
       if (U.n == 0) {
-        for (int e = tg * 8; e < my_rows * kD; e += kGroupThreads * 8)
-          *reinterpret_cast<uint4 *>(orow + e) = make_uint4(0, 0, 0, 0);
-        if (lrow && tg < my_rows) lrow[tg] = -INFINITY;
+        uint16_t *o = static_cast<uint16_t *>(P.out) + ((size_t)U.bh_q * P.s_q + q0) * kD;
+        for (int e = tid * 8; e < rows * kD; e += kSoftmaxThreads * 8)
+          *reinterpret_cast<uint4 *>(o + e) = make_uint4(0, 0, 0, 0);
+        if (P.lse && tid < rows) P.lse[(size_t)U.bh_q * P.s_q + q0 + tid] = -INFINITY;
         continue;
       }
       const int npairs = (U.n + 1) >> 1;
-      // running max per query (log2 domain) lives in m_s; l holds this key's
-      // share of the row sums, as packed fp32 pairs (queries 2i, 2i+1)
-      uint64_t l2[kCW / 2];
-#pragma unroll
-      for (int i = 0; i < kCW / 2; ++i) l2[i] = 0ull;
-      if (tg < kCW) m_s[tg] = -INFINITY;
-      named_sync(barid, kGroupThreads);
-      const uint64_t sl2x2 = f2_pack(P.sl2, P.sl2);
-      int j_next = (key >> 6) < U.n ? entry_of(U, key >> 6) : -1;
+      const int qpos = q0 + row;
+      float m = -INFINITY;                 // running max of the row (log2 domain)
+      uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};  // this thread's share of the row sum
+      int j_next = half < U.n ? entry_of(U, half) : -1;
       for (int p = 0; p < npairs; ++p) {
-        const int g = pc + p, slot = g & 1;
-        // this thread's key: block t of the row, offset key & 63
+        const int g = pc + p, ss = g % kSSlots, pb = g % kPBufs;
         const int j = j_next;
         {
-          const int tn = 2 * (p + 1) + (key >> 6);
+          const int tn = 2 * (p + 1) + half;
           j_next = (p + 1 < npairs && tn < U.n) ? entry_of(U, tn) : -1;
         }
         const bool jvalid = j >= 0 && j < P.nk;
-        const int kpos = (jvalid ? j : 0) * 64 + (key & 63);
-        const bool kvalid = jvalid && kpos < P.s_k;
-        // queries cb + q with q < qmin cannot see this key (causal)
-        const int qmin = P.causal ? kpos - q0 - cb : -1;
-        const bool plain = kvalid && qmin <= 0;  // the whole column range is visible
-        ok = ok && mbar_wait(bar(B_SF + slot), (g >> 1) & 1, abort_flag, kWaitNs);
+        const int kpos0 = (jvalid ? j : 0) * 64;
+        // every key of this thread's block visible to its row
+        const bool plain = jvalid && kpos0 + 64 <= P.s_k && (!P.causal || kpos0 + 63 <= qpos);
+        ok = ok && mbar_wait(bar(B_SF + ss), (g / kSSlots) & 1, abort_flag, kWaitNs);
         tc_fence_after();
-        uint32_t r[kCW];
-        tmem_ld_cols(tl + slot * 64 + cb, r);
+        uint32_t sv[64];
+        tmem_ld_rowhalf64(tl + kTS + ss * 128, sv);
         tmem_wait_ld();
-        uint64_t x2[kCW / 2];
+        // the S slot is free for S(g + kSSlots) as soon as it is in registers
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SE + ss));
+        if (!plain) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int kpos = kpos0 + c;
+            const bool vis = jvalid && kpos < P.s_k && (!P.causal || kpos <= qpos);
+            if (!vis) sv[c] = __float_as_uint(-INFINITY);
+          }
+        }
+        // row max over the pair (this thread's 64 keys, then the other half)
         float mx;
-        if (plain) {
-#pragma unroll
-          for (int i4 = 0; i4 < kCW / 4; ++i4) {
-            const float4 mv = reinterpret_cast<const float4 *>(m_s)[i4];
-            x2[2 * i4] = f2_fma(f2_pack(__uint_as_float(r[4 * i4]), __uint_as_float(r[4 * i4 + 1])),
-                                sl2x2, f2_pack(-mv.x, -mv.y));
-            x2[2 * i4 + 1] = f2_fma(f2_pack(__uint_as_float(r[4 * i4 + 2]), __uint_as_float(r[4 * i4 + 3])),
-                                    sl2x2, f2_pack(-mv.z, -mv.w));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < kCW / 2; ++i) {
-            const int q = 2 * i;
-            const float a = (kvalid && q >= qmin) ? fmaf(__uint_as_float(r[q]), P.sl2, -m_s[q]) : -INFINITY;
-            const float b = (kvalid && q + 1 >= qmin) ? fmaf(__uint_as_float(r[q + 1]), P.sl2, -m_s[q + 1]) : -INFINITY;
-            x2[i] = f2_pack(a, b);
-          }
-        }
         {
-          float t[kCW / 4];
+          float t[8];
 #pragma unroll
-          for (int i = 0; i < kCW / 4; ++i) {
-            const float2 a = f2_unpack(x2[2 * i]), b = f2_unpack(x2[2 * i + 1]);
-            t[i] = fmax3(a.x, a.y, fmaxf(b.x, b.y));
+          for (int i = 0; i < 8; ++i) {
+            const float *v = reinterpret_cast<const float *>(sv) + 8 * i;
+            t[i] = fmaxf(fmax3(fmax3(v[0], v[1], v[2]), v[3], v[4]), fmax3(v[5], v[6], v[7]));
           }
-          mx = t[0];
-#pragma unroll
-          for (int i = 1; i < kCW / 4; i += 2)
-            mx = (i + 1 < kCW / 4) ? fmax3(mx, t[i], t[i + 1]) : fmaxf(mx, t[i]);
+          mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
         }
-        if (named_or(barid, kGroupThreads, mx > 8.0f)) {
-          // rare: some score exceeds the running max by > 2^8 (always on the
-          // first pair): exact column max over the 128 keys, then rescale
-          float v[kCW];
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mxs = mx * P.sl2;
+        const bool need = mxs > m + 8.0f;
+        if (__any_sync(0xffffffffu, need)) {
+          // rare: some score of the warp's rows exceeds its running max by more
+          // than 2^8 (always on the first pair): move the max, rescale l and O
+          const float mn = need ? mxs : m;
+          const float alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - mn);
+          m = mn;
+          const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-          for (int q = 0; q < kCW; ++q)
-            v[q] = (kvalid && q >= qmin) ? __uint_as_float(r[q]) * P.sl2 : -INFINITY;
-          // transpose-reduce within the warp: lanes l and l + 16 end with column l & 15
-#pragma unroll
-          for (int o = kCW / 2; o >= 1; o >>= 1) {
-            const bool hi = (lane & o) != 0;
-#pragma unroll
-            for (int x = 0; x < o; ++x) {
-              const float send = hi ? v[x] : v[x + o];
-              const float keep = hi ? v[x + o] : v[x];
-              v[x] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
-            }
-          }
-          if constexpr (kCW == 16) v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 16));
-          if (lane < kCW) red[qd * kCW + lane] = v[0];
-          named_sync(barid, kGroupThreads);
-          if (tg < kCW) {
-            const int q = tg;
-            const float cm = fmaxf(fmaxf(red[q], red[kCW + q]), fmaxf(red[2 * kCW + q], red[3 * kCW + q]));
-            const float mo = m_s[q];
-            const float mn = fmaxf(mo, cm);
-            alpha_s[q] = (mn == -INFINITY) ? 1.f : fast_exp2(mo - mn);
-            m_s[q] = mn;
-          }
-          named_sync(barid, kGroupThreads);
-#pragma unroll
-          for (int i = 0; i < kCW / 2; ++i)
-            l2[i] = f2_mul(l2[i], f2_pack(alpha_s[2 * i], alpha_s[2 * i + 1]));
+          for (int i = 0; i < 4; ++i) l2[i] = f2_mul(l2[i], a2);
           if (p > 0) {
-            // O^T holds PV(0 .. p-1): wait for the last of them, then scale
+            // O holds PV(0 .. p-1): wait for the last of them, then scale
             const int gp = g - 1;
-            ok = ok && mbar_wait(bar(B_PV + (gp & 1)), (gp >> 1) & 1, abort_flag, kWaitNs);
+            ok = ok && mbar_wait(bar(B_PV + gp % kPBufs), (gp / kPBufs) & 1, abort_flag, kWaitNs);
             tc_fence_after();
-            uint32_t o[kCW];
-            tmem_ld_cols(tl + 128 + cb, o);
+            uint32_t o[64];
+            tmem_ld_rowhalf64(tl + kTO, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < kCW; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha_s[q]);
-            tmem_st_cols(tl + 128 + cb, o);
+            for (int c = 0; c < 64; c += 2) {
+              const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[c]), __uint_as_float(o[c + 1])), a2);
+              const float2 w2 = f2_unpack(v);
+              o[c] = __float_as_uint(w2.x);
+              o[c + 1] = __float_as_uint(w2.y);
+            }
+            tmem_st_rowhalf64(tl + kTO, o);
             tmem_wait_st();
-            tc_fence_before();
-          }
-#pragma unroll
-          for (int i = 0; i < kCW / 2; ++i) {
-            const int q = 2 * i;
-            const float a = (kvalid && q >= qmin) ? fmaf(__uint_as_float(r[q]), P.sl2, -m_s[q]) : -INFINITY;
-            const float b = (kvalid && q + 1 >= qmin) ? fmaf(__uint_as_float(r[q + 1]), P.sl2, -m_s[q + 1]) : -INFINITY;
-            x2[i] = f2_pack(a, b);
           }
         }
-        // P(p) goes to buffer `slot`, last read by PV(g - 2)
-        if (p >= 2) {
-          const int gp = g - 2;
-          ok = ok && mbar_wait(bar(B_PV + slot), (gp >> 1) & 1, abort_flag, kWaitNs);
-        }
-        uint8_t *prow = smem + OFF_P + slot * kPBytes + key * 128;
+        // P = exp2(s * scale * log2 e - m), packed to 16-bit pairs
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        const uint64_t negm = f2_pack(-mu, -mu);
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < kCW / 8; ++c) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int z = 0; z < 4; ++z) {
-            const float2 xv = f2_unpack(x2[4 * c + z]);
-            const float e0 = fast_exp2(xv.x), e1 = fast_exp2(xv.y);
-            l2[4 * c + z] = f2_add(l2[4 * c + z], f2_pack(e0, e1));
-            pk[z] = E::from_f2(e0, e1);
-          }
-          const int chunk = wg * (kCW / 8) + c;
-          *reinterpret_cast<uint4 *>(prow + ((chunk ^ (key & 7)) << 4)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int i = 0; i < 32; ++i) {
+          const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
+                                    sl2x2, negm);
+          const float2 xv = f2_unpack(x);
+          const float e0 = fast_exp2(xv.x), e1 = fast_exp2(xv.y);
+          l2[i & 3] = f2_add(l2[i & 3], f2_pack(e0, e1));
+          pk[i] = E::from_f2(e0, e1);
         }
-        fence_proxy_async();
+        // P buffer pb was last read by PV(g - kPBufs) (at the start of a row the
+        // previous row's epilogue has already waited for its last PV)
+        if (p >= kPBufs) {
+          const int gp = g - kPBufs;
+          ok = ok && mbar_wait(bar(B_PV + pb), (gp / kPBufs) & 1, abort_flag, kWaitNs);
+        }
+        tc_fence_after();
+        tmem_st_rowhalf32(tl + kTP + pb * 64, pk);
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(B_PF + slot));
-        mbar_arrive(bar(B_SE + slot));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PF + pb));
       }
-      // ---- epilogue: O = O^T / l, LSE = m ln2 + ln l (this group's kCW queries)
+      // ---- epilogue: O = O / l, LSE = m ln 2 + ln l
       {
         const int gl = pc + npairs - 1;
-        ok = ok && mbar_wait(bar(B_PV + (gl & 1)), (gl >> 1) & 1, abort_flag, kWaitNs);
+        ok = ok && mbar_wait(bar(B_PV + gl % kPBufs), (gl / kPBufs) & 1, abort_flag, kWaitNs);
         tc_fence_after();
-        // sum l over the 128 keys
-        float l[kCW];
-#pragma unroll
-        for (int i = 0; i < kCW / 2; ++i) {
-          const float2 v = f2_unpack(l2[i]);
-          l[2 * i] = v.x;
-          l[2 * i + 1] = v.y;
-        }
-#pragma unroll
-        for (int o = kCW / 2; o >= 1; o >>= 1) {
-          const bool hi = (lane & o) != 0;
-#pragma unroll
-          for (int x = 0; x < o; ++x) {
-            const float send = hi ? l[x] : l[x + o];
-            const float keep = hi ? l[x + o] : l[x];
-            l[x] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-          }
-        }
-        if constexpr (kCW == 16) l[0] += __shfl_xor_sync(0xffffffffu, l[0], 16);
-        if (lane < kCW) red[qd * kCW + lane] = l[0];
-        named_sync(barid, kGroupThreads);
-        if (tg < kCW) {
-          const int q = tg;
-          const float lt = (red[q] + red[kCW + q]) + (red[2 * kCW + q] + red[3 * kCW + q]);
-          invl_s[q] = lt > 0.f ? 1.0f / lt : 0.f;
-          if (lrow && q < my_rows)
-            lrow[q] = lt > 0.f ? m_s[q] * 0.6931471805599453f + logf(lt) : -INFINITY;
-        }
-        named_sync(barid, kGroupThreads);
-        // O^T row `key` (= d), columns cb.. -> staging rows cb.. of [64 q][128 d]
-        uint16_t *stage = reinterpret_cast<uint16_t *>(smem + OFF_STAGE);
-        {
-          uint32_t r[kCW];
-          tmem_ld_cols(tl + 128 + cb, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < kCW; ++q)
-            stage[(cb + q) * kD + key] = E::bits(__uint_as_float(r[q]) * invl_s[q]);
-        }
+        uint32_t o[64];
+        tmem_ld_rowhalf64(tl + kTO, o);
+        tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar(B_OF));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_OF));  // O may take the next row's first PV
+        float lt;
+        {
+          const float2 a = f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])));
+          lt = a.x + a.y;
+        }
+        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+        const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+        if (P.lse && half == 0 && row < rows)
+          P.lse[(size_t)U.bh_q * P.s_q + qpos] =
+              lt > 0.f ? m * 0.6931471805599453f + logf(lt) : -INFINITY;
+        // staging: d half `half` of row `row`, eight 16-byte chunks, 128-byte swizzle
+        uint8_t *srow = smem + OFF_STAGE + half * kQChunk + row * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int z = 0; z < 4; ++z)
+            w[z] = E::from_f2(__uint_as_float(o[8 * c + 2 * z]) * inv,
+                              __uint_as_float(o[8 * c + 2 * z + 1]) * inv);
+          *reinterpret_cast<uint4 *>(srow + ((c ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
         fence_proxy_async();
-        named_sync(barid, kGroupThreads);
-        if (tg == 0 && my_rows > 0) {
-          bulk_store(orow, sbase + OFF_STAGE + cb * kD * 2, (uint32_t)(my_rows * kD * 2));
+        named_sync(kSoftmaxBar, kSoftmaxThreads);
+        if (tid == 0) {
+          // rows past the end of the sequence are clipped by the tensor map
+          tma_store_3d(&P.to, sbase + OFF_STAGE, 0, q0, U.bh_q);
+          tma_store_3d(&P.to, sbase + OFF_STAGE + kQChunk, 64, q0, U.bh_q);
           bulk_commit();
           bulk_wait_read0();
         }
-        named_sync(barid, kGroupThreads);
+        named_sync(kSoftmaxBar, kSoftmaxThreads);  // the staging tile is free again
       }
       pc += npairs;
     }
     if (!ok) fail(FBM_DEVERR_TIMEOUT);
-    if (tg == 0) bulk_wait0();
+    if (tid == 0) bulk_wait0();
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) {
+  if (warp == kWarpS) {
     __syncwarp();
     tmem_dealloc(tbase, kTmemCols);
   }
@@ -608,7 +547,8 @@ cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   TcParams P;
   memset(&P, 0, sizeof(P));
   if (!make_map(&P.tq, L.q, L.b * L.hq, L.s_q, BF16) || !make_map(&P.tk, L.k, L.b * L.hk, L.s_k, BF16) ||
-      !make_map(&P.tv, L.v, L.b * L.hk, L.s_k, BF16))
+      !make_map(&P.tv, L.v, L.b * L.hk, L.s_k, BF16) ||
+      !make_map(&P.to, L.out, L.b * L.hq, L.s_q, BF16))
     return cudaErrorInvalidValue;
   P.lut = L.lut;
   P.cnt = L.cnt;
