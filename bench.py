@@ -40,8 +40,8 @@ TOPKS = (0.1, 0.2, 0.4, 0.6, 1.0)
 # profiles/), keyed by the sha256 of the kernel source it was taken on; a
 # kernel edited since then reports traffic = null.
 NCU_TRAFFIC = {
-    # profiles/sparse_fmha_tc_b2h32s16384d128_topk04.md: 813.92 MB read + 256.37 MB written
-    "3f8b180bf0ae6cd4": 1070294528,
+    # profiles/sparse_fmha_tc_b2h32s16384d128_topk04.md: 814.69 MB read + 257.47 MB written
+    "590798618900305b": 1072162304,
 }
 
 
