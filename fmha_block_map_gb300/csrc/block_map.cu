@@ -8,13 +8,19 @@
 //                 sum of unit rows (self-similarity = ||sum u||^2 / n^2).
 //                 HBM-bound: it reads Q and K once and writes (d + 1) floats
 //                 per block.
-//  k_score_select one CTA per 32 q blocks of one (batch, head): pooled scores
-//                 by an fp32 4x4 register-tiled product (K-block means streamed
-//                 through double-buffered shared memory in 32-dimension chunks
-//                 by cp.async, shared by the 32 rows), then one warp per row for
-//                 the pooled softmax, a radix (bitwise) threshold search for
-//                 top-k / cdf, and ballot-scan emission of the ascending LUT
-//                 row.  No atomics take part in slot assignment.
+//  k_pooled_scores one CTA per 32 q blocks of one (batch, head): the pooled
+//                 scores scale * qbar . kbar by an fp32 4x4 register-tiled
+//                 product (K-block means streamed through double-buffered shared
+//                 memory in 32-dimension chunks by cp.async, shared by the 32
+//                 rows), written as fp32 into the caller's LUT buffer, which has
+//                 exactly the size of the score matrix.
+//  k_select       one warp per q block: loads its score row, then the pooled
+//                 softmax, a radix (bitwise) threshold search for top-k / cdf,
+//                 and ballot-scan emission of the ascending LUT row over the
+//                 scores it has read.  No atomics take part in slot assignment.
+//                 Apart from the product (which keeps every SM's FMA pipe busy)
+//                 the selection is a chain of warp reductions; a kernel of its
+//                 own runs it at full occupancy.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -125,7 +131,7 @@ __global__ void __launch_bounds__(256, 2) k_pool_sim(PoolSide qs, PoolSide ks) {
 }
 
 // ---------------------------------------------------------------------------
-// k_score_select
+// k_pooled_scores, k_select
 // ---------------------------------------------------------------------------
 
 constexpr int kSelRows = 32;   // q blocks per CTA
@@ -139,24 +145,22 @@ FBM_DEVICE uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-template <int D, int NT>
-__global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
+template <int D>
+__global__ void __launch_bounds__(256) k_pooled_scores(SelectArgs a) {
   extern __shared__ __align__(16) float smem[];
   constexpr int LDQ = D + 4;
   constexpr int NCH = D / kSelDC;                    // d chunks per column tile
   float *q_s = smem;                                 // [32][LDQ]
   float *k_s = q_s + kSelRows * LDQ;                 // [2][128][kSelLDK]
-  float *S_s = k_s + 2 * kSelCols * kSelLDK;         // [32][NT * 32]
   const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.y, bi = blockIdx.z;
+  // scores of this (batch, head): [nq][nk] fp32 over the int32 LUT buffer
+  float *S = reinterpret_cast<float *>(a.lut) + (size_t)(bi * a.hq + h) * a.nq * a.nk;
   const int ratio = a.hq / a.hk;
   const int g = h / ratio;
   const int i0 = blockIdx.x * kSelRows;
   const float *qbar = a.qbar + ((size_t)(bi * a.hq + h) * a.nq) * D;
   const float *kbar = a.kbar + ((size_t)(bi * a.hk + g) * a.nk) * D;
-  const float *qsim = a.qsim + (size_t)(bi * a.hq + h) * a.nq;
-  const float *ksim = a.ksim + (size_t)(bi * a.hk + g) * a.nk;
 
   // chunk c of the whole sweep = (column tile c / NCH, d chunk c % NCH)
   const int ntiles = (a.nk + kSelCols - 1) / kSelCols;
@@ -226,17 +230,29 @@ __global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           const int j = col0 + tc + 32 * m;
-          if (j < a.nk) S_s[(tr * 4 + r) * (NT * 32) + j] = a.scale * acc[r][m];
+          const int i = i0 + tr * 4 + r;
+          if (j < a.nk && i < a.nq) S[(size_t)i * a.nk + j] = a.scale * acc[r][m];
         }
     }
     __syncthreads();
   }
-  __syncthreads();
+}
 
+// one warp per q block (row): 8 warps per CTA
+template <int NT>
+__global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
+  const int lane = threadIdx.x & 31;
+  const int rowid = blockIdx.x * 8 + (threadIdx.x >> 5);  // (batch, head, q block)
+  if (rowid >= a.b * a.hq * a.nq) return;
+  const int i = rowid % a.nq;
+  const int bh = rowid / a.nq;
+  const int h = bh % a.hq, bi = bh / a.hq;
+  const int g = h / (a.hq / a.hk);
+  const float *qsim = a.qsim + (size_t)(bi * a.hq + h) * a.nq;
+  const float *ksim = a.ksim + (size_t)(bi * a.hk + g) * a.nk;
+  const float *srow = reinterpret_cast<const float *>(a.lut) + (size_t)rowid * a.nk;
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int rr = warp; rr < kSelRows; rr += 8) {
-    const int i = i0 + rr;
-    if (i >= a.nq) break;
+  {
     const float theta = hp.theta[h];
     const bool q_similar = qsim[i] > theta;
     const int last_q = (i + 1) * a.blkq - 1;
@@ -253,7 +269,7 @@ __global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid
       elig[t] = valid && (!a.causal || j * a.blkk <= last_q);
       ksim_ok[t] = valid && ksim[j] > theta;
       const bool fin = elig[t] && ksim_ok[t];
-      sc[t] = valid ? S_s[rr * (NT * 32) + j] : 0.f;
+      sc[t] = valid ? srow[j] : 0.f;  // a plain load: this kernel rewrites the row
       key[t] = fin ? order_key(sc[t]) : 0u;
       if (fin) mloc = fmaxf(mloc, sc[t]);
       nfin += fin ? 1 : 0;
@@ -340,7 +356,9 @@ __global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid
       }
     }
     // forced columns / rows, sink, causal; ascending emission by ballot scan
-    const size_t row = ((size_t)(bi * a.hq + h) * a.nq + i);
+    // (over the scores every lane has already read)
+    __syncwarp();
+    const size_t row = (size_t)rowid;
     int32_t *lut = a.lut + row * a.nk;
     int run = 0;
 #pragma unroll
@@ -363,26 +381,32 @@ __global__ void __launch_bounds__(256) k_score_select(SelectArgs a, const __grid
 // ---------------------------------------------------------------------------
 
 size_t block_map_smem_bytes(int d, int nt) {
-  return sizeof(float) * ((size_t)kSelRows * (d + 4) + 2 * (size_t)kSelCols * kSelLDK +
-                          (size_t)kSelRows * nt * 32);
-}
-
-template <int D, int NT>
-static cudaError_t launch_select(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {
-  const size_t smem = block_map_smem_bytes(D, NT);
-  cudaError_t e = cudaFuncSetAttribute(k_score_select<D, NT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((a.nq + kSelRows - 1) / kSelRows, a.hq, a.b);
-  k_score_select<D, NT><<<grid, 256, smem, st>>>(a, hp);
-  return cudaGetLastError();
+  (void)nt;
+  return sizeof(float) * ((size_t)kSelRows * (d + 4) + 2 * (size_t)kSelCols * kSelLDK);
 }
 
 template <int D>
+static cudaError_t launch_scores(const SelectArgs &a, cudaStream_t st) {
+  const size_t smem = block_map_smem_bytes(D, 0);
+  cudaError_t e = cudaFuncSetAttribute(k_pooled_scores<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.nq + kSelRows - 1) / kSelRows, a.hq, a.b);
+  k_pooled_scores<D><<<grid, 256, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int NT>
+static cudaError_t launch_select(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {
+  const int rows = a.b * a.hq * a.nq;
+  k_select<NT><<<(rows + 7) / 8, 256, 0, st>>>(a, hp);
+  return cudaGetLastError();
+}
+
 static cudaError_t launch_select_nt(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {
-  if (a.nk <= 256) return launch_select<D, 8>(a, hp, st);
-  if (a.nk <= 512) return launch_select<D, 16>(a, hp, st);
-  return launch_select<D, 32>(a, hp, st);
+  if (a.nk <= 256) return launch_select<8>(a, hp, st);
+  if (a.nk <= 512) return launch_select<16>(a, hp, st);
+  return launch_select<32>(a, hp, st);
 }
 
 cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
@@ -405,7 +429,9 @@ cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
   a.blkq = kBlk; a.blkk = kBlk;
   a.scale = L.scale; a.causal = L.causal; a.sink = L.sink; a.mode_cdf = L.mode_cdf;
   a.lut = L.lut; a.cnt = L.cnt; a.bmap = L.bmap;
-  return L.d == 128 ? launch_select_nt<128>(a, L.hp, st) : launch_select_nt<64>(a, L.hp, st);
+  e = L.d == 128 ? launch_scores<128>(a, st) : launch_scores<64>(a, st);
+  if (e != cudaSuccess) return e;
+  return launch_select_nt(a, L.hp, st);
 }
 
 }  // namespace fbm
