@@ -108,7 +108,10 @@ size_t fbm_block_map_workspace_bytes(int b, int hq, int hk, int s, int d, int bl
  * hq <= FBM_MAX_HEADS.
  * topk, cdfthreshd, simthreshd1: host float[hq]; exactly one of topk /
  *   cdfthreshd is non-NULL; topk and cdfthreshd values in (0, 1].
- * lut: device int32 [b, hq, nq, nk]; lut_count: device int32 [b, hq, nq];
+ * lut: device int32 [b, hq, nq, nk]; lut_count: device int32 [b, hq, nq].
+ *   During the call the lut buffer also holds the fp32 pooled scores of step 4
+ *   (the same size); it holds the LUT once the stream reaches the end of the
+ *   call, and is unspecified if the call fails.
  * block_map: device uint8 [b, hq, nq, nk] (1 = kept) or NULL.
  * workspace: device, >= fbm_block_map_workspace_bytes(...) bytes, 16-byte
  *   aligned; its contents are scratch between calls.
