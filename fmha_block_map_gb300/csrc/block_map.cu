@@ -285,12 +285,22 @@ __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_const
         const int kcount = min((int)ceilf(prod), nfin);
         // largest T with #(key >= T) >= kcount: the kcount-th largest key
         uint32_t T = 0;
+        // The counts are taken as fp32 work (the ALU pipe is this kernel's
+        // busiest): key >= cand  <=>  score >= float(cand), order_key being
+        // order-preserving on finite scores; excluded entries count as -inf.
+        // A candidate never lies in the key range of NaN or -inf: the
+        // candidate with bit 23 alone is -FLT_MAX's key, which every finite
+        // score reaches, so it is accepted before any lower bit is tried.
+        float fs[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) fs[t] = key[t] ? sc[t] : -INFINITY;
         for (int bit = 31; bit >= 0; --bit) {
           const uint32_t cand = T | (1u << bit);
-          int c = 0;
+          const float cf = __uint_as_float((cand & 0x80000000u) ? (cand & 0x7FFFFFFFu) : ~cand);
+          float cnt = 0.f;
 #pragma unroll
-          for (int t = 0; t < NT; ++t) c += key[t] >= cand ? 1 : 0;
-          const int tot = __reduce_add_sync(0xffffffffu, c);
+          for (int t = 0; t < NT; ++t) cnt += fs[t] >= cf ? 1.f : 0.f;
+          const int tot = __reduce_add_sync(0xffffffffu, (int)cnt);
           if (tot >= kcount) T = cand;
           if (tot == kcount) break;  // exactly kcount keys >= T: no tie left to resolve
         }
