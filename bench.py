@@ -57,6 +57,8 @@ def parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     p.add_argument("--no-extra", action="store_true",
                    help="skip the causal-GQA prefill and sparse-decode measurements")
+    p.add_argument("--decode-only", action="store_true",
+                   help="only the sparse-decode measurement (a small command for profiling it)")
     return p.parse_args()
 
 
@@ -553,6 +555,12 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.decode_only:
+        import torch
+
+        torch.cuda.set_device(0)
+        print(json.dumps({"decode": measure_decode(load_peaks()[0]["hbm_gbs"])}))
+        return
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:
         print(json.dumps(res))
