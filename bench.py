@@ -368,7 +368,8 @@ def run_ours(args):
         "sweep": sweep,
         "e2e": e2e,
         "clocks": clocks,
-        "gpu_launches": 3 * args.steps,
+        # per step: k_pool_sim, k_pooled_scores, k_select and k_fmha_tc
+        "gpu_launches": 4 * args.steps,
     }
     if rank == 0 and not args.no_extra:
         res["causal_gqa"] = measure_causal_gqa(peaks["hbm_gbs"], peak)
