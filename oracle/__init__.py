@@ -32,6 +32,9 @@ Sources (web pages; cited by title and section):
 Block map, as computed here (the pages only name the steps; where they leave a
 step open, the plainest reading is taken):
 
+0. optional K smoothing (README 'Not yet ported': pre-pool k -= km): every key
+   row minus the mean key row of its (batch, KV head) sequence; steps 1-7 then
+   use the smoothed keys (queries unchanged);
 1. pool: qbar_i, kbar_j = mean of the rows of each 64-token block (a partial
    last block averages the rows it has);
 2. self-similarity of a block X of n rows: the mean cosine over all ordered
@@ -61,6 +64,7 @@ from .block_map import (  # noqa: F401
     topk_count,
     select_row,
     block_map_head,
+    smooth_keys,
     sparge_block_map,
 )
 from .attention import (  # noqa: F401

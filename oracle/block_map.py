@@ -102,11 +102,21 @@ def select_row(score: np.ndarray, topk: Optional[float], cdf: Optional[float],
     return sel
 
 
+def smooth_keys(kg: np.ndarray) -> np.ndarray:
+    """K smoothing: every key row minus the mean key row of the sequence,
+    k - km with km = mean over the s_k rows ("Sparge Attention (Composable
+    Kernel)" README, 'Not yet ported': pre-pool k -= km)."""
+    return kg - kg.mean(axis=0, keepdims=True)
+
+
 def block_map_head(qh: np.ndarray, kg: np.ndarray, theta: float, topk: Optional[float],
                    cdf: Optional[float], scale: float, causal: bool, sink: bool,
-                   blkq: int = 64, blkk: int = 64) -> dict:
+                   blkq: int = 64, blkk: int = 64, smooth_k: bool = False) -> dict:
     """Block map of one query head ``qh`` [s_q, d] against its KV head ``kg``
-    [s_k, d] (steps 1-7 of the package header)."""
+    [s_k, d] (steps 1-7 of the package header).  With ``smooth_k`` every step
+    runs on the smoothed keys (``smooth_keys``); the queries are unchanged."""
+    if smooth_k:
+        kg = smooth_keys(kg)
     qbar = pool_blocks(qh, blkq)
     kbar = pool_blocks(kg, blkk)
     nq, nk = qbar.shape[0], kbar.shape[0]
@@ -147,7 +157,8 @@ def sparge_block_map(q: np.ndarray, k: np.ndarray, topk: Optional[np.ndarray],
                      cdfthreshd: Optional[np.ndarray], simthreshd1: np.ndarray,
                      scale: float, causal: bool, attention_sink: bool,
                      blkq: int = 64, blkk: int = 64, keep_aux: bool = False,
-                     dtype: Optional[str] = None, heads: Optional[list] = None) -> dict:
+                     dtype: Optional[str] = None, heads: Optional[list] = None,
+                     smooth_k: bool = False) -> dict:
     """Block map of every (batch, query head): q [b, hq, s, d], k [b, hk, s, d],
     float64 values or, with ``dtype`` = "f16" / "bf16", their bit patterns
     (widened exactly one head at a time).  ``heads`` restricts the work to a
@@ -155,8 +166,9 @@ def sparge_block_map(q: np.ndarray, k: np.ndarray, topk: Optional[np.ndarray],
     Query head h reads KV head h // (hq // hk) (the GQA mapping of ROCm/aiter
     pull 6841: query head j reads KV head j // (hq / hk)).  Per-head
     hyperparameters are arrays of length hq; exactly one of topk / cdfthreshd
-    is given.  Returns the LUT [b, hq, nq, nk] (ascending, -1 padded), the
-    count [b, hq, nq] and the boolean block map."""
+    is given.  ``smooth_k`` applies K smoothing per KV head before pooling.
+    Returns the LUT [b, hq, nq, nk] (ascending, -1 padded), the count
+    [b, hq, nq] and the boolean block map."""
     b, hq, s_q, d = q.shape
     hk = k.shape[1]
     if (topk is None) == (cdfthreshd is None):
@@ -174,7 +186,7 @@ def sparge_block_map(q: np.ndarray, k: np.ndarray, topk: Optional[np.ndarray],
                            float(simthreshd1[h]),
                            None if topk is None else float(topk[h]),
                            None if cdfthreshd is None else float(cdfthreshd[h]),
-                           scale, causal, attention_sink, blkq, blkk)
+                           scale, causal, attention_sink, blkq, blkk, smooth_k)
         lut[bi, h] = r["lut"]
         count[bi, h] = r["count"]
         bmap[bi, h] = r["block_map"]

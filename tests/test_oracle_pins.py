@@ -210,6 +210,56 @@ def test_block_map_hand_example():
     assert r["count"][1] == 1 and r["lut"][1, 0] == 1
 
 
+def test_smooth_k_hand_example():
+    """K smoothing subtracts the mean key row of the sequence (README 'Not yet
+    ported': pre-pool k -= km).  blk = 2, d = 2, two kv blocks whose rows are
+    the constants a = (3, 1) and b = (1, 1): km = (2, 1), the smoothed rows are
+    (1, 0) and (-1, 0), each block still parallel (sim 1), pooled to (1, 0)
+    and (-1, 0).  With q pooled to (1, 1) and (-1, 3) the raw scores are
+    [[4, 2], [0, 2]] without smoothing and [[1, -1], [-1, 1]] with it: each
+    row moves by the constant -qbar_i . km, so the ranking, the softmax and the
+    LUT are unchanged ([[0], [1]] at topk 0.5).  Smoothing changes the map
+    through the self-similarity alone: identical blocks a = b smooth to zero
+    rows, sim 0, and both columns are forced on."""
+    q = np.array([[1, 1], [1, 1], [-1, 3], [-1, 3]], dtype=np.float64)
+    k = np.array([[3, 1], [3, 1], [1, 1], [1, 1]], dtype=np.float64)
+    assert obm.smooth_keys(k).tolist() == [[1, 0], [1, 0], [-1, 0], [-1, 0]]
+    r0 = obm.block_map_head(q, k, 0.5, 0.5, None, 1.0, False, False, 2, 2)
+    r1 = obm.block_map_head(q, k, 0.5, 0.5, None, 1.0, False, False, 2, 2, smooth_k=True)
+    assert r0["raw"].tolist() == [[4, 2], [0, 2]]
+    assert r1["raw"].tolist() == [[1, -1], [-1, 1]]
+    assert r1["kbar"].tolist() == [[1, 0], [-1, 0]]
+    assert r1["simk"].tolist() == [1.0, 1.0]
+    assert r0["lut"].tolist() == r1["lut"].tolist() == [[0, -1], [1, -1]]
+    same = np.array([[3, 1]] * 4, dtype=np.float64)
+    r2 = obm.block_map_head(q, same, 0.5, 0.5, None, 1.0, False, False, 2, 2)
+    r3 = obm.block_map_head(q, same, 0.5, 0.5, None, 1.0, False, False, 2, 2, smooth_k=True)
+    assert np.allclose(r2["simk"], [1.0, 1.0], atol=1e-12)
+    assert r2["lut"].tolist() == [[0, -1], [0, -1]]
+    assert r3["simk"].tolist() == [0.0, 0.0] and r3["lut"].tolist() == [[0, 1], [0, 1]]
+
+
+def test_smooth_k_invariant_to_a_common_key_offset():
+    """Smoothed keys do not depend on a row c added to every key, so neither
+    does the smoothed block map; the unsmoothed map does (through the
+    self-similarity of the shifted rows)."""
+    rng = np.random.default_rng(7)
+    s, d, blk = 256, 16, 16
+    q = rng.standard_normal((s, d))
+    k = np.repeat(rng.standard_normal((s // blk, d)), blk, axis=0) + 0.8 * rng.standard_normal((s, d))
+    c = 6.0 * rng.standard_normal(d)
+    args = (0.3, 0.25, None, 0.25, False, False, blk, blk)
+    a = obm.block_map_head(q, k, *args, smooth_k=True)
+    b = obm.block_map_head(q, k + c, *args, smooth_k=True)
+    assert np.array_equal(a["lut"], b["lut"]) and np.array_equal(a["count"], b["count"])
+    assert np.allclose(a["raw"], b["raw"], atol=1e-9) and np.allclose(a["simk"], b["simk"], atol=1e-12)
+    # the smoothed pooled means of equal-size blocks sum to zero
+    assert np.abs(a["kbar"].sum(axis=0)).max() < 1e-12
+    u = obm.block_map_head(q, k, *args)
+    v = obm.block_map_head(q, k + c, *args)
+    assert not np.allclose(u["simk"], v["simk"], atol=1e-3)
+
+
 def test_all_dissimilar_gives_dense_map():
     cfg = synth.C1
     x = synth.prefill(cfg)
@@ -488,3 +538,18 @@ def test_planted_mistakes_are_caught():
     o1, o2 = np.array([[1.0, 0.0]]), np.array([[0.0, 1.0]])
     o, _ = bad_combine(np.stack([o1, o2]), np.array([[math.log(3.0)], [0.0]]))
     assert np.abs(o[0] - [0.75, 0.25]).max() > 1e-3
+
+
+def test_planted_smoothing_mistake_is_caught(monkeypatch):
+    """Subtracting each block's own mean instead of the sequence mean turns
+    every block of the hand example into zero rows (sim 0, all columns forced):
+    the hand-example pin fails."""
+    def block_mean_smoothing(kg, blk=2):  # planted: per-block instead of per-sequence mean
+        out = kg.copy()
+        for j in range(0, kg.shape[0], blk):
+            out[j:j + blk] -= kg[j:j + blk].mean(axis=0)
+        return out
+
+    monkeypatch.setattr(obm, "smooth_keys", block_mean_smoothing)
+    with pytest.raises(AssertionError):
+        test_smooth_k_hand_example()
