@@ -49,9 +49,9 @@ def lib() -> ctypes.CDLL:
         L.fbm_block_map_workspace_bytes.argtypes = [i32] * 7
         L.fbm_block_map_workspace_bytes.restype = sz
         L.sparge_block_map.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp,
-                                        f32, i32, i32, vp, vp, vp, vp, sz, vp])
+                                        f32, i32, i32, i32, vp, vp, vp, vp, sz, vp])
         L.sparge_block_map_static.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp,
-                                               vp, f32, i32, i32, vp, vp, vp, vp])
+                                               vp, f32, i32, i32, i32, vp, vp, vp, vp])
         L.sparse_fmha_fwd.argtypes = ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                        vp, vp, i32, i32, f32, i32, vp, vp, vp, vp, vp])
         L.attn_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
@@ -133,10 +133,12 @@ def sparge_block_map(q: torch.Tensor, k: torch.Tensor, *, topk=None, cdfthreshd=
                      scale: Optional[float] = None, causal: bool = False,
                      attention_sink: bool = False, return_block_map: bool = False,
                      lut: Optional[torch.Tensor] = None, lut_count: Optional[torch.Tensor] = None,
-                     workspace: Optional[torch.Tensor] = None, stream=None):
+                     workspace: Optional[torch.Tensor] = None, smooth_k: bool = False,
+                     stream=None):
     """Block map of q [b, hq, s, d] against k [b, hk, s, d]; returns
     (lut [b, hq, nq, nk] int32, lut_count [b, hq, nq] int32, block_map or None).
-    topk / cdfthreshd / simthreshd1 are a float or one value per query head."""
+    topk / cdfthreshd / simthreshd1 are a float or one value per query head;
+    smooth_k subtracts the mean key row of each (batch, KV head) first."""
     _cuda(q, "q"), _cuda(k, "k")
     b, hq, s, d = q.shape
     hk = k.shape[1]
@@ -156,7 +158,8 @@ def sparge_block_map(q: torch.Tensor, k: torch.Tensor, *, topk=None, cdfthreshd=
         _ptr(q), _ptr(k), _dt(q), b, hq, hk, s, d, 64, 64,
         _per_head(topk, hq, "topk"), _per_head(cdfthreshd, hq, "cdfthreshd"),
         _per_head(simthreshd1, hq, "simthreshd1"), float(scale), int(causal),
-        int(attention_sink), _ptr(lut), _ptr(lut_count), _ptr(bmap), _ptr(workspace),
+        int(attention_sink), int(smooth_k), _ptr(lut), _ptr(lut_count), _ptr(bmap),
+        _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return lut, lut_count, bmap
 
@@ -166,7 +169,8 @@ def sparge_block_map_static(q: torch.Tensor, k: torch.Tensor, *, topk=None, cdft
                             scale: Optional[float] = None, causal: bool = False,
                             attention_sink: bool = False, return_block_map: bool = False,
                             lut: Optional[torch.Tensor] = None,
-                            lut_count: Optional[torch.Tensor] = None, stream=None):
+                            lut_count: Optional[torch.Tensor] = None, smooth_k: bool = False,
+                            stream=None):
     """sparge_block_map with the library's static scratch array instead of a
     workspace, for callers that cannot allocate device scratch (the outputs
     are still the caller's: pass lut / lut_count to allocate nothing here)."""
@@ -186,7 +190,8 @@ def sparge_block_map_static(q: torch.Tensor, k: torch.Tensor, *, topk=None, cdft
         _ptr(q), _ptr(k), _dt(q), b, hq, hk, s, d, 64, 64,
         _per_head(topk, hq, "topk"), _per_head(cdfthreshd, hq, "cdfthreshd"),
         _per_head(simthreshd1, hq, "simthreshd1"), float(scale), int(causal),
-        int(attention_sink), _ptr(lut), _ptr(lut_count), _ptr(bmap), _stream(stream)))
+        int(attention_sink), int(smooth_k), _ptr(lut), _ptr(lut_count), _ptr(bmap),
+        _stream(stream)))
     return lut, lut_count, bmap
 
 

@@ -56,7 +56,7 @@ fbm_status cuda_status(cudaError_t e, const char *what) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t qbar, qsim, kbar, ksim, total;
+  size_t qbar, qsim, kbar, ksim, kmu, total;
 };
 
 WsLayout ws_layout(int b, int hq, int hk, int s, int d) {
@@ -67,6 +67,7 @@ WsLayout ws_layout(int b, int hq, int hk, int s, int d) {
   w.qsim = off; off = align256(off + sizeof(float) * b * hq * nq);
   w.kbar = off; off = align256(off + sizeof(float) * b * hk * nk * d);
   w.ksim = off; off = align256(off + sizeof(float) * b * hk * nk);
+  w.kmu = off; off = align256(off + sizeof(float) * b * hk * d);
   w.total = off;
   return w;
 }
@@ -116,9 +117,9 @@ size_t fbm_block_map_workspace_bytes(int b, int hq, int hk, int s, int d, int bl
 fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int hq, int hk,
                             int s, int d, int blkq, int blkk, const float *topk,
                             const float *cdfthreshd, const float *simthreshd1, float scale,
-                            int causal, int attention_sink, int32_t *lut, int32_t *lut_count,
-                            uint8_t *block_map, void *workspace, size_t workspace_bytes,
-                            void *stream) {
+                            int causal, int attention_sink, int smooth_k, int32_t *lut,
+                            int32_t *lut_count, uint8_t *block_map, void *workspace,
+                            size_t workspace_bytes, void *stream) {
   if (!q || !k || !lut || !lut_count || !workspace || !simthreshd1)
     return fail(FBM_ERR_INVALID_ARG, "sparge_block_map: null pointer argument");
   if (b <= 0 || hq <= 0 || hk <= 0 || s <= 0 || d <= 0)
@@ -159,11 +160,13 @@ fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int 
   L.b = b; L.hq = hq; L.hk = hk; L.s = s; L.d = d; L.nq = nq; L.nk = nq;
   L.scale = scale; L.causal = causal != 0; L.sink = attention_sink != 0;
   L.mode_cdf = topk == nullptr;
+  L.smooth_k = smooth_k != 0;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   L.qbar = reinterpret_cast<float *>(ws + w.qbar);
   L.qsim = reinterpret_cast<float *>(ws + w.qsim);
   L.kbar = reinterpret_cast<float *>(ws + w.kbar);
   L.ksim = reinterpret_cast<float *>(ws + w.ksim);
+  L.kmu = reinterpret_cast<float *>(ws + w.kmu);
   L.lut = lut; L.cnt = lut_count; L.bmap = block_map;
   return cuda_status(fbm::launch_block_map(L, static_cast<cudaStream_t>(stream)),
                      "sparge_block_map launch");

@@ -8,6 +8,11 @@
 //                 sum of unit rows (self-similarity = ||sum u||^2 / n^2).
 //                 HBM-bound: it reads Q and K once and writes (d + 1) floats
 //                 per block.
+//  k_key_mean     K smoothing only: one CTA per (batch, KV head) forms the mean
+//                 key row from the block sums of the first pooling pass (fixed
+//                 summation order, so the result is deterministic); a second
+//                 pooling pass over K then subtracts it from every key row
+//                 before the norms and sums.
 //  k_pooled_scores one CTA per 32 q blocks of one (batch, head): the pooled
 //                 scores scale * qbar . kbar by an fp32 4x4 register-tiled
 //                 product (K-block means streamed through double-buffered shared
@@ -37,10 +42,13 @@ struct PoolSide {
   int s;              // rows per (batch, head)
   int nb;             // blocks per (batch, head)
   int nunits;         // bh * nb
+  const float *mu;    // [bh, D] row subtracted before pooling (SMOOTH only)
 };
 
-template <class E, int D>
-__global__ void __launch_bounds__(256, 2) k_pool_sim(PoolSide qs, PoolSide ks) {
+template <class E, int D, bool SMOOTH>
+__global__ void __launch_bounds__(256, SMOOTH ? 1 : 2) k_pool_sim(PoolSide qs, PoolSide ks) {
+  // (the centring row of the smoothing pass takes 16 more registers a thread:
+  // one CTA per SM then, instead of spilling)
   // a lane owns 16 consecutive elements (32 bytes) of a row; a row spans LPR
   // lanes and one warp-wide step covers RPI rows
   constexpr int LPR = D / 16;
@@ -59,6 +67,15 @@ __global__ void __launch_bounds__(256, 2) k_pool_sim(PoolSide qs, PoolSide ks) {
   const uint16_t *base = side.x + ((size_t)bh * side.s + row0) * D;
   const int sub = lane % LPR;
   const int rgrp = lane / LPR;
+  float mu[16];
+  if constexpr (SMOOTH) {
+    const float4 *m4 = reinterpret_cast<const float4 *>(side.mu + (size_t)bh * D) + sub * 4;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float4 m = m4[c];
+      mu[4 * c] = m.x; mu[4 * c + 1] = m.y; mu[4 * c + 2] = m.z; mu[4 * c + 3] = m.w;
+    }
+  }
 
   // two interleaved partial sums per element keep the fp32 sums short
   float msum[2][16], usum[16];
@@ -89,6 +106,14 @@ __global__ void __launch_bounds__(256, 2) k_pool_sim(PoolSide qs, PoolSide ks) {
         const float2 f = E::to_f2(w[p]);
         x[2 * p] = f.x;
         x[2 * p + 1] = f.y;
+      }
+      if constexpr (SMOOTH) {
+        // rows past the end stay zero: they add nothing to either sum
+        const int r = (s0 + u) * RPI + rgrp;
+        if (r < n) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) x[e] -= mu[e];
+        }
       }
       float ss = 0.f;
 #pragma unroll
@@ -127,6 +152,34 @@ __global__ void __launch_bounds__(256, 2) k_pool_sim(PoolSide qs, PoolSide ks) {
       dst[c] = make_float4(tot[4 * c] / fn, tot[4 * c + 1] / fn, tot[4 * c + 2] / fn,
                            tot[4 * c + 3] / fn);
     if (sub == 0) side.sim[unit] = su / (fn * fn);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// k_key_mean
+// ---------------------------------------------------------------------------
+
+// mean key row of every (batch, KV head): sum_j n_j * kbar_j / s over the K
+// blocks, n_j the rows of block j.  256 threads = (256 / D) groups of D; group
+// g sums the blocks j = g mod (256 / D), then thread g = 0 adds the groups in
+// order.
+template <int D>
+__global__ void __launch_bounds__(256) k_key_mean(const float *__restrict__ kbar,
+                                                  float *__restrict__ mu, int s, int nk) {
+  constexpr int G = 256 / D;
+  __shared__ float part[G][D];
+  const int e = threadIdx.x % D, g = threadIdx.x / D;
+  const float *base = kbar + (size_t)blockIdx.x * nk * D + e;
+  float acc = 0.f;
+#pragma unroll 8
+  for (int j = g; j < nk; j += G) acc = fmaf((float)min(kBlk, s - j * kBlk), base[(size_t)j * D], acc);
+  part[g][e] = acc;
+  __syncthreads();
+  if (g == 0) {
+    float tot = part[0][e];
+#pragma unroll
+    for (int i = 1; i < G; ++i) tot += part[i][e];
+    mu[(size_t)blockIdx.x * D + e] = tot / (float)s;
   }
 }
 
@@ -419,20 +472,41 @@ static cudaError_t launch_select_nt(const SelectArgs &a, const HeadParams &hp, c
   return launch_select<32>(a, hp, st);
 }
 
-cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
-  PoolSide qs{static_cast<const uint16_t *>(L.q), L.qbar, L.qsim, L.s, L.nq, L.b * L.hq * L.nq};
-  PoolSide ks{static_cast<const uint16_t *>(L.k), L.kbar, L.ksim, L.s, L.nk, L.b * L.hk * L.nk};
-  const int units = qs.nunits + ks.nunits;
-  const int grid = (units + 7) / 8;
+template <bool SMOOTH>
+static void launch_pool(const BlockMapLaunch &L, const PoolSide &qs, const PoolSide &ks,
+                        cudaStream_t st) {
+  const int grid = (qs.nunits + ks.nunits + 7) / 8;
   if (L.d == 128) {
-    if (L.bf16) k_pool_sim<BF16, 128><<<grid, 256, 0, st>>>(qs, ks);
-    else k_pool_sim<F16, 128><<<grid, 256, 0, st>>>(qs, ks);
+    if (L.bf16) k_pool_sim<BF16, 128, SMOOTH><<<grid, 256, 0, st>>>(qs, ks);
+    else k_pool_sim<F16, 128, SMOOTH><<<grid, 256, 0, st>>>(qs, ks);
   } else {
-    if (L.bf16) k_pool_sim<BF16, 64><<<grid, 256, 0, st>>>(qs, ks);
-    else k_pool_sim<F16, 64><<<grid, 256, 0, st>>>(qs, ks);
+    if (L.bf16) k_pool_sim<BF16, 64, SMOOTH><<<grid, 256, 0, st>>>(qs, ks);
+    else k_pool_sim<F16, 64, SMOOTH><<<grid, 256, 0, st>>>(qs, ks);
   }
+}
+
+cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
+  PoolSide qs{static_cast<const uint16_t *>(L.q), L.qbar, L.qsim, L.s, L.nq, L.b * L.hq * L.nq,
+              nullptr};
+  PoolSide ks{static_cast<const uint16_t *>(L.k), L.kbar, L.ksim, L.s, L.nk, L.b * L.hk * L.nk,
+              nullptr};
+  launch_pool<false>(L, qs, ks, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (L.smooth_k) {
+    // K smoothing: mean key row from the block means just written, then pool
+    // and measure K again on the centred rows (Q results are kept)
+    if (L.d == 128) k_key_mean<128><<<L.b * L.hk, 256, 0, st>>>(L.kbar, L.kmu, L.s, L.nk);
+    else k_key_mean<64><<<L.b * L.hk, 256, 0, st>>>(L.kbar, L.kmu, L.s, L.nk);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    PoolSide none = qs;
+    none.nunits = 0;
+    ks.mu = L.kmu;
+    launch_pool<true>(L, none, ks, st);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   SelectArgs a{};
   a.qbar = L.qbar; a.qsim = L.qsim; a.kbar = L.kbar; a.ksim = L.ksim;
   a.b = L.b; a.hq = L.hq; a.hk = L.hk; a.nq = L.nq; a.nk = L.nk;

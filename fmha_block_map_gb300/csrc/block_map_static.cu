@@ -59,7 +59,7 @@ extern "C" fbm_status sparge_block_map_static(const void *q, const void *k, int 
                                               int hq, int hk, int s, int d, int blkq, int blkk,
                                               const float *topk, const float *cdfthreshd,
                                               const float *simthreshd1, float scale, int causal,
-                                              int attention_sink, int32_t *lut,
+                                              int attention_sink, int smooth_k, int32_t *lut,
                                               int32_t *lut_count, uint8_t *block_map,
                                               void *stream) {
   const size_t need = fbm_block_map_workspace_bytes(b, hq, hk, s, d, blkq, blkk);
@@ -80,6 +80,6 @@ extern "C" fbm_status sparge_block_map_static(const void *q, const void *k, int 
     return fbm::set_message(FBM_ERR_CUDA, msg);
   }
   return sparge_block_map(q, k, dtype, b, hq, hk, s, d, blkq, blkk, topk, cdfthreshd, simthreshd1,
-                          scale, causal, attention_sink, lut, lut_count, block_map, ws,
+                          scale, causal, attention_sink, smooth_k, lut, lut_count, block_map, ws,
                           FBM_STATIC_SCRATCH_BYTES, stream);
 }

@@ -26,9 +26,9 @@ struct BlockMapLaunch {
   const void *q, *k;
   int bf16, b, hq, hk, s, d, nq, nk;
   float scale;
-  int causal, sink, mode_cdf;
+  int causal, sink, mode_cdf, smooth_k;
   HeadParams hp;
-  float *qbar, *qsim, *kbar, *ksim;  // workspace carve-out
+  float *qbar, *qsim, *kbar, *ksim, *kmu;  // workspace carve-out
   int32_t *lut, *cnt;
   uint8_t *bmap;
 };

@@ -76,7 +76,8 @@ fbm_status fbm_get_error(void *stream, uint32_t *detail);
 
 /*
  * Workspace (bytes) that sparge_block_map needs for the given shape: pooled
- * means (fp32) and self-similarities (fp32) of every Q and K block.
+ * means (fp32) and self-similarities (fp32) of every Q and K block, and the
+ * mean key row (fp32) of every (batch, KV head) for K smoothing.
  */
 size_t fbm_block_map_workspace_bytes(int b, int hq, int hk, int s, int d, int blkq,
                                      int blkk);
@@ -86,6 +87,11 @@ size_t fbm_block_map_workspace_bytes(int b, int hq, int hk, int s, int d, int bl
  * Kernel)" README: mean-pool -> cosine sim -> pooled QK -> top-k LUT).
  *
  * For every (batch, query head h, q block i), with KV head g = h / (hq / hk):
+ *   0. smooth_k != 0 (K smoothing; the README lists it, pre-pool k -= km, as
+ *      'Not yet ported'): every key row of (batch, g) minus the mean key row
+ *      km of its s rows; steps 1-7 use the smoothed keys, queries unchanged.
+ *      The pooled scores of a q row move by one constant, so only the K
+ *      self-similarities (step 2) can change the result;
  *   1. qbar_i, kbar_j = means of the rows of each block (a partial last block
  *      averages the rows it has);
  *   2. sim(X) = || sum_t x_t / ||x_t|| ||^2 / n^2 of every block; a block is
@@ -119,9 +125,9 @@ size_t fbm_block_map_workspace_bytes(int b, int hq, int hk, int s, int d, int bl
 fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int hq, int hk,
                             int s, int d, int blkq, int blkk, const float *topk,
                             const float *cdfthreshd, const float *simthreshd1, float scale,
-                            int causal, int attention_sink, int32_t *lut, int32_t *lut_count,
-                            uint8_t *block_map, void *workspace, size_t workspace_bytes,
-                            void *stream);
+                            int causal, int attention_sink, int smooth_k, int32_t *lut,
+                            int32_t *lut_count, uint8_t *block_map, void *workspace,
+                            size_t workspace_bytes, void *stream);
 
 /*
  * sparge_block_map_static - sparge_block_map for callers that cannot allocate.
@@ -145,7 +151,7 @@ fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int 
 fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int b, int hq, int hk,
                                    int s, int d, int blkq, int blkk, const float *topk,
                                    const float *cdfthreshd, const float *simthreshd1, float scale,
-                                   int causal, int attention_sink, int32_t *lut,
+                                   int causal, int attention_sink, int smooth_k, int32_t *lut,
                                    int32_t *lut_count, uint8_t *block_map, void *stream);
 
 /*

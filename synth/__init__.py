@@ -107,6 +107,7 @@ class PrefillConfig:
     diffuse_frac: float = 0.25
     drift: float = 0.0
     antithetic_diffuse: bool = False  # diffuse blocks built from +/- row pairs
+    key_offset: float = 0.0  # std of one offset vector shared by all keys of a (batch, head)
 
     @property
     def scale(self) -> float:
@@ -172,7 +173,7 @@ def _tensor_f32(rng: np.random.Generator, b: int, h: int, s: int, d: int,
 def prefill(cfg: PrefillConfig) -> dict:
     """Q, K, V bit patterns (uint16, [b,h,s,d] contiguous) for a prefill config."""
     ss = np.random.SeedSequence(cfg.seed)
-    s_q, s_k, s_v, s_cs = ss.spawn(4)
+    s_q, s_k, s_v, s_cs, s_off = ss.spawn(5)
     rng_cs = np.random.default_rng(s_cs)
     if cfg.cs_range is not None:
         cs_q = rng_cs.uniform(cfg.cs_range[0], cfg.cs_range[1], size=cfg.hq)
@@ -185,6 +186,11 @@ def prefill(cfg: PrefillConfig) -> dict:
     q = _tensor_f32(np.random.default_rng(s_q), cfg.b, cfg.hq, cfg.s, cfg.d, cfg, cs_q)
     k = _tensor_f32(np.random.default_rng(s_k), cfg.b, cfg.hk, cfg.s, cfg.d, cfg, cs_k)
     v = _tensor_f32(np.random.default_rng(s_v), cfg.b, cfg.hk, cfg.s, cfg.d, cfg, cs_k)
+    if cfg.key_offset > 0.0:
+        # a channel bias common to every key of a head (the structure K
+        # smoothing removes), drawn from its own stream so the rest is unchanged
+        off = np.random.default_rng(s_off).standard_normal((cfg.b, cfg.hk, 1, cfg.d))
+        k = k + (off * cfg.key_offset).astype(np.float32)
     return {
         "q": to_bits(q, cfg.dtype),
         "k": to_bits(k, cfg.dtype),

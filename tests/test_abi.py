@@ -42,8 +42,9 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_workspace_size(L):
     n = fbm.block_map_workspace_bytes(2, 32, 32, 16384, 128)
-    # pooled means (fp32) and sims (fp32) of 2*32*256 q and k blocks, 256-B aligned pieces
-    assert n >= 2 * (2 * 32 * 256 * 128 * 4 + 2 * 32 * 256 * 4)
+    # pooled means (fp32) and sims (fp32) of 2*32*256 q and k blocks, the mean key rows of
+    # 2*32 KV heads, 256-B aligned pieces
+    assert n >= 2 * (2 * 32 * 256 * 128 * 4 + 2 * 32 * 256 * 4) + 2 * 32 * 128 * 4
     assert L.fbm_block_map_workspace_bytes(1, 1, 1, 64, 64, 32, 64) == 0
 
 
@@ -53,12 +54,13 @@ FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: checks fail befo
 def _bm(L, **kw):
     a = dict(q=FAKE, k=FAKE, dtype=0, b=1, hq=2, hk=2, s=512, d=64, blkq=64, blkk=64,
              topk=(ctypes.c_float * 2)(0.5, 0.5), cdf=None,
-             sim=(ctypes.c_float * 2)(0.001, 0.001), scale=0.125, causal=0, sink=0,
+             sim=(ctypes.c_float * 2)(0.001, 0.001), scale=0.125, causal=0, sink=0, smooth=0,
              lut=FAKE, cnt=FAKE, bmap=None, ws=FAKE, wsb=1 << 30)
     a.update(kw)
     return L.sparge_block_map(a["q"], a["k"], a["dtype"], a["b"], a["hq"], a["hk"], a["s"],
                               a["d"], a["blkq"], a["blkk"], a["topk"], a["cdf"], a["sim"],
-                              a["scale"], a["causal"], a["sink"], a["lut"], a["cnt"], a["bmap"],
+                              a["scale"], a["causal"], a["sink"], a["smooth"], a["lut"], a["cnt"],
+                              a["bmap"],
                               a["ws"], a["wsb"], None)
 
 
@@ -141,7 +143,7 @@ def test_static_block_map_rejects_oversized_shapes_on_the_host(L):
     assert need > fbm.FBM_STATIC_SCRATCH_BYTES
     arr = (ctypes.c_float * 64)(*([0.1] * 64))
     st = L.sparge_block_map_static(FAKE, FAKE, 0, 2, 64, 64, 32768, 128, 64, 64, arr, None, arr,
-                                   0.08, 0, 0, FAKE, FAKE, None, None)
+                                   0.08, 0, 0, 0, FAKE, FAKE, None, None)
     assert st == fbm.FBM_ERR_UNSUPPORTED
     assert b"static array" in L.fbm_last_error_message()
 

@@ -12,20 +12,21 @@ from _util import SIM_MARGIN, cached_prefill, compare_lut_rows, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_case(fbm, cfg, mode, param, heads=None, check_sim_margin=True):
+def run_case(fbm, cfg, mode, param, heads=None, check_sim_margin=True, smooth_k=False):
     x = cached_prefill(cfg)
     q, k = to_dev(x["q"], cfg.dtype), to_dev(x["k"], cfg.dtype)
     kw = {"topk": param} if mode == "topk" else {"cdfthreshd": param}
     lut, cnt, bmap = fbm.sparge_block_map(q, k, simthreshd1=cfg.simthreshd1, scale=cfg.scale,
                                           causal=cfg.causal, attention_sink=cfg.attention_sink,
-                                          return_block_map=True, **kw)
+                                          return_block_map=True, smooth_k=smooth_k, **kw)
     assert fbm.get_error() == 0
     lut, cnt, bmap = lut.cpu().numpy(), cnt.cpu().numpy(), bmap.cpu().numpy()
     ph = synth.per_head(cfg, param)
     ora = oracle.sparge_block_map(x["q"], x["k"], ph if mode == "topk" else None,
                                   ph if mode == "cdf" else None,
                                   synth.per_head(cfg, cfg.simthreshd1), cfg.scale, cfg.causal,
-                                  cfg.attention_sink, keep_aux=True, dtype=cfg.dtype, heads=heads)
+                                  cfg.attention_sink, keep_aux=True, dtype=cfg.dtype, heads=heads,
+                                  smooth_k=smooth_k)
     todo = heads or [(b, h) for b in range(cfg.b) for h in range(cfg.hq)]
     exact = near = 0
     for b, h in todo:
@@ -115,3 +116,40 @@ def test_block_map_is_deterministic(fbm_gpu):
         if ref is None:
             ref = cur
         assert torch.equal(cur[0], ref[0]) and torch.equal(cur[1], ref[1])
+
+
+# K smoothing (pre-pool k -= km): keys carry a channel bias common to the whole
+# head (key_offset), which makes every unsmoothed K block look similar; the
+# thresholds sit where smoothing changes the similar / non-similar split.
+
+def test_smooth_k_c1_key_offset(fbm_gpu):
+    cfg = synth.C1.replace(key_offset=2.0, simthreshd1=0.5)
+    lut, cnt, _, _ = run_case(fbm_gpu, cfg, "topk", 0.5, smooth_k=True)
+    raw_lut, raw_cnt, _, _ = run_case(fbm_gpu, cfg, "topk", 0.5, smooth_k=False)
+    assert not np.array_equal(cnt, raw_cnt)  # smoothing changed the map on this input
+
+
+def test_smooth_k_causal_gqa_sink(fbm_gpu):
+    cfg = synth.C1.replace(hq=4, hk=2, causal=True, attention_sink=True, key_offset=2.0,
+                           simthreshd1=0.5)
+    lut, cnt, _, _ = run_case(fbm_gpu, cfg, "topk", 0.3, smooth_k=True)
+    assert (lut[..., 0] == 0).all()
+
+
+def test_smooth_k_ragged_sequence(fbm_gpu):
+    # s = 1000: the last K block has 40 rows and weighs 40 / 1000 in the mean
+    cfg = synth.C2.replace(b=2, hq=2, hk=1, s=1000, cs_range=None, dtype="f16",
+                           key_offset=1.5, simthreshd1=0.4)
+    run_case(fbm_gpu, cfg, "topk", 0.25, smooth_k=True)
+    run_case(fbm_gpu, cfg.replace(causal=True, attention_sink=True), "cdf", 0.8, smooth_k=True)
+
+
+def test_smooth_k_c2_cdf(fbm_gpu):
+    cfg = synth.C2.replace(key_offset=2.0, simthreshd1=0.3)
+    run_case(fbm_gpu, cfg, "cdf", 0.9, smooth_k=True)
+
+
+def test_smooth_k_c3_sampled_heads(fbm_gpu):
+    heads = [(0, 3), (1, 30)]
+    run_case(fbm_gpu, synth.C3, "topk", 0.4, heads=heads, smooth_k=True)
+

@@ -35,7 +35,7 @@ def _call_static(fbm, q, k, mode, param, theta, causal, sink, bmap):
     st = fbm.lib().sparge_block_map_static(
         ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
         fbm.FBM_F16 if q.dtype == torch.float16 else fbm.FBM_BF16, b, hq, hk, s, d, 64, 64,
-        topk, cdf, arr(theta), 1.0 / math.sqrt(d), int(causal), int(sink),
+        topk, cdf, arr(theta), 1.0 / math.sqrt(d), int(causal), int(sink), 0,
         ctypes.c_void_p(lut.data_ptr()), ctypes.c_void_p(cnt.data_ptr()),
         ctypes.c_void_p(bmap.data_ptr()), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == fbm.FBM_OK, fbm.lib().fbm_last_error_message()
@@ -73,3 +73,14 @@ def test_static_scratch_headline_shape_fits_and_matches(fbm_gpu):
     for _ in range(2):
         lut, cnt, _ = fbm_gpu.sparge_block_map_static(q, k, topk=0.4, scale=cfg.scale)
         assert torch.equal(lut, ref_lut) and torch.equal(cnt, ref_cnt)
+
+
+def test_static_scratch_with_k_smoothing_matches(fbm_gpu):
+    cfg = synth.C2.replace(hq=4, hk=2, key_offset=2.0, simthreshd1=0.3)
+    x = synth.prefill(cfg)
+    q, k = to_dev(x["q"], cfg.dtype), to_dev(x["k"], cfg.dtype)
+    a = fbm_gpu.sparge_block_map(q, k, cdfthreshd=0.9, simthreshd1=0.3, scale=cfg.scale,
+                                 smooth_k=True)
+    b = fbm_gpu.sparge_block_map_static(q, k, cdfthreshd=0.9, simthreshd1=0.3, scale=cfg.scale,
+                                        smooth_k=True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
