@@ -74,6 +74,8 @@ from .attention import (  # noqa: F401
     split_bounds,
     split_partials_unit,
     combine,
+    shard_lut_row,
+    context_parallel_unit,
     decode_rows,
     decode_attention,
     decode_partials,

@@ -11,6 +11,9 @@ Sources:
   LSE = -inf.
 * ROCm/aiter pull 6841: the exported LSE is the logsumexp of the scores that
   were actually computed (the selected blocks), -inf for an empty LUT row.
+* ROCm/aiter pull 6841: the LSE is exported so that partial attentions over
+  disjoint key sets can be merged across ranks (ring / context parallelism);
+  here the kv blocks are cut into contiguous per-rank ranges.
 * ROCm/aiter pull 4919: sparse MLA decode - each query lists top-k token
   positions, resolved through a page table into rows of a paged cache; a K row
   is 512 latent + 64 rotary values and V is its latent plane; the key list is
@@ -147,6 +150,35 @@ def combine(o_parts: np.ndarray, lse_parts: np.ndarray):
         out[live] = (w[:, :, None] * o_parts[:, live]).sum(axis=0) / wsum[:, None]
         lse[live] = m[live] + np.log(wsum)
     return out, lse
+
+
+# ----------------------------------------------------------------------------
+# Context parallelism over the kv blocks
+# ----------------------------------------------------------------------------
+
+def shard_lut_row(lut_row: Iterable[int], lo: int, hi: int) -> list:
+    """The entries of a LUT row inside the kv-block range [lo, hi), in their
+    order, re-based to the range (e - lo): the row as seen by the rank that
+    holds K/V blocks lo .. hi - 1."""
+    return [int(e) - lo for e in lut_row if lo <= int(e) < hi]
+
+
+def context_parallel_unit(qh: np.ndarray, kg: np.ndarray, vg: np.ndarray, lut_row, i: int,
+                          world: int, blkq: int, blkk: int, scale: float):
+    """Partials of one q block under context parallelism over ``world`` ranks
+    (non-causal): rank r holds the kv blocks of split_bounds(nk, world)[r] (K/V
+    rows [lo * blkk, min(hi * blkk, s_k))) and attends over its shard of the
+    LUT row.  Returns (O_parts [world, rows, dv], LSE_parts [world, rows]);
+    ``combine`` of them is the attention of the whole row."""
+    nk = (kg.shape[0] + blkk - 1) // blkk
+    outs, lses = [], []
+    for lo, hi in split_bounds(nk, world):
+        r0, r1 = lo * blkk, min(hi * blkk, kg.shape[0])
+        o, l = attention_unit(qh, kg[r0:r1], vg[r0:r1], shard_lut_row(lut_row, lo, hi), i,
+                              blkq, blkk, scale, False)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
 
 
 # ----------------------------------------------------------------------------

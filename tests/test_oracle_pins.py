@@ -469,6 +469,64 @@ def test_split_partials_combine_to_the_full_row(S):
 
 
 # ----------------------------------------------------------------------------
+# context parallelism over the kv blocks
+# ----------------------------------------------------------------------------
+
+def test_shard_lut_row_hand_example():
+    row = [0, 2, 3, 5, 7]
+    assert oatt.shard_lut_row(row, 0, 2) == [0]
+    assert oatt.shard_lut_row(row, 2, 6) == [0, 1, 3]
+    assert oatt.shard_lut_row(row, 6, 8) == [1]
+    assert oatt.shard_lut_row(row, 8, 9) == []
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 5])
+def test_shards_partition_every_row(world):
+    rng = np.random.default_rng(world)
+    nk = 13
+    bounds = oracle.split_bounds(nk, world)
+    for _ in range(200):
+        row = sorted(rng.choice(nk, size=int(rng.integers(0, nk + 1)), replace=False).tolist())
+        back = []
+        for lo, hi in bounds:
+            sh = oatt.shard_lut_row(row, lo, hi)
+            assert all(0 <= e < hi - lo for e in sh)
+            assert all(a < b for a, b in zip(sh, sh[1:]))
+            back += [e + lo for e in sh]
+        assert back == row
+
+
+def _cp_case(world):
+    rng = np.random.default_rng(100 + world)
+    q = rng.standard_normal((256, 32))
+    k = rng.standard_normal((1000, 32))       # 16 kv blocks, the last one 40 rows
+    v = rng.standard_normal((1000, 16))
+    row = [1, 4, 5, 6, 15]                      # no block of 7 .. 14: some ranks empty
+    parts = oatt.context_parallel_unit(q, k, v, row, 3, world, 64, 64, 0.3)
+    ref = oatt.attention_unit(q, k, v, row, 3, 64, 64, 0.3, False)
+    return parts, ref
+
+
+@pytest.mark.parametrize("world", [2, 3, 5])
+def test_context_parallel_combines_to_the_full_row(world):
+    (o_parts, l_parts), ref = _cp_case(world)
+    assert o_parts.shape[0] == world
+    o, l = oracle.combine(o_parts, l_parts)
+    assert np.abs(o - ref[0]).max() < 1e-10 and np.abs(l - ref[1]).max() < 1e-10
+    if world == 5:   # blocks 7 .. 9 and 10 .. 12 hold no entry: empty partials
+        assert np.isneginf(l_parts[2]).all() and (o_parts[2] == 0).all()
+
+
+def test_planted_cp_mistake_is_caught(monkeypatch):
+    """A shard that keeps the global block index (no re-basing to the rank's
+    own K rows) attends over the wrong keys: the combine pin fails."""
+    monkeypatch.setattr(oatt, "shard_lut_row",
+                        lambda row, lo, hi: [int(e) for e in row if lo <= int(e) < hi])
+    with pytest.raises(AssertionError):
+        test_context_parallel_combines_to_the_full_row(2)
+
+
+# ----------------------------------------------------------------------------
 # decode
 # ----------------------------------------------------------------------------
 
