@@ -266,6 +266,36 @@ def run_ours(args):
                           "speedup_vs_dense_step": round(dense_ms / (a + bm), 3)})
         block_map(args.topk)
 
+    # ---- context parallelism over kv-block ranges, two ranks emulated one after
+    # the other on this GPU: each rank's LUT shard + fp32 partial, then the combine
+    cp_res = None
+    if rank == 0 and not args.no_extra:
+        from fmha_block_map_gb300 import cp
+
+        bounds = cp.kv_shard_bounds(cfg.nq, 2)
+        shards = []
+        for lo, hi in bounds:
+            r0, r1 = cp.shard_rows(cfg.s, lo, hi)
+            shards.append((k[:, :, r0:r1].contiguous(), v[:, :, r0:r1].contiguous(), lo, hi))
+        o_all = torch.empty((2,) + tuple(out.shape), dtype=torch.float32, device="cuda")
+        l_all = torch.empty((2,) + tuple(out.shape[:-1]), dtype=torch.float32, device="cuda")
+
+        def cp_step():
+            for r, (ks, vs, lo, hi) in enumerate(shards):
+                cp.rank_partial(q, ks, vs, lut, cnt, lo, hi, scale=cfg.scale, o_slot=o_all[r],
+                                lse_slot=l_all[r])
+            fbm.attn_combine(o_all, l_all, out_dtype=q.dtype, out=out)
+
+        cp_ms = timed(cp_step, 5, 1)
+        comb_ms = timed(lambda: fbm.attn_combine(o_all, l_all, out_dtype=q.dtype, out=out), 5, 1)
+        cp_res = {"ranks": 2, "emulated": "both ranks on one GPU, one after the other",
+                  "ms": round(cp_ms, 4), "combine_ms": round(comb_ms, 4),
+                  "eff_tflops": round(flops / (cp_ms * 1e-3) / 1e12, 1),
+                  "partial_kernel": ("tcgen05" if fbm.fmha_kernel_kind(q.dtype, cfg.d, cfg.d, 1,
+                                                                   cfg.s, cfg.s) == 1
+                                     else "mma.sync") + " (fp32 partial output)"}
+        del shards, o_all, l_all
+
     # ---- end to end through the public API with host buffers: every step copies
     # its Q, K, V from pinned host memory and reads its O back.  Double buffers;
     # the uploads and the read-backs run on two copy streams (the host link is
@@ -369,6 +399,7 @@ def run_ours(args):
                      "traffic": traffic, "selected_tiles": tiles,
                      "flop_per_tile": FLOP_PER_TILE, "attn_ms": round(at_ms, 4)},
         "sweep": sweep,
+        "context_parallel": cp_res,
         "e2e": e2e,
         "clocks": clocks,
         # per step: k_pool_sim, k_pooled_scores, k_select and k_fmha_tc

@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
         L.sparse_fmha_fwd.argtypes = ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                        vp, vp, i32, i32, f32, i32, vp, vp, vp, vp, vp])
         L.attn_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
+        L.lut_shard.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp]
         L.sparse_decode_fwd.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, i32, vp,
                                          i32, i32, f32, vp, vp, vp])
         L.fbm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
@@ -62,7 +63,7 @@ def lib() -> ctypes.CDLL:
         L.fbm_fmha_kernel_kind.argtypes = [i32] * 6
         L.fbm_fmha_kernel_kind.restype = i32
         for name in ("fbm_get_error", "sparge_block_map", "sparge_block_map_static",
-                     "sparse_fmha_fwd", "attn_combine", "sparse_decode_fwd"):
+                     "sparse_fmha_fwd", "attn_combine", "lut_shard", "sparse_decode_fwd"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -201,10 +202,12 @@ def sparse_fmha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                     return_lse: bool = False, num_splits: int = 1,
                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                     o_partial: Optional[torch.Tensor] = None,
-                    lse_partial: Optional[torch.Tensor] = None, stream=None):
+                    lse_partial: Optional[torch.Tensor] = None, partial: bool = False,
+                    stream=None):
     """Sparse (lut given) or dense (lut None) attention.  num_splits == 1
-    returns (out, lse or None); num_splits > 1 returns the fp32 partials
-    (o_partial [S, b, hq, s_q, dv], lse_partial [S, b, hq, s_q])."""
+    returns (out, lse or None); num_splits > 1, or ``partial`` (one whole-row
+    partial, e.g. one slot of a context-parallel stack), returns the fp32
+    partials (o_partial [S, b, hq, s_q, dv], lse_partial [S, b, hq, s_q])."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _cuda(t, n)
     b, hq, s_q, d = q.shape
@@ -218,7 +221,8 @@ def sparse_fmha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
             raise TypeError("lut / lut_count must be int32")
         stride = lut.shape[-1]
     dev = q.device
-    if num_splits == 1:
+    partial = partial or num_splits > 1
+    if not partial:
         if out is None:
             out = torch.empty((b, hq, s_q, dv), dtype=q.dtype, device=dev)
         if return_lse and lse is None:
@@ -231,9 +235,10 @@ def sparse_fmha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     _check(lib().sparse_fmha_fwd(
         _ptr(q), _ptr(k), _ptr(v), _dt(q), b, hq, hk, s_q, s_k, d, dv, 64, 64,
         _ptr(lut), _ptr(lut_count), stride, num_splits, float(scale), int(causal),
-        _ptr(out) if num_splits == 1 else None, _ptr(lse) if num_splits == 1 else None,
-        _ptr(o_partial), _ptr(lse_partial), _stream(stream)))
-    if num_splits == 1:
+        None if partial else _ptr(out), None if partial else _ptr(lse),
+        _ptr(o_partial) if partial else None, _ptr(lse_partial) if partial else None,
+        _stream(stream)))
+    if not partial:
         return out, lse
     return o_partial, lse_partial
 
@@ -254,6 +259,30 @@ def attn_combine(o_part: torch.Tensor, lse_part: torch.Tensor, *, out_dtype=torc
     _check(lib().attn_combine(_ptr(o_part), _ptr(lse_part), S, rows, dv, codes[out.dtype],
                               _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
+
+
+def lut_shard(lut: torch.Tensor, lut_count: torch.Tensor, lo: int, hi: int, *,
+              out_lut: Optional[torch.Tensor] = None, out_count: Optional[torch.Tensor] = None,
+              stream=None):
+    """The entries of every LUT row (lut [..., stride], lut_count [...]) inside
+    the kv-block range [lo, hi), re-based to lo: (out_lut [..., hi - lo],
+    out_count [...]), -1 padded."""
+    _cuda(lut, "lut"), _cuda(lut_count, "lut_count")
+    if lut.dtype != torch.int32 or lut_count.dtype != torch.int32:
+        raise TypeError("lut / lut_count must be int32")
+    lead = tuple(lut.shape[:-1])
+    if tuple(lut_count.shape) != lead:
+        raise ValueError("lut_count must have the shape of lut without its last dimension")
+    if out_lut is None:
+        out_lut = torch.empty(lead + (hi - lo,), dtype=torch.int32, device=lut.device)
+    if out_count is None:
+        out_count = torch.empty(lead, dtype=torch.int32, device=lut.device)
+    _cuda(out_lut, "out_lut"), _cuda(out_count, "out_count")
+    if tuple(out_lut.shape[:-1]) != lead or tuple(out_count.shape) != lead:
+        raise ValueError("out_lut / out_count must have the leading shape of lut")
+    _check(lib().lut_shard(_ptr(lut), _ptr(lut_count), lut_count.numel(), lut.shape[-1], lo, hi,
+                           _ptr(out_lut), _ptr(out_count), out_lut.shape[-1], _stream(stream)))
+    return out_lut, out_count
 
 
 def sparse_decode_fwd(q: torch.Tensor, kv_cache: torch.Tensor, page_table: torch.Tensor,

@@ -203,9 +203,11 @@ fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtyp
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: lut_stride must be >= 1");
   if (num_splits < 1 || num_splits > 64)
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: num_splits in [1, 64]");
-  if (num_splits == 1 && !out) return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: null out");
-  if (num_splits > 1 && (!o_partial || !lse_partial))
-    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: split mode needs o_partial and lse_partial");
+  const bool partial = num_splits > 1 || out == nullptr;
+  if (partial && (!o_partial || !lse_partial))
+    return fail(FBM_ERR_INVALID_ARG,
+                num_splits > 1 ? "sparse_fmha_fwd: split mode needs o_partial and lse_partial"
+                               : "sparse_fmha_fwd: null out (and no o_partial / lse_partial)");
   if (!(scale > 0.f) || !std::isfinite(scale))
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: scale must be positive and finite");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (out && !aligned16(out)) ||
@@ -219,7 +221,10 @@ fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtyp
   L.b = b; L.hq = hq; L.hk = hk; L.s_q = s_q; L.s_k = s_k; L.d = d; L.nq = nq; L.nk = nk;
   L.lut = lut; L.cnt = lut_count; L.lut_stride = lut ? lut_stride : nk;
   L.num_splits = num_splits; L.causal = causal != 0; L.scale = scale;
-  L.out = out; L.lse = lse; L.o_part = o_partial; L.lse_part = lse_partial;
+  L.out = partial ? nullptr : out;
+  L.lse = partial ? nullptr : lse;
+  L.o_part = partial ? o_partial : nullptr;
+  L.lse_part = partial ? lse_partial : nullptr;
   L.err = error_word();
   if (!L.err) return fail(FBM_ERR_CUDA, "sparse_fmha_fwd: error word lookup failed");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -245,6 +250,26 @@ fbm_status attn_combine(const float *o_part, const float *lse_part, int num_spli
   fbm::CombineLaunch L{o_part, lse_part, num_splits, rows, dv, out_dtype, out, lse_out};
   return cuda_status(fbm::launch_combine(L, static_cast<cudaStream_t>(stream)),
                      "attn_combine launch");
+}
+
+fbm_status lut_shard(const int32_t *lut, const int32_t *lut_count, int64_t rows, int lut_stride,
+                     int lo, int hi, int32_t *out_lut, int32_t *out_count, int out_stride,
+                     void *stream) {
+  if (!lut || !lut_count || !out_lut || !out_count)
+    return fail(FBM_ERR_INVALID_ARG, "lut_shard: null pointer");
+  if (rows <= 0 || lut_stride < 1 || out_stride < 1)
+    return fail(FBM_ERR_INVALID_ARG, "lut_shard: rows, lut_stride and out_stride must be positive");
+  if (lo < 0 || hi <= lo)
+    return fail(FBM_ERR_INVALID_ARG, "lut_shard: need 0 <= lo < hi");
+  if (out_stride < hi - lo)
+    return fail(FBM_ERR_INVALID_ARG, "lut_shard: out_stride (%d) < hi - lo (%d)", out_stride,
+                hi - lo);
+  if (rows > (int64_t)0x7fffffff * 8) return fail(FBM_ERR_UNSUPPORTED, "lut_shard: too many rows");
+  fbm::LutShardLaunch L{lut, lut_count, rows, lut_stride, lo, hi, out_stride, out_lut, out_count,
+                        error_word()};
+  if (!L.err) return fail(FBM_ERR_CUDA, "lut_shard: error word lookup failed");
+  return cuda_status(fbm::launch_lut_shard(L, static_cast<cudaStream_t>(stream)),
+                     "lut_shard launch");
 }
 
 fbm_status sparse_decode_fwd(const void *q, const void *kv_cache, int dtype, int n_q, int hq,

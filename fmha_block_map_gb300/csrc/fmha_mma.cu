@@ -5,8 +5,8 @@
 // dense mode) are streamed through a double-buffered cp.async pipeline into
 // XOR-swizzled shared memory; S = Q K^T and O += P V run on mma.sync with an
 // online softmax in the base-2 domain (scale * log2(e) folded into one FMA).
-// This is the general path (d = 64 or 128, split-KV partials); the tcgen05
-// kernel covers the d = 128 hot shape.
+// This is the d = 64 path (whole rows, split-KV and fp32 partials); the
+// tcgen05 kernel covers d = 128.
 //
 // Loop shape: the per-row-block loop over a block list of the
 // Incremental_FlashAttention updating_log, Stage 3 (prefetch the next listed
@@ -272,7 +272,10 @@ cudaError_t launch3(const FmhaLaunch &L, cudaStream_t st) {
 
 template <class E, int D>
 cudaError_t launch2(const FmhaLaunch &L, cudaStream_t st) {
-  return L.num_splits > 1 ? launch3<E, D, true>(L, st) : launch3<E, D, false>(L, st);
+  // fp32 partials for a split, or for one whole row when the caller asks for
+  // them instead of out (num_splits = 1, out = NULL)
+  const bool partial = L.num_splits > 1 || L.out == nullptr;
+  return partial ? launch3<E, D, true>(L, st) : launch3<E, D, false>(L, st);
 }
 
 }  // namespace

@@ -1,6 +1,13 @@
 // Sparse FMHA forward for sm_103a on 5th-generation tensor cores (tcgen05,
 // TMEM accumulators, TMA loads and stores), d = 128.
 //
+// A work unit is one (batch, head, q block, split): with num_splits = S the
+// q block's kv list is cut into S contiguous chunks (the first n mod S hold
+// ceil(n / S) entries) and each chunk is a unit.  Whole rows (S = 1 with a
+// dtype output) leave through a swizzled staging tile and TMA stores; split
+// chunks, and whole rows asked for as fp32 partials, are written as fp32 O
+// (already divided by the row sum) and LSE straight from registers.
+//
 // The per-q-block work of the sparse FMHA stage (the "Sparge Attention
 // (Composable Kernel)" README) visits only the kv blocks of the q block's LUT
 // row, two at a time (a "pair", 128 keys):
@@ -98,38 +105,56 @@ constexpr int kSoftmaxBar = 1;  // named barrier of the softmax warps
 struct TcParams {
   CUtensorMap tq, tk, tv, to;
   const int32_t *lut, *cnt;
-  void *out;
-  float *lse;
+  void *out;      // dtype output (whole rows), or
+  float *opart;   // fp32 partials [splits, b * hq * s_q, kD] (split-KV / partial mode)
+  float *lse;     // [b * hq * s_q], or [splits, b * hq * s_q] with opart
   uint32_t *err;
-  int b, hq, hk, s_q, s_k, nq, nk, lut_stride, causal, units;
-  float sl2;  // scale * log2(e)
+  int b, hq, hk, s_q, s_k, nq, nk, lut_stride, causal, splits, units;
+  size_t plane;   // b * hq * s_q
+  float sl2;      // scale * log2(e)
 };
 
+// one (batch, head, q block, split): kv-list entries off .. off + n of the row
 struct Unit {
-  int bh_q, bh_k, i, n;
+  int bh_q, bh_k, i, split, off, n;
   const int32_t *row;
 };
 
+template <bool kPartial>
 FBM_DEVICE Unit unit_of(const TcParams &P, int u) {
   Unit U;
-  U.bh_q = u / P.nq;
-  U.i = u - U.bh_q * P.nq;
+  // whole rows (no partial output) are never split: keep the division out of
+  // that kernel
+  const int qu = kPartial ? u / P.splits : u;
+  U.split = u - qu * (kPartial ? P.splits : 1);
+  U.bh_q = qu / P.nq;
+  U.i = qu - U.bh_q * P.nq;
   const int b = U.bh_q / P.hq, h = U.bh_q - b * P.hq;
   U.bh_k = b * P.hk + h / (P.hq / P.hk);
+  int n_list;
   if (P.lut) {
-    U.row = P.lut + (size_t)u * P.lut_stride;
-    int n = __ldg(P.cnt + u);
-    U.n = max(0, min(n, min(P.nk, P.lut_stride)));
+    U.row = P.lut + (size_t)qu * P.lut_stride;
+    n_list = max(0, min(__ldg(P.cnt + qu), min(P.nk, P.lut_stride)));
   } else {
     U.row = nullptr;
-    U.n = P.causal ? min(P.nk, U.i + 1) : P.nk;
+    n_list = P.causal ? min(P.nk, U.i + 1) : P.nk;
+  }
+  if constexpr (kPartial) {
+    // contiguous chunks: the first n mod S hold ceil(n / S) entries
+    const int base = n_list / P.splits, extra = n_list - base * P.splits;
+    U.off = U.split * base + min(U.split, extra);
+    U.n = base + (U.split < extra ? 1 : 0);
+    if (U.row) U.row += U.off;
+  } else {
+    U.off = 0;
+    U.n = n_list;
   }
   return U;
 }
 
-FBM_DEVICE int entry_of(const Unit &U, int t) { return U.row ? __ldg(U.row + t) : t; }
+FBM_DEVICE int entry_of(const Unit &U, int t) { return U.row ? __ldg(U.row + t) : U.off + t; }
 
-template <bool kBf16>
+template <bool kBf16, bool kPartial>
 __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__ TcParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -152,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     prefetch_map(&P.tq);
     prefetch_map(&P.tk);
     prefetch_map(&P.tv);
-    prefetch_map(&P.to);
+    if (!kPartial) prefetch_map(&P.to);
   }
   if (warp == kWarpS) {
     tmem_alloc(sbase + OFF_MISC, kTmemCols);
@@ -207,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       int pc = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-        const Unit U = unit_of(P, u);
+        const Unit U = unit_of<kPartial>(P, u);
         if (U.n == 0) continue;
         const int npairs = (U.n + 1) >> 1;
         const int qb = uc & 1;
@@ -228,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       int pc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-        const Unit U = unit_of(P, u);
+        const Unit U = unit_of<kPartial>(P, u);
         if (U.n == 0) continue;
         const int npairs = (U.n + 1) >> 1;
         for (int p = 0; p < npairs && ok; ++p) ok = load_pair(U, pc, p, true);
@@ -243,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       int pc = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-        const Unit U = unit_of(P, u);
+        const Unit U = unit_of<kPartial>(P, u);
         if (U.n == 0) continue;
         const int npairs = (U.n + 1) >> 1;
         const int qb = uc & 1;
@@ -283,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       int pc = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-        const Unit U = unit_of(P, u);
+        const Unit U = unit_of<kPartial>(P, u);
         if (U.n == 0) continue;
         const int npairs = (U.n + 1) >> 1;
         for (int p = 0; p < npairs; ++p) {
@@ -325,14 +350,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     int pc = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
-      const Unit U = unit_of(P, u);
+      const Unit U = unit_of<kPartial>(P, u);
       const int q0 = U.i * 64;
       const int rows = min(64, P.s_q - q0);
       if (U.n == 0) {
-        uint16_t *o = static_cast<uint16_t *>(P.out) + ((size_t)U.bh_q * P.s_q + q0) * kD;
-        for (int e = tid * 8; e < rows * kD; e += kSoftmaxThreads * 8)
-          *reinterpret_cast<uint4 *>(o + e) = make_uint4(0, 0, 0, 0);
-        if (P.lse && tid < rows) P.lse[(size_t)U.bh_q * P.s_q + q0 + tid] = -INFINITY;
+        const size_t orow0 = (kPartial ? (size_t)U.split * P.plane : 0) + (size_t)U.bh_q * P.s_q + q0;
+        if constexpr (kPartial) {
+          float *o = P.opart + orow0 * kD;
+          for (int e = tid * 4; e < rows * kD; e += kSoftmaxThreads * 4)
+            *reinterpret_cast<float4 *>(o + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          uint16_t *o = static_cast<uint16_t *>(P.out) + orow0 * kD;
+          for (int e = tid * 8; e < rows * kD; e += kSoftmaxThreads * 8)
+            *reinterpret_cast<uint4 *>(o + e) = make_uint4(0, 0, 0, 0);
+        }
+        if (P.lse && tid < rows) P.lse[orow0 + tid] = -INFINITY;
         continue;
       }
       const int npairs = (U.n + 1) >> 1;
@@ -454,9 +486,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         }
         lt += __shfl_xor_sync(0xffffffffu, lt, 16);
         const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+        const size_t orow0 = (kPartial ? (size_t)U.split * P.plane : 0) + (size_t)U.bh_q * P.s_q + q0;
         if (P.lse && half == 0 && row < rows)
-          P.lse[(size_t)U.bh_q * P.s_q + qpos] =
-              lt > 0.f ? m * 0.6931471805599453f + logf(lt) : -INFINITY;
+          P.lse[orow0 + row] = lt > 0.f ? m * 0.6931471805599453f + logf(lt) : -INFINITY;
+        if constexpr (kPartial) {
+          // fp32 partial: this thread's 64 values of row `row`, d half `half`
+          if (row < rows) {
+            float4 *dst = reinterpret_cast<float4 *>(P.opart + (orow0 + row) * kD + half * 64);
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv, __uint_as_float(o[4 * c + 1]) * inv,
+                                   __uint_as_float(o[4 * c + 2]) * inv,
+                                   __uint_as_float(o[4 * c + 3]) * inv);
+          }
+          pc += npairs;
+          continue;
+        }
         // staging: d half `half` of row `row`, eight 16-byte chunks, 128-byte swizzle
         uint8_t *srow = smem + OFF_STAGE + half * kQChunk + row * 128;
 #pragma unroll
@@ -535,12 +580,12 @@ int sm_count() {
   return n[dev] > 0 ? n[dev] : 148;
 }
 
-template <bool BF16>
+template <bool BF16, bool PARTIAL>
 cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_fmha_tc<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(k_fmha_tc<BF16, PARTIAL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -548,31 +593,37 @@ cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   memset(&P, 0, sizeof(P));
   if (!make_map(&P.tq, L.q, L.b * L.hq, L.s_q, BF16) || !make_map(&P.tk, L.k, L.b * L.hk, L.s_k, BF16) ||
       !make_map(&P.tv, L.v, L.b * L.hk, L.s_k, BF16) ||
-      !make_map(&P.to, L.out, L.b * L.hq, L.s_q, BF16))
+      (L.out && !make_map(&P.to, L.out, L.b * L.hq, L.s_q, BF16)))
     return cudaErrorInvalidValue;
   P.lut = L.lut;
   P.cnt = L.cnt;
   P.out = L.out;
-  P.lse = L.lse;
+  P.opart = PARTIAL ? L.o_part : nullptr;
+  P.lse = PARTIAL ? L.lse_part : L.lse;
+  P.splits = L.num_splits;
+  P.plane = (size_t)L.b * L.hq * L.s_q;
   P.err = L.err;
   P.b = L.b; P.hq = L.hq; P.hk = L.hk; P.s_q = L.s_q; P.s_k = L.s_k; P.nq = L.nq; P.nk = L.nk;
   P.lut_stride = L.lut_stride;
   P.causal = L.causal;
-  P.units = L.b * L.hq * L.nq;
+  P.units = L.b * L.hq * L.nq * L.num_splits;
   P.sl2 = L.scale * 1.4426950408889634f;
   const int grid = std::min(P.units, sm_count());
-  k_fmha_tc<BF16><<<grid, kThreads, SMEM_ALLOC, st>>>(P);
+  k_fmha_tc<BF16, PARTIAL><<<grid, kThreads, SMEM_ALLOC, st>>>(P);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool fmha_tc_supported(int d, int dv, int num_splits, int s_q, int s_k) {
-  return d == kD && dv == kD && num_splits == 1 && s_q > 0 && s_k > 0;
+  return d == kD && dv == kD && num_splits >= 1 && s_q > 0 && s_k > 0;
 }
 
 cudaError_t launch_fmha_tc(const FmhaLaunch &L, cudaStream_t st) {
-  return L.bf16 ? launch_t<true>(L, st) : launch_t<false>(L, st);
+  // whole rows in dtype, or fp32 partials (split chunks, or rows for a combine)
+  if (L.out == nullptr)
+    return L.bf16 ? launch_t<true, true>(L, st) : launch_t<false, true>(L, st);
+  return L.bf16 ? launch_t<true, false>(L, st) : launch_t<false, false>(L, st);
 }
 
 }  // namespace fbm

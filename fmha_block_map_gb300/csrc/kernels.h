@@ -59,6 +59,15 @@ struct CombineLaunch {
 };
 cudaError_t launch_combine(const CombineLaunch &L, cudaStream_t st);
 
+struct LutShardLaunch {
+  const int32_t *lut, *cnt;
+  int64_t rows;
+  int lut_stride, lo, hi, out_stride;
+  int32_t *out_lut, *out_cnt;
+  uint32_t *err;
+};
+cudaError_t launch_lut_shard(const LutShardLaunch &L, cudaStream_t st);
+
 struct DecodeLaunch {
   const void *q, *cache;
   int bf16, n_q, hq, d, dv, page;

@@ -1,0 +1,53 @@
+// Context-parallel LUT shard: the part of every LUT row that falls in one
+// rank's contiguous kv-block range [lo, hi), re-based to the rank's own K/V
+// rows (entry e becomes e - lo).  With the key set of a row split this way,
+// the ranks' partial attentions recombine to the full row through the LSE
+// combine (Incremental_FlashAttention updating_log, Stage 1; the LSE export
+// exists for ring / context-parallel merging, ROCm/aiter pull 6841).
+//
+// One warp per row: the row is read in 32-entry chunks, a ballot marks the
+// entries in range, and each lane writes its entry at the running count plus
+// the popcount of the lower lanes' marks.  The order of the row is kept, no
+// atomics take part, and the rest of the output row is padded with -1.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fbm {
+namespace {
+
+__global__ void __launch_bounds__(256) k_lut_shard(const LutShardLaunch L) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (row >= L.rows) return;
+  const int32_t *src = L.lut + row * L.lut_stride;
+  int32_t *dst = L.out_lut + row * L.out_stride;
+  const int n = min(max(L.cnt[row], 0), L.lut_stride);
+  int kept = 0;
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    const int c = c0 + lane;
+    const int e = c < n ? src[c] : -1;
+    const bool in = c < n && e >= L.lo && e < L.hi;
+    const unsigned m = __ballot_sync(0xffffffffu, in);
+    const int slot = kept + __popc(m & ((1u << lane) - 1u));
+    // an entry past out_stride cannot occur when the row is strictly ascending;
+    // for any other row it is dropped and flagged
+    if (in) {
+      if (slot < L.out_stride) dst[slot] = e - L.lo;
+      else atomicOr(L.err, FBM_DEVERR_LUT_RANGE);
+    }
+    kept += __popc(m);
+  }
+  kept = min(kept, L.out_stride);
+  for (int c = kept + lane; c < L.out_stride; c += 32) dst[c] = -1;
+  if (lane == 0) L.out_cnt[row] = kept;
+}
+
+}  // namespace
+
+cudaError_t launch_lut_shard(const LutShardLaunch &L, cudaStream_t st) {
+  const int64_t blocks = (L.rows + 7) / 8;
+  k_lut_shard<<<(unsigned)blocks, 256, 0, st>>>(L);
+  return cudaGetLastError();
+}
+
+}  // namespace fbm

@@ -174,6 +174,12 @@ fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int 
  *   block (every causally visible one under causal).
  * num_splits == 1: out = device [b, hq, s_q, dv] in dtype; lse = device fp32
  *   [b, hq, s_q] or NULL (return_lse off); o_partial / lse_partial unused.
+ * num_splits == 1 with out == NULL (partial mode): the whole row's normalised
+ *   O and its LSE go to o_partial = device fp32 [1, b, hq, s_q, dv] and
+ *   lse_partial = device fp32 [1, b, hq, s_q] (empty row: 0 and -inf), one
+ *   slot of a stack that attn_combine merges (context-parallel shards,
+ *   see lut_shard; two passes over disjoint key sets).  Both pointers are
+ *   required.
  * num_splits > 1 (split-KV): the LUT row of each q block is cut into
  *   num_splits contiguous chunks (the first n mod S chunks hold ceil(n/S)
  *   entries, the rest floor(n/S)); chunk s writes its normalised partial to
@@ -201,6 +207,31 @@ fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtyp
 fbm_status attn_combine(const float *o_part, const float *lse_part, int num_splits,
                         int64_t rows, int dv, int out_dtype, void *out, float *lse_out,
                         void *stream);
+
+/*
+ * lut_shard - the part of every LUT row inside one rank's kv-block range
+ * [lo, hi), re-based to that rank's own K/V rows (context-parallel attention:
+ * the LSE export exists so that partials over disjoint key sets can be merged
+ * across ranks, ROCm/aiter pull 6841; the merge is updating_log Stage 1).
+ *
+ * For each row r < rows: the entries e of lut[r][0 .. min(lut_count[r],
+ * lut_stride)) with lo <= e < hi, in their order, written as e - lo to
+ * out_lut[r][0 .. out_count[r]); the rest of out_lut[r] (out_stride entries)
+ * is -1.  A rank holding K/V rows [lo * 64, min(hi * 64, s_k)) then calls
+ * sparse_fmha_fwd (partial mode) with out_lut / out_count and lut_stride =
+ * out_stride, and attn_combine over the ranks' slots gives the attention of
+ * the full LUT.
+ *
+ * lut: device int32 [rows, lut_stride]; lut_count: device int32 [rows];
+ * out_lut: device int32 [rows, out_stride] with out_stride >= hi - lo;
+ * out_count: device int32 [rows]; 0 <= lo < hi.  Invalid arguments return
+ * FBM_ERR_INVALID_ARG before any launch.  A row that is not strictly ascending
+ * can hold more in-range entries than out_stride: the excess is dropped and
+ * FBM_DEVERR_LUT_RANGE is set.
+ */
+fbm_status lut_shard(const int32_t *lut, const int32_t *lut_count, int64_t rows, int lut_stride,
+                     int lo, int hi, int32_t *out_lut, int32_t *out_count, int out_stride,
+                     void *stream);
 
 /*
  * sparse_decode_fwd - sparse decode over per-query token index lists through a

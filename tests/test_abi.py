@@ -131,6 +131,20 @@ def test_combine_and_decode_reject(L):
     assert L.sparse_decode_fwd(*bad) == fbm.FBM_ERR_INVALID_ARG
 
 
+def test_lut_shard_rejects(L):
+    # valid apart from the one bad argument each case plants; never called as is
+    args = [FAKE, FAKE, 10, 16, 4, 8, FAKE, FAKE, 4, None]
+    for i, bad in ((0, None), (2, 0), (3, 0), (4, -1), (5, 4), (8, 3)):
+        a = list(args)
+        a[i] = bad
+        assert L.lut_shard(*a) == fbm.FBM_ERR_INVALID_ARG, (i, bad)
+
+
+def test_partial_mode_needs_both_partial_buffers(L):
+    assert _fm(L, out=None, op=FAKE, lp=None) == fbm.FBM_ERR_INVALID_ARG
+    assert _fm(L, out=None, op=None, lp=FAKE) == fbm.FBM_ERR_INVALID_ARG
+
+
 def test_kernel_kind_is_host_only(L):
     assert L.fbm_fmha_kernel_kind(0, 96, 96, 1, 128, 128) == 0
     assert L.fbm_fmha_kernel_kind(1, 64, 64, 2, 128, 128) == 2

@@ -114,9 +114,9 @@ def test_dense_mode_matches_full_lut(fbm_gpu, causal):
     assert torch.equal(o_dense, o_full) and torch.equal(l_dense, l_full)
 
 
-@pytest.mark.parametrize("S", [2, 3, 5])
-def test_split_kv_partials_and_combine(fbm_gpu, S):
-    cfg = synth.C1.replace(b=1, hq=4, hk=2, s=640, d=128, dtype="bf16")
+@pytest.mark.parametrize("S,d", [(2, 128), (3, 128), (5, 128), (3, 64)])
+def test_split_kv_partials_and_combine(fbm_gpu, S, d):
+    cfg = synth.C1.replace(b=1, hq=4, hk=2, s=640, d=d, dtype="bf16")
     lut, cnt = hand_lut(cfg, seed=S)
     x, (q, k, v) = prefill_on_gpu(cfg)
     op, lp = fbm_gpu.sparse_fmha_fwd(q, k, v, torch.from_numpy(lut).cuda(),
@@ -132,6 +132,16 @@ def test_split_kv_partials_and_combine(fbm_gpu, S):
                 assert_close_o(op[s, 0, h, i * 64:(i + 1) * 64], parts[0][s], f"Opart{s}")
                 assert_close_lse(lp[s, 0, h, i * 64:(i + 1) * 64], parts[1][s], f"LSEpart{s}")
     check(fbm_gpu, cfg, lut, cnt, num_splits=S)
+
+
+@pytest.mark.parametrize("S", [2, 4])
+def test_split_kv_dense_causal_ragged(fbm_gpu, S):
+    # dense list (every causally visible block) cut into chunks; s = 1000
+    cfg = synth.C1.replace(b=1, hq=2, hk=1, s=1000, d=128, dtype="f16", causal=True)
+    nq = cfg.nq
+    lut = np.tile(np.arange(nq, dtype=np.int32), (1, 2, nq, 1))
+    cnt = np.tile(np.arange(1, nq + 1, dtype=np.int32), (1, 2, 1))
+    check(fbm_gpu, cfg, lut, cnt, num_splits=S, dense=True)
 
 
 def test_c2_cdf_attention(fbm_gpu):
@@ -195,4 +205,4 @@ def test_d128_runs_on_the_tcgen05_kernel(fbm_gpu):
         assert fbm_gpu.fmha_kernel_kind(dt, 128, 128, 1, 16384, 16384) == 1
         assert fbm_gpu.fmha_kernel_kind(dt, 128, 128, 1, 1000, 1000) == 1
     assert fbm_gpu.fmha_kernel_kind(torch.float16, 64, 64, 1, 512, 512) == 2
-    assert fbm_gpu.fmha_kernel_kind(torch.float16, 128, 128, 4, 512, 512) == 2
+    assert fbm_gpu.fmha_kernel_kind(torch.float16, 128, 128, 4, 512, 512) == 1

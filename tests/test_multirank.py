@@ -61,3 +61,56 @@ def test_two_gloo_ranks(tmp_path):
     assert (r0[3:] == r1[3:]).all()                            # same gathered view
     assert r0[3] == r0[3 + 0] and r0[3] > 0 and r0[4] > 0      # work on both ranks
     assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def _cp_worker(rank, world, port, out_dir):
+    """One context-parallel rank on CPU: the oracle stands in for the GPU
+    partial of this rank's kv range; the exchange is the library's own
+    all-gather."""
+    import sys
+
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    from fmha_block_map_gb300 import cp
+
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((256, 32))
+    k = rng.standard_normal((1000, 32))
+    v = rng.standard_normal((1000, 16))
+    rows = {2: [0, 3, 8, 9, 15], 3: [1, 2, 14]}           # q block -> LUT row
+    lo, hi = cp.kv_shard_bounds(16, world)[rank]
+    r0, r1 = cp.shard_rows(1000, lo, hi)
+    o = np.zeros((2, 64, 16))
+    l = np.zeros((2, 64))
+    for n, (i, row) in enumerate(sorted(rows.items())):
+        sub = oracle.shard_lut_row(row, lo, hi)
+        o[n], l[n] = oracle.attention_unit(q, k[r0:r1], v[r0:r1], sub, i, 64, 64, 0.3, False)
+    o_all, l_all = cp.gather_partials(torch.from_numpy(o), torch.from_numpy(l))
+    res = []
+    for n, (i, row) in enumerate(sorted(rows.items())):
+        got = oracle.combine(o_all[:, n].numpy(), l_all[:, n].numpy())
+        ref = oracle.attention_unit(q, k, v, row, i, 64, 64, 0.3, False)
+        res.append(max(np.abs(got[0] - ref[0]).max(), np.abs(got[1] - ref[1]).max()))
+    np.save(os.path.join(out_dir, f"cp{rank}.npy"), np.array([lo, hi, r0, r1] + res))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_context_parallel_exchange_on_gloo_ranks(tmp_path, world):
+    mp.start_processes(_cp_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       start_method="spawn", join=True)
+    got = [np.load(tmp_path / f"cp{r}.npy") for r in range(world)]
+    import oracle
+    from fmha_block_map_gb300 import cp
+
+    # the library's ranges follow the oracle's chunk rule; they tile the kv blocks
+    assert cp.kv_shard_bounds(16, world) == oracle.split_bounds(16, world)
+    assert [tuple(g[:2].astype(int)) for g in got] == oracle.split_bounds(16, world)
+    assert got[-1][3] == 1000 and all(got[r][3] == got[r + 1][2] for r in range(world - 1))
+    for g in got:            # every rank combined the gathered partials to the full row
+        assert (g[4:] < 1e-10).all()
+    with pytest.raises(ValueError):
+        cp.kv_shard_bounds(2, 3)
