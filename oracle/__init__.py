@@ -74,6 +74,7 @@ from .attention import (  # noqa: F401
     split_bounds,
     split_partials_unit,
     combine,
+    attention_unit_pv_skip,
     shard_lut_row,
     context_parallel_unit,
     decode_rows,

@@ -153,6 +153,58 @@ def combine(o_parts: np.ndarray, lse_parts: np.ndarray):
 
 
 # ----------------------------------------------------------------------------
+# PV skip (pv_threshold)
+# ----------------------------------------------------------------------------
+
+def attention_unit_pv_skip(q: np.ndarray, k: np.ndarray, v: np.ndarray, lut_row: Iterable[int],
+                           i: int, blkq: int, blkk: int, scale: float, causal: bool,
+                           pv_threshold: float):
+    """Attention of q block ``i`` with the per-Q-tile PV skip ("Sparge
+    Attention (Composable Kernel)" README, 'Not yet ported': pv_threshold
+    per-Q-tile skip in the attention kernel, a pure performance feature).
+
+    The kv blocks are visited in LUT order with a running row max m (the
+    largest score of the blocks visited so far, -inf before the first).  A
+    block whose every row has all its scores below m - pv_threshold (natural
+    log units, the scores already scaled) contributes nothing to the P.V
+    product; its probabilities still count in the softmax denominator, and the
+    LSE is unchanged.  So every skipped probability is below e^-pv_threshold
+    times the row's largest one.  Returns (O [rows, dv], LSE [rows], the list
+    of skipped kv blocks)."""
+    s_q, s_k = q.shape[0], k.shape[0]
+    t = np.arange(i * blkq, min((i + 1) * blkq, s_q))
+    rows, dv = len(t), v.shape[1]
+    m = np.full(rows, -np.inf)
+    l = np.zeros(rows)
+    num = np.zeros((rows, dv))
+    skipped = []
+    for j in lut_row:
+        keys = row_keys([j], blkk, s_k)
+        s = scale * (q[t] @ k[keys].T)
+        if causal:
+            s = np.where(keys[None, :] <= t[:, None], s, -np.inf)
+        tmax = s.max(axis=1)
+        skip = bool(np.all(tmax < m - pv_threshold))
+        m_new = np.maximum(m, tmax)
+        live = np.isfinite(m_new)
+        alpha = np.where(live, np.exp(np.where(live, m - m_new, 0.0)), 0.0)
+        p = np.where(live[:, None], np.exp(s - np.where(live, m_new, 0.0)[:, None]), 0.0)
+        l = l * alpha + p.sum(axis=1)
+        num = num * alpha[:, None]
+        if skip:
+            skipped.append(int(j))
+        else:
+            num = num + p @ v[keys]
+        m = m_new
+    out = np.zeros((rows, dv))
+    lse = np.full(rows, -np.inf)
+    ok = l > 0
+    out[ok] = num[ok] / l[ok, None]
+    lse[ok] = m[ok] + np.log(l[ok])
+    return out, lse, skipped
+
+
+# ----------------------------------------------------------------------------
 # Context parallelism over the kv blocks
 # ----------------------------------------------------------------------------
 

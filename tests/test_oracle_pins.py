@@ -469,6 +469,87 @@ def test_split_partials_combine_to_the_full_row(S):
 
 
 # ----------------------------------------------------------------------------
+# PV skip (pv_threshold)
+# ----------------------------------------------------------------------------
+
+_PV_Q = np.array([[1.0]])
+_PV_K = np.array([[2.0], [2.0], [-3.0], [-3.0]])       # block 0 scores 2, block 1 scores -3
+_PV_V = np.array([[1.0], [1.0], [10.0], [10.0]])
+
+
+def test_pv_skip_hand_example():
+    den = 2 * math.exp(2) + 2 * math.exp(-3)
+    o, l, sk = oatt.attention_unit_pv_skip(_PV_Q, _PV_K, _PV_V, [0, 1], 0, 1, 2, 1.0, False, 4.0)
+    assert sk == [1]                                        # -3 < 2 - 4
+    assert abs(o[0, 0] - 2 * math.exp(2) / den) < 1e-14
+    assert abs(l[0] - math.log(den)) < 1e-14                # the denominator keeps block 1
+    o, l, sk = oatt.attention_unit_pv_skip(_PV_Q, _PV_K, _PV_V, [0, 1], 0, 1, 2, 1.0, False, 6.0)
+    assert sk == [] and abs(o[0, 0] - (2 * math.exp(2) + 20 * math.exp(-3)) / den) < 1e-14
+
+
+def test_pv_skip_uses_the_running_max_in_lut_order():
+    # block 1 first: nothing was visited before it, and block 0 raises the max
+    o, _, sk = oatt.attention_unit_pv_skip(_PV_Q, _PV_K, _PV_V, [1, 0], 0, 1, 2, 1.0, False, 4.0)
+    full = oatt.attention_unit(_PV_Q, _PV_K, _PV_V, [1, 0], 0, 1, 2, 1.0, False)
+    assert sk == [] and abs(o[0, 0] - full[0][0, 0]) < 1e-14
+
+
+def test_pv_skip_needs_every_row_of_the_q_tile():
+    q = np.array([[1.0], [-1.0]])       # row 1 scores block 0 at -2 and block 1 at 3
+    _, _, sk = oatt.attention_unit_pv_skip(q, _PV_K, _PV_V, [0, 1], 0, 2, 2, 1.0, False, 4.0)
+    assert sk == []
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_pv_skip_infinite_threshold_is_plain_attention(causal):
+    rng = np.random.default_rng(11)
+    q, k, v = (rng.standard_normal((256, 16)) for _ in range(3))
+    row = [0, 1, 2, 3] if causal else [3, 0, 2]
+    o, l, sk = oatt.attention_unit_pv_skip(q, k, v, row, 3, 64, 64, 0.5, causal, math.inf)
+    ref = oatt.attention_unit(q, k, v, row, 3, 64, 64, 0.5, causal)
+    assert sk == []
+    assert np.abs(o - ref[0]).max() < 1e-12 and np.abs(l - ref[1]).max() < 1e-12
+
+
+def test_pv_skip_error_bound():
+    # large score spread: blocks whose every score is far below the running max
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((64, 16))
+    k = rng.standard_normal((512, 16)) * np.repeat(rng.uniform(0.1, 3.0, 8), 64)[:, None]
+    v = rng.standard_normal((512, 8))
+    row = list(range(8))
+    ref = oatt.attention_unit(q, k, v, row, 0, 64, 64, 1.0, False)
+    for tau in (0.5, 2.0, 5.0):
+        o, l, sk = oatt.attention_unit_pv_skip(q, k, v, row, 0, 64, 64, 1.0, False, tau)
+        assert np.abs(l - ref[1]).max() < 1e-12                    # LSE unchanged
+        bound = 64 * len(sk) * math.exp(-tau) * np.abs(v).max()
+        assert np.abs(o - ref[0]).max() <= bound + 1e-12
+    assert oatt.attention_unit_pv_skip(q, k, v, row, 0, 64, 64, 1.0, False, 0.5)[2]  # skips some
+
+
+def test_planted_pv_skip_mistake_is_caught(monkeypatch):
+    """Testing each block against the final row max instead of the running
+    max skips block 1 even when it is visited first: the order pin fails."""
+    real = oatt.attention_unit_pv_skip
+
+    def final_max(q, k, v, lut_row, i, blkq, blkk, scale, causal, tau):
+        t = np.arange(i * blkq, min((i + 1) * blkq, q.shape[0]))
+        keys = oatt.row_keys(lut_row, blkk, k.shape[0])
+        mfin = (scale * (q[t] @ k[keys].T)).max(axis=1)
+        o, l, _ = real(q, k, v, lut_row, i, blkq, blkk, scale, causal, math.inf)
+        sk = []
+        for j in lut_row:
+            kj = oatt.row_keys([j], blkk, k.shape[0])
+            if np.all((scale * (q[t] @ k[kj].T)).max(axis=1) < mfin - tau):
+                sk.append(j)
+        return o, l, sk
+
+    monkeypatch.setattr(oatt, "attention_unit_pv_skip", final_max)
+    with pytest.raises(AssertionError):
+        test_pv_skip_uses_the_running_max_in_lut_order()
+
+
+# ----------------------------------------------------------------------------
 # context parallelism over the kv blocks
 # ----------------------------------------------------------------------------
 
