@@ -40,9 +40,9 @@ TOPKS = (0.1, 0.2, 0.4, 0.6, 1.0)
 # profiles/), keyed by the sha256 of the kernel source it was taken on; a
 # kernel edited since then reports traffic = null.
 NCU_TRAFFIC = {
-    # profiles/sparse_fmha_tc_b2h32s16384d128_topk04.md (current source): 815.46 MB read +
-    # 256.13 MB written
-    "6cf3808412a77c3a": 1071586560,
+    # profiles/sparse_fmha_tc_b2h32s16384d128_topk04.md (current source): 814.06 MB read +
+    # 256.26 MB written
+    "5f02de1f66743078": 1070325504,
 }
 
 
@@ -297,6 +297,17 @@ def run_ours(args):
                                      else "mma.sync") + " (fp32 partial output)"}
         del shards, o_all, l_all
 
+    # ---- per-Q-tile PV skip: the same step's attention with pv_threshold set
+    pv_res = None
+    if rank == 0 and not args.no_extra:
+        pv_res = []
+        for tau in (2.0, 6.0):
+            ms = timed(lambda: fbm.sparse_fmha_fwd(q, k, v, lut, cnt, scale=cfg.scale, out=out,
+                                                   pv_threshold=tau), 5, 1)
+            pv_res.append({"pv_threshold": tau, "attn_ms": round(ms, 4),
+                           "vs_no_skip": round(at_ms / ms, 3),
+                           "eff_tflops_attn": round(flops / (ms * 1e-3) / 1e12, 1)})
+
     # ---- end to end through the public API with host buffers: every step copies
     # its Q, K, V from pinned host memory and reads its O back.  Double buffers;
     # the uploads and the read-backs run on two copy streams (the host link is
@@ -401,6 +412,7 @@ def run_ours(args):
                      "flop_per_tile": FLOP_PER_TILE, "attn_ms": round(at_ms, 4)},
         "sweep": sweep,
         "context_parallel": cp_res,
+        "pv_skip": pv_res,
         "e2e": e2e,
         "clocks": clocks,
         # per step: k_pool_sim, k_pooled_scores, k_select and k_fmha_tc
@@ -531,11 +543,11 @@ def measure_decode(hbm_gbs):
 # ----------------------------------------------------------------------------
 
 
-def cpu_baseline(cfg, x, topk, qblocks=None, heads=6):
+def cpu_baseline(cfg, x, topk, qblocks=None, heads=10):
     """The oracle as it stands on a bounded sample of the same workload: the
     block map of `heads` (batch, head) pairs, then sparse attention of
-    `qblocks` q blocks of each (all of them by default, about 10 s of CPU
-    work for 6 heads); effective TFLOP/s over the selected tiles of the
+    `qblocks` q blocks of each (all of them by default: about 10 s of work
+    for 10 heads on 16 Arm cores); effective TFLOP/s over the selected tiles of the
     sample, charging the block map in proportion to the q blocks done."""
     import numpy as np
 

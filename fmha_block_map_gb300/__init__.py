@@ -53,7 +53,7 @@ def lib() -> ctypes.CDLL:
         L.sparge_block_map_static.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp,
                                                vp, f32, i32, i32, i32, vp, vp, vp, vp])
         L.sparse_fmha_fwd.argtypes = ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-                                       vp, vp, i32, i32, f32, i32, vp, vp, vp, vp, vp])
+                                       vp, vp, i32, i32, f32, i32, f32, vp, vp, vp, vp, vp])
         L.attn_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
         L.lut_shard.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp]
         L.sparse_decode_fwd.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, i32, vp,
@@ -203,11 +203,12 @@ def sparse_fmha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                     o_partial: Optional[torch.Tensor] = None,
                     lse_partial: Optional[torch.Tensor] = None, partial: bool = False,
-                    stream=None):
+                    pv_threshold: Optional[float] = None, stream=None):
     """Sparse (lut given) or dense (lut None) attention.  num_splits == 1
     returns (out, lse or None); num_splits > 1, or ``partial`` (one whole-row
     partial, e.g. one slot of a context-parallel stack), returns the fp32
-    partials (o_partial [S, b, hq, s_q, dv], lse_partial [S, b, hq, s_q])."""
+    partials (o_partial [S, b, hq, s_q, dv], lse_partial [S, b, hq, s_q]).
+    pv_threshold (None: off) enables the per-Q-tile PV skip on whole rows."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _cuda(t, n)
     b, hq, s_q, d = q.shape
@@ -235,6 +236,7 @@ def sparse_fmha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     _check(lib().sparse_fmha_fwd(
         _ptr(q), _ptr(k), _ptr(v), _dt(q), b, hq, hk, s_q, s_k, d, dv, 64, 64,
         _ptr(lut), _ptr(lut_count), stride, num_splits, float(scale), int(causal),
+        math.inf if pv_threshold is None else float(pv_threshold),
         None if partial else _ptr(out), None if partial else _ptr(lse),
         _ptr(o_partial) if partial else None, _ptr(lse_partial) if partial else None,
         _stream(stream)))

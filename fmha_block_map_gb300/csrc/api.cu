@@ -182,8 +182,9 @@ int fbm_fmha_kernel_kind(int dtype, int d, int dv, int num_splits, int s_q, int 
 fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtype, int b,
                            int hq, int hk, int s_q, int s_k, int d, int dv, int blkq, int blkk,
                            const int32_t *lut, const int32_t *lut_count, int lut_stride,
-                           int num_splits, float scale, int causal, void *out, float *lse,
-                           float *o_partial, float *lse_partial, void *stream) {
+                           int num_splits, float scale, int causal, float pv_threshold,
+                           void *out, float *lse, float *o_partial, float *lse_partial,
+                           void *stream) {
   if (!q || !k || !v) return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: null q / k / v");
   if ((lut == nullptr) != (lut_count == nullptr))
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: lut and lut_count must both be set or both NULL");
@@ -210,6 +211,11 @@ fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtyp
                                : "sparse_fmha_fwd: null out (and no o_partial / lse_partial)");
   if (!(scale > 0.f) || !std::isfinite(scale))
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: scale must be positive and finite");
+  if (!(pv_threshold >= 0.f))
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: pv_threshold must be >= 0 (+inf: off)");
+  if (pv_threshold < INFINITY && (partial || !fbm::fmha_tc_supported(d, dv, num_splits, s_q, s_k)))
+    return fail(FBM_ERR_UNSUPPORTED,
+                "sparse_fmha_fwd: pv_threshold needs whole rows (num_splits = 1, out given) and d = 128");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (out && !aligned16(out)) ||
       (o_partial && !aligned16(o_partial)))
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: tensors must be 16-byte aligned");
@@ -221,6 +227,7 @@ fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtyp
   L.b = b; L.hq = hq; L.hk = hk; L.s_q = s_q; L.s_k = s_k; L.d = d; L.nq = nq; L.nk = nk;
   L.lut = lut; L.cnt = lut_count; L.lut_stride = lut ? lut_stride : nk;
   L.num_splits = num_splits; L.causal = causal != 0; L.scale = scale;
+  L.pv_threshold = pv_threshold;
   L.out = partial ? nullptr : out;
   L.lse = partial ? nullptr : lse;
   L.o_part = partial ? o_partial : nullptr;

@@ -84,7 +84,8 @@ enum {
   B_PV = B_PF + kPBufs, B_OF = B_PV + kPBufs, B_DRAIN = B_OF + 1, B_DRAIN2 = B_DRAIN + 1,
   NBAR = B_DRAIN2 + 1
 };
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] tmem base, [1] abort flag
+// [0] tmem base, [1] abort flag, bytes 8 .. 15: PV-skip votes [P buffer][softmax warp]
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
@@ -112,6 +113,7 @@ struct TcParams {
   int b, hq, hk, s_q, s_k, nq, nk, lut_stride, causal, splits, units;
   size_t plane;   // b * hq * s_q
   float sl2;      // scale * log2(e)
+  float tau2;     // pv_threshold * log2(e) (PV-skip variant)
 };
 
 // one (batch, head, q block, split): kv-list entries off .. off + n of the row
@@ -154,7 +156,7 @@ FBM_DEVICE Unit unit_of(const TcParams &P, int u) {
 
 FBM_DEVICE int entry_of(const Unit &U, int t) { return U.row ? __ldg(U.row + t) : U.off + t; }
 
-template <bool kBf16, bool kPartial>
+template <bool kBf16, bool kPartial, bool kPvSkip>
 __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__ TcParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -320,9 +322,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           const uint32_t v_lo = sdesc_lo(sbase + OFF_V + slot * kPairBytes, kPairChunk);
           const uint32_t tP = tbase + kTP + pb * 64;
           const bool half = 2 * p + 1 >= U.n;  // a half pair has 64 keys: 4 steps
+          bool skip_a = false, skip_b = false;
+          if constexpr (kPvSkip) {
+            // a block is skipped when all four softmax warps voted for it; the
+            // first block of a row never is (its running max is still -inf), so
+            // the first MMA below always starts the accumulator
+            const uint32_t vw = *reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC + 8 + pb * 4);
+            const uint32_t all4 = vw & (vw >> 8) & (vw >> 16) & (vw >> 24);
+            skip_a = (all4 & 1u) != 0;
+            skip_b = (all4 & 2u) != 0;
+          }
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            if (kk < 4 || !half)
+            if (kk < 4 ? !skip_a : (!half && !skip_b))
               mma_f16_ta(tO, tP + kk * 8, v_lo + kk * 128, kDescHi, idO,
                          (p > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(B_PV + pb));
@@ -370,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       const int npairs = (U.n + 1) >> 1;
       const int qpos = q0 + row;
       float m = -INFINITY;                 // running max of the row (log2 domain)
+      float mt = -INFINITY;                // exact running max (PV-skip variant)
       uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};  // this thread's share of the row sum
       int j_next = half < U.n ? entry_of(U, half) : -1;
       for (int p = 0; p < npairs; ++p) {
@@ -411,7 +424,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           }
           mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        uint32_t vote = 0;
+        if constexpr (kPvSkip) {
+          const float mx_other = __shfl_xor_sync(0xffffffffu, mx, 16);
+          // block A (entry 2p) then block B (entry 2p + 1) against the exact
+          // running max of the blocks visited before each; rows past the end
+          // of the sequence do not veto
+          const float a = (half == 0 ? mx : mx_other) * P.sl2;
+          const float b = (half == 0 ? mx_other : mx) * P.sl2;
+          const bool real = qpos < P.s_q;
+          const bool sa = !real || a < mt - P.tau2;
+          mt = fmaxf(mt, a);
+          const bool sb = !real || b < mt - P.tau2;
+          mt = fmaxf(mt, b);
+          vote = (__all_sync(0xffffffffu, sa) ? 1u : 0u) | (__all_sync(0xffffffffu, sb) ? 2u : 0u);
+          mx = fmaxf(mx, mx_other);
+        } else {
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        }
         const float mxs = mx * P.sl2;
         const bool need = mxs > m + 8.0f;
         if (__any_sync(0xffffffffu, need)) {
@@ -466,6 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
+        if (kPvSkip && lane == 0)  // read by the PV issuer once B_PF(pb) completes
+          *reinterpret_cast<volatile uint8_t *>(smem + OFF_MISC + 8 + pb * 4 + sw) = (uint8_t)vote;
         if (lane == 0) mbar_arrive(bar(B_PF + pb));
       }
       // ---- epilogue: O = O / l, LSE = m ln 2 + ln l
@@ -580,11 +612,12 @@ int sm_count() {
   return n[dev] > 0 ? n[dev] : 148;
 }
 
-template <bool BF16, bool PARTIAL>
+template <bool BF16, bool PARTIAL, bool PVSKIP>
 cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
+  static_assert(!(PARTIAL && PVSKIP), "the PV skip runs on whole rows only");
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_fmha_tc<BF16, PARTIAL>,
+    cudaError_t e = cudaFuncSetAttribute(k_fmha_tc<BF16, PARTIAL, PVSKIP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_done = true;
@@ -608,8 +641,9 @@ cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   P.causal = L.causal;
   P.units = L.b * L.hq * L.nq * L.num_splits;
   P.sl2 = L.scale * 1.4426950408889634f;
+  P.tau2 = L.pv_threshold * 1.4426950408889634f;
   const int grid = std::min(P.units, sm_count());
-  k_fmha_tc<BF16, PARTIAL><<<grid, kThreads, SMEM_ALLOC, st>>>(P);
+  k_fmha_tc<BF16, PARTIAL, PVSKIP><<<grid, kThreads, SMEM_ALLOC, st>>>(P);
   return cudaGetLastError();
 }
 
@@ -622,8 +656,10 @@ bool fmha_tc_supported(int d, int dv, int num_splits, int s_q, int s_k) {
 cudaError_t launch_fmha_tc(const FmhaLaunch &L, cudaStream_t st) {
   // whole rows in dtype, or fp32 partials (split chunks, or rows for a combine)
   if (L.out == nullptr)
-    return L.bf16 ? launch_t<true, true>(L, st) : launch_t<false, true>(L, st);
-  return L.bf16 ? launch_t<true, false>(L, st) : launch_t<false, false>(L, st);
+    return L.bf16 ? launch_t<true, true, false>(L, st) : launch_t<false, true, false>(L, st);
+  if (L.pv_threshold < INFINITY)
+    return L.bf16 ? launch_t<true, false, true>(L, st) : launch_t<false, false, true>(L, st);
+  return L.bf16 ? launch_t<true, false, false>(L, st) : launch_t<false, false, false>(L, st);
 }
 
 }  // namespace fbm

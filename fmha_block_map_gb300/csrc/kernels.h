@@ -41,6 +41,7 @@ struct FmhaLaunch {
   const int32_t *lut, *cnt;  // lut == nullptr: dense
   int lut_stride, num_splits, causal;
   float scale;
+  float pv_threshold;  // +inf: no PV skip
   void *out;
   float *lse, *o_part, *lse_part;
   uint32_t *err;

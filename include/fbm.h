@@ -172,6 +172,15 @@ fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int 
  *   FBM_DEVERR_LUT_RANGE); lut_count: device int32 [b, hq, nq].
  *   lut == NULL (and lut_count == NULL) selects dense attention: every kv
  *   block (every causally visible one under causal).
+ * pv_threshold: +inf turns the PV skip off.  A finite value >= 0 (natural log
+ *   units of the scaled scores) enables the per-Q-tile PV skip (README, 'Not
+ *   yet ported': pv_threshold per-Q-tile skip): the listed kv blocks are
+ *   visited in LUT order with an exact running max m per row, and a block
+ *   whose scores lie below m - pv_threshold in every row of the q block
+ *   (rows past s_q do not count) is left out of O's P.V sum while its
+ *   probabilities stay in the denominator and in the LSE.  Whole rows on the
+ *   d = 128 kernel only (num_splits == 1, out given); otherwise
+ *   FBM_ERR_UNSUPPORTED.  NaN or a negative value: FBM_ERR_INVALID_ARG.
  * num_splits == 1: out = device [b, hq, s_q, dv] in dtype; lse = device fp32
  *   [b, hq, s_q] or NULL (return_lse off); o_partial / lse_partial unused.
  * num_splits == 1 with out == NULL (partial mode): the whole row's normalised
@@ -190,8 +199,9 @@ fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int 
 fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtype, int b,
                            int hq, int hk, int s_q, int s_k, int d, int dv, int blkq, int blkk,
                            const int32_t *lut, const int32_t *lut_count, int lut_stride,
-                           int num_splits, float scale, int causal, void *out, float *lse,
-                           float *o_partial, float *lse_partial, void *stream);
+                           int num_splits, float scale, int causal, float pv_threshold,
+                           void *out, float *lse, float *o_partial, float *lse_partial,
+                           void *stream);
 
 /*
  * attn_combine - merge split-KV partials over disjoint key sets

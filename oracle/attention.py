@@ -158,7 +158,7 @@ def combine(o_parts: np.ndarray, lse_parts: np.ndarray):
 
 def attention_unit_pv_skip(q: np.ndarray, k: np.ndarray, v: np.ndarray, lut_row: Iterable[int],
                            i: int, blkq: int, blkk: int, scale: float, causal: bool,
-                           pv_threshold: float):
+                           pv_threshold: float, margins: Optional[list] = None):
     """Attention of q block ``i`` with the per-Q-tile PV skip ("Sparge
     Attention (Composable Kernel)" README, 'Not yet ported': pv_threshold
     per-Q-tile skip in the attention kernel, a pure performance feature).
@@ -170,7 +170,9 @@ def attention_unit_pv_skip(q: np.ndarray, k: np.ndarray, v: np.ndarray, lut_row:
     product; its probabilities still count in the softmax denominator, and the
     LSE is unchanged.  So every skipped probability is below e^-pv_threshold
     times the row's largest one.  Returns (O [rows, dv], LSE [rows], the list
-    of skipped kv blocks)."""
+    of skipped kv blocks).  ``margins``, if given, receives per visited block
+    the smallest over rows of m - pv_threshold - (block max): the block is
+    skipped when it is positive."""
     s_q, s_k = q.shape[0], k.shape[0]
     t = np.arange(i * blkq, min((i + 1) * blkq, s_q))
     rows, dv = len(t), v.shape[1]
@@ -185,6 +187,8 @@ def attention_unit_pv_skip(q: np.ndarray, k: np.ndarray, v: np.ndarray, lut_row:
             s = np.where(keys[None, :] <= t[:, None], s, -np.inf)
         tmax = s.max(axis=1)
         skip = bool(np.all(tmax < m - pv_threshold))
+        if margins is not None:
+            margins.append(float(np.min(m - pv_threshold - tmax)))
         m_new = np.maximum(m, tmax)
         live = np.isfinite(m_new)
         alpha = np.where(live, np.exp(np.where(live, m - m_new, 0.0)), 0.0)

@@ -88,12 +88,12 @@ def test_block_map_rejects(L, kw, code):
 def _fm(L, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=1, b=1, hq=4, hk=2, s_q=256, s_k=256, d=128, dv=128,
              blkq=64, blkk=64, lut=FAKE, cnt=FAKE, stride=4, S=1, scale=0.1, causal=0,
-             out=FAKE, lse=None, op=None, lp=None)
+             pv=float("inf"), out=FAKE, lse=None, op=None, lp=None)
     a.update(kw)
     return L.sparse_fmha_fwd(a["q"], a["k"], a["v"], a["dtype"], a["b"], a["hq"], a["hk"],
                              a["s_q"], a["s_k"], a["d"], a["dv"], a["blkq"], a["blkk"],
                              a["lut"], a["cnt"], a["stride"], a["S"], a["scale"], a["causal"],
-                             a["out"], a["lse"], a["op"], a["lp"], None)
+                             a["pv"], a["out"], a["lse"], a["op"], a["lp"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -109,6 +109,11 @@ def _fm(L, **kw):
     (dict(stride=0), fbm.FBM_ERR_INVALID_ARG),
     (dict(blkk=128), fbm.FBM_ERR_UNSUPPORTED),
     (dict(k=ctypes.c_void_p((1 << 20) + 2)), fbm.FBM_ERR_INVALID_ARG),
+    (dict(pv=float("nan")), fbm.FBM_ERR_INVALID_ARG),
+    (dict(pv=-1.0), fbm.FBM_ERR_INVALID_ARG),
+    (dict(pv=4.0, S=2, out=None, op=FAKE, lp=FAKE), fbm.FBM_ERR_UNSUPPORTED),   # split
+    (dict(pv=4.0, out=None, op=FAKE, lp=FAKE), fbm.FBM_ERR_UNSUPPORTED),        # partial
+    (dict(pv=4.0, d=64, dv=64), fbm.FBM_ERR_UNSUPPORTED),                      # mma.sync
 ])
 def test_fmha_rejects(L, kw, code):
     assert _fm(L, **kw) == code

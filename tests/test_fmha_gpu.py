@@ -1,6 +1,8 @@
 """GPU sparse FMHA (sparse_fmha_fwd, attn_combine) against the fp64 oracle on
 the same seeded inputs and the oracle's own LUTs: O within atol 4e-2 / rtol
 1e-2, LSE within 1e-3 nats, empty rows exactly (0, -inf)."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -206,3 +208,70 @@ def test_d128_runs_on_the_tcgen05_kernel(fbm_gpu):
         assert fbm_gpu.fmha_kernel_kind(dt, 128, 128, 1, 1000, 1000) == 1
     assert fbm_gpu.fmha_kernel_kind(torch.float16, 64, 64, 1, 512, 512) == 2
     assert fbm_gpu.fmha_kernel_kind(torch.float16, 128, 128, 4, 512, 512) == 1
+
+
+# ---- per-Q-tile PV skip (pv_threshold) on the tcgen05 kernel
+
+def _pv_case(fbm, cfg, tau, lut, cnt):
+    x, (q, k, v) = prefill_on_gpu(cfg)
+    out, lse = fbm.sparse_fmha_fwd(q, k, v, torch.from_numpy(lut).cuda(),
+                                   torch.from_numpy(cnt).cuda(), scale=cfg.scale,
+                                   causal=cfg.causal, return_lse=True, pv_threshold=tau)
+    assert fbm.get_error() == 0
+    o_np, l_np = out.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64)
+    ratio = cfg.hq // cfg.hk
+    skipped = changed = 0
+    for b in range(cfg.b):
+        for h in range(cfg.hq):
+            qh = synth.bits_to_f64(x["q"][b, h], cfg.dtype)
+            kg = synth.bits_to_f64(x["k"][b, h // ratio], cfg.dtype)
+            vg = synth.bits_to_f64(x["v"][b, h // ratio], cfg.dtype)
+            for i in range(cfg.nq):
+                row = lut[b, h, i, :cnt[b, h, i]]
+                mg = []
+                o_ref, l_ref, sk = oracle.attention_unit_pv_skip(qh, kg, vg, row, i, 64, 64,
+                                                                 cfg.scale, cfg.causal, tau,
+                                                                 margins=mg)
+                fin = [abs(z) for z in mg if math.isfinite(z)]
+                # every skip decision is far from its boundary in fp64 (checked)
+                assert not fin or min(fin) > 1e-3, f"decision margin {min(fin)} at {(b, h, i)}"
+                rows = slice(i * 64, i * 64 + o_ref.shape[0])
+                assert_close_o(o_np[b, h, rows], o_ref, f"O {(b, h, i)} tau={tau}")
+                assert_close_lse(l_np[b, h, rows], l_ref, f"LSE {(b, h, i)}")
+                full = oracle.attention_unit(qh, kg, vg, row, i, 64, 64, cfg.scale, cfg.causal)[0]
+                skipped += len(sk)
+                changed += int(np.abs(full - o_ref).max() > 4e-2)
+    print(f"{cfg.name} tau={tau}: {skipped} blocks skipped, {changed} q blocks visibly changed")
+    return skipped, changed
+
+
+@pytest.mark.parametrize("tau", [0.5, 2.0, 6.0])
+def test_pv_skip_full_rows_ragged(fbm_gpu, tau):
+    cfg = synth.C1.replace(hq=2, hk=1, s=1000, d=128, dtype="f16")
+    nq = cfg.nq
+    lut = np.tile(np.arange(nq, dtype=np.int32), (1, 2, nq, 1))
+    cnt = np.full((1, 2, nq), nq, dtype=np.int32)
+    skipped, changed = _pv_case(fbm_gpu, cfg, tau, lut, cnt)
+    assert skipped > 0
+    if tau == 0.5:
+        assert changed > 0      # the skip visibly changes O: a wrong decision would show
+
+
+def test_pv_skip_causal_bf16_block_map_lut(fbm_gpu):
+    cfg = synth.C1.replace(hq=4, hk=2, s=1000, d=128, dtype="bf16", causal=True, cs=3.0)
+    x = cached_prefill(cfg)
+    ph = synth.per_head(cfg, 0.5)
+    r = oracle.sparge_block_map(x["q"], x["k"], ph, None, synth.per_head(cfg, cfg.simthreshd1),
+                                cfg.scale, True, False, dtype="bf16")
+    skipped, _ = _pv_case(fbm_gpu, cfg, 2.0, r["lut"], r["count"])
+    assert skipped > 0
+
+
+def test_pv_skip_infinite_threshold_is_bit_identical(fbm_gpu):
+    cfg = synth.C1.replace(hq=2, hk=1, s=640, d=128, dtype="f16")
+    lut, cnt = hand_lut(cfg, seed=3)
+    x, (q, k, v) = prefill_on_gpu(cfg)
+    args = (q, k, v, torch.from_numpy(lut).cuda(), torch.from_numpy(cnt).cuda())
+    a = fbm_gpu.sparse_fmha_fwd(*args, scale=cfg.scale, return_lse=True)
+    b = fbm_gpu.sparse_fmha_fwd(*args, scale=cfg.scale, return_lse=True, pv_threshold=math.inf)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
