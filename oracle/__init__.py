@@ -67,6 +67,14 @@ from .block_map import (  # noqa: F401
     smooth_keys,
     sparge_block_map,
 )
+from .fp8 import (  # noqa: F401
+    E4M3_MAX,
+    e4m3_values,
+    round_e4m3,
+    quantize_block_e4m3,
+    quantize_blocks_e4m3,
+    attention_unit_fp8,
+)
 from .attention import (  # noqa: F401
     row_keys,
     attention_unit,

@@ -550,6 +550,136 @@ def test_planted_pv_skip_mistake_is_caught(monkeypatch):
 
 
 # ----------------------------------------------------------------------------
+# fp8 (e4m3) Q/K
+# ----------------------------------------------------------------------------
+
+from oracle import fp8 as ofp8  # noqa: E402
+
+
+def test_e4m3_value_table():
+    tab = oracle.e4m3_values()
+    assert len(tab) == 127 and (np.diff(tab) > 0).all()
+    assert tab[0] == 0.0 and tab[1] == 2.0 ** -9 and tab[7] == 7 * 2.0 ** -9
+    assert tab[8] == 2.0 ** -6 and tab[-1] == 448.0 and tab[-2] == 416.0
+    assert tab[np.searchsorted(tab, 1.0)] == 1.0 and tab[np.searchsorted(tab, 1.0) + 1] == 1.125
+
+
+def test_e4m3_rounding_hand_cases():
+    x = np.array([1.0625, 1.1875, 464.0, 500.0, 1e30, 2.0 ** -10, 3 * 2.0 ** -11, -1.0625,
+                  -448.0, 0.0, 17.0, 18.0])
+    want = [1.0, 1.25, 448.0, 448.0, 448.0, 0.0, 2.0 ** -9, -1.0, -448.0, 0.0, 16.0, 18.0]
+    assert oracle.round_e4m3(x).tolist() == want
+
+
+def test_e4m3_rounding_matches_torch_cast_in_range():
+    # a library routine for the in-range case: ties, subnormals, every binade
+    rng = np.random.default_rng(21)
+    tab = oracle.e4m3_values()
+    mids = (tab[1:] + tab[:-1]) / 2                     # exact ties
+    x = np.concatenate([tab, mids, rng.uniform(-448, 448, 20000),
+                        rng.uniform(-2.0 ** -5, 2.0 ** -5, 20000), -mids])
+    x = x.astype(np.float32).astype(np.float64)
+    want = torch.from_numpy(x).float().to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(oracle.round_e4m3(x), want)
+
+
+def test_e4m3_block_quantisation_is_lossless_on_representable_blocks():
+    rng = np.random.default_rng(22)
+    tab = oracle.e4m3_values()
+    for k2 in (-12, 0, 5):
+        codes = rng.choice(tab, (64, 32)) * rng.choice([-1.0, 1.0], (64, 32))
+        codes[3, 7] = 448.0                                # amax = 448 * 2^k2
+        x = codes * 2.0 ** k2
+        vals, qs = oracle.quantize_block_e4m3(x)
+        assert qs == 2.0 ** k2 and np.array_equal(vals * qs, x)
+
+
+def test_e4m3_scales_are_per_block():
+    # a tiny block next to a large one keeps its own relative precision
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((128, 16))
+    x[64:] *= 2.0 ** -20
+    vals, qs = oracle.quantize_blocks_e4m3(x, 64)
+    rel = np.abs(vals * np.repeat(qs, 64)[:, None] - x) / np.abs(x)
+    assert rel[np.abs(x) > 1e-3 * np.abs(x).max(axis=1, keepdims=True)].max() <= 2.0 ** -4
+
+
+def _fp8_case(seed=24):
+    rng = np.random.default_rng(seed)
+    q, k, v = rng.standard_normal((256, 32)), rng.standard_normal((256, 32)), \
+        rng.standard_normal((256, 16))
+    return q, k, v
+
+
+def test_fp8_attention_equals_plain_attention_on_representable_inputs():
+    rng = np.random.default_rng(25)
+    tab = oracle.e4m3_values()
+
+    def rep(n):  # 64-row blocks of e4m3 values times a power of two, amax 448 * 2^k
+        x = rng.choice(tab, (n, 32)) * rng.choice([-1.0, 1.0], (n, 32))
+        for b0 in range(0, n, 64):
+            x[b0, 0] = 448.0
+            x[b0:b0 + 64] *= 2.0 ** int(rng.integers(-9, -5))
+        return x
+
+    q, k = rep(256), rep(256)
+    v = rng.standard_normal((256, 16))
+    for causal in (False, True):
+        row = [0, 1, 2] if causal else [3, 0, 2]
+        o8 = oracle.attention_unit_fp8(q, k, v, row, 2, 64, 64, 0.25, causal)
+        ref = oracle.attention_unit(q, k, v, row, 2, 64, 64, 0.25, causal)
+        assert np.abs(o8[0] - ref[0]).max() < 1e-12 and np.abs(o8[1] - ref[1]).max() < 1e-12
+
+
+def test_fp8_score_and_lse_error_bound():
+    q, k, v = _fp8_case()
+    row = [0, 1, 3]
+    cq, sq = oracle.quantize_block_e4m3(q[128:192])
+    # |x - qscale * code| <= 2^-4 |x| for normal codes, <= 2^-10 qscale below them
+    for x in (q[128:192], k[0:64]):
+        c, s = oracle.quantize_block_e4m3(x)
+        err = np.abs(c * s - x)
+        assert (err <= np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * s) * (1 + 1e-6)).all()
+    o8, l8 = oracle.attention_unit_fp8(q, k, v, row, 2, 64, 64, 0.2, False)
+    o, l = oracle.attention_unit(q, k, v, row, 2, 64, 64, 0.2, False)
+    # score error bound from the element bounds; the LSE moves by at most the
+    # largest score error (logsumexp is 1-Lipschitz in the max norm)
+    keys = oatt.row_keys(row, 64, 256)
+    dq = np.maximum(2.0 ** -4 * np.abs(q[128:192]), 2.0 ** -10 * sq)
+    dk = np.concatenate([np.maximum(2.0 ** -4 * np.abs(k[j * 64:(j + 1) * 64]),
+                                    2.0 ** -10 * oracle.quantize_block_e4m3(k[j * 64:(j + 1) * 64])[1])
+                         for j in row])
+    aq, ak = np.abs(q[128:192]), np.abs(k[keys])
+    bound = 0.2 * (aq @ dk.T + dq @ ak.T + dq @ dk.T)
+    assert np.abs(l8 - l).max() <= bound.max()
+    assert np.abs(l8 - l).max() > 0                       # the quantisation does change it
+
+
+def test_planted_fp8_mistakes_are_caught(monkeypatch):
+    # one scale for the whole tensor instead of one per block
+    real = ofp8.quantize_block_e4m3
+    big = {}
+
+    def per_tensor(x):
+        vals, qs = real(x)
+        qs_t = big.setdefault("s", qs)
+        return oracle.round_e4m3(np.asarray(x, np.float64) / qs_t), qs_t
+
+    monkeypatch.setattr(ofp8, "quantize_block_e4m3", per_tensor)
+    with pytest.raises(AssertionError):
+        test_e4m3_scales_are_per_block()
+    monkeypatch.undo()
+    # rounding ties toward zero (the first nearest value) instead of to the even code
+    def ties_down(x):
+        a = np.minimum(np.abs(np.asarray(x, np.float64)), oracle.E4M3_MAX)
+        return np.copysign(ofp8._TABLE[np.abs(a[..., None] - ofp8._TABLE).argmin(-1)], x)
+
+    monkeypatch.setattr(oracle, "round_e4m3", ties_down)
+    with pytest.raises(AssertionError):
+        test_e4m3_rounding_hand_cases()
+
+
+# ----------------------------------------------------------------------------
 # context parallelism over the kv blocks
 # ----------------------------------------------------------------------------
 
