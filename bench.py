@@ -40,9 +40,9 @@ TOPKS = (0.1, 0.2, 0.4, 0.6, 1.0)
 # profiles/), keyed by the sha256 of the kernel source it was taken on; a
 # kernel edited since then reports traffic = null.
 NCU_TRAFFIC = {
-    # profiles/sparse_fmha_tc_b2h32s16384d128_topk04.md (current source): 814.06 MB read +
-    # 256.26 MB written
-    "5f02de1f66743078": 1070325504,
+    # profiles/sparse_fmha_tc_b2h32s16384d128_topk04.md (current source): 814.14 MB read +
+    # 256.63 MB written
+    "43ae43e463ccc9fa": 1070770944,
 }
 
 
@@ -386,6 +386,26 @@ def run_ours(args):
     # and read back once, the -1-padded LUT rows and the counts written
     pooled = (cfg.b * cfg.hq * nq + cfg.b * cfg.hk * nq) * (cfg.d + 1) * 4
     bm_bytes = (q.numel() + k.numel()) * 2 + 2 * pooled + lut.numel() * 4 + cnt.numel() * 4
+
+    # ---- fp8 (e4m3) Q / K: block quantisation of Q and K, then the attention
+    # over the quantised scores (same LUT; V, P and O 16-bit)
+    fp8_res = None
+    if rank == 0 and not args.no_extra:
+        q8, qsc = fbm.quantize_e4m3_blocks(q)
+        k8, ksc = fbm.quantize_e4m3_blocks(k)
+        quant_ms = timed(lambda: (fbm.quantize_e4m3_blocks(q, codes=q8, scales=qsc),
+                                  fbm.quantize_e4m3_blocks(k, codes=k8, scales=ksc)), 5, 1)
+        a8_ms = timed(lambda: fbm.sparse_fmha_fwd_fp8(q8, qsc, k8, ksc, v, lut, cnt,
+                                                      scale=cfg.scale, out=out), 5, 1)
+        qbytes = (q.numel() + k.numel()) * (2 + 1) + (qsc.numel() + ksc.numel()) * 4
+        fp8_res = {"quant_ms": round(quant_ms, 4),
+                   "quant_GB_s": round(qbytes / (quant_ms * 1e-3) / 1e9, 1),
+                   "attn_ms": round(a8_ms, 4), "vs_16bit_attn": round(at_ms / a8_ms, 3),
+                   "eff_tflops_attn": round(flops / (a8_ms * 1e-3) / 1e12, 1),
+                   "eff_tflops_quant_plus_attn": round(flops / ((a8_ms + quant_ms) * 1e-3) / 1e12,
+                                                       1)}
+        del q8, k8, qsc, ksc
+
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
@@ -413,6 +433,7 @@ def run_ours(args):
         "sweep": sweep,
         "context_parallel": cp_res,
         "pv_skip": pv_res,
+        "fp8_qk": fp8_res,
         "e2e": e2e,
         "clocks": clocks,
         # per step: k_pool_sim, k_pooled_scores, k_select and k_fmha_tc

@@ -56,6 +56,9 @@ def lib() -> ctypes.CDLL:
                                        vp, vp, i32, i32, f32, i32, f32, vp, vp, vp, vp, vp])
         L.attn_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
         L.lut_shard.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp]
+        L.quantize_e4m3_blocks.argtypes = [vp, i32, i64, i32, i32, vp, vp, vp]
+        L.sparse_fmha_fwd_fp8.argtypes = ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                           i32, vp, vp, i32, f32, i32, vp, vp, vp])
         L.sparse_decode_fwd.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, i32, vp,
                                          i32, i32, f32, vp, vp, vp])
         L.fbm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
@@ -63,7 +66,8 @@ def lib() -> ctypes.CDLL:
         L.fbm_fmha_kernel_kind.argtypes = [i32] * 6
         L.fbm_fmha_kernel_kind.restype = i32
         for name in ("fbm_get_error", "sparge_block_map", "sparge_block_map_static",
-                     "sparse_fmha_fwd", "attn_combine", "lut_shard", "sparse_decode_fwd"):
+                     "sparse_fmha_fwd", "attn_combine", "lut_shard", "sparse_decode_fwd",
+                     "quantize_e4m3_blocks", "sparse_fmha_fwd_fp8"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -260,6 +264,56 @@ def attn_combine(o_part: torch.Tensor, lse_part: torch.Tensor, *, out_dtype=torc
         if return_lse else None
     _check(lib().attn_combine(_ptr(o_part), _ptr(lse_part), S, rows, dv, codes[out.dtype],
                               _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse
+
+
+def quantize_e4m3_blocks(x: torch.Tensor, *, codes: Optional[torch.Tensor] = None,
+                         scales: Optional[torch.Tensor] = None, stream=None):
+    """x [..., s, 128] fp16 / bf16 -> (codes uint8 [..., s, 128], scales fp32
+    [..., ceil(s / 64)]): e4m3 codes with one scale per 64-row block."""
+    _cuda(x, "x")
+    s, d = x.shape[-2], x.shape[-1]
+    lead = tuple(x.shape[:-2])
+    bh = 1
+    for n in lead:
+        bh *= n
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(lead + ((s + 63) // 64,), dtype=torch.float32, device=x.device)
+    _check(lib().quantize_e4m3_blocks(_ptr(x), _dt(x), bh, s, d, _ptr(codes), _ptr(scales),
+                                      _stream(stream)))
+    return codes, scales
+
+
+def sparse_fmha_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor,
+                        k_scale: torch.Tensor, v: torch.Tensor, lut: Optional[torch.Tensor],
+                        lut_count: Optional[torch.Tensor], *, scale: Optional[float] = None,
+                        causal: bool = False, return_lse: bool = False,
+                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                        stream=None):
+    """Sparse attention with e4m3 Q / K (from quantize_e4m3_blocks) and
+    16-bit V: returns (out [b, hq, s_q, 128] in v's dtype, lse or None)."""
+    for t_, n in ((q8, "q8"), (q_scale, "q_scale"), (k8, "k8"), (k_scale, "k_scale"), (v, "v")):
+        _cuda(t_, n)
+    if q8.dtype != torch.uint8 or k8.dtype != torch.uint8:
+        raise TypeError("q8 / k8 must be uint8 e4m3 codes")
+    b, hq, s_q, d = q8.shape
+    hk, s_k, dv = k8.shape[1], k8.shape[2], v.shape[3]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    stride = 0
+    if lut is not None:
+        _cuda(lut, "lut"), _cuda(lut_count, "lut_count")
+        stride = lut.shape[-1]
+    if out is None:
+        out = torch.empty((b, hq, s_q, dv), dtype=v.dtype, device=v.device)
+    if return_lse and lse is None:
+        lse = torch.empty((b, hq, s_q), dtype=torch.float32, device=v.device)
+    _check(lib().sparse_fmha_fwd_fp8(
+        _ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale), _ptr(v), _dt(v), b, hq, hk, s_q, s_k,
+        d, dv, _ptr(lut), _ptr(lut_count), stride, float(scale), int(causal), _ptr(out),
+        _ptr(lse), _stream(stream)))
     return out, lse
 
 

@@ -259,6 +259,64 @@ fbm_status attn_combine(const float *o_part, const float *lse_part, int num_spli
                      "attn_combine launch");
 }
 
+fbm_status quantize_e4m3_blocks(const void *x, int dtype, int64_t bh, int s, int d,
+                                uint8_t *codes, float *scales, void *stream) {
+  if (!x || !codes || !scales) return fail(FBM_ERR_INVALID_ARG, "quantize_e4m3_blocks: null pointer");
+  if (bh <= 0 || s <= 0) return fail(FBM_ERR_INVALID_ARG, "quantize_e4m3_blocks: sizes must be positive");
+  if (dtype != FBM_F16 && dtype != FBM_BF16)
+    return fail(FBM_ERR_INVALID_ARG, "quantize_e4m3_blocks: dtype must be f16 or bf16");
+  if (d != 128) return fail(FBM_ERR_UNSUPPORTED, "quantize_e4m3_blocks: d = 128 only");
+  if (!aligned16(x) || !aligned16(codes))
+    return fail(FBM_ERR_INVALID_ARG, "quantize_e4m3_blocks: x and codes must be 16-byte aligned");
+  const int nb = (s + 63) / 64;
+  if (bh * nb > (int64_t)0x7fffffff * 8)
+    return fail(FBM_ERR_UNSUPPORTED, "quantize_e4m3_blocks: too many blocks");
+  fbm::QuantLaunch L{x, dtype == FBM_BF16, s, nb, bh * nb, codes, scales};
+  return cuda_status(fbm::launch_quant_e4m3(L, static_cast<cudaStream_t>(stream)),
+                     "quantize_e4m3_blocks launch");
+}
+
+fbm_status sparse_fmha_fwd_fp8(const uint8_t *q8, const float *q_scale, const uint8_t *k8,
+                               const float *k_scale, const void *v, int dtype, int b, int hq,
+                               int hk, int s_q, int s_k, int d, int dv, const int32_t *lut,
+                               const int32_t *lut_count, int lut_stride, float scale, int causal,
+                               void *out, float *lse, void *stream) {
+  if (!q8 || !q_scale || !k8 || !k_scale || !v || !out)
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_fp8: null pointer argument");
+  if ((lut == nullptr) != (lut_count == nullptr))
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_fp8: lut and lut_count must both be set or both NULL");
+  if (b <= 0 || hq <= 0 || hk <= 0 || s_q <= 0 || s_k <= 0)
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_fp8: sizes must be positive");
+  if (hq % hk != 0) return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_fp8: hq %% hk != 0");
+  if (dtype != FBM_F16 && dtype != FBM_BF16)
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_fp8: dtype (of v and out) must be f16 or bf16");
+  if (d != 128 || dv != 128) return fail(FBM_ERR_UNSUPPORTED, "sparse_fmha_fwd_fp8: d = dv = 128 only");
+  if (causal && s_q != s_k)
+    return fail(FBM_ERR_UNSUPPORTED, "sparse_fmha_fwd_fp8: causal needs s_q == s_k");
+  const int nq = (s_q + 63) / 64, nk = (s_k + 63) / 64;
+  if (lut && lut_stride < 1)
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_fp8: lut_stride must be >= 1");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_fp8: scale must be positive and finite");
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v) || !aligned16(out))
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_fp8: tensors must be 16-byte aligned");
+  if ((long long)b * hq * nq > 0x7fffffffLL)
+    return fail(FBM_ERR_UNSUPPORTED, "sparse_fmha_fwd_fp8: grid too large");
+  fbm::FmhaLaunch L{};
+  L.q = q8; L.k = k8; L.v = v;
+  L.bf16 = dtype == FBM_BF16;
+  L.b = b; L.hq = hq; L.hk = hk; L.s_q = s_q; L.s_k = s_k; L.d = d; L.nq = nq; L.nk = nk;
+  L.lut = lut; L.cnt = lut_count; L.lut_stride = lut ? lut_stride : nk;
+  L.num_splits = 1; L.causal = causal != 0; L.scale = scale;
+  L.pv_threshold = INFINITY;
+  L.q_scale = q_scale; L.k_scale = k_scale;
+  L.out = out; L.lse = lse;
+  L.err = error_word();
+  if (!L.err) return fail(FBM_ERR_CUDA, "sparse_fmha_fwd_fp8: error word lookup failed");
+  return cuda_status(fbm::launch_fmha_tc(L, static_cast<cudaStream_t>(stream)),
+                     "sparse_fmha_fwd_fp8 launch (tcgen05)");
+}
+
 fbm_status lut_shard(const int32_t *lut, const int32_t *lut_count, int64_t rows, int lut_stride,
                      int lo, int hi, int32_t *out_lut, int32_t *out_count, int out_stride,
                      void *stream) {

@@ -114,6 +114,7 @@ struct TcParams {
   size_t plane;   // b * hq * s_q
   float sl2;      // scale * log2(e)
   float tau2;     // pv_threshold * log2(e) (PV-skip variant)
+  const float *qscale, *kscale;  // fp8 variant: [b * hq, nq] and [b * hk, nk] block scales
 };
 
 // one (batch, head, q block, split): kv-list entries off .. off + n of the row
@@ -156,8 +157,9 @@ FBM_DEVICE Unit unit_of(const TcParams &P, int u) {
 
 FBM_DEVICE int entry_of(const Unit &U, int t) { return U.row ? __ldg(U.row + t) : U.off + t; }
 
-template <bool kBf16, bool kPartial, bool kPvSkip>
+template <bool kBf16, bool kPartial, bool kPvSkip, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__ TcParams P) {
+  static_assert(!(kFp8 && (kPartial || kPvSkip)), "the fp8 variant runs whole rows");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -204,6 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     if (!mbar_wait(bar(eb), ((g / ns) & 1) ^ 1, abort_flag, kWaitNs)) return false;
     int js[2] = {-1, -1};
     uint32_t bytes = 0;
+    // an fp8 K block is one 128-byte-wide box; 16-bit blocks are two
+    const int nchunk = (kFp8 && !is_v) ? 1 : 2;
     for (int hf = 0; hf < 2; ++hf) {
       const int t = 2 * p + hf;
       if (t >= U.n) break;
@@ -215,13 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         j = 0;
       }
       js[hf] = j;
-      bytes += 2 * kQChunk;
+      bytes += nchunk * kQChunk;
     }
     mbar_arrive_tx(bar(fb), bytes);
     const uint32_t dst0 = sbase + (is_v ? OFF_V : OFF_K) + slot * kPairBytes;
     for (int hf = 0; hf < 2; ++hf) {
       if (js[hf] < 0) continue;
-      for (int c = 0; c < 2; ++c)
+      for (int c = 0; c < nchunk; ++c)
         tma_load_3d(dst0 + c * kPairChunk + hf * kQChunk, is_v ? &P.tv : &P.tk, c * 64,
                     js[hf] * 64, U.bh_k, bar(fb));
     }
@@ -239,8 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         const int npairs = (U.n + 1) >> 1;
         const int qb = uc & 1;
         if (!(ok = mbar_wait(bar(B_QE + qb), ((uc >> 1) & 1) ^ 1, abort_flag, kWaitNs))) break;
-        mbar_arrive_tx(bar(B_QF + qb), kQBytes);
-        for (int c = 0; c < 2; ++c)
+        constexpr int qchunks = kFp8 ? 1 : 2;  // an fp8 Q tile is one 128-byte-wide box
+        mbar_arrive_tx(bar(B_QF + qb), qchunks * kQChunk);
+        for (int c = 0; c < qchunks; ++c)
           tma_load_3d(sbase + OFF_Q + qb * kQBytes + c * kQChunk, &P.tq, c * 64, U.i * 64,
                       U.bh_q, bar(B_QF + qb));
         for (int p = 0; p < npairs && ok; ++p) ok = load_pair(U, pc, p, false);
@@ -266,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
   } else if (warp == kWarpS) {
     // ------------------------------------------------------------ S issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_f16(kBf16, false, false, 64, 128);
+      // (kind::f8f6f4 with e4m3 A and B uses format code 0, as f16 does)
+      constexpr uint32_t idS = idesc_f16(kFp8 ? false : kBf16, false, false, 64, 128);
       int pc = 0, uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
@@ -284,11 +290,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           tc_fence_after();
           const uint32_t k_lo = sdesc_lo(sbase + OFF_K + slot * kPairBytes, 16);
           const uint32_t dS = tbase + kTS + ss * 128;
+          if constexpr (kFp8) {
+            // e4m3 rows are 128 bytes: one swizzle atom wide, 32 values of K per MMA
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_f16_lo(dS, q_lo + (((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4),
-                       k_lo + (((kk >> 2) * kPairChunk + (kk & 3) * 32) >> 4), kDescHi, idS,
-                       kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kD / 32; ++kk)
+              mma_f8_lo(dS, q_lo + ((kk * 32) >> 4), k_lo + ((kk * 32) >> 4), kDescHi, idS,
+                        kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_f16_lo(dS, q_lo + (((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4),
+                         k_lo + (((kk >> 2) * kPairChunk + (kk & 3) * 32) >> 4), kDescHi, idS,
+                         kk > 0 ? 1u : 0u);
+          }
           mma_commit(bar(B_SF + ss));
           mma_commit(bar(B_KE + slot));
         }
@@ -381,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       }
       const int npairs = (U.n + 1) >> 1;
       const int qpos = q0 + row;
+      const float qsl2 = kFp8 ? P.sl2 * __ldg(P.qscale + (size_t)U.bh_q * P.nq + U.i) : P.sl2;
       float m = -INFINITY;                 // running max of the row (log2 domain)
       float mt = -INFINITY;                // exact running max (PV-skip variant)
       uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};  // this thread's share of the row sum
@@ -424,6 +439,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           }
           mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
         }
+        // fp8: the two block scales fold into this thread's factor (its 64 keys
+        // are one kv block); the pair max is then taken over scaled scores
+        float fsc = P.sl2;
+        if constexpr (kFp8) {
+          fsc = qsl2 * (jvalid ? __ldg(P.kscale + (size_t)U.bh_k * P.nk + j) : 1.f);
+          mx *= fsc;
+        }
         uint32_t vote = 0;
         if constexpr (kPvSkip) {
           const float mx_other = __shfl_xor_sync(0xffffffffu, mx, 16);
@@ -442,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         } else {
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         }
-        const float mxs = mx * P.sl2;
+        const float mxs = kFp8 ? mx : mx * P.sl2;
         const bool need = mxs > m + 8.0f;
         if (__any_sync(0xffffffffu, need)) {
           // rare: some score of the warp's rows exceeds its running max by more
@@ -475,11 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         // P = exp2(s * scale * log2 e - m), packed to 16-bit pairs
         const float mu = (m == -INFINITY) ? 0.f : m;
         const uint64_t negm = f2_pack(-mu, -mu);
+        const uint64_t fx2 = kFp8 ? f2_pack(fsc, fsc) : sl2x2;
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
-                                    sl2x2, negm);
+                                    fx2, negm);
           const float2 xv = f2_unpack(x);
           const float e0 = fast_exp2(xv.x), e1 = fast_exp2(xv.y);
           l2[i & 3] = f2_add(l2[i & 3], f2_pack(e0, e1));
@@ -603,6 +626,20 @@ bool make_map(CUtensorMap *m, const void *base, int bh, int s, bool bf16) {
   return r == CUDA_SUCCESS;
 }
 
+// e4m3 codes [bh, s, 128]: one 128-byte-wide box of 64 rows, 128-byte swizzle
+bool make_map8(CUtensorMap *m, const void *base, int bh, int s) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)s, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)kD, (cuuint64_t)s * kD};
+  cuuint32_t box[3] = {128, 64, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n[64] = {};
   int dev = 0;
@@ -612,20 +649,23 @@ int sm_count() {
   return n[dev] > 0 ? n[dev] : 148;
 }
 
-template <bool BF16, bool PARTIAL, bool PVSKIP>
+template <bool BF16, bool PARTIAL, bool PVSKIP, bool FP8 = false>
 cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   static_assert(!(PARTIAL && PVSKIP), "the PV skip runs on whole rows only");
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_fmha_tc<BF16, PARTIAL, PVSKIP>,
+    cudaError_t e = cudaFuncSetAttribute(k_fmha_tc<BF16, PARTIAL, PVSKIP, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   TcParams P;
   memset(&P, 0, sizeof(P));
-  if (!make_map(&P.tq, L.q, L.b * L.hq, L.s_q, BF16) || !make_map(&P.tk, L.k, L.b * L.hk, L.s_k, BF16) ||
-      !make_map(&P.tv, L.v, L.b * L.hk, L.s_k, BF16) ||
+  const bool qk_ok = FP8 ? (make_map8(&P.tq, L.q, L.b * L.hq, L.s_q) &&
+                            make_map8(&P.tk, L.k, L.b * L.hk, L.s_k))
+                         : (make_map(&P.tq, L.q, L.b * L.hq, L.s_q, BF16) &&
+                            make_map(&P.tk, L.k, L.b * L.hk, L.s_k, BF16));
+  if (!qk_ok || !make_map(&P.tv, L.v, L.b * L.hk, L.s_k, BF16) ||
       (L.out && !make_map(&P.to, L.out, L.b * L.hq, L.s_q, BF16)))
     return cudaErrorInvalidValue;
   P.lut = L.lut;
@@ -642,8 +682,10 @@ cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   P.units = L.b * L.hq * L.nq * L.num_splits;
   P.sl2 = L.scale * 1.4426950408889634f;
   P.tau2 = L.pv_threshold * 1.4426950408889634f;
+  P.qscale = L.q_scale;
+  P.kscale = L.k_scale;
   const int grid = std::min(P.units, sm_count());
-  k_fmha_tc<BF16, PARTIAL, PVSKIP><<<grid, kThreads, SMEM_ALLOC, st>>>(P);
+  k_fmha_tc<BF16, PARTIAL, PVSKIP, FP8><<<grid, kThreads, SMEM_ALLOC, st>>>(P);
   return cudaGetLastError();
 }
 
@@ -655,6 +697,9 @@ bool fmha_tc_supported(int d, int dv, int num_splits, int s_q, int s_k) {
 
 cudaError_t launch_fmha_tc(const FmhaLaunch &L, cudaStream_t st) {
   // whole rows in dtype, or fp32 partials (split chunks, or rows for a combine)
+  if (L.q_scale)  // e4m3 Q and K (whole rows; the caller has checked)
+    return L.bf16 ? launch_t<true, false, false, true>(L, st)
+                  : launch_t<false, false, false, true>(L, st);
   if (L.out == nullptr)
     return L.bf16 ? launch_t<true, true, false>(L, st) : launch_t<false, true, false>(L, st);
   if (L.pv_threshold < INFINITY)

@@ -42,6 +42,7 @@ struct FmhaLaunch {
   int lut_stride, num_splits, causal;
   float scale;
   float pv_threshold;  // +inf: no PV skip
+  const float *q_scale, *k_scale;  // fp8 Q / K (q, k hold e4m3 codes) or nullptr
   void *out;
   float *lse, *o_part, *lse_part;
   uint32_t *err;
@@ -59,6 +60,15 @@ struct CombineLaunch {
   float *lse_out;
 };
 cudaError_t launch_combine(const CombineLaunch &L, cudaStream_t st);
+
+struct QuantLaunch {
+  const void *x;     // [bh, s, 128] fp16 / bf16
+  int bf16, s, nb;   // nb = ceil(s / 64)
+  int64_t units;     // bh * nb
+  uint8_t *codes;    // [bh, s, 128] e4m3
+  float *scales;     // [bh, nb]
+};
+cudaError_t launch_quant_e4m3(const QuantLaunch &L, cudaStream_t st);
 
 struct LutShardLaunch {
   const int32_t *lut, *cnt;

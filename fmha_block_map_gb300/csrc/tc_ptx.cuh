@@ -179,6 +179,17 @@ FBM_DEVICE void mma_f16_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32
       "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same with kind::f8f6f4 (A and B both e4m3 here, 32 values of K per
+// instruction).
+FBM_DEVICE void mma_f8_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 a, b;\n setp.ne.b32 p, %5, 0;\n"
+      " mov.b64 a, {%1, %3};\n mov.b64 b, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // MMA with the A operand in TMEM (`a_tmem`: M rows in the accumulator lane
 // layout, K values packed two per 32-bit column) and B in shared memory
 // (low descriptor word `b_lo`, high word `hi`).
@@ -325,7 +336,8 @@ __host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo) {
   return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
 
-// Instruction descriptor of kind::f16 with fp32 accumulation.
+// Instruction descriptor of kind::f16 with fp32 accumulation (also that of
+// kind::f8f6f4 with e4m3 A and B: format code 0 in the same fields).
 //   [4,6) D format (1 = f32), [7,10) A format, [10,13) B format (0 = f16,
 //   1 = bf16), [15] A major, [16] B major (0 = K, 1 = MN), [17,23) N >> 3,
 //   [24,29) M >> 4.

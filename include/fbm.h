@@ -219,6 +219,41 @@ fbm_status attn_combine(const float *o_part, const float *lse_part, int num_spli
                         void *stream);
 
 /*
+ * quantize_e4m3_blocks - fp8 Q or K for sparse_fmha_fwd_fp8: one scale per
+ * 64-row block ("Sparge Attention (Composable Kernel)" README, 'Not yet
+ * ported': Q/K quantisation fused into the pool stage; ROCm/aiter pull 6841:
+ * the bf16fp8 recipe).
+ *
+ * For every (head, 64-row block) of x: amax = max |x| (fp32), scales[block] =
+ * amax / 448 and codes = e4m3(x * (448 / amax)) (fp32, round to nearest; e4m3
+ * "fn": round to nearest even, saturating at +-448); an all-zero block gets
+ * scale 1 and zero codes.  x ~= scale * code.
+ *
+ * x: device [bh, s, d] fp16 / bf16 (dtype); d == 128.  codes: device uint8
+ * [bh, s, d]; scales: device fp32 [bh, ceil(s / 64)].  x and codes 16-byte
+ * aligned.
+ */
+fbm_status quantize_e4m3_blocks(const void *x, int dtype, int64_t bh, int s, int d,
+                                uint8_t *codes, float *scales, void *stream);
+
+/*
+ * sparse_fmha_fwd_fp8 - sparse_fmha_fwd with e4m3 Q and K: the scores of
+ * q block i against kv block j are scale * q_scale[i] * k_scale[j] *
+ * (Q codes . K codes^T) (tcgen05 kind::f8f6f4, fp32 accumulation); V, P, the
+ * softmax, O and the LSE as in sparse_fmha_fwd (whole rows, num_splits = 1).
+ *
+ * q8 / q_scale: quantize_e4m3_blocks of Q [b * hq, s_q, 128]; k8 / k_scale:
+ * of K [b * hk, s_k, 128].  v: device [b, hk, s_k, 128] in dtype; out: device
+ * [b, hq, s_q, 128] in dtype; lse: device fp32 [b, hq, s_q] or NULL.  lut,
+ * lut_count, lut_stride, causal as in sparse_fmha_fwd.  d = dv = 128.
+ */
+fbm_status sparse_fmha_fwd_fp8(const uint8_t *q8, const float *q_scale, const uint8_t *k8,
+                               const float *k_scale, const void *v, int dtype, int b, int hq,
+                               int hk, int s_q, int s_k, int d, int dv, const int32_t *lut,
+                               const int32_t *lut_count, int lut_stride, float scale, int causal,
+                               void *out, float *lse, void *stream);
+
+/*
  * lut_shard - the part of every LUT row inside one rank's kv-block range
  * [lo, hi), re-based to that rank's own K/V rows (context-parallel attention:
  * the LSE export exists so that partials over disjoint key sets can be merged

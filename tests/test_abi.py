@@ -145,6 +145,26 @@ def test_lut_shard_rejects(L):
         assert L.lut_shard(*a) == fbm.FBM_ERR_INVALID_ARG, (i, bad)
 
 
+def test_fp8_entry_points_reject(L):
+    q = [FAKE, 0, 2, 512, 128, FAKE, FAKE, None]
+    for i, bad in ((0, None), (1, 7), (2, 0), (4, 64), (5, None)):
+        a = list(q)
+        a[i] = bad
+        assert L.quantize_e4m3_blocks(*a) in (fbm.FBM_ERR_INVALID_ARG, fbm.FBM_ERR_UNSUPPORTED)
+    f = [FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 4, 2, 256, 256, 128, 128, FAKE, FAKE, 4, 0.1, 0,
+         FAKE, None, None]
+    for i, bad, code in ((1, None, fbm.FBM_ERR_INVALID_ARG), (8, 3, fbm.FBM_ERR_INVALID_ARG),
+                         (11, 64, fbm.FBM_ERR_UNSUPPORTED), (14, None, fbm.FBM_ERR_INVALID_ARG),
+                         (16, 0.0, fbm.FBM_ERR_INVALID_ARG), (5, 2, fbm.FBM_ERR_INVALID_ARG),
+                         (18, None, fbm.FBM_ERR_INVALID_ARG)):
+        a = list(f)
+        a[i] = bad
+        assert L.sparse_fmha_fwd_fp8(*a) == code, (i, bad)
+    a = list(f)
+    a[17], a[10] = 1, 512           # causal with s_q != s_k
+    assert L.sparse_fmha_fwd_fp8(*a) == fbm.FBM_ERR_UNSUPPORTED
+
+
 def test_partial_mode_needs_both_partial_buffers(L):
     assert _fm(L, out=None, op=FAKE, lp=None) == fbm.FBM_ERR_INVALID_ARG
     assert _fm(L, out=None, op=None, lp=FAKE) == fbm.FBM_ERR_INVALID_ARG
