@@ -305,6 +305,8 @@ def sparse_fmha_fwd_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tenso
     stride = 0
     if lut is not None:
         _cuda(lut, "lut"), _cuda(lut_count, "lut_count")
+        if lut.dtype != torch.int32 or lut_count.dtype != torch.int32:
+            raise TypeError("lut / lut_count must be int32")
         stride = lut.shape[-1]
     if out is None:
         out = torch.empty((b, hq, s_q, dv), dtype=v.dtype, device=v.device)
