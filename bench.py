@@ -217,6 +217,20 @@ def run_ours(args):
         barrier()
         return e0.elapsed_time(e1) / steps
 
+    def timed_local(fn, steps, warm):
+        # for the rank-0-only measurements: no collective (the other ranks are
+        # not there to meet it)
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
     # ---- the timed step: block map + sparse attention, per-kernel events
     for _ in range(args.warmup):
         block_map(args.topk)
@@ -287,8 +301,9 @@ def run_ours(args):
                                 lse_slot=l_all[r])
             fbm.attn_combine(o_all, l_all, out_dtype=q.dtype, out=out)
 
-        cp_ms = timed(cp_step, 5, 1)
-        comb_ms = timed(lambda: fbm.attn_combine(o_all, l_all, out_dtype=q.dtype, out=out), 5, 1)
+        cp_ms = timed_local(cp_step, 5, 1)
+        comb_ms = timed_local(lambda: fbm.attn_combine(o_all, l_all, out_dtype=q.dtype, out=out),
+                              5, 1)
         cp_res = {"ranks": 2, "emulated": "both ranks on one GPU, one after the other",
                   "ms": round(cp_ms, 4), "combine_ms": round(comb_ms, 4),
                   "eff_tflops": round(flops / (cp_ms * 1e-3) / 1e12, 1),
@@ -302,8 +317,8 @@ def run_ours(args):
     if rank == 0 and not args.no_extra:
         pv_res = []
         for tau in (2.0, 6.0):
-            ms = timed(lambda: fbm.sparse_fmha_fwd(q, k, v, lut, cnt, scale=cfg.scale, out=out,
-                                                   pv_threshold=tau), 5, 1)
+            ms = timed_local(lambda: fbm.sparse_fmha_fwd(q, k, v, lut, cnt, scale=cfg.scale,
+                                                         out=out, pv_threshold=tau), 5, 1)
             pv_res.append({"pv_threshold": tau, "attn_ms": round(ms, 4),
                            "vs_no_skip": round(at_ms / ms, 3),
                            "eff_tflops_attn": round(flops / (ms * 1e-3) / 1e12, 1)})
@@ -393,10 +408,10 @@ def run_ours(args):
     if rank == 0 and not args.no_extra:
         q8, qsc = fbm.quantize_e4m3_blocks(q)
         k8, ksc = fbm.quantize_e4m3_blocks(k)
-        quant_ms = timed(lambda: (fbm.quantize_e4m3_blocks(q, codes=q8, scales=qsc),
-                                  fbm.quantize_e4m3_blocks(k, codes=k8, scales=ksc)), 5, 1)
-        a8_ms = timed(lambda: fbm.sparse_fmha_fwd_fp8(q8, qsc, k8, ksc, v, lut, cnt,
-                                                      scale=cfg.scale, out=out), 5, 1)
+        quant_ms = timed_local(lambda: (fbm.quantize_e4m3_blocks(q, codes=q8, scales=qsc),
+                                        fbm.quantize_e4m3_blocks(k, codes=k8, scales=ksc)), 5, 1)
+        a8_ms = timed_local(lambda: fbm.sparse_fmha_fwd_fp8(q8, qsc, k8, ksc, v, lut, cnt,
+                                                            scale=cfg.scale, out=out), 5, 1)
         qbytes = (q.numel() + k.numel()) * (2 + 1) + (qsc.numel() + ksc.numel()) * 4
         fp8_res = {"quant_ms": round(quant_ms, 4),
                    "quant_GB_s": round(qbytes / (quant_ms * 1e-3) / 1e9, 1),
