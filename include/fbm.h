@@ -231,7 +231,9 @@ fbm_status attn_combine(const float *o_part, const float *lse_part, int num_spli
  *
  * x: device [bh, s, d] fp16 / bf16 (dtype); d == 128.  codes: device uint8
  * [bh, s, d]; scales: device fp32 [bh, ceil(s / 64)].  x and codes 16-byte
- * aligned.
+ * aligned; all buffers are the caller's.  A null pointer, a non-positive size,
+ * another dtype or a misaligned buffer returns FBM_ERR_INVALID_ARG, d != 128
+ * FBM_ERR_UNSUPPORTED, before any launch.  Asynchronous on `stream`.
  */
 fbm_status quantize_e4m3_blocks(const void *x, int dtype, int64_t bh, int s, int d,
                                 uint8_t *codes, float *scales, void *stream);
@@ -245,7 +247,12 @@ fbm_status quantize_e4m3_blocks(const void *x, int dtype, int64_t bh, int s, int
  * q8 / q_scale: quantize_e4m3_blocks of Q [b * hq, s_q, 128]; k8 / k_scale:
  * of K [b * hk, s_k, 128].  v: device [b, hk, s_k, 128] in dtype; out: device
  * [b, hq, s_q, 128] in dtype; lse: device fp32 [b, hq, s_q] or NULL.  lut,
- * lut_count, lut_stride, causal as in sparse_fmha_fwd.  d = dv = 128.
+ * lut_count, lut_stride, causal as in sparse_fmha_fwd (lut == NULL: dense).
+ * d = dv = 128.  All buffers are the caller's.  Argument errors return
+ * FBM_ERR_INVALID_ARG (null pointers, sizes, dtype, hq % hk, scale,
+ * alignment) or FBM_ERR_UNSUPPORTED (d, causal with s_q != s_k) before any
+ * launch; device-detected LUT range errors and wait expiry set the error word
+ * as in sparse_fmha_fwd.  Asynchronous on `stream`.
  */
 fbm_status sparse_fmha_fwd_fp8(const uint8_t *q8, const float *q_scale, const uint8_t *k8,
                                const float *k_scale, const void *v, int dtype, int b, int hq,
