@@ -114,6 +114,10 @@ size_t fbm_block_map_workspace_bytes(int b, int hq, int hk, int s, int d, int bl
   return ws_layout(b, hq, hk, s, d).total;
 }
 
+size_t fbm_workspace_bytes(int b, int hq, int hk, int s, int d) {
+  return fbm_block_map_workspace_bytes(b, hq, hk, s, d, 64, 64);
+}
+
 fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int hq, int hk,
                             int s, int d, int blkq, int blkk, const float *topk,
                             const float *cdfthreshd, const float *simthreshd1, float scale,

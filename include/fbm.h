@@ -82,6 +82,9 @@ fbm_status fbm_get_error(void *stream, uint32_t *detail);
 size_t fbm_block_map_workspace_bytes(int b, int hq, int hk, int s, int d, int blkq,
                                      int blkk);
 
+/* The same for the implemented block size (blkq = blkk = 64). */
+size_t fbm_workspace_bytes(int b, int hq, int hk, int s, int d);
+
 /*
  * sparge_block_map - block-map prediction ("Sparge Attention (Composable
  * Kernel)" README: mean-pool -> cosine sim -> pooled QK -> top-k LUT).

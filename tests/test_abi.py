@@ -46,6 +46,8 @@ def test_workspace_size(L):
     # 2*32 KV heads, 256-B aligned pieces
     assert n >= 2 * (2 * 32 * 256 * 128 * 4 + 2 * 32 * 256 * 4) + 2 * 32 * 128 * 4
     assert L.fbm_block_map_workspace_bytes(1, 1, 1, 64, 64, 32, 64) == 0
+    L.fbm_workspace_bytes.restype = ctypes.c_size_t
+    assert L.fbm_workspace_bytes(2, 32, 32, 16384, 128) == n
 
 
 FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: checks fail before any launch
