@@ -210,6 +210,94 @@ def test_block_map_hand_example():
     assert r["count"][1] == 1 and r["lut"][1, 0] == 1
 
 
+def _gqa_hand_inputs():
+    """b = 1, hq = 4 query heads on hk = 2 KV heads, blk = 2, d = 2, s = 4.
+
+    Every query head pools to qbar_0 = (1, 0), qbar_1 = (0, 1).  KV head 0
+    pools to kbar = (2, 0), (0, 3) -> scores [[2, 0], [0, 3]]; KV head 1 to
+    (0, 1), (1, 0) -> scores [[0, 1], [1, 0]] (scale 1).  Rows of every block
+    are parallel, so every self-similarity is exactly 1."""
+    qh = np.array([[1, 0], [1, 0], [0, 1], [0, 1]], dtype=np.float64)
+    q = np.stack([qh] * 4)[None]
+    k0 = np.array([[2, 0], [2, 0], [0, 3], [0, 3]], dtype=np.float64)
+    k1 = np.array([[0, 1], [0, 1], [1, 0], [1, 0]], dtype=np.float64)
+    k = np.stack([k0, k1])[None]
+    return q, k
+
+
+# per query head h: KV head h // 2, topk, simthreshd1 and the LUT rows
+GQA_TOPK = np.array([0.5, 1.0, 0.5, 0.5], dtype=np.float32)
+GQA_THETA = np.array([0.5, 0.5, 0.5, 2.0], dtype=np.float32)
+GQA_TOPK_LUT = [
+    [[0, -1], [1, -1]],  # h0: KV head 0, one block per row: the row argmax
+    [[0, 1], [0, 1]],    # h1: KV head 0, topk 1.0: both blocks
+    [[1, -1], [0, -1]],  # h2: KV head 1, one block per row
+    [[0, 1], [0, 1]],    # h3: KV head 1, theta 2 > sim 1: every row and column forced
+]
+GQA_CDF = np.array([0.5, 0.95, 0.5, 0.8], dtype=np.float32)
+GQA_CDF_LUT = [
+    [[0, -1], [1, -1]],  # h0: p = (0.881, 0.119) and (0.047, 0.953): the top entry reaches 0.5
+    [[0, 1], [1, -1]],   # h1: 0.881 < 0.95 takes both; 0.953 >= 0.95 takes one
+    [[1, -1], [0, -1]],  # h2: KV head 1, p = (0.269, 0.731): the top entry reaches 0.5
+    [[0, 1], [0, 1]],    # h3: 0.731 < 0.8 takes both
+]
+
+
+def test_per_head_hyperparameters_and_gqa_mapping_hand_example():
+    """Per-head topk / simthreshd1 / cdfthreshd ("Sparge Attention (Composable
+    Kernel)" README, 'Status vs Upstream') and the GQA mapping query head
+    j -> KV head j / (hq / hk) (ROCm/aiter pull 6841), on values worked by
+    hand.  Query heads 0 and 1 share KV head 0, heads 2 and 3 share KV head 1;
+    the two KV heads rank the kv blocks in opposite orders, so a wrong KV head
+    changes a LUT, and every head's hyperparameters differ from head 0's where
+    that changes its LUT."""
+    q, k = _gqa_hand_inputs()
+    r = oracle.sparge_block_map(q, k, GQA_TOPK, None, GQA_THETA, 1.0, False, False, 2, 2)
+    assert r["lut"][0].tolist() == GQA_TOPK_LUT
+    assert r["count"][0].tolist() == [[1, 1], [2, 2], [1, 1], [2, 2]]
+    r = oracle.sparge_block_map(q, k, None, GQA_CDF, np.full(4, 0.5, np.float32), 1.0, False,
+                                False, 2, 2)
+    assert r["lut"][0].tolist() == GQA_CDF_LUT
+    # the closed-form probabilities behind the cdf rows
+    assert math.exp(2) / (math.exp(2) + 1) == pytest.approx(0.8808, abs=1e-4)
+    assert math.exp(3) / (math.exp(3) + 1) == pytest.approx(0.9526, abs=1e-4)
+
+
+def test_planted_gqa_and_per_head_mistakes_are_caught(monkeypatch):
+    """Three plausible slips in sparge_block_map, each caught by the hand
+    example: the KV head taken as h % hk instead of h // (hq / hk), head 0's
+    topk (or cdfthreshd) used for every head, head 0's simthreshd1 used for
+    every head."""
+    real_head = obm.block_map_head
+
+    def run(q, k, topk, cdf, theta):
+        return oracle.sparge_block_map(q, k, topk, cdf, theta, 1.0, False, False, 2, 2)["lut"][0]
+
+    q, k = _gqa_hand_inputs()
+    # KV head h % hk: rebuild the call with the permuted KV heads
+    hq, hk = 4, 2
+    k_mod = np.stack([k[0, h % hk] for h in range(hq)])[None]
+    q_one = q  # one KV head per query head: ratio 1 reads k_mod[h] for head h
+    got = run(q_one, k_mod, GQA_TOPK, None, GQA_THETA)
+    assert got.tolist() != GQA_TOPK_LUT
+    # head 0's selection parameter for every head
+    got = run(q, k, np.full(4, GQA_TOPK[0], np.float32), None, GQA_THETA)
+    assert got.tolist() != GQA_TOPK_LUT
+    got = run(q, k, None, np.full(4, GQA_CDF[0], np.float32), np.full(4, 0.5, np.float32))
+    assert got.tolist() != GQA_CDF_LUT
+    # head 0's threshold for every head, planted inside the per-head call
+    calls = []
+
+    def head_with_theta0(qh, kg, theta, *a, **kw):
+        calls.append(theta)
+        return real_head(qh, kg, float(GQA_THETA[0]), *a, **kw)
+
+    monkeypatch.setattr(obm, "block_map_head", head_with_theta0)
+    got = run(q, k, GQA_TOPK, None, GQA_THETA)
+    assert calls == [float(t) for t in GQA_THETA]  # the oracle passes each head its own
+    assert got.tolist() != GQA_TOPK_LUT
+
+
 def test_smooth_k_hand_example():
     """K smoothing subtracts the mean key row of the sequence (README 'Not yet
     ported': pre-pool k -= km).  blk = 2, d = 2, two kv blocks whose rows are
