@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(HERE, "libfbm.so")
 
 FBM_OK, FBM_ERR_INVALID_ARG, FBM_ERR_UNSUPPORTED, FBM_ERR_CUDA, FBM_ERR_DEVICE = range(5)
 FBM_F16, FBM_BF16, FBM_F32 = 0, 1, 2
-FBM_DEVERR_LUT_RANGE, FBM_DEVERR_TIMEOUT = 0x1, 0x2
+FBM_DEVERR_LUT_RANGE, FBM_DEVERR_TIMEOUT, FBM_DEVERR_LUT_ORDER = 0x1, 0x2, 0x4
 FBM_MAX_HEADS = 256
 FBM_STATIC_SCRATCH_BYTES = 24 << 20
 

@@ -322,7 +322,10 @@ __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_const
       elig[t] = valid && (!a.causal || j * a.blkk <= last_q);
       ksim_ok[t] = valid && ksim[j] > theta;
       const bool fin = elig[t] && ksim_ok[t];
-      sc[t] = valid ? srow[j] : 0.f;  // a plain load: this kernel rewrites the row
+      // a plain load (this kernel rewrites the row); adding +0 turns a -0
+      // score into +0, so the float compares of the threshold search and the
+      // integer keys order signed zeros alike
+      sc[t] = valid ? __fadd_rn(srow[j], 0.0f) : 0.f;
       key[t] = fin ? order_key(sc[t]) : 0u;
       if (fin) mloc = fmaxf(mloc, sc[t]);
       nfin += fin ? 1 : 0;

@@ -6,15 +6,18 @@
 // operation only its inputs and outputs has no workspace to give, and code
 // whose hot path must never enter the allocator (cudaMalloc can synchronise
 // the device and takes unbounded time) cannot make one either.  This entry
-// point serves them: it runs the same two kernels as sparge_block_map, with
+// point serves them: it runs the same kernels as sparge_block_map, with
 // the pooled means and self-similarities placed in g_block_map_scratch.
 //
 // The array is part of the library's device image, so every GPU that loads
 // the library holds its FBM_STATIC_SCRATCH_BYTES until the process exits.
 // Its device address is looked up once per device, by the first call made
-// with that device current; make that first call before any stream capture.
+// with that device current.  Under CUDA's lazy module loading (the default)
+// that lookup may itself load this file's module and so reserve the array's
+// memory: make one warm-up call per device at start-up, outside any stream
+// capture and outside the hot path.
 // All calls share the one array and nothing in it needs to start at zero (the
-// first kernel overwrites every byte the second reads), so calls that overlap
+// pooling kernel overwrites every byte the later kernels read), so calls that overlap
 // on the GPU, e.g. on two streams, race on it.
 #include <cstdio>
 #include <mutex>

@@ -105,8 +105,14 @@ __global__ void __launch_bounds__(128) k_fmha_mma(const FmhaLaunch L) {
 
   const int q_row0 = i * kBlk;
   const int q_rows = min(kBlk, L.s_q - q_row0);
-  auto block_of = [&](int t) -> int {
-    return lut_row ? __ldg(lut_row + lo + t) : lo + t;
+  // kv block of entry t of this chunk, or -1 for an unusable LUT entry
+  // (lut_entry: out of range, or not above the entry before it)
+  auto block_of = [&](int t, uint32_t *why) -> int {
+    if (!lut_row) {
+      *why = 0;
+      return lo + t;
+    }
+    return lut_entry(lut_row, lo + t, L.nk, why);
   };
 
   float o[D / 8][4];
@@ -118,8 +124,9 @@ __global__ void __launch_bounds__(128) k_fmha_mma(const FmhaLaunch L) {
   if (n > 0) {
     load_tile<D>(sQ, q, q_row0, q_rows, true);
     {
-      const int j0 = block_of(0);
-      const bool ok = j0 >= 0 && j0 < L.nk;
+      uint32_t why;
+      const int j0 = block_of(0, &why);
+      const bool ok = j0 >= 0;
       load_tile<D>(sK, k, j0 * kBlk, ok ? L.s_k - j0 * kBlk : 0, ok);
       load_tile<D>(sV, v, j0 * kBlk, ok ? L.s_k - j0 * kBlk : 0, ok);
     }
@@ -128,8 +135,9 @@ __global__ void __launch_bounds__(128) k_fmha_mma(const FmhaLaunch L) {
     for (int t = 0; t < n; ++t) {
       const int stage = t & 1;
       if (t + 1 < n) {
-        const int jn = block_of(t + 1);
-        const bool ok = jn >= 0 && jn < L.nk;
+        uint32_t why;
+        const int jn = block_of(t + 1, &why);
+        const bool ok = jn >= 0;
         load_tile<D>(sK + (stage ^ 1) * TILE, k, jn * kBlk, ok ? L.s_k - jn * kBlk : 0, ok);
         load_tile<D>(sV + (stage ^ 1) * TILE, v, jn * kBlk, ok ? L.s_k - jn * kBlk : 0, ok);
         cp_async_commit();
@@ -144,9 +152,10 @@ __global__ void __launch_bounds__(128) k_fmha_mma(const FmhaLaunch L) {
           ldsm_x4(sQ + swz<D>(warp * 16 + (lane & 15), ks * 2 + (lane >> 4)), qf[ks][0], qf[ks][1],
                   qf[ks][2], qf[ks][3]);
       }
-      const int j = block_of(t);
-      const bool jok = j >= 0 && j < L.nk;
-      if (!jok && threadIdx.x == 0) set_error(L.err, FBM_DEVERR_LUT_RANGE);
+      uint32_t why;
+      const int j = block_of(t, &why);
+      const bool jok = j >= 0;
+      if (!jok && threadIdx.x == 0) set_error(L.err, why);
       const uint32_t kt = sK + stage * TILE, vt = sV + stage * TILE;
       // S = Q K^T (16 rows x 64 keys per warp)
       float s[8][4];

@@ -52,6 +52,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <type_traits>
 
@@ -119,8 +120,9 @@ struct TcParams {
 
 // one (batch, head, q block, split): kv-list entries off .. off + n of the row
 struct Unit {
-  int bh_q, bh_k, i, split, off, n;
-  const int32_t *row;
+  int bh_q, bh_k, i, split, off, n, nk;
+  const int32_t *row;  // the LUT row's first entry (nullptr: dense)
+  bool bad_count;      // the row's count lay outside [0, min(nk, lut_stride)]
 };
 
 template <bool kPartial>
@@ -135,9 +137,13 @@ FBM_DEVICE Unit unit_of(const TcParams &P, int u) {
   const int b = U.bh_q / P.hq, h = U.bh_q - b * P.hq;
   U.bh_k = b * P.hk + h / (P.hq / P.hk);
   int n_list;
+  U.nk = P.nk;
+  U.bad_count = false;
   if (P.lut) {
     U.row = P.lut + (size_t)qu * P.lut_stride;
-    n_list = max(0, min(__ldg(P.cnt + qu), min(P.nk, P.lut_stride)));
+    const int raw = __ldg(P.cnt + qu), lim = min(P.nk, P.lut_stride);
+    U.bad_count = raw < 0 || raw > lim;
+    n_list = max(0, min(raw, lim));
   } else {
     U.row = nullptr;
     n_list = P.causal ? min(P.nk, U.i + 1) : P.nk;
@@ -147,7 +153,6 @@ FBM_DEVICE Unit unit_of(const TcParams &P, int u) {
     const int base = n_list / P.splits, extra = n_list - base * P.splits;
     U.off = U.split * base + min(U.split, extra);
     U.n = base + (U.split < extra ? 1 : 0);
-    if (U.row) U.row += U.off;
   } else {
     U.off = 0;
     U.n = n_list;
@@ -155,7 +160,19 @@ FBM_DEVICE Unit unit_of(const TcParams &P, int u) {
   return U;
 }
 
-FBM_DEVICE int entry_of(const Unit &U, int t) { return U.row ? __ldg(U.row + t) : U.off + t; }
+// kv block of entry t of the unit's chunk, or -1 for an unusable LUT entry
+// (out of range, or not above the entry before it: lut_entry)
+FBM_DEVICE int entry_of(const Unit &U, int t, uint32_t *why) {
+  if (!U.row) {
+    *why = 0;
+    return U.off + t;
+  }
+  return lut_entry(U.row, U.off + t, U.nk, why);
+}
+FBM_DEVICE int entry_of(const Unit &U, int t) {
+  uint32_t why;
+  return entry_of(U, t, &why);
+}
 
 template <bool kBf16, bool kPartial, bool kPvSkip, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__ TcParams P) {
@@ -211,11 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     for (int hf = 0; hf < 2; ++hf) {
       const int t = 2 * p + hf;
       if (t >= U.n) break;
-      int j = entry_of(U, t);
-      if (j < 0 || j >= P.nk) {
-        // out of range: flagged; block 0 is fetched in its place so that the
-        // masked keys (P = 0) meet finite V rows
-        set_error(P.err, FBM_DEVERR_LUT_RANGE);
+      uint32_t why;
+      int j = entry_of(U, t, &why);
+      if (j < 0) {
+        // unusable entry: flagged; block 0 is fetched in its place so that
+        // the masked keys (P = 0) meet finite V rows
+        set_error(P.err, why);
         j = 0;
       }
       js[hf] = j;
@@ -239,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       bool ok = true;
       for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
         const Unit U = unit_of<kPartial>(P, u);
+        if (U.bad_count && U.split == 0) set_error(P.err, FBM_DEVERR_LUT_RANGE);
         if (U.n == 0) continue;
         const int npairs = (U.n + 1) >> 1;
         const int qb = uc & 1;
@@ -407,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           const int tn = 2 * (p + 1) + half;
           j_next = (p + 1 < npairs && tn < U.n) ? entry_of(U, tn) : -1;
         }
-        const bool jvalid = j >= 0 && j < P.nk;
+        const bool jvalid = j >= 0;  // entry_of has range- and order-checked it
         const int kpos0 = (jvalid ? j : 0) * 64;
         // every key of this thread's block visible to its row
         const bool plain = jvalid && kpos0 + 64 <= P.s_k && (!P.causal || kpos0 + 63 <= qpos);
@@ -640,8 +659,10 @@ bool make_map8(CUtensorMap *m, const void *base, int bh, int s) {
   return r == CUDA_SUCCESS;
 }
 
+constexpr int kMaxDevices = 64;
+
 int sm_count() {
-  static int n[64] = {};
+  static int n[kMaxDevices] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return 148;
@@ -652,12 +673,16 @@ int sm_count() {
 template <bool BF16, bool PARTIAL, bool PVSKIP, bool FP8 = false>
 cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   static_assert(!(PARTIAL && PVSKIP), "the PV skip runs on whole rows only");
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_fmha_tc<BF16, PARTIAL, PVSKIP, FP8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  // the shared-memory attribute is per device: set it once on each
+  static std::atomic<bool> attr_done[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !attr_done[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(k_fmha_tc<BF16, PARTIAL, PVSKIP, FP8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    if (dev >= 0 && dev < kMaxDevices) attr_done[dev].store(true, std::memory_order_release);
   }
   TcParams P;
   memset(&P, 0, sizeof(P));

@@ -59,6 +59,7 @@ typedef enum { FBM_F16 = 0, FBM_BF16 = 1, FBM_F32 = 2 } fbm_dtype;
 /* Bits of the device error word. */
 #define FBM_DEVERR_LUT_RANGE 0x1u /* a LUT / index entry outside [0, n) or a count > n */
 #define FBM_DEVERR_TIMEOUT 0x2u   /* a bounded wait on an mbarrier expired */
+#define FBM_DEVERR_LUT_ORDER 0x4u /* a LUT entry not above the one before it (duplicate or descending) */
 
 /* Largest number of query heads a call may pass per-head parameters for. */
 #define FBM_MAX_HEADS 256
@@ -146,7 +147,10 @@ fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int 
  * FBM_STATIC_SCRATCH_BYTES that every GPU loading the library holds until the
  * process exits.  A shape whose scratch (fbm_block_map_workspace_bytes) is
  * larger returns FBM_ERR_UNSUPPORTED and launches nothing.  The first call on
- * a device looks the array's address up (make it before any stream capture).
+ * a device looks the array's address up; under CUDA's lazy module loading
+ * (the default) that lookup may be what loads the module and reserves the
+ * array's device memory.  Make one warm-up call per device at start-up,
+ * outside any stream capture and outside the hot path.
  * All calls share the array, so calls that overlap on the GPU race; nothing
  * in it needs to start at zero.  The library allocates nothing.
  */
@@ -171,8 +175,12 @@ fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int 
  * q: device [b, hq, s_q, d]; k: device [b, hk, s_k, d]; v: device [b, hk, s_k, dv];
  * dtype FBM_F16 / FBM_BF16; d = dv in {64, 128}; blkq = blkk = 64.
  * lut: device int32 [b, hq, nq, lut_stride] with nq = ceil(s_q / 64), entries in
- *   [0, ceil(s_k / 64)), ascending (an out-of-range entry is skipped and sets
- *   FBM_DEVERR_LUT_RANGE); lut_count: device int32 [b, hq, nq].
+ *   [0, ceil(s_k / 64)), strictly ascending; lut_count: device int32
+ *   [b, hq, nq], in [0, min(nk, lut_stride)].  Every entry is checked on the
+ *   device: one out of range is skipped and sets FBM_DEVERR_LUT_RANGE, one not
+ *   above the entry before it in its row (a duplicate or a descending entry)
+ *   is skipped and sets FBM_DEVERR_LUT_ORDER, and a count outside its range is
+ *   clamped into it and sets FBM_DEVERR_LUT_RANGE.
  *   lut == NULL (and lut_count == NULL) selects dense attention: every kv
  *   block (every causally visible one under causal).
  * pv_threshold: +inf turns the PV skip off.  A finite value >= 0 (natural log

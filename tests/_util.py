@@ -83,6 +83,15 @@ def compare_lut_rows(gpu_lut, gpu_cnt, ora_lut, ora_cnt, aux, mode: str, param: 
         chosen = sel[i] & finite[i]
         bnd = score[i][chosen].min()
         if np.all(np.abs(score[i][D] - bnd) < SCORE_GAP):
+            if mode == "topk":
+                # K_i fixes how many blocks are selected: a near-tie swaps
+                # entries but keeps the count, except when the sink column
+                # (forced on whether or not it is also selected) is one of the
+                # tied entries
+                oc = int(ora_cnt[i])
+                sink_tie = sink and finite[i][0] and abs(score[i][0] - bnd) < SCORE_GAP
+                assert gc == oc or (sink_tie and abs(gc - oc) == 1), \
+                    f"row {i}: topk count {gc} != oracle {oc}"
             near += 1
             continue
         if mode == "cdf":

@@ -189,6 +189,14 @@ def test_static_block_map_rejects_oversized_shapes_on_the_host(L):
     assert b"static array" in L.fbm_last_error_message()
 
 
+def test_static_block_map_holds_the_headline_shape(L):
+    # b2 h32 s16384 d128 (with its K-smoothing row) fits in the static array,
+    # as do the causal GQA shape b1 hq32 hk8 s32768 and a tiny one
+    for shape in ((2, 32, 32, 16384, 128), (1, 32, 8, 32768, 128), (1, 2, 2, 512, 64)):
+        need = L.fbm_block_map_workspace_bytes(*shape, 64, 64)
+        assert 0 < need <= fbm.FBM_STATIC_SCRATCH_BYTES, (shape, need)
+
+
 def test_selftest_checks_its_limit_on_the_host(L):
     assert L.fbm_selftest_wait_timeout(0, None) == fbm.FBM_ERR_INVALID_ARG
     assert L.fbm_selftest_wait_timeout(20_000_000_000, None) == fbm.FBM_ERR_INVALID_ARG

@@ -12,19 +12,24 @@ from _util import SIM_MARGIN, cached_prefill, compare_lut_rows, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_case(fbm, cfg, mode, param, heads=None, check_sim_margin=True, smooth_k=False):
+def run_case(fbm, cfg, mode, param, heads=None, check_sim_margin=True, smooth_k=False,
+             theta=None):
+    """param (topk or cdfthreshd) and theta (simthreshd1, default the
+    config's) are one value for every head or one value per query head."""
     x = cached_prefill(cfg)
     q, k = to_dev(x["q"], cfg.dtype), to_dev(x["k"], cfg.dtype)
-    kw = {"topk": param} if mode == "topk" else {"cdfthreshd": param}
-    lut, cnt, bmap = fbm.sparge_block_map(q, k, simthreshd1=cfg.simthreshd1, scale=cfg.scale,
+    ph = (synth.per_head(cfg, param) if np.isscalar(param)
+          else np.asarray(param, dtype=np.float32))
+    th = (synth.per_head(cfg, cfg.simthreshd1 if theta is None else theta)
+          if theta is None or np.isscalar(theta) else np.asarray(theta, dtype=np.float32))
+    kw = {"topk": ph.tolist()} if mode == "topk" else {"cdfthreshd": ph.tolist()}
+    lut, cnt, bmap = fbm.sparge_block_map(q, k, simthreshd1=th.tolist(), scale=cfg.scale,
                                           causal=cfg.causal, attention_sink=cfg.attention_sink,
                                           return_block_map=True, smooth_k=smooth_k, **kw)
     assert fbm.get_error() == 0
     lut, cnt, bmap = lut.cpu().numpy(), cnt.cpu().numpy(), bmap.cpu().numpy()
-    ph = synth.per_head(cfg, param)
     ora = oracle.sparge_block_map(x["q"], x["k"], ph if mode == "topk" else None,
-                                  ph if mode == "cdf" else None,
-                                  synth.per_head(cfg, cfg.simthreshd1), cfg.scale, cfg.causal,
+                                  ph if mode == "cdf" else None, th, cfg.scale, cfg.causal,
                                   cfg.attention_sink, keep_aux=True, dtype=cfg.dtype, heads=heads,
                                   smooth_k=smooth_k)
     todo = heads or [(b, h) for b in range(cfg.b) for h in range(cfg.hq)]
@@ -33,9 +38,9 @@ def run_case(fbm, cfg, mode, param, heads=None, check_sim_margin=True, smooth_k=
         aux = ora["aux"][(b, h)]
         if check_sim_margin:
             for v in (aux["simq"], aux["simk"]):
-                assert np.all(np.abs(v - cfg.simthreshd1) > SIM_MARGIN), "sim too close to theta"
+                assert np.all(np.abs(v - th[h]) > SIM_MARGIN), "sim too close to theta"
         e, n = compare_lut_rows(lut[b, h], cnt[b, h], ora["lut"][b, h], ora["count"][b, h], aux,
-                                mode, param, cfg.causal, cfg.attention_sink)
+                                mode, float(ph[h]), cfg.causal, cfg.attention_sink)
         exact += e
         near += n
         for i in range(lut.shape[2]):
@@ -103,6 +108,33 @@ def test_c3_sampled_heads(fbm_gpu, topk):
 def test_c4_causal_gqa_sink(fbm_gpu):
     lut, cnt, _, _ = run_case(fbm_gpu, synth.C4, "topk", 0.2)
     assert (lut[..., 0] == 0).all()
+
+
+# Per-head hyperparameters ("Sparge Attention (Composable Kernel)" README,
+# 'Status vs Upstream') on the causal GQA shape of config C4 (32 query heads on
+# 8 KV heads, sink), shortened to s = 4096: every head has its own topk or
+# cdfthreshd and one of three thresholds (0.001: nothing forced; 0.5: splits
+# the diffuse and the compact blocks; 0.99: every block dissimilar, dense
+# rows), and every group of four query heads reads a different KV head, so a
+# wrong per-head index or KV-head mapping changes the LUT.
+C4_SHORT = synth.C4.replace(s=4096)
+THETAS = np.array([0.001, 0.5, 0.99, 0.5] * 8, dtype=np.float32)
+
+
+def test_per_head_topk_and_theta_gqa(fbm_gpu):
+    topk = np.linspace(0.05, 0.95, C4_SHORT.hq).astype(np.float32)[::-1].copy()
+    lut, cnt, _, _ = run_case(fbm_gpu, C4_SHORT, "topk", topk, theta=THETAS)
+    assert (lut[..., 0] == 0).all()
+    dense = [h for h in range(C4_SHORT.hq) if THETAS[h] > 0.9]
+    nq = C4_SHORT.nq
+    for h in dense:  # every block dissimilar: every causally eligible column
+        assert (cnt[0, h] == np.arange(1, nq + 1)).all()
+
+
+def test_per_head_cdf_and_theta_gqa(fbm_gpu):
+    cdf = np.linspace(0.5, 0.99, C4_SHORT.hq).astype(np.float32)
+    run_case(fbm_gpu, C4_SHORT.replace(topk=None, cdfthreshd=0.9), "cdf", cdf,
+             theta=np.roll(THETAS, 1))
 
 
 def test_block_map_is_deterministic(fbm_gpu):

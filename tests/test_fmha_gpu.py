@@ -9,19 +9,23 @@ import torch
 
 import oracle
 import synth
-from _util import (assert_close_lse, assert_close_o, cached_prefill, prefill_on_gpu, to_dev)
+from _util import (assert_close_lse, assert_close_o, cached_prefill, compare_lut_rows,
+                   prefill_on_gpu, to_dev)
 
 pytestmark = pytest.mark.gpu
 
 
-def oracle_lut(cfg, mode="topk", param=None):
+def oracle_lut(cfg, mode="topk", param=None, heads=None, keep_aux=False):
     x = cached_prefill(cfg)
     param = cfg.topk if param is None else param
     ph = synth.per_head(cfg, param)
     r = oracle.sparge_block_map(x["q"], x["k"], ph if mode == "topk" else None,
                                 ph if mode == "cdf" else None,
                                 synth.per_head(cfg, cfg.simthreshd1), cfg.scale, cfg.causal,
-                                cfg.attention_sink, dtype=cfg.dtype)
+                                cfg.attention_sink, dtype=cfg.dtype, heads=heads,
+                                keep_aux=keep_aux)
+    if keep_aux:
+        return r["lut"], r["count"], r["aux"]
     return r["lut"], r["count"]
 
 
@@ -151,12 +155,45 @@ def test_c2_cdf_attention(fbm_gpu):
     check(fbm_gpu, synth.C2, lut, cnt)
 
 
-@pytest.mark.parametrize("topk", [0.1, 0.4])
+@pytest.mark.parametrize("topk", synth.C3_TOPKS)
 def test_c3_sampled(fbm_gpu, topk):
+    # every point of the headline topk sweep: 8 sampled q blocks (the first
+    # and last always) of every 8th head, at full size
     cfg = synth.C3
-    lut, cnt = oracle_lut(cfg, "topk", topk)
+    heads = [(b, h) for b in range(cfg.b) for h in range(0, cfg.hq, 8)]
+    lut, cnt = oracle_lut(cfg, "topk", topk, heads=heads)
     units = [u for u in synth.sample_qblocks(cfg, 8) if u[1] % 8 == 0]
     check(fbm_gpu, cfg, lut, cnt, units=units)
+
+
+def test_headline_step_gpu_lut_into_gpu_fmha(fbm_gpu):
+    """The step the bench times, chained on the GPU: sparge_block_map's LUT
+    fed straight to sparse_fmha_fwd at b2 h32 s16384 d128 fp16, topk 0.4.
+    The GPU LUT of sampled heads must equal the oracle's up to counted
+    near-ties; the oracle's attention then runs on the GPU's LUT (so a
+    near-tie row is checked against the blocks the GPU actually chose)."""
+    cfg = synth.C3
+    x, (q, k, v) = prefill_on_gpu(cfg)
+    lut, cnt, _ = fbm_gpu.sparge_block_map(q, k, topk=0.4, simthreshd1=cfg.simthreshd1,
+                                           scale=cfg.scale)
+    out, lse = fbm_gpu.sparse_fmha_fwd(q, k, v, lut, cnt, scale=cfg.scale, return_lse=True)
+    assert fbm_gpu.get_error() == 0
+    g_lut, g_cnt = lut.cpu().numpy(), cnt.cpu().numpy()
+    heads = [(0, 0), (0, 13), (1, 22), (1, 31)]
+    o_lut, o_cnt, aux = oracle_lut(cfg, "topk", 0.4, heads=heads, keep_aux=True)
+    near = 0
+    for b, h in heads:
+        near += compare_lut_rows(g_lut[b, h], g_cnt[b, h], o_lut[b, h], o_cnt[b, h], aux[(b, h)],
+                                 "topk", 0.4, False, False)[1]
+    units = [u for u in synth.sample_qblocks(cfg, 8) if (u[0], u[1]) in heads]
+    res = oracle.sparse_fmha(x["q"], x["k"], x["v"], g_lut, g_cnt, cfg.scale, False, units=units,
+                             dtype=cfg.dtype)
+    o_np, l_np = out.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64)
+    for (b, h, i), (o_ref, lse_ref) in res.items():
+        rows = slice(i * 64, i * 64 + o_ref.shape[0])
+        assert_close_o(o_np[b, h, rows], o_ref, f"O{(b, h, i)}")
+        assert_close_lse(l_np[b, h, rows], lse_ref, f"LSE{(b, h, i)}")
+    print(f"headline step: {len(res)} q blocks checked, {near} near-tie LUT rows")
 
 
 def test_c4_sampled_with_lse(fbm_gpu):
@@ -199,6 +236,59 @@ def test_out_of_range_entry_is_skipped_and_flagged(fbm_gpu):
     o_np = out.double().cpu().numpy()
     for (b, h, i), (o_ref, _) in res.items():
         assert_close_o(o_np[b, h, i * 64:(i + 1) * 64], o_ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_lut_validation_skips_and_flags(fbm_gpu, d):
+    """Every entry is checked on the device: a duplicate or a descending entry
+    is skipped with FBM_DEVERR_LUT_ORDER, a count above min(nk, stride) is
+    clamped with FBM_DEVERR_LUT_RANGE, a negative count gives an empty row.
+    The result equals the oracle over the usable entries."""
+    cfg = synth.C1.replace(b=1, hq=4, hk=2, s=512, d=d, dtype="f16")
+    nq = cfg.nq
+    x, (q, k, v) = prefill_on_gpu(cfg)
+
+    def run(lut, cnt):
+        out, lse = fbm_gpu.sparse_fmha_fwd(q, k, v, torch.from_numpy(lut).cuda(),
+                                           torch.from_numpy(cnt).cuda(), scale=cfg.scale,
+                                           return_lse=True)
+        return fbm_gpu.get_error(), out.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64)
+
+    def expect(o_np, l_np, good, good_cnt):
+        res = oracle.sparse_fmha(x["q"], x["k"], x["v"], good, good_cnt, cfg.scale, False,
+                                 dtype="f16")
+        for (b, h, i), (o_ref, l_ref) in res.items():
+            assert_close_o(o_np[b, h, i * 64:(i + 1) * 64], o_ref)
+            assert_close_lse(l_np[b, h, i * 64:(i + 1) * 64], l_ref)
+
+    base = np.full((1, 4, nq, nq), -1, dtype=np.int32)
+    # duplicates and descending entries
+    lut, cnt = base.copy(), np.zeros((1, 4, nq), dtype=np.int32)
+    good, gcnt = base.copy(), np.zeros_like(cnt)
+    rows = {0: ([1, 1, 3], [1, 3]), 1: ([5, 2], [5]), 2: ([0, 4, 4, 4, 6], [0, 4, 6]),
+            3: ([2, 7, 3, 1], [2, 7])}
+    for h, (row, ok) in rows.items():
+        for i in range(nq):
+            lut[0, h, i, :len(row)] = row
+            cnt[0, h, i] = len(row)
+            good[0, h, i, :len(ok)] = ok
+            gcnt[0, h, i] = len(ok)
+    bits, o_np, l_np = run(lut, cnt)
+    assert bits == fbm_gpu.FBM_DEVERR_LUT_ORDER
+    expect(o_np, l_np, good, gcnt)
+    # counts out of range: above nk (clamped to nk) and negative (empty row)
+    lut = np.tile(np.arange(nq, dtype=np.int32), (1, 4, nq, 1))
+    cnt = np.full((1, 4, nq), nq, dtype=np.int32)
+    cnt[0, 1] = nq + 5
+    cnt[0, 2] = -3
+    bits, o_np, l_np = run(lut, cnt)
+    assert bits == fbm_gpu.FBM_DEVERR_LUT_RANGE
+    gcnt = cnt.copy()
+    gcnt[0, 1] = nq
+    gcnt[0, 2] = 0
+    expect(o_np, l_np, lut, gcnt)
+    assert (o_np[0, 2] == 0).all() and np.isneginf(l_np[0, 2]).all()
+    assert fbm_gpu.get_error() == 0
 
 
 def test_d128_runs_on_the_tcgen05_kernel(fbm_gpu):
