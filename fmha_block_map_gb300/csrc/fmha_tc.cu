@@ -26,19 +26,23 @@
 //
 // TMEM (512 columns): S slots at columns 0 and 128 (fp32), P buffers at 256 and
 // 320 (two 16-bit values per column), O at 384.  An M = 64 accumulator keeps
-// row i in lane (i mod 16) + 32 (i / 16): softmax warp w (subpartition w) owns
-// rows 16w .. 16w + 15, and with the 16x32bx2 load shape thread t holds row
-// 16w + (t mod 16), keys 64 (t / 16) .. + 63 of the pair, i.e. one kv block.
-// The running max of a row is kept lazily (O and l are rescaled only when a
-// score exceeds it by more than 2^8); both threads of a row agree on it through
-// one shuffle.
+// row i in lane (i mod 16) + 32 (i / 16), so subpartition sw holds rows
+// 16 sw .. 16 sw + 15.  Two softmax warps share a subpartition, one per kv
+// block of the pair: with the 16x32bx2 shape thread t of the warp for block b
+// holds row 16 sw + (t mod 16) and 32 keys (64 b + 32 (t / 16) ..) of it, and
+// the same 32 columns of O.  The running max of a row is kept lazily (O and l
+// are rescaled only when a score exceeds it by more than 2^8): the two halves
+// of a block agree through one shuffle, the two warps through one OR-barrier
+// per pair (and a shared-memory exchange of their block maxima when either
+// has to move the max).
 //
-// Roles (one persistent CTA per SM, 8 warps):
+// Roles (one persistent CTA per SM, 12 warps):
 //   warp 0   TMA producer of Q (double buffer) and K pairs (3-slot ring)
 //   warp 1   TMA producer of V pairs (2-slot ring)
 //   warp 2   TMEM owner and S issuer
 //   warp 3   PV issuer
-//   warps 4-7 softmax and epilogue (TMEM subpartitions 0-3)
+//   warps 4-11 softmax and epilogue (warps 4-7: the first kv block of a pair on
+//            subpartitions 0-3; warps 8-11: the second)
 // Pipeline: S(g) is issued once K(g) has landed and its TMEM slot is free (the
 // softmax releases a slot as soon as it holds the scores in registers), so the
 // S MMA of pair g + 1 runs during the softmax of pair g; PV(g) once P(g) is in
@@ -85,9 +89,12 @@ enum {
   B_PV = B_PF + kPBufs, B_OF = B_PV + kPBufs, B_DRAIN = B_OF + 1, B_DRAIN2 = B_DRAIN + 1,
   NBAR = B_DRAIN2 + 1
 };
-// [0] tmem base, [1] abort flag, bytes 8 .. 15: PV-skip votes [P buffer][softmax warp]
+// [0] tmem base, [1] abort flag, bytes 8 .. 15: PV-skip votes [P buffer][subpartition]
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16;
+// softmax exchange: block maxima [pair parity][kv block][64 rows] and row sums
+// [kv block][64 rows], fp32
+constexpr int OFF_XCH = OFF_MISC + 16;
+constexpr int SMEM_BYTES = OFF_XCH + (2 * 2 * 64 + 2 * 64) * 4;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
@@ -99,10 +106,11 @@ constexpr uint32_t kDescHi = sdesc_hi_sw128(1024);  // every operand: 1024-byte 
 constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
 
 constexpr int kWarpQK = 0, kWarpV = 1, kWarpS = 2, kWarpPV = 3, kWarpSm = 4;
-constexpr int kSoftmaxWarps = 4;
+constexpr int kSoftmaxWarps = 8;  // two per TMEM subpartition: one per kv block of a pair
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kThreads = 32 * (kWarpSm + kSoftmaxWarps);
 constexpr int kSoftmaxBar = 1;  // named barrier of the softmax warps
+constexpr int kPairBar0 = 2;    // named barriers 2 .. 5: the two warps of one subpartition
 
 struct TcParams {
   CUtensorMap tq, tk, tv, to;
@@ -382,13 +390,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    // Eight warps: warp w reads TMEM subpartition sw = w % 4 (query rows
+    // 16 sw .. 16 sw + 15) and handles kv block `blk` of every pair (keys
+    // 64 blk .. 64 blk + 63); the two warps of a subpartition hold the same
+    // rows.  Thread t: row 16 sw + (t mod 16), keys 64 blk + 32 (t / 16) + 0..31,
+    // O columns 64 blk + 32 (t / 16) + 0..31 of that row.
     using E = typename std::conditional<kBf16, BF16, F16>::type;
-    const int sw = warp - kWarpSm;            // == warp % 4: TMEM subpartition
-    const int half = lane >> 4;               // block of the pair / d half of O
-    const int row = sw * 16 + (lane & 15);    // query row within the q block
+    const int sw = warp & 3;                  // TMEM subpartition
+    const int blk = (warp - kWarpSm) >> 2;    // kv block of the pair
+    const int half = lane >> 4;               // 32-key / 32-column half
+    const int r16 = lane & 15;
+    const int row = sw * 16 + r16;            // query row within the q block
     const int tid = threadIdx.x - kWarpSm * 32;
+    const int pair_bar = kPairBar0 + sw;      // named barrier of the two warps of these rows
     const uint32_t tl = tbase + ((uint32_t)(sw * 32) << 16);
     const uint64_t sl2x2 = f2_pack(P.sl2, P.sl2);
+    // block maxima exchanged between the two warps of a row group, double
+    // buffered by pair parity: [parity][blk][row]; row sums at the epilogue
+    volatile float *xmax = reinterpret_cast<volatile float *>(smem + OFF_XCH);
+    volatile float *xsum = xmax + 2 * 2 * 64;
     // Every softmax thread runs the same loop trip counts and barriers whatever
     // happens: a failed (timed-out) wait only clears `ok`, and later waits
     // return at once.
@@ -418,22 +438,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       float m = -INFINITY;                 // running max of the row (log2 domain)
       float mt = -INFINITY;                // exact running max (PV-skip variant)
       uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};  // this thread's share of the row sum
-      int j_next = half < U.n ? entry_of(U, half) : -1;
+      int j_next = blk < U.n ? entry_of(U, blk) : -1;
       for (int p = 0; p < npairs; ++p) {
         const int g = pc + p, ss = g % kSSlots, pb = g % kPBufs;
         const int j = j_next;
         {
-          const int tn = 2 * (p + 1) + half;
+          const int tn = 2 * (p + 1) + blk;
           j_next = (p + 1 < npairs && tn < U.n) ? entry_of(U, tn) : -1;
         }
         const bool jvalid = j >= 0;  // entry_of has range- and order-checked it
-        const int kpos0 = (jvalid ? j : 0) * 64;
-        // every key of this thread's block visible to its row
-        const bool plain = jvalid && kpos0 + 64 <= P.s_k && (!P.causal || kpos0 + 63 <= qpos);
+        const int kpos0 = (jvalid ? j : 0) * 64 + half * 32;
+        // every key of this thread's 32 visible to its row
+        const bool plain = jvalid && kpos0 + 32 <= P.s_k && (!P.causal || kpos0 + 31 <= qpos);
         ok = ok && mbar_wait(bar(B_SF + ss), (g / kSSlots) & 1, abort_flag, kWaitNs);
         tc_fence_after();
-        uint32_t sv[64];
-        tmem_ld_rowhalf64(tl + kTS + ss * 128, sv);
+        uint32_t sv[32];
+        tmem_ld_rowhalf32(tl + kTS + ss * 128 + blk * 64, sv);
         tmem_wait_ld();
         // the S slot is free for S(g + kSSlots) as soon as it is in registers
         tc_fence_before();
@@ -441,54 +461,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         if (lane == 0) mbar_arrive(bar(B_SE + ss));
         if (!plain) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
+          for (int c = 0; c < 32; ++c) {
             const int kpos = kpos0 + c;
             const bool vis = jvalid && kpos < P.s_k && (!P.causal || kpos <= qpos);
             if (!vis) sv[c] = __float_as_uint(-INFINITY);
           }
         }
-        // row max over the pair (this thread's 64 keys, then the other half)
+        // row max over this warp's block (this thread's 32 keys, then the other half)
         float mx;
         {
-          float t[8];
+          float t[4];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
+          for (int i = 0; i < 4; ++i) {
             const float *v = reinterpret_cast<const float *>(sv) + 8 * i;
             t[i] = fmaxf(fmax3(fmax3(v[0], v[1], v[2]), v[3], v[4]), fmax3(v[5], v[6], v[7]));
           }
-          mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+          mx = fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
         }
-        // fp8: the two block scales fold into this thread's factor (its 64 keys
-        // are one kv block); the pair max is then taken over scaled scores
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        // fp8: the two block scales fold into this warp's factor (its keys are
+        // one kv block); the max is then taken over scaled scores
         float fsc = P.sl2;
-        if constexpr (kFp8) {
-          fsc = qsl2 * (jvalid ? __ldg(P.kscale + (size_t)U.bh_k * P.nk + j) : 1.f);
-          mx *= fsc;
-        }
+        if constexpr (kFp8) fsc = qsl2 * (jvalid ? __ldg(P.kscale + (size_t)U.bh_k * P.nk + j) : 1.f);
+        const float mxs = mx * fsc;        // this block's row max, log2 domain
+        // agree with the partner warp: publish this block's max, then one
+        // OR-barrier tells both warps whether either needs to move the max
+        volatile float *xm = xmax + (g & 1) * 128;
+        if (half == 0) xm[blk * 64 + row] = mxs;
+        const bool need_me = mxs > m + 8.0f;
+        const bool any_need = named_or(pair_bar, 64, need_me);
         uint32_t vote = 0;
         if constexpr (kPvSkip) {
-          const float mx_other = __shfl_xor_sync(0xffffffffu, mx, 16);
           // block A (entry 2p) then block B (entry 2p + 1) against the exact
           // running max of the blocks visited before each; rows past the end
           // of the sequence do not veto
-          const float a = (half == 0 ? mx : mx_other) * P.sl2;
-          const float b = (half == 0 ? mx_other : mx) * P.sl2;
+          const float other = xm[(blk ^ 1) * 64 + row];
+          const float a = blk == 0 ? mxs : other;
+          const float b = blk == 0 ? other : mxs;
           const bool real = qpos < P.s_q;
           const bool sa = !real || a < mt - P.tau2;
           mt = fmaxf(mt, a);
           const bool sb = !real || b < mt - P.tau2;
           mt = fmaxf(mt, b);
           vote = (__all_sync(0xffffffffu, sa) ? 1u : 0u) | (__all_sync(0xffffffffu, sb) ? 2u : 0u);
-          mx = fmaxf(mx, mx_other);
-        } else {
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         }
-        const float mxs = kFp8 ? mx : mx * P.sl2;
-        const bool need = mxs > m + 8.0f;
-        if (__any_sync(0xffffffffu, need)) {
-          // rare: some score of the warp's rows exceeds its running max by more
-          // than 2^8 (always on the first pair): move the max, rescale l and O
-          const float mn = need ? mxs : m;
+        if (any_need) {
+          // rare: some score of these rows exceeds the running max by more
+          // than 2^8 (always on the first pair): move the max to the pair's
+          // row max, rescale l and this warp's half of O
+          const float mrow = fmaxf(mxs, xm[(blk ^ 1) * 64 + row]);
+          const float mn = mrow > m + 8.0f ? mrow : m;
           const float alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - mn);
           m = mn;
           const uint64_t a2 = f2_pack(alpha, alpha);
@@ -499,27 +521,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             const int gp = g - 1;
             ok = ok && mbar_wait(bar(B_PV + gp % kPBufs), (gp / kPBufs) & 1, abort_flag, kWaitNs);
             tc_fence_after();
-            uint32_t o[64];
-            tmem_ld_rowhalf64(tl + kTO, o);
+            uint32_t o[32];
+            tmem_ld_rowhalf32(tl + kTO + blk * 64, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
+            for (int c = 0; c < 32; c += 2) {
               const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[c]), __uint_as_float(o[c + 1])), a2);
               const float2 w2 = f2_unpack(v);
               o[c] = __float_as_uint(w2.x);
               o[c + 1] = __float_as_uint(w2.y);
             }
-            tmem_st_rowhalf64(tl + kTO, o);
+            tmem_st_rowhalf32(tl + kTO + blk * 64, o);
             tmem_wait_st();
           }
         }
-        // P = exp2(s * scale * log2 e - m), packed to 16-bit pairs
+        // P = exp2(s * factor - m), packed to 16-bit pairs
         const float mu = (m == -INFINITY) ? 0.f : m;
         const uint64_t negm = f2_pack(-mu, -mu);
         const uint64_t fx2 = kFp8 ? f2_pack(fsc, fsc) : sl2x2;
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 16; ++i) {
           const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
                                     fx2, negm);
           const float2 xv = f2_unpack(x);
@@ -534,11 +556,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           ok = ok && mbar_wait(bar(B_PV + pb), (gp / kPBufs) & 1, abort_flag, kWaitNs);
         }
         tc_fence_after();
-        tmem_st_rowhalf32(tl + kTP + pb * 64, pk);
+        tmem_st_rowhalf16(tl + kTP + pb * 64 + blk * 32, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (kPvSkip && lane == 0)  // read by the PV issuer once B_PF(pb) completes
+        if (kPvSkip && blk == 0 && lane == 0)  // read by the PV issuer once B_PF(pb) completes
           *reinterpret_cast<volatile uint8_t *>(smem + OFF_MISC + 8 + pb * 4 + sw) = (uint8_t)vote;
         if (lane == 0) mbar_arrive(bar(B_PF + pb));
       }
@@ -547,8 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         const int gl = pc + npairs - 1;
         ok = ok && mbar_wait(bar(B_PV + gl % kPBufs), (gl / kPBufs) & 1, abort_flag, kWaitNs);
         tc_fence_after();
-        uint32_t o[64];
-        tmem_ld_rowhalf64(tl + kTO, o);
+        uint32_t o[32];
+        tmem_ld_rowhalf32(tl + kTO + blk * 64, o);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -558,34 +580,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           const float2 a = f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])));
           lt = a.x + a.y;
         }
-        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 16);   // this warp's keys of the row
+        if (half == 0) xsum[blk * 64 + row] = lt;
+        named_sync(pair_bar, 64);
+        lt += xsum[(blk ^ 1) * 64 + row];              // plus the partner warp's keys
         const float inv = lt > 0.f ? 1.0f / lt : 0.f;
         const size_t orow0 = (kPartial ? (size_t)U.split * P.plane : 0) + (size_t)U.bh_q * P.s_q + q0;
-        if (P.lse && half == 0 && row < rows)
+        if (P.lse && blk == 0 && half == 0 && row < rows)
           P.lse[orow0 + row] = lt > 0.f ? m * 0.6931471805599453f + logf(lt) : -INFINITY;
         if constexpr (kPartial) {
-          // fp32 partial: this thread's 64 values of row `row`, d half `half`
+          // fp32 partial: this thread's 32 values of row `row`
           if (row < rows) {
-            float4 *dst = reinterpret_cast<float4 *>(P.opart + (orow0 + row) * kD + half * 64);
+            float4 *dst = reinterpret_cast<float4 *>(P.opart + (orow0 + row) * kD + blk * 64 + half * 32);
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
+            for (int c = 0; c < 8; ++c)
               dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv, __uint_as_float(o[4 * c + 1]) * inv,
                                    __uint_as_float(o[4 * c + 2]) * inv,
                                    __uint_as_float(o[4 * c + 3]) * inv);
           }
+          // the row sums of this unit have been read before the next unit's
+          // epilogue writes them again (its pairs pass the pair barrier first)
           pc += npairs;
           continue;
         }
-        // staging: d half `half` of row `row`, eight 16-byte chunks, 128-byte swizzle
-        uint8_t *srow = smem + OFF_STAGE + half * kQChunk + row * 128;
+        // staging: d chunk `blk` of row `row`, 16-byte pieces 4 half .. 4 half + 3,
+        // 128-byte swizzle
+        uint8_t *srow = smem + OFF_STAGE + blk * kQChunk + row * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
           uint32_t w[4];
 #pragma unroll
           for (int z = 0; z < 4; ++z)
             w[z] = E::from_f2(__uint_as_float(o[8 * c + 2 * z]) * inv,
                               __uint_as_float(o[8 * c + 2 * z + 1]) * inv);
-          *reinterpret_cast<uint4 *>(srow + ((c ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          const int piece = 4 * half + c;
+          *reinterpret_cast<uint4 *>(srow + ((piece ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async();
         named_sync(kSoftmaxBar, kSoftmaxThreads);

@@ -85,6 +85,7 @@ from .attention import (  # noqa: F401
     attention_unit_pv_skip,
     shard_lut_row,
     context_parallel_unit,
+    speculative_two_pass_unit,
     decode_rows,
     decode_attention,
     decode_partials,

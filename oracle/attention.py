@@ -56,18 +56,23 @@ def _softmax_attend(scores: np.ndarray, vals: np.ndarray):
 
 
 def attention_unit(q: np.ndarray, k: np.ndarray, v: np.ndarray, lut_row: Iterable[int],
-                   i: int, blkq: int, blkk: int, scale: float, causal: bool):
+                   i: int, blkq: int, blkk: int, scale: float, causal: bool,
+                   key_offset: int = 0):
     """Attention of the rows of q block ``i`` over the keys of the listed kv
     blocks.  q [s_q, d], k [s_k, d], v [s_k, dv] are one head's float64
-    values.  Under ``causal`` (s_q == s_k) a key at position u is visible to
-    the query at position t only when u <= t.  Returns (O [rows, dv], LSE
-    [rows])."""
+    values.  Under ``causal`` the key at index u is visible to the query at
+    index t only when u <= t + key_offset: key_offset = 0 when queries and keys
+    start at the same position, s_k - s_q when the queries are the last s_q
+    positions of the keys' sequence (the causal alignment of a speculative
+    dense pass over caller-gathered keys, "Incremental_FlashAttention
+    updating_log.md" Stage 5), -lo when a rank's keys start at position lo
+    (causal context parallelism).  Returns (O [rows, dv], LSE [rows])."""
     s_q, s_k = q.shape[0], k.shape[0]
     t = np.arange(i * blkq, min((i + 1) * blkq, s_q))
     keys = row_keys(lut_row, blkk, s_k)
     scores = scale * (q[t] @ k[keys].T)
     if causal:
-        scores = np.where(keys[None, :] <= t[:, None], scores, -np.inf)
+        scores = np.where(keys[None, :] <= t[:, None] + key_offset, scores, -np.inf)
     return _softmax_attend(scores, v[keys])
 
 
@@ -79,11 +84,13 @@ def _head(x: np.ndarray, bi: int, h: int, dtype: Optional[str]) -> np.ndarray:
 
 def sparse_fmha(q: np.ndarray, k: np.ndarray, v: np.ndarray, lut: np.ndarray,
                 count: np.ndarray, scale: float, causal: bool, units: Optional[list] = None,
-                blkq: int = 64, blkk: int = 64, dtype: Optional[str] = None) -> dict:
+                blkq: int = 64, blkk: int = 64, dtype: Optional[str] = None,
+                key_offset: int = 0) -> dict:
     """Block-sparse attention of q [b, hq, s_q, d] over k, v [b, hk, s_k, *]
     with LUT [b, hq, nq, nk] / count [b, hq, nq] (values, or bit patterns when
-    ``dtype`` is given).  Query head h reads KV head h // (hq // hk).
-    ``units`` lists (b, h, i) q blocks to compute (default: all).  Returns
+    ``dtype`` is given).  Query head h reads KV head h // (hq // hk).  The
+    causal mask takes ``key_offset`` as attention_unit does.  ``units`` lists
+    (b, h, i) q blocks to compute (default: all).  Returns
     {(b, h, i): (O, LSE)}."""
     b, hq, s_q, _ = q.shape
     hk = k.shape[1]
@@ -101,7 +108,8 @@ def sparse_fmha(q: np.ndarray, k: np.ndarray, v: np.ndarray, lut: np.ndarray,
                           _head(v, bi, h // ratio, dtype))
         qh, kg, vg = cache[key]
         row = lut[bi, h, i, :count[bi, h, i]]
-        res[(bi, h, i)] = attention_unit(qh, kg, vg, row, i, blkq, blkk, scale, causal)
+        res[(bi, h, i)] = attention_unit(qh, kg, vg, row, i, blkq, blkk, scale, causal,
+                                         key_offset)
     return res
 
 
@@ -220,21 +228,51 @@ def shard_lut_row(lut_row: Iterable[int], lo: int, hi: int) -> list:
 
 
 def context_parallel_unit(qh: np.ndarray, kg: np.ndarray, vg: np.ndarray, lut_row, i: int,
-                          world: int, blkq: int, blkk: int, scale: float):
-    """Partials of one q block under context parallelism over ``world`` ranks
-    (non-causal): rank r holds the kv blocks of split_bounds(nk, world)[r] (K/V
-    rows [lo * blkk, min(hi * blkk, s_k))) and attends over its shard of the
-    LUT row.  Returns (O_parts [world, rows, dv], LSE_parts [world, rows]);
-    ``combine`` of them is the attention of the whole row."""
+                          world: int, blkq: int, blkk: int, scale: float, causal: bool = False):
+    """Partials of one q block under context parallelism over ``world`` ranks:
+    rank r holds the kv blocks of split_bounds(nk, world)[r] (K/V rows
+    [lo * blkk, min(hi * blkk, s_k))) and attends over its shard of the LUT
+    row; under ``causal`` (queries and the full key sequence start at the same
+    position) its local key index u is position lo * blkk + u, so the key
+    offset of its mask is -lo * blkk.  Returns (O_parts [world, rows, dv],
+    LSE_parts [world, rows]); ``combine`` of them is the attention of the
+    whole row."""
     nk = (kg.shape[0] + blkk - 1) // blkk
     outs, lses = [], []
     for lo, hi in split_bounds(nk, world):
         r0, r1 = lo * blkk, min(hi * blkk, kg.shape[0])
         o, l = attention_unit(qh, kg[r0:r1], vg[r0:r1], shard_lut_row(lut_row, lo, hi), i,
-                              blkq, blkk, scale, False)
+                              blkq, blkk, scale, causal, key_offset=-lo * blkk)
         outs.append(o)
         lses.append(l)
     return np.stack(outs), np.stack(lses)
+
+
+# ----------------------------------------------------------------------------
+# Speculative two-pass attention
+# ----------------------------------------------------------------------------
+
+def speculative_two_pass_unit(qh: np.ndarray, k_spec: np.ndarray, v_spec: np.ndarray,
+                              kg: np.ndarray, vg: np.ndarray, missed_row, i: int, blkq: int,
+                              blkk: int, scale: float, causal_spec: bool = True):
+    """The two-pass recipe of "Incremental_FlashAttention updating_log.md",
+    Stage 5, for the rows of q block ``i``:
+      pass 1 - dense attention over the caller-gathered speculative keys
+               k_spec / v_spec [s_spec, *], causal with the queries aligned to
+               the last s_q of them (key offset s_spec - s_q), so the block
+               holding each query's own position is masked as usual;
+      pass 2 - sparse attention over the missed kv blocks of the full K/V
+               (``missed_row``: fully historical blocks, every key before the
+               q block's first query, so no mask);
+      combine - the Stage 1 merge of the two (O, LSE) partials.
+    Returns (O [rows, dv], LSE [rows]) and the two partials."""
+    s_q, s_spec = qh.shape[0], k_spec.shape[0]
+    nspec = (s_spec + blkk - 1) // blkk
+    o1, l1 = attention_unit(qh, k_spec, v_spec, range(nspec), i, blkq, blkk, scale, causal_spec,
+                            key_offset=s_spec - s_q)
+    o2, l2 = attention_unit(qh, kg, vg, missed_row, i, blkq, blkk, scale, False)
+    o, l = combine(np.stack([o1, o2]), np.stack([l1, l2]))
+    return o, l, (o1, l1), (o2, l2)
 
 
 # ----------------------------------------------------------------------------

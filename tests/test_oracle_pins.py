@@ -830,6 +830,122 @@ def test_planted_cp_mistake_is_caught(monkeypatch):
 # ----------------------------------------------------------------------------
 
 
+# ----------------------------------------------------------------------------
+# causal key offset, speculative two-pass, causal context parallelism
+# ----------------------------------------------------------------------------
+
+
+def _masked_sdpa(q, k, v, scale, visible):
+    """torch scaled_dot_product_attention (fp64) with an explicit boolean mask."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))[None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(
+        t(q), t(k), t(v), attn_mask=torch.from_numpy(visible)[None, None], scale=scale)
+    return o[0, 0].numpy()
+
+
+@pytest.mark.parametrize("s_q,s_k,off", [(192, 192, 0), (100, 260, 160), (128, 320, -70),
+                                          (150, 150, 35)])
+def test_causal_key_offset_matches_masked_sdpa(s_q, s_k, off):
+    """Key u visible to query t iff u <= t + key_offset, checked against sdpa
+    with that mask written out; rows without a visible key give (0, -inf)."""
+    rng = np.random.default_rng(s_q + s_k)
+    d = 16
+    q, k, v = (rng.standard_normal((n, d)) for n in (s_q, s_k, s_k))
+    nk = (s_k + 63) // 64
+    vis = np.arange(s_k)[None, :] <= np.arange(s_q)[:, None] + off
+    ref = _masked_sdpa(q, k, v, 0.25, vis)
+    for i in range((s_q + 63) // 64):
+        o, l = oatt.attention_unit(q, k, v, range(nk), i, 64, 64, 0.25, True, key_offset=off)
+        rows = np.arange(i * 64, min((i + 1) * 64, s_q))
+        live = vis[rows].any(axis=1)
+        if live.any():
+            assert np.abs(o[live] - ref[rows][live]).max() < 1e-12
+        assert (o[~live] == 0).all() and np.isneginf(l[~live]).all()
+        assert np.isfinite(l[live]).all()
+
+
+def test_causal_key_offset_hand_example():
+    """One dimension, scale 1: queries q = (1, 1), keys k = (0, 1, 2), values
+    v = (10, 20, 30), key offset 1.  Query 0 sees keys 0 and 1: weights
+    (1, e) / (1 + e), O = (10 + 20 e) / (1 + e), LSE = ln(1 + e).  Query 1
+    sees all three: O = (10 + 20 e + 30 e^2) / (1 + e + e^2)."""
+    q = np.array([[1.0], [1.0]])
+    k = np.array([[0.0], [1.0], [2.0]])
+    v = np.array([[10.0], [20.0], [30.0]])
+    o, l = oatt.attention_unit(q, k, v, [0], 0, 64, 64, 1.0, True, key_offset=1)
+    e = math.e
+    assert o[0, 0] == pytest.approx((10 + 20 * e) / (1 + e), abs=1e-12)
+    assert l[0] == pytest.approx(math.log(1 + e), abs=1e-12)
+    assert o[1, 0] == pytest.approx((10 + 20 * e + 30 * e * e) / (1 + e + e * e), abs=1e-12)
+    # offset 0: query 0 sees key 0 alone
+    o, l = oatt.attention_unit(q, k, v, [0], 0, 64, 64, 1.0, True, key_offset=0)
+    assert o[0, 0] == 10.0 and l[0] == 0.0
+
+
+def _spec_case(seed=3, n_blocks=6, s_q=64, window=2, d=16):
+    rng = np.random.default_rng(seed)
+    s = n_blocks * 64
+    q = rng.standard_normal((s_q, d))   # the last s_q positions of the sequence
+    k, v = rng.standard_normal((s, d)), rng.standard_normal((s, d))
+    w0 = (n_blocks - window) * 64        # the speculative window: keys w0 .. s-1
+    return q, k, v, w0, s
+
+
+def test_speculative_two_pass_equals_causal_attention():
+    """Stage 5 of the Incremental_FlashAttention updating_log: a dense causal
+    pass over the speculative window (the last blocks, holding the queries'
+    own positions) plus a sparse pass over every missed historical block,
+    combined, is causal attention over the whole sequence (sdpa with the
+    causal mask of queries placed at the end)."""
+    q, k, v, w0, s = _spec_case()
+    missed = list(range(w0 // 64))
+    o, l, _, _ = oatt.speculative_two_pass_unit(q, k[w0:], v[w0:], k, v, missed, 0, 64, 64, 0.25)
+    vis = np.arange(s)[None, :] <= np.arange(q.shape[0])[:, None] + (s - q.shape[0])
+    assert np.abs(o - _masked_sdpa(q, k, v, 0.25, vis)).max() < 1e-12
+    # a sparse miss set: attention over the window plus the listed blocks only
+    some = [0, 2]
+    o, l, _, _ = oatt.speculative_two_pass_unit(q, k[w0:], v[w0:], k, v, some, 0, 64, 64, 0.25)
+    keep = np.zeros(s, dtype=bool)
+    keep[w0:] = True
+    for j in some:
+        keep[j * 64:(j + 1) * 64] = True
+    assert np.abs(o - _masked_sdpa(q, k, v, 0.25, vis & keep[None, :])).max() < 1e-12
+    # no missed block: pass 2 is the empty partial, the result is pass 1 alone
+    o, l, p1, p2 = oatt.speculative_two_pass_unit(q, k[w0:], v[w0:], k, v, [], 0, 64, 64, 0.25)
+    assert np.isneginf(p2[1]).all() and np.abs(o - p1[0]).max() == 0.0
+
+
+@pytest.mark.parametrize("world", [2, 3, 5])
+def test_causal_context_parallel_combines_to_causal_attention(world):
+    """Causal context parallelism: rank r's keys start at position lo * 64, so
+    its mask is key index u <= t - lo * 64; the ranks' partials combine to the
+    causal attention of the whole LUT row (a causal LUT: blocks <= i, the
+    diagonal included)."""
+    rng = np.random.default_rng(world)
+    s, d = 5 * 64 + 17, 16
+    qh, kg, vg = (rng.standard_normal((s, d)) for _ in range(3))
+    for i in range(6):
+        row = sorted(set(rng.choice(i + 1, size=max(1, (i + 1) // 2), replace=False).tolist())
+                     | {i})
+        parts = oatt.context_parallel_unit(qh, kg, vg, row, i, world, 64, 64, 0.25, causal=True)
+        o, l = oatt.combine(*parts)
+        o_ref, l_ref = oatt.attention_unit(qh, kg, vg, row, i, 64, 64, 0.25, True)
+        assert np.abs(o - o_ref).max() < 1e-12 and np.abs(l - l_ref).max() < 1e-12
+
+
+def test_planted_key_offset_mistake_is_caught(monkeypatch):
+    """A rank mask that adds lo * 64 instead of subtracting it (a flipped
+    sign) breaks the causal context-parallel pin."""
+    real = oatt.attention_unit
+
+    def flipped(q, k, v, row, i, blkq, blkk, scale, causal, key_offset=0):
+        return real(q, k, v, row, i, blkq, blkk, scale, causal, -key_offset)
+
+    monkeypatch.setattr(oatt, "attention_unit", flipped)
+    with pytest.raises(AssertionError):
+        test_causal_context_parallel_combines_to_causal_attention(3)
+
+
 def test_decode_rows_hand_example():
     rows = oatt.decode_rows(np.array([[3, 1]]), np.array([[0, 5, 7]]), 4)
     assert rows.tolist() == [[12, 5, 7]]
