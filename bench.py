@@ -305,9 +305,7 @@ def run_ours(args):
         cp_res = {"ranks": 2, "emulated": "both ranks on one GPU, one after the other",
                   "ms": round(cp_ms, 4), "combine_ms": round(comb_ms, 4),
                   "eff_tflops": round(flops / (cp_ms * 1e-3) / 1e12, 1),
-                  "partial_kernel": ("tcgen05" if fbm.fmha_kernel_kind(q.dtype, cfg.d, cfg.d, 1,
-                                                                   cfg.s, cfg.s) == 1
-                                     else "mma.sync") + " (fp32 partial output)"}
+                  "partial_kernel": "tcgen05 (fp32 partial output)"}
         del shards, o_all, l_all
 
     # ---- per-Q-tile PV skip: the same step's attention with pv_threshold set
@@ -439,8 +437,7 @@ def run_ours(args):
                       "frac_hbm": round(bm_bytes / (bm_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
                       "share_of_step": round(bm_ms / step_ms, 3),
                       "smooth_k_ms": round(smooth_ms, 4)},
-        "roofline": {"kernel": "sparse_fmha_fwd (" + ("tcgen05" if kind == 1 else "mma.sync") +
-                     ")", "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+        "roofline": {"kernel": "sparse_fmha_fwd (k_fmha_tc, tcgen05)", "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} bf16 burst (fp16 tensor rate = bf16)",
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_sustained": peak_sus,
@@ -461,6 +458,7 @@ def run_ours(args):
         res["decode"] = measure_decode(peaks["hbm_gbs"])
     if rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(cfg, x, args.topk)
+        res["cpu_baselines"] = cpu_baselines()
     if world > 1:
         import torch.distributed as dist
 
@@ -611,6 +609,77 @@ def cpu_baseline(cfg, x, topk, qblocks=None, heads=10):
             "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"block map of {heads} (batch, head), attention of {len(todo)} q blocks "
                       f"({tiles} selected tiles) at topk={topk}; {t_bm + t_at:.1f} s of CPU work"}
+
+
+def _oracle_config_time(name, heads=None, qblocks=None):
+    """Seconds the oracle takes on config `name` (C1, C2, C4: block map then
+    attention; a (batch, head) / q-block sample when given) and the selected
+    tiles it covered; C5: the decode of every query over its listed tokens."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    if name == "C5":
+        cfg = synth.C5
+        inp = synth.decode(cfg)
+        t0 = time.perf_counter()
+        rows = oracle.decode_rows(inp["page_table"], inp["idx"], cfg.page)
+        qf = synth.bits_to_f64(inp["q"], "bf16")
+        for c in range(cfg.n_queries):
+            kv = synth.bits_to_f64(synth.cache_rows(cfg, rows[c]), "bf16")
+            oracle.decode_attention(qf[c], kv, cfg.dv, cfg.sm_scale)
+        return time.perf_counter() - t0, cfg.n_queries * cfg.topk
+    cfg = synth.PREFILL_CONFIGS[name]
+    x = synth.prefill(cfg)
+    mode = "topk" if cfg.topk is not None else "cdf"
+    ph = synth.per_head(cfg, cfg.topk if mode == "topk" else cfg.cdfthreshd)
+    todo = heads or [(b, h) for b in range(cfg.b) for h in range(cfg.hq)]
+    t0 = time.perf_counter()
+    r = oracle.sparge_block_map(x["q"], x["k"], ph if mode == "topk" else None,
+                                ph if mode == "cdf" else None,
+                                synth.per_head(cfg, cfg.simthreshd1), cfg.scale, cfg.causal,
+                                cfg.attention_sink, dtype=cfg.dtype, heads=todo)
+    rng = np.random.default_rng(0)
+    units = [(b, h, int(i)) for b, h in todo
+             for i in (range(cfg.nq) if qblocks is None
+                       else rng.choice(cfg.nq, qblocks, replace=False))]
+    oracle.sparse_fmha(x["q"], x["k"], x["v"], r["lut"], r["count"], cfg.scale, cfg.causal,
+                       units=units, dtype=cfg.dtype)
+    tiles = sum(int(r["count"][b, h, i]) for b, h, i in units)
+    return time.perf_counter() - t0, tiles
+
+
+def cpu_baselines():
+    """The oracle's own costs beside the headline sample: full C1, C2 and C5
+    runs on all host cores, C4 on a sample (2 heads, 16 q blocks each) with
+    its full-config time extrapolated by selected tiles, and the headline
+    sample again on one core (a child process with one BLAS / OpenMP
+    thread)."""
+    out = {"cores": os.cpu_count()}
+    for name in ("C1", "C2", "C5"):
+        t, units = _oracle_config_time(name)
+        out[name] = {"seconds": round(t, 2), "full": True,
+                     ("listed_tokens" if name == "C5" else "selected_tiles"): units}
+    import synth
+
+    t, tiles = _oracle_config_time("C4", heads=[(0, 0), (0, 17)], qblocks=16)
+    full_tiles = 858381  # selected tiles of C4 (b1 hq32 s32768, topk 0.2 + sink), from the GPU map
+    out["C4"] = {"seconds": round(t, 2), "sample": "2 heads x 16 q blocks",
+                 "sample_tiles": tiles,
+                 "full_config_seconds_extrapolated": round(t * full_tiles / max(tiles, 1), 1)}
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, bench, synth; cfg = synth.C3; x = synth.prefill(cfg.replace(b=1, hq=2, hk=2)); "
+            "print(json.dumps(bench.cpu_baseline(cfg, x, 0.4, qblocks=64, heads=2)))")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                           text=True, timeout=600)
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+        one["cores"] = 1
+        out["C3_one_core"] = one
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        out["C3_one_core"] = {"error": str(e)[:200]}
+    return out
 
 
 def run_reference(args):

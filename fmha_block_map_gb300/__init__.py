@@ -53,9 +53,10 @@ def lib() -> ctypes.CDLL:
         L.sparge_block_map_static.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp,
                                                vp, f32, i32, i32, i32, vp, vp, vp, vp])
         L.sparse_fmha_fwd.argtypes = ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
-                                       vp, vp, i32, i32, f32, i32, f32, vp, vp, vp, vp, vp])
+                                       vp, vp, i32, i32, f32, i32, i32, f32, vp, vp, vp, vp, vp])
         L.attn_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
         L.lut_shard.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp]
+        L.lut_validate.argtypes = [vp, vp, i64, i32, i32, vp]
         L.quantize_e4m3_blocks.argtypes = [vp, i32, i64, i32, i32, vp, vp, vp]
         L.sparse_fmha_fwd_fp8.argtypes = ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                            i32, vp, vp, i32, f32, i32, vp, vp, vp])
@@ -66,7 +67,8 @@ def lib() -> ctypes.CDLL:
         L.fbm_fmha_kernel_kind.argtypes = [i32] * 6
         L.fbm_fmha_kernel_kind.restype = i32
         for name in ("fbm_get_error", "sparge_block_map", "sparge_block_map_static",
-                     "sparse_fmha_fwd", "attn_combine", "lut_shard", "sparse_decode_fwd",
+                     "sparse_fmha_fwd", "attn_combine", "lut_shard", "lut_validate",
+                     "sparse_decode_fwd",
                      "quantize_e4m3_blocks", "sparse_fmha_fwd_fp8"):
             getattr(L, name).restype = i32
         _lib = L
@@ -202,7 +204,7 @@ def sparge_block_map_static(q: torch.Tensor, k: torch.Tensor, *, topk=None, cdft
 
 def sparse_fmha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                     lut: Optional[torch.Tensor], lut_count: Optional[torch.Tensor], *,
-                    scale: Optional[float] = None, causal: bool = False,
+                    scale: Optional[float] = None, causal: bool = False, key_offset: int = 0,
                     return_lse: bool = False, num_splits: int = 1,
                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                     o_partial: Optional[torch.Tensor] = None,
@@ -212,7 +214,9 @@ def sparse_fmha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     returns (out, lse or None); num_splits > 1, or ``partial`` (one whole-row
     partial, e.g. one slot of a context-parallel stack), returns the fp32
     partials (o_partial [S, b, hq, s_q, dv], lse_partial [S, b, hq, s_q]).
-    pv_threshold (None: off) enables the per-Q-tile PV skip on whole rows."""
+    pv_threshold (None: off) enables the per-Q-tile PV skip on whole rows.
+    Under causal, key index u is visible to query row t when
+    u <= t + key_offset (0: queries and keys start at the same position)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _cuda(t, n)
     b, hq, s_q, d = q.shape
@@ -239,7 +243,7 @@ def sparse_fmha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
             lse_partial = torch.empty((num_splits, b, hq, s_q), dtype=torch.float32, device=dev)
     _check(lib().sparse_fmha_fwd(
         _ptr(q), _ptr(k), _ptr(v), _dt(q), b, hq, hk, s_q, s_k, d, dv, 64, 64,
-        _ptr(lut), _ptr(lut_count), stride, num_splits, float(scale), int(causal),
+        _ptr(lut), _ptr(lut_count), stride, num_splits, float(scale), int(causal), int(key_offset),
         math.inf if pv_threshold is None else float(pv_threshold),
         None if partial else _ptr(out), None if partial else _ptr(lse),
         _ptr(o_partial) if partial else None, _ptr(lse_partial) if partial else None,
@@ -343,6 +347,21 @@ def lut_shard(lut: torch.Tensor, lut_count: torch.Tensor, lo: int, hi: int, *,
     return out_lut, out_count
 
 
+def lut_validate(lut: torch.Tensor, lut_count: torch.Tensor, nk: int, *, stream=None) -> int:
+    """Check lut [..., stride] / lut_count [...] (int32) against the contract of
+    sparse_fmha_fwd: counts in [0, min(nk, stride)], entries in [0, nk),
+    strictly ascending.  Returns the device error bits found
+    (FBM_DEVERR_LUT_RANGE | FBM_DEVERR_LUT_ORDER; 0: valid); synchronises."""
+    _cuda(lut, "lut"), _cuda(lut_count, "lut_count")
+    if lut.dtype != torch.int32 or lut_count.dtype != torch.int32:
+        raise TypeError("lut / lut_count must be int32")
+    if tuple(lut_count.shape) != tuple(lut.shape[:-1]):
+        raise ValueError("lut_count must have the shape of lut without its last dimension")
+    _check(lib().lut_validate(_ptr(lut), _ptr(lut_count), lut_count.numel(), lut.shape[-1], nk,
+                              _stream(stream)))
+    return get_error(stream)
+
+
 def sparse_decode_fwd(q: torch.Tensor, kv_cache: torch.Tensor, page_table: torch.Tensor,
                       indices: torch.Tensor, *, dv: int, scale: float, num_splits: int = 1,
                       o_partial: Optional[torch.Tensor] = None,
@@ -375,6 +394,6 @@ def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
 
 def fmha_kernel_kind(dtype: torch.dtype, d: int, dv: int, num_splits: int, s_q: int,
                      s_k: int) -> int:
-    """1 = tcgen05 kernel, 2 = mma.sync kernel, 0 = rejected."""
+    """1 = the tcgen05 kernel, 0 = rejected."""
     code = {torch.float16: FBM_F16, torch.bfloat16: FBM_BF16}[dtype]
     return int(lib().fbm_fmha_kernel_kind(code, d, dv, num_splits, s_q, s_k))

@@ -172,23 +172,24 @@ fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int 
   L.ksim = reinterpret_cast<float *>(ws + w.ksim);
   L.kmu = reinterpret_cast<float *>(ws + w.kmu);
   L.lut = lut; L.cnt = lut_count; L.bmap = block_map;
+  L.err = error_word();
+  if (!L.err) return fail(FBM_ERR_CUDA, "sparge_block_map: error word lookup failed");
   return cuda_status(fbm::launch_block_map(L, static_cast<cudaStream_t>(stream)),
                      "sparge_block_map launch");
 }
 
 int fbm_fmha_kernel_kind(int dtype, int d, int dv, int num_splits, int s_q, int s_k) {
   if (dtype != FBM_F16 && dtype != FBM_BF16) return 0;
-  if (d != dv || (d != 64 && d != 128) || num_splits < 1) return 0;
-  if (fbm::fmha_tc_supported(d, dv, num_splits, s_q, s_k)) return 1;
-  return 2;
+  if (d != dv || (d != 64 && d != 128) || num_splits < 1 || num_splits > 64) return 0;
+  return fbm::fmha_tc_supported(d, dv, num_splits, s_q, s_k) ? 1 : 0;
 }
 
 fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtype, int b,
                            int hq, int hk, int s_q, int s_k, int d, int dv, int blkq, int blkk,
                            const int32_t *lut, const int32_t *lut_count, int lut_stride,
-                           int num_splits, float scale, int causal, float pv_threshold,
-                           void *out, float *lse, float *o_partial, float *lse_partial,
-                           void *stream) {
+                           int num_splits, float scale, int causal, int key_offset,
+                           float pv_threshold, void *out, float *lse, float *o_partial,
+                           float *lse_partial, void *stream) {
   if (!q || !k || !v) return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: null q / k / v");
   if ((lut == nullptr) != (lut_count == nullptr))
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: lut and lut_count must both be set or both NULL");
@@ -201,11 +202,11 @@ fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtyp
     return fail(FBM_ERR_UNSUPPORTED, "sparse_fmha_fwd: blkq = blkk = 64 only");
   if (d != dv || (d != 64 && d != 128))
     return fail(FBM_ERR_UNSUPPORTED, "sparse_fmha_fwd: d = dv in {64, 128}");
-  if (causal && s_q != s_k)
-    return fail(FBM_ERR_UNSUPPORTED, "sparse_fmha_fwd: causal needs s_q == s_k");
   const int nq = (s_q + 63) / 64, nk = (s_k + 63) / 64;
   if (lut && lut_stride < 1)
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: lut_stride must be >= 1");
+  if (causal && (key_offset < -(1 << 30) || key_offset > (1 << 30)))
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: |key_offset| must be at most 2^30");
   if (num_splits < 1 || num_splits > 64)
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: num_splits in [1, 64]");
   const bool partial = num_splits > 1 || out == nullptr;
@@ -217,9 +218,9 @@ fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtyp
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: scale must be positive and finite");
   if (!(pv_threshold >= 0.f))
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: pv_threshold must be >= 0 (+inf: off)");
-  if (pv_threshold < INFINITY && (partial || !fbm::fmha_tc_supported(d, dv, num_splits, s_q, s_k)))
+  if (pv_threshold < INFINITY && partial)
     return fail(FBM_ERR_UNSUPPORTED,
-                "sparse_fmha_fwd: pv_threshold needs whole rows (num_splits = 1, out given) and d = 128");
+                "sparse_fmha_fwd: pv_threshold needs whole rows (num_splits = 1, out given)");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (out && !aligned16(out)) ||
       (o_partial && !aligned16(o_partial)))
     return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd: tensors must be 16-byte aligned");
@@ -231,6 +232,7 @@ fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtyp
   L.b = b; L.hq = hq; L.hk = hk; L.s_q = s_q; L.s_k = s_k; L.d = d; L.nq = nq; L.nk = nk;
   L.lut = lut; L.cnt = lut_count; L.lut_stride = lut ? lut_stride : nk;
   L.num_splits = num_splits; L.causal = causal != 0; L.scale = scale;
+  L.key_offset = causal ? key_offset : 0;
   L.pv_threshold = pv_threshold;
   L.out = partial ? nullptr : out;
   L.lse = partial ? nullptr : lse;
@@ -238,10 +240,8 @@ fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtyp
   L.lse_part = partial ? lse_partial : nullptr;
   L.err = error_word();
   if (!L.err) return fail(FBM_ERR_CUDA, "sparse_fmha_fwd: error word lookup failed");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (fbm::fmha_tc_supported(d, dv, num_splits, s_q, s_k))
-    return cuda_status(fbm::launch_fmha_tc(L, st), "sparse_fmha_fwd launch (tcgen05)");
-  return cuda_status(fbm::launch_fmha_mma(L, st), "sparse_fmha_fwd launch (mma.sync)");
+  return cuda_status(fbm::launch_fmha_tc(L, static_cast<cudaStream_t>(stream)),
+                     "sparse_fmha_fwd launch");
 }
 
 fbm_status attn_combine(const float *o_part, const float *lse_part, int num_splits,
@@ -339,6 +339,18 @@ fbm_status lut_shard(const int32_t *lut, const int32_t *lut_count, int64_t rows,
   if (!L.err) return fail(FBM_ERR_CUDA, "lut_shard: error word lookup failed");
   return cuda_status(fbm::launch_lut_shard(L, static_cast<cudaStream_t>(stream)),
                      "lut_shard launch");
+}
+
+fbm_status lut_validate(const int32_t *lut, const int32_t *lut_count, int64_t rows,
+                        int lut_stride, int nk, void *stream) {
+  if (!lut || !lut_count) return fail(FBM_ERR_INVALID_ARG, "lut_validate: null pointer");
+  if (rows <= 0 || lut_stride < 1 || nk < 1)
+    return fail(FBM_ERR_INVALID_ARG, "lut_validate: rows, lut_stride and nk must be positive");
+  if (rows > (int64_t)0x7fffffff * 8) return fail(FBM_ERR_UNSUPPORTED, "lut_validate: too many rows");
+  fbm::LutValidateLaunch L{lut, lut_count, rows, lut_stride, nk, error_word()};
+  if (!L.err) return fail(FBM_ERR_CUDA, "lut_validate: error word lookup failed");
+  return cuda_status(fbm::launch_lut_validate(L, static_cast<cudaStream_t>(stream)),
+                     "lut_validate launch");
 }
 
 fbm_status sparse_decode_fwd(const void *q, const void *kv_cache, int dtype, int n_q, int hq,

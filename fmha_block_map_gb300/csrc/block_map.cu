@@ -198,6 +198,142 @@ FBM_DEVICE uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The kcount-th largest key of a warp's row (NT keys per lane; key 0 = not
+// selectable; 1 <= kcount <= number of selectable keys), by radix selection:
+//  1. a coarse digit: each selectable score s maps to bin
+//     min(255, floor((s - lo) * 256 / (hi - lo))) over the row's range
+//     [lo, hi], a monotone map, so every key of a higher bin is larger than
+//     every key of a lower one;
+//  2. a 256-bin histogram of the digits (shared-memory counters of the warp)
+//     and a warp scan from the top bin down find the bin holding the
+//     kcount-th largest key and how many keys lie above it;
+//  3. that bin's keys are ranked exactly: when the bin is taken whole the
+//     answer is its smallest key; else, with at most 32 keys in the bin, each
+//     lane ranks one of them against the others; else (many scores within one
+//     bin) a bitwise search over the 32 key bits among the bin's keys.
+// Any monotone digit gives the exact result; this one spreads the pooled
+// scores of a row evenly over the bins, where the leading bits of the
+// order-preserving key (sign and exponent) would crowd them into a few.
+template <int NT>
+FBM_DEVICE uint32_t fin_mask(const uint32_t (&key)[NT]) {
+  uint32_t msk = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) msk |= (key[t] != 0u ? 1u : 0u) << t;
+  return msk;
+}
+
+template <int NT>
+FBM_DEVICE uint32_t bitwise_kth(const uint32_t (&key)[NT], uint32_t cand, int kcount) {
+  // largest T with #(candidate key >= T) >= kcount
+  uint32_t T = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t c = T | (1u << bit);
+    int cnt = 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) cnt += ((cand >> t) & 1u) && key[t] >= c ? 1 : 0;
+    const int tot = __reduce_add_sync(0xffffffffu, cnt);
+    if (tot >= kcount) T = c;
+    if (tot == kcount) break;  // exactly kcount keys >= T: no tie left to resolve
+  }
+  // T may sit below the smallest qualifying key: move it up to that key
+  uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+    if (((cand >> t) & 1u) && key[t] >= T) mn = min(mn, key[t]);
+  return __reduce_min_sync(0xffffffffu, mn);
+}
+
+template <int NT>
+FBM_DEVICE uint32_t kth_largest_key(const uint32_t (&key)[NT], const float (&sc)[NT],
+                                    uint32_t fin, int kcount, float hi, int *hist, int lane) {
+  float lo_l = INFINITY;
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+    if ((fin >> t) & 1u) lo_l = fminf(lo_l, sc[t]);
+  float lo = lo_l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+  const float range = hi - lo;
+  const float inv = 256.0f / range;
+  if (!(range > 0.f) || !(inv < INFINITY) || !(inv > 0.f))
+    return bitwise_kth<NT>(key, fin, kcount);  // one value, or a range fp32 cannot split
+  int dig[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) dig[t] = min(255, (int)((sc[t] - lo) * inv));
+  // histogram: this warp's 256 counters
+  reinterpret_cast<int4 *>(hist)[2 * lane] = make_int4(0, 0, 0, 0);
+  reinterpret_cast<int4 *>(hist)[2 * lane + 1] = make_int4(0, 0, 0, 0);
+  __syncwarp();
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+    if ((fin >> t) & 1u) atomicAdd(hist + dig[t], 1);
+  __syncwarp();
+  // lane L owns bins 255 - 8 L down to 248 - 8 L
+  int c[8];
+  {
+    const int4 x = reinterpret_cast<const int4 *>(hist)[62 - 2 * lane];  // bins 248-8L .. 251-8L
+    const int4 y = reinterpret_cast<const int4 *>(hist)[63 - 2 * lane];  // bins 252-8L .. 255-8L
+    c[0] = y.w; c[1] = y.z; c[2] = y.y; c[3] = y.x;
+    c[4] = x.w; c[5] = x.z; c[6] = x.y; c[7] = x.x;
+  }
+  int ssum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ssum += c[i];
+  int incl = ssum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int up = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += up;
+  }
+  int run = incl - ssum, found = -1, above = 0, binc = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (found < 0 && run + c[i] >= kcount) {
+      found = 255 - 8 * lane - i;
+      above = run;
+      binc = c[i];
+    }
+    run += c[i];
+  }
+  // the first crossing from the top (lanes after it cross at once)
+  const unsigned bal = __ballot_sync(0xffffffffu, found >= 0);
+  const int src = __ffs(bal) - 1;
+  const int dsel = __shfl_sync(0xffffffffu, found, src);
+  const int need = kcount - __shfl_sync(0xffffffffu, above, src);
+  const int nbin = __shfl_sync(0xffffffffu, binc, src);
+  uint32_t cand = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) cand |= (((fin >> t) & 1u) && dig[t] == dsel ? 1u : 0u) << t;
+  if (need == nbin) {
+    // the bin is taken whole: its smallest key
+    uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+      if ((cand >> t) & 1u) mn = min(mn, key[t]);
+    return __reduce_min_sync(0xffffffffu, mn);
+  }
+  if (nbin > 32) return bitwise_kth<NT>(key, cand, need);
+  // compact the bin's keys, one per lane, in the warp's counters (done with)
+  __syncwarp();
+  uint32_t *slot = reinterpret_cast<uint32_t *>(hist);
+  const unsigned lt = (1u << lane) - 1u;
+  int base = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const bool cnd = (cand >> t) & 1u;
+    const unsigned b = __ballot_sync(0xffffffffu, cnd);
+    if (cnd) slot[base + __popc(b & lt)] = key[t];
+    base += __popc(b);
+  }
+  __syncwarp();
+  const uint32_t mine = lane < nbin ? slot[lane] : 0u;
+  int gt = 0;
+  for (int i = 0; i < nbin; ++i) gt += slot[i] > mine ? 1 : 0;
+  // the need-th largest: the smallest key with fewer than `need` keys above it
+  const uint32_t v = (lane < nbin && gt < need) ? mine : 0xFFFFFFFFu;
+  return __reduce_min_sync(0xffffffffu, v);
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) k_pooled_scores(SelectArgs a) {
   extern __shared__ __align__(16) float smem[];
@@ -294,7 +430,9 @@ __global__ void __launch_bounds__(256) k_pooled_scores(SelectArgs a) {
 // one warp per q block (row): 8 warps per CTA
 template <int NT>
 __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
+  __shared__ __align__(16) int hist_all[8][256];  // radix-select counters, one set per warp
   const int lane = threadIdx.x & 31;
+  int *hist = hist_all[threadIdx.x >> 5];
   const int rowid = blockIdx.x * 8 + (threadIdx.x >> 5);  // (batch, head, q block)
   if (rowid >= a.b * a.hq * a.nq) return;
   const int i = rowid % a.nq;
@@ -339,27 +477,7 @@ __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_const
       if (!a.mode_cdf) {
         const float prod = __fmul_rn(hp.sel[h], (float)n_elig);
         const int kcount = min((int)ceilf(prod), nfin);
-        // largest T with #(key >= T) >= kcount: the kcount-th largest key
-        uint32_t T = 0;
-        // The counts are taken as fp32 work (the ALU pipe is this kernel's
-        // busiest): key >= cand  <=>  score >= float(cand), order_key being
-        // order-preserving on finite scores; excluded entries count as -inf.
-        // A candidate never lies in the key range of NaN or -inf: the
-        // candidate with bit 23 alone is -FLT_MAX's key, which every finite
-        // score reaches, so it is accepted before any lower bit is tried.
-        float fs[NT];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) fs[t] = key[t] ? sc[t] : -INFINITY;
-        for (int bit = 31; bit >= 0; --bit) {
-          const uint32_t cand = T | (1u << bit);
-          const float cf = __uint_as_float((cand & 0x80000000u) ? (cand & 0x7FFFFFFFu) : ~cand);
-          float cnt = 0.f;
-#pragma unroll
-          for (int t = 0; t < NT; ++t) cnt += fs[t] >= cf ? 1.f : 0.f;
-          const int tot = __reduce_add_sync(0xffffffffu, (int)cnt);
-          if (tot >= kcount) T = cand;
-          if (tot == kcount) break;  // exactly kcount keys >= T: no tie left to resolve
-        }
+        const uint32_t T = kth_largest_key<NT>(key, sc, fin_mask(key), kcount, m, hist, lane);
         int cgt = 0;
 #pragma unroll
         for (int t = 0; t < NT; ++t) cgt += key[t] > T ? 1 : 0;
@@ -516,7 +634,12 @@ cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
   a.blkq = kBlk; a.blkk = kBlk;
   a.scale = L.scale; a.causal = L.causal; a.sink = L.sink; a.mode_cdf = L.mode_cdf;
   a.lut = L.lut; a.cnt = L.cnt; a.bmap = L.bmap;
+  a.err = L.err;
+#ifdef FBM_SCORES_SIMT
   e = L.d == 128 ? launch_scores<128>(a, st) : launch_scores<64>(a, st);
+#else
+  e = launch_pooled_scores_tc(a, L.d, st);
+#endif
   if (e != cudaSuccess) return e;
   return launch_select_nt(a, L.hp, st);
 }

@@ -50,24 +50,6 @@ FBM_DEVICE void set_error(uint32_t *err, uint32_t bits) {
   if (err) atomicOr(err, bits);
 }
 
-// Entry t of a LUT row (`row` = the row's first entry), checked the way every
-// attention kernel reads it: an entry outside [0, nk), or one not strictly
-// above the entry before it (a duplicate or a descending entry), is unusable.
-// Returns the kv block, or -1 with the FBM_DEVERR_* bit that says why in *why.
-FBM_DEVICE int lut_entry(const int32_t *row, int t, int nk, uint32_t *why) {
-  const int j = __ldg(row + t);
-  if (j < 0 || j >= nk) {
-    *why = FBM_DEVERR_LUT_RANGE;
-    return -1;
-  }
-  if (t > 0 && j <= __ldg(row + t - 1)) {
-    *why = FBM_DEVERR_LUT_ORDER;
-    return -1;
-  }
-  *why = 0;
-  return j;
-}
-
 FBM_DEVICE uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

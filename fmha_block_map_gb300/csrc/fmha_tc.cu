@@ -26,23 +26,19 @@
 //
 // TMEM (512 columns): S slots at columns 0 and 128 (fp32), P buffers at 256 and
 // 320 (two 16-bit values per column), O at 384.  An M = 64 accumulator keeps
-// row i in lane (i mod 16) + 32 (i / 16), so subpartition sw holds rows
-// 16 sw .. 16 sw + 15.  Two softmax warps share a subpartition, one per kv
-// block of the pair: with the 16x32bx2 shape thread t of the warp for block b
-// holds row 16 sw + (t mod 16) and 32 keys (64 b + 32 (t / 16) ..) of it, and
-// the same 32 columns of O.  The running max of a row is kept lazily (O and l
-// are rescaled only when a score exceeds it by more than 2^8): the two halves
-// of a block agree through one shuffle, the two warps through one OR-barrier
-// per pair (and a shared-memory exchange of their block maxima when either
-// has to move the max).
+// row i in lane (i mod 16) + 32 (i / 16): softmax warp w (subpartition w) owns
+// rows 16w .. 16w + 15, and with the 16x32bx2 load shape thread t holds row
+// 16w + (t mod 16), keys 64 (t / 16) .. + 63 of the pair, i.e. one kv block.
+// The running max of a row is kept lazily (O and l are rescaled only when a
+// score exceeds it by more than 2^8); both threads of a row agree on it through
+// one shuffle.
 //
-// Roles (one persistent CTA per SM, 12 warps):
+// Roles (one persistent CTA per SM, 8 warps):
 //   warp 0   TMA producer of Q (double buffer) and K pairs (3-slot ring)
 //   warp 1   TMA producer of V pairs (2-slot ring)
 //   warp 2   TMEM owner and S issuer
 //   warp 3   PV issuer
-//   warps 4-11 softmax and epilogue (warps 4-7: the first kv block of a pair on
-//            subpartitions 0-3; warps 8-11: the second)
+//   warps 4-7 softmax and epilogue (TMEM subpartitions 0-3)
 // Pipeline: S(g) is issued once K(g) has landed and its TMEM slot is free (the
 // softmax releases a slot as soon as it holds the scores in registers), so the
 // S MMA of pair g + 1 runs during the softmax of pair g; PV(g) once P(g) is in
@@ -68,9 +64,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int kD = 128;
-constexpr int kQBytes = 64 * kD * 2;      // 16 KB: a 64-row Q (or output) tile
-constexpr int kPairBytes = 128 * kD * 2;  // 32 KB: two 64-row kv blocks
 constexpr int kQChunk = 64 * 128;         // 8 KB: one 64-wide d chunk of a 64-row tile
 constexpr int kPairChunk = 128 * 128;     // 16 KB: one 64-wide d chunk of a 128-row pair
 constexpr int kKSlots = 3;                // K ring (S(g) may run ahead of the softmax)
@@ -78,48 +71,52 @@ constexpr int kVSlots = 2;                // V ring
 constexpr int kSSlots = 2;                // S slots in TMEM
 constexpr int kPBufs = 2;                 // P buffers in TMEM
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + 2 * kQBytes;
-constexpr int OFF_V = OFF_K + kKSlots * kPairBytes;
-constexpr int OFF_STAGE = OFF_V + kVSlots * kPairBytes;  // output tile, [chunk][64 rows][128 B] SW128
-constexpr int OFF_BAR = OFF_STAGE + kQBytes;
 enum {
   B_QF = 0, B_QE = 2, B_KF = 4, B_KE = B_KF + kKSlots, B_VF = B_KE + kKSlots,
   B_VE = B_VF + kVSlots, B_SF = B_VE + kVSlots, B_SE = B_SF + kSSlots, B_PF = B_SE + kSSlots,
   B_PV = B_PF + kPBufs, B_OF = B_PV + kPBufs, B_DRAIN = B_OF + 1, B_DRAIN2 = B_DRAIN + 1,
   NBAR = B_DRAIN2 + 1
 };
-// [0] tmem base, [1] abort flag, bytes 8 .. 15: PV-skip votes [P buffer][subpartition]
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-// softmax exchange: block maxima [pair parity][kv block][64 rows] and row sums
-// [kv block][64 rows], fp32
-constexpr int OFF_XCH = OFF_MISC + 16;
-constexpr int SMEM_BYTES = OFF_XCH + (2 * 2 * 64 + 2 * 64) * 4;
-constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
-static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+// Shared-memory layout for head dim D (64 or 128): a 64-row tile of D 16-bit
+// values is D / 64 chunks of 64 columns (128-byte rows, 128-byte swizzle).
+template <int D>
+struct Lay {
+  static constexpr int NCH = D / 64;             // 64-wide d chunks
+  static constexpr int QBytes = 64 * D * 2;      // a 64-row Q (or output) tile
+  static constexpr int PairBytes = 128 * D * 2;  // two 64-row kv blocks
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * QBytes;
+  static constexpr int OFF_V = OFF_K + kKSlots * PairBytes;
+  static constexpr int OFF_STAGE = OFF_V + kVSlots * PairBytes;  // output tile [chunk][64 rows][128 B]
+  static constexpr int OFF_BAR = OFF_STAGE + QBytes;
+  // [0] tmem base, [1] abort flag, bytes 8 .. 15: PV-skip votes [P buffer][softmax warp]
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTS = 0;    // S slot s at kTS + 128 s
 constexpr uint32_t kTP = 256;  // P buffer b at kTP + 64 b
-constexpr uint32_t kTO = 384;  // O
+constexpr uint32_t kTO = 384;  // O (D columns)
 constexpr uint32_t kDescHi = sdesc_hi_sw128(1024);  // every operand: 1024-byte 8-row atoms
 constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
 
 constexpr int kWarpQK = 0, kWarpV = 1, kWarpS = 2, kWarpPV = 3, kWarpSm = 4;
-constexpr int kSoftmaxWarps = 8;  // two per TMEM subpartition: one per kv block of a pair
+constexpr int kSoftmaxWarps = 4;
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kThreads = 32 * (kWarpSm + kSoftmaxWarps);
 constexpr int kSoftmaxBar = 1;  // named barrier of the softmax warps
-constexpr int kPairBar0 = 2;    // named barriers 2 .. 5: the two warps of one subpartition
 
 struct TcParams {
   CUtensorMap tq, tk, tv, to;
   const int32_t *lut, *cnt;
   void *out;      // dtype output (whole rows), or
-  float *opart;   // fp32 partials [splits, b * hq * s_q, kD] (split-KV / partial mode)
+  float *opart;   // fp32 partials [splits, b * hq * s_q, D] (split-KV / partial mode)
   float *lse;     // [b * hq * s_q], or [splits, b * hq * s_q] with opart
   uint32_t *err;
   int b, hq, hk, s_q, s_k, nq, nk, lut_stride, causal, splits, units;
+  int koff;       // causal: key index u visible to query row t when u <= t + koff
   size_t plane;   // b * hq * s_q
   float sl2;      // scale * log2(e)
   float tau2;     // pv_threshold * log2(e) (PV-skip variant)
@@ -154,7 +151,9 @@ FBM_DEVICE Unit unit_of(const TcParams &P, int u) {
     n_list = max(0, min(raw, lim));
   } else {
     U.row = nullptr;
-    n_list = P.causal ? min(P.nk, U.i + 1) : P.nk;
+    // dense: every kv block up to the one holding the q block's last visible key
+    const int lastk = U.i * 64 + 63 + P.koff;
+    n_list = !P.causal ? P.nk : (lastk < 0 ? 0 : min(P.nk, lastk / 64 + 1));
   }
   if constexpr (kPartial) {
     // contiguous chunks: the first n mod S hold ceil(n / S) entries
@@ -168,23 +167,36 @@ FBM_DEVICE Unit unit_of(const TcParams &P, int u) {
   return U;
 }
 
-// kv block of entry t of the unit's chunk, or -1 for an unusable LUT entry
-// (out of range, or not above the entry before it: lut_entry)
-FBM_DEVICE int entry_of(const Unit &U, int t, uint32_t *why) {
-  if (!U.row) {
-    *why = 0;
-    return U.off + t;
-  }
-  return lut_entry(U.row, U.off + t, U.nk, why);
-}
+// kv block of entry t of the unit's chunk (dense rows: the index itself).  The
+// kernel checks the range of every entry (an entry outside [0, nk) is skipped
+// and flagged); their order is the caller's contract, checked on request by
+// lut_validate, so the read stays a plain load whose value nothing waits on
+// until the pair after it.
 FBM_DEVICE int entry_of(const Unit &U, int t) {
-  uint32_t why;
-  return entry_of(U, t, &why);
+  return U.row ? __ldg(U.row + U.off + t) : U.off + t;
 }
 
-template <bool kBf16, bool kPartial, bool kPvSkip, bool kFp8>
+// O of one row as seen by one softmax thread: D / 2 columns (16x32bx2 shape,
+// the two threads of a row holding the two halves)
+template <int D>
+FBM_DEVICE void ld_o(uint32_t taddr, uint32_t (&o)[D / 2]) {
+  if constexpr (D == 128) tmem_ld_rowhalf64(taddr, o);
+  else tmem_ld_rowhalf32(taddr, o);
+}
+template <int D>
+FBM_DEVICE void st_o(uint32_t taddr, const uint32_t (&o)[D / 2]) {
+  if constexpr (D == 128) tmem_st_rowhalf64(taddr, o);
+  else tmem_st_rowhalf32(taddr, o);
+}
+
+template <int D, bool kBf16, bool kPartial, bool kPvSkip, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__ TcParams P) {
   static_assert(!(kFp8 && (kPartial || kPvSkip)), "the fp8 variant runs whole rows");
+  static_assert(!kFp8 || D == 128, "fp8 Q / K at d = 128");
+  using Ly = Lay<D>;
+  constexpr int OFF_Q = Ly::OFF_Q, OFF_K = Ly::OFF_K, OFF_V = Ly::OFF_V,
+                OFF_STAGE = Ly::OFF_STAGE, OFF_BAR = Ly::OFF_BAR, OFF_MISC = Ly::OFF_MISC;
+  constexpr int kQBytes = Ly::QBytes, kPairBytes = Ly::PairBytes, kNch = Ly::NCH;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -231,17 +243,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     if (!mbar_wait(bar(eb), ((g / ns) & 1) ^ 1, abort_flag, kWaitNs)) return false;
     int js[2] = {-1, -1};
     uint32_t bytes = 0;
-    // an fp8 K block is one 128-byte-wide box; 16-bit blocks are two
-    const int nchunk = (kFp8 && !is_v) ? 1 : 2;
+    // an fp8 K block is one 128-byte-wide box; a 16-bit block is D / 64
+    const int nchunk = (kFp8 && !is_v) ? 1 : kNch;
     for (int hf = 0; hf < 2; ++hf) {
       const int t = 2 * p + hf;
       if (t >= U.n) break;
-      uint32_t why;
-      int j = entry_of(U, t, &why);
-      if (j < 0) {
-        // unusable entry: flagged; block 0 is fetched in its place so that
-        // the masked keys (P = 0) meet finite V rows
-        set_error(P.err, why);
+      int j = entry_of(U, t);
+      if (j < 0 || j >= P.nk) {
+        // out of range: flagged (by the K producer); block 0 is fetched in
+        // its place so that the masked keys (P = 0) meet finite V rows
+        if (!is_v) set_error(P.err, FBM_DEVERR_LUT_RANGE);
         j = 0;
       }
       js[hf] = j;
@@ -270,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         const int npairs = (U.n + 1) >> 1;
         const int qb = uc & 1;
         if (!(ok = mbar_wait(bar(B_QE + qb), ((uc >> 1) & 1) ^ 1, abort_flag, kWaitNs))) break;
-        constexpr int qchunks = kFp8 ? 1 : 2;  // an fp8 Q tile is one 128-byte-wide box
+        constexpr int qchunks = kFp8 ? 1 : kNch;  // an fp8 Q tile is one 128-byte-wide box
         mbar_arrive_tx(bar(B_QF + qb), qchunks * kQChunk);
         for (int c = 0; c < qchunks; ++c)
           tma_load_3d(sbase + OFF_Q + qb * kQBytes + c * kQChunk, &P.tq, c * 64, U.i * 64,
@@ -320,12 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           if constexpr (kFp8) {
             // e4m3 rows are 128 bytes: one swizzle atom wide, 32 values of K per MMA
 #pragma unroll
-            for (int kk = 0; kk < kD / 32; ++kk)
+            for (int kk = 0; kk < D / 32; ++kk)
               mma_f8_lo(dS, q_lo + ((kk * 32) >> 4), k_lo + ((kk * 32) >> 4), kDescHi, idS,
                         kk > 0 ? 1u : 0u);
           } else {
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)
+            for (int kk = 0; kk < D / 16; ++kk)
               mma_f16_lo(dS, q_lo + (((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4),
                          k_lo + (((kk >> 2) * kPairChunk + (kk & 3) * 32) >> 4), kDescHi, idS,
                          kk > 0 ? 1u : 0u);
@@ -346,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     // ------------------------------------------------------------ PV issuer
     if (lane == 0) {
       // A = P (TMEM, K-major), B = V pair (MN-major: d contiguous)
-      constexpr uint32_t idO = idesc_f16(kBf16, false, true, 64, 128);
+      constexpr uint32_t idO = idesc_f16(kBf16, false, true, 64, D);
       const uint32_t tO = tbase + kTO;
       int pc = 0, uc = 0;
       bool ok = true;
@@ -390,25 +401,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    // Eight warps: warp w reads TMEM subpartition sw = w % 4 (query rows
-    // 16 sw .. 16 sw + 15) and handles kv block `blk` of every pair (keys
-    // 64 blk .. 64 blk + 63); the two warps of a subpartition hold the same
-    // rows.  Thread t: row 16 sw + (t mod 16), keys 64 blk + 32 (t / 16) + 0..31,
-    // O columns 64 blk + 32 (t / 16) + 0..31 of that row.
     using E = typename std::conditional<kBf16, BF16, F16>::type;
-    const int sw = warp & 3;                  // TMEM subpartition
-    const int blk = (warp - kWarpSm) >> 2;    // kv block of the pair
-    const int half = lane >> 4;               // 32-key / 32-column half
-    const int r16 = lane & 15;
-    const int row = sw * 16 + r16;            // query row within the q block
+    const int sw = warp - kWarpSm;            // == warp % 4: TMEM subpartition
+    const int half = lane >> 4;               // block of the pair / d half of O
+    const int row = sw * 16 + (lane & 15);    // query row within the q block
     const int tid = threadIdx.x - kWarpSm * 32;
-    const int pair_bar = kPairBar0 + sw;      // named barrier of the two warps of these rows
     const uint32_t tl = tbase + ((uint32_t)(sw * 32) << 16);
     const uint64_t sl2x2 = f2_pack(P.sl2, P.sl2);
-    // block maxima exchanged between the two warps of a row group, double
-    // buffered by pair parity: [parity][blk][row]; row sums at the epilogue
-    volatile float *xmax = reinterpret_cast<volatile float *>(smem + OFF_XCH);
-    volatile float *xsum = xmax + 2 * 2 * 64;
     // Every softmax thread runs the same loop trip counts and barriers whatever
     // happens: a failed (timed-out) wait only clears `ok`, and later waits
     // return at once.
@@ -421,12 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       if (U.n == 0) {
         const size_t orow0 = (kPartial ? (size_t)U.split * P.plane : 0) + (size_t)U.bh_q * P.s_q + q0;
         if constexpr (kPartial) {
-          float *o = P.opart + orow0 * kD;
-          for (int e = tid * 4; e < rows * kD; e += kSoftmaxThreads * 4)
+          float *o = P.opart + orow0 * D;
+          for (int e = tid * 4; e < rows * D; e += kSoftmaxThreads * 4)
             *reinterpret_cast<float4 *>(o + e) = make_float4(0.f, 0.f, 0.f, 0.f);
         } else {
-          uint16_t *o = static_cast<uint16_t *>(P.out) + orow0 * kD;
-          for (int e = tid * 8; e < rows * kD; e += kSoftmaxThreads * 8)
+          uint16_t *o = static_cast<uint16_t *>(P.out) + orow0 * D;
+          for (int e = tid * 8; e < rows * D; e += kSoftmaxThreads * 8)
             *reinterpret_cast<uint4 *>(o + e) = make_uint4(0, 0, 0, 0);
         }
         if (P.lse && tid < rows) P.lse[orow0 + tid] = -INFINITY;
@@ -438,22 +437,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       float m = -INFINITY;                 // running max of the row (log2 domain)
       float mt = -INFINITY;                // exact running max (PV-skip variant)
       uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};  // this thread's share of the row sum
-      int j_next = blk < U.n ? entry_of(U, blk) : -1;
+      int j_next = half < U.n ? entry_of(U, half) : -1;
       for (int p = 0; p < npairs; ++p) {
         const int g = pc + p, ss = g % kSSlots, pb = g % kPBufs;
         const int j = j_next;
         {
-          const int tn = 2 * (p + 1) + blk;
+          const int tn = 2 * (p + 1) + half;
           j_next = (p + 1 < npairs && tn < U.n) ? entry_of(U, tn) : -1;
         }
-        const bool jvalid = j >= 0;  // entry_of has range- and order-checked it
-        const int kpos0 = (jvalid ? j : 0) * 64 + half * 32;
-        // every key of this thread's 32 visible to its row
-        const bool plain = jvalid && kpos0 + 32 <= P.s_k && (!P.causal || kpos0 + 31 <= qpos);
+        const bool jvalid = j >= 0 && j < P.nk;
+        const int kpos0 = (jvalid ? j : 0) * 64;
+        // every key of this thread's block visible to its row
+        const bool plain = jvalid && kpos0 + 64 <= P.s_k && (!P.causal || kpos0 + 63 <= qpos + P.koff);
         ok = ok && mbar_wait(bar(B_SF + ss), (g / kSSlots) & 1, abort_flag, kWaitNs);
         tc_fence_after();
-        uint32_t sv[32];
-        tmem_ld_rowhalf32(tl + kTS + ss * 128 + blk * 64, sv);
+        uint32_t sv[64];
+        tmem_ld_rowhalf64(tl + kTS + ss * 128, sv);
         tmem_wait_ld();
         // the S slot is free for S(g + kSSlots) as soon as it is in registers
         tc_fence_before();
@@ -461,56 +460,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         if (lane == 0) mbar_arrive(bar(B_SE + ss));
         if (!plain) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
+          for (int c = 0; c < 64; ++c) {
             const int kpos = kpos0 + c;
-            const bool vis = jvalid && kpos < P.s_k && (!P.causal || kpos <= qpos);
+            const bool vis = jvalid && kpos < P.s_k && (!P.causal || kpos <= qpos + P.koff);
             if (!vis) sv[c] = __float_as_uint(-INFINITY);
           }
         }
-        // row max over this warp's block (this thread's 32 keys, then the other half)
+        // row max over the pair (this thread's 64 keys, then the other half)
         float mx;
         {
-          float t[4];
+          float t[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < 8; ++i) {
             const float *v = reinterpret_cast<const float *>(sv) + 8 * i;
             t[i] = fmaxf(fmax3(fmax3(v[0], v[1], v[2]), v[3], v[4]), fmax3(v[5], v[6], v[7]));
           }
-          mx = fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
+          mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        // fp8: the two block scales fold into this warp's factor (its keys are
-        // one kv block); the max is then taken over scaled scores
+        // fp8: the two block scales fold into this thread's factor (its 64 keys
+        // are one kv block); the pair max is then taken over scaled scores
         float fsc = P.sl2;
-        if constexpr (kFp8) fsc = qsl2 * (jvalid ? __ldg(P.kscale + (size_t)U.bh_k * P.nk + j) : 1.f);
-        const float mxs = mx * fsc;        // this block's row max, log2 domain
-        // agree with the partner warp: publish this block's max, then one
-        // OR-barrier tells both warps whether either needs to move the max
-        volatile float *xm = xmax + (g & 1) * 128;
-        if (half == 0) xm[blk * 64 + row] = mxs;
-        const bool need_me = mxs > m + 8.0f;
-        const bool any_need = named_or(pair_bar, 64, need_me);
+        if constexpr (kFp8) {
+          fsc = qsl2 * (jvalid ? __ldg(P.kscale + (size_t)U.bh_k * P.nk + j) : 1.f);
+          mx *= fsc;
+        }
         uint32_t vote = 0;
         if constexpr (kPvSkip) {
+          const float mx_other = __shfl_xor_sync(0xffffffffu, mx, 16);
           // block A (entry 2p) then block B (entry 2p + 1) against the exact
           // running max of the blocks visited before each; rows past the end
           // of the sequence do not veto
-          const float other = xm[(blk ^ 1) * 64 + row];
-          const float a = blk == 0 ? mxs : other;
-          const float b = blk == 0 ? other : mxs;
+          const float a = (half == 0 ? mx : mx_other) * P.sl2;
+          const float b = (half == 0 ? mx_other : mx) * P.sl2;
           const bool real = qpos < P.s_q;
           const bool sa = !real || a < mt - P.tau2;
           mt = fmaxf(mt, a);
           const bool sb = !real || b < mt - P.tau2;
           mt = fmaxf(mt, b);
           vote = (__all_sync(0xffffffffu, sa) ? 1u : 0u) | (__all_sync(0xffffffffu, sb) ? 2u : 0u);
+          mx = fmaxf(mx, mx_other);
+        } else {
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         }
-        if (any_need) {
-          // rare: some score of these rows exceeds the running max by more
-          // than 2^8 (always on the first pair): move the max to the pair's
-          // row max, rescale l and this warp's half of O
-          const float mrow = fmaxf(mxs, xm[(blk ^ 1) * 64 + row]);
-          const float mn = mrow > m + 8.0f ? mrow : m;
+        const float mxs = kFp8 ? mx : mx * P.sl2;
+        const bool need = mxs > m + 8.0f;
+        if (__any_sync(0xffffffffu, need)) {
+          // rare: some score of the warp's rows exceeds its running max by more
+          // than 2^8 (always on the first pair): move the max, rescale l and O
+          const float mn = need ? mxs : m;
           const float alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - mn);
           m = mn;
           const uint64_t a2 = f2_pack(alpha, alpha);
@@ -521,27 +518,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
             const int gp = g - 1;
             ok = ok && mbar_wait(bar(B_PV + gp % kPBufs), (gp / kPBufs) & 1, abort_flag, kWaitNs);
             tc_fence_after();
-            uint32_t o[32];
-            tmem_ld_rowhalf32(tl + kTO + blk * 64, o);
+            uint32_t o[D / 2];
+            ld_o<D>(tl + kTO, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
+            for (int c = 0; c < D / 2; c += 2) {
               const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[c]), __uint_as_float(o[c + 1])), a2);
               const float2 w2 = f2_unpack(v);
               o[c] = __float_as_uint(w2.x);
               o[c + 1] = __float_as_uint(w2.y);
             }
-            tmem_st_rowhalf32(tl + kTO + blk * 64, o);
+            st_o<D>(tl + kTO, o);
             tmem_wait_st();
           }
         }
-        // P = exp2(s * factor - m), packed to 16-bit pairs
+        // P = exp2(s * scale * log2 e - m), packed to 16-bit pairs
         const float mu = (m == -INFINITY) ? 0.f : m;
         const uint64_t negm = f2_pack(-mu, -mu);
         const uint64_t fx2 = kFp8 ? f2_pack(fsc, fsc) : sl2x2;
-        uint32_t pk[16];
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 32; ++i) {
           const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
                                     fx2, negm);
           const float2 xv = f2_unpack(x);
@@ -556,11 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           ok = ok && mbar_wait(bar(B_PV + pb), (gp / kPBufs) & 1, abort_flag, kWaitNs);
         }
         tc_fence_after();
-        tmem_st_rowhalf16(tl + kTP + pb * 64 + blk * 32, pk);
+        tmem_st_rowhalf32(tl + kTP + pb * 64, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (kPvSkip && blk == 0 && lane == 0)  // read by the PV issuer once B_PF(pb) completes
+        if (kPvSkip && lane == 0)  // read by the PV issuer once B_PF(pb) completes
           *reinterpret_cast<volatile uint8_t *>(smem + OFF_MISC + 8 + pb * 4 + sw) = (uint8_t)vote;
         if (lane == 0) mbar_arrive(bar(B_PF + pb));
       }
@@ -569,8 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         const int gl = pc + npairs - 1;
         ok = ok && mbar_wait(bar(B_PV + gl % kPBufs), (gl / kPBufs) & 1, abort_flag, kWaitNs);
         tc_fence_after();
-        uint32_t o[32];
-        tmem_ld_rowhalf32(tl + kTO + blk * 64, o);
+        uint32_t o[D / 2];
+        ld_o<D>(tl + kTO, o);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -580,48 +577,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           const float2 a = f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])));
           lt = a.x + a.y;
         }
-        lt += __shfl_xor_sync(0xffffffffu, lt, 16);   // this warp's keys of the row
-        if (half == 0) xsum[blk * 64 + row] = lt;
-        named_sync(pair_bar, 64);
-        lt += xsum[(blk ^ 1) * 64 + row];              // plus the partner warp's keys
+        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
         const float inv = lt > 0.f ? 1.0f / lt : 0.f;
         const size_t orow0 = (kPartial ? (size_t)U.split * P.plane : 0) + (size_t)U.bh_q * P.s_q + q0;
-        if (P.lse && blk == 0 && half == 0 && row < rows)
+        if (P.lse && half == 0 && row < rows)
           P.lse[orow0 + row] = lt > 0.f ? m * 0.6931471805599453f + logf(lt) : -INFINITY;
         if constexpr (kPartial) {
-          // fp32 partial: this thread's 32 values of row `row`
+          // fp32 partial: this thread's D / 2 values of row `row`, d half `half`
           if (row < rows) {
-            float4 *dst = reinterpret_cast<float4 *>(P.opart + (orow0 + row) * kD + blk * 64 + half * 32);
+            float4 *dst = reinterpret_cast<float4 *>(P.opart + (orow0 + row) * D + half * (D / 2));
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
+            for (int c = 0; c < D / 8; ++c)
               dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv, __uint_as_float(o[4 * c + 1]) * inv,
                                    __uint_as_float(o[4 * c + 2]) * inv,
                                    __uint_as_float(o[4 * c + 3]) * inv);
           }
-          // the row sums of this unit have been read before the next unit's
-          // epilogue writes them again (its pairs pass the pair barrier first)
           pc += npairs;
           continue;
         }
-        // staging: d chunk `blk` of row `row`, 16-byte pieces 4 half .. 4 half + 3,
-        // 128-byte swizzle
-        uint8_t *srow = smem + OFF_STAGE + blk * kQChunk + row * 128;
+        // staging: d half `half` of row `row` as D / 16 pieces of 16 bytes in
+        // the 128-byte-swizzled [chunk][64 rows][128 B] tile (d = 128: the half
+        // is chunk `half`; d = 64: pieces 4 half .. 4 half + 3 of the one chunk)
+        uint8_t *srow = smem + OFF_STAGE + (D == 128 ? half * kQChunk : 0) + row * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < D / 16; ++c) {
           uint32_t w[4];
 #pragma unroll
           for (int z = 0; z < 4; ++z)
             w[z] = E::from_f2(__uint_as_float(o[8 * c + 2 * z]) * inv,
                               __uint_as_float(o[8 * c + 2 * z + 1]) * inv);
-          const int piece = 4 * half + c;
+          const int piece = D == 128 ? c : 4 * half + c;
           *reinterpret_cast<uint4 *>(srow + ((piece ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async();
         named_sync(kSoftmaxBar, kSoftmaxThreads);
         if (tid == 0) {
           // rows past the end of the sequence are clipped by the tensor map
-          tma_store_3d(&P.to, sbase + OFF_STAGE, 0, q0, U.bh_q);
-          tma_store_3d(&P.to, sbase + OFF_STAGE + kQChunk, 64, q0, U.bh_q);
+#pragma unroll
+          for (int c = 0; c < kNch; ++c)
+            tma_store_3d(&P.to, sbase + OFF_STAGE + c * kQChunk, c * 64, q0, U.bh_q);
           bulk_commit();
           bulk_wait_read0();
         }
@@ -659,12 +653,13 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// [bh, s, d=128] 16-bit tensor, box = 64 d x 64 rows x 1 head, 128B swizzle
-bool make_map(CUtensorMap *m, const void *base, int bh, int s, bool bf16) {
+// [bh, s, d] 16-bit tensor (d = 64 or 128), box = 64 d x 64 rows x 1 head,
+// 128B swizzle
+bool make_map(CUtensorMap *m, const void *base, int bh, int s, int d, bool bf16) {
   auto enc = get_encode();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)s, (cuuint64_t)bh};
-  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)s * kD * 2};
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)s, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)s * d * 2};
   cuuint32_t box[3] = {64, 64, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -678,8 +673,8 @@ bool make_map(CUtensorMap *m, const void *base, int bh, int s, bool bf16) {
 bool make_map8(CUtensorMap *m, const void *base, int bh, int s) {
   auto enc = get_encode();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)s, (cuuint64_t)bh};
-  cuuint64_t strides[2] = {(cuuint64_t)kD, (cuuint64_t)s * kD};
+  cuuint64_t dims[3] = {128, (cuuint64_t)s, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {128, (cuuint64_t)s * 128};
   cuuint32_t box[3] = {128, 64, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
@@ -699,8 +694,9 @@ int sm_count() {
   return n[dev] > 0 ? n[dev] : 148;
 }
 
-template <bool BF16, bool PARTIAL, bool PVSKIP, bool FP8 = false>
+template <int D, bool BF16, bool PARTIAL, bool PVSKIP, bool FP8 = false>
 cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
+  constexpr int SMEM_ALLOC = Lay<D>::SMEM_ALLOC;
   static_assert(!(PARTIAL && PVSKIP), "the PV skip runs on whole rows only");
   // the shared-memory attribute is per device: set it once on each
   static std::atomic<bool> attr_done[kMaxDevices];
@@ -708,7 +704,7 @@ cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !attr_done[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(k_fmha_tc<BF16, PARTIAL, PVSKIP, FP8>,
+    e = cudaFuncSetAttribute(k_fmha_tc<D, BF16, PARTIAL, PVSKIP, FP8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) attr_done[dev].store(true, std::memory_order_release);
@@ -717,10 +713,10 @@ cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   memset(&P, 0, sizeof(P));
   const bool qk_ok = FP8 ? (make_map8(&P.tq, L.q, L.b * L.hq, L.s_q) &&
                             make_map8(&P.tk, L.k, L.b * L.hk, L.s_k))
-                         : (make_map(&P.tq, L.q, L.b * L.hq, L.s_q, BF16) &&
-                            make_map(&P.tk, L.k, L.b * L.hk, L.s_k, BF16));
-  if (!qk_ok || !make_map(&P.tv, L.v, L.b * L.hk, L.s_k, BF16) ||
-      (L.out && !make_map(&P.to, L.out, L.b * L.hq, L.s_q, BF16)))
+                         : (make_map(&P.tq, L.q, L.b * L.hq, L.s_q, D, BF16) &&
+                            make_map(&P.tk, L.k, L.b * L.hk, L.s_k, D, BF16));
+  if (!qk_ok || !make_map(&P.tv, L.v, L.b * L.hk, L.s_k, D, BF16) ||
+      (L.out && !make_map(&P.to, L.out, L.b * L.hq, L.s_q, D, BF16)))
     return cudaErrorInvalidValue;
   P.lut = L.lut;
   P.cnt = L.cnt;
@@ -733,32 +729,40 @@ cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   P.b = L.b; P.hq = L.hq; P.hk = L.hk; P.s_q = L.s_q; P.s_k = L.s_k; P.nq = L.nq; P.nk = L.nk;
   P.lut_stride = L.lut_stride;
   P.causal = L.causal;
+  P.koff = L.key_offset;
   P.units = L.b * L.hq * L.nq * L.num_splits;
   P.sl2 = L.scale * 1.4426950408889634f;
   P.tau2 = L.pv_threshold * 1.4426950408889634f;
   P.qscale = L.q_scale;
   P.kscale = L.k_scale;
   const int grid = std::min(P.units, sm_count());
-  k_fmha_tc<BF16, PARTIAL, PVSKIP, FP8><<<grid, kThreads, SMEM_ALLOC, st>>>(P);
+  k_fmha_tc<D, BF16, PARTIAL, PVSKIP, FP8><<<grid, kThreads, SMEM_ALLOC, st>>>(P);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool fmha_tc_supported(int d, int dv, int num_splits, int s_q, int s_k) {
-  return d == kD && dv == kD && num_splits >= 1 && s_q > 0 && s_k > 0;
+  return (d == 64 || d == 128) && dv == d && num_splits >= 1 && s_q > 0 && s_k > 0;
 }
 
-cudaError_t launch_fmha_tc(const FmhaLaunch &L, cudaStream_t st) {
+namespace {
+template <int D>
+cudaError_t launch_d(const FmhaLaunch &L, cudaStream_t st) {
   // whole rows in dtype, or fp32 partials (split chunks, or rows for a combine)
-  if (L.q_scale)  // e4m3 Q and K (whole rows; the caller has checked)
-    return L.bf16 ? launch_t<true, false, false, true>(L, st)
-                  : launch_t<false, false, false, true>(L, st);
   if (L.out == nullptr)
-    return L.bf16 ? launch_t<true, true, false>(L, st) : launch_t<false, true, false>(L, st);
+    return L.bf16 ? launch_t<D, true, true, false>(L, st) : launch_t<D, false, true, false>(L, st);
   if (L.pv_threshold < INFINITY)
-    return L.bf16 ? launch_t<true, false, true>(L, st) : launch_t<false, false, true>(L, st);
-  return L.bf16 ? launch_t<true, false, false>(L, st) : launch_t<false, false, false>(L, st);
+    return L.bf16 ? launch_t<D, true, false, true>(L, st) : launch_t<D, false, false, true>(L, st);
+  return L.bf16 ? launch_t<D, true, false, false>(L, st) : launch_t<D, false, false, false>(L, st);
+}
+}  // namespace
+
+cudaError_t launch_fmha_tc(const FmhaLaunch &L, cudaStream_t st) {
+  if (L.q_scale)  // e4m3 Q and K, d = 128 (whole rows; the caller has checked)
+    return L.bf16 ? launch_t<128, true, false, false, true>(L, st)
+                  : launch_t<128, false, false, false, true>(L, st);
+  return L.d == 128 ? launch_d<128>(L, st) : launch_d<64>(L, st);
 }
 
 }  // namespace fbm

@@ -20,7 +20,9 @@ struct SelectArgs {
   int causal, sink, mode_cdf;
   int32_t *lut, *cnt;
   uint8_t *bmap;
+  uint32_t *err;  // device error word
 };
+cudaError_t launch_pooled_scores_tc(const SelectArgs &a, int d, cudaStream_t st);
 
 struct BlockMapLaunch {
   const void *q, *k;
@@ -31,6 +33,7 @@ struct BlockMapLaunch {
   float *qbar, *qsim, *kbar, *ksim, *kmu;  // workspace carve-out
   int32_t *lut, *cnt;
   uint8_t *bmap;
+  uint32_t *err;  // device error word
 };
 cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st);
 size_t block_map_smem_bytes(int d, int nt);
@@ -40,6 +43,7 @@ struct FmhaLaunch {
   int bf16, b, hq, hk, s_q, s_k, d, nq, nk;
   const int32_t *lut, *cnt;  // lut == nullptr: dense
   int lut_stride, num_splits, causal;
+  int key_offset;      // causal: key index u visible to query row t when u <= t + key_offset
   float scale;
   float pv_threshold;  // +inf: no PV skip
   const float *q_scale, *k_scale;  // fp8 Q / K (q, k hold e4m3 codes) or nullptr
@@ -47,7 +51,6 @@ struct FmhaLaunch {
   float *lse, *o_part, *lse_part;
   uint32_t *err;
 };
-cudaError_t launch_fmha_mma(const FmhaLaunch &L, cudaStream_t st);
 cudaError_t launch_fmha_tc(const FmhaLaunch &L, cudaStream_t st);
 bool fmha_tc_supported(int d, int dv, int num_splits, int s_q, int s_k);
 
@@ -78,6 +81,14 @@ struct LutShardLaunch {
   uint32_t *err;
 };
 cudaError_t launch_lut_shard(const LutShardLaunch &L, cudaStream_t st);
+
+struct LutValidateLaunch {
+  const int32_t *lut, *cnt;
+  int64_t rows;
+  int lut_stride, nk;
+  uint32_t *err;
+};
+cudaError_t launch_lut_validate(const LutValidateLaunch &L, cudaStream_t st);
 
 struct DecodeLaunch {
   const void *q, *cache;

@@ -168,7 +168,13 @@ fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int 
  *
  * For each query row t of q block i (head h, KV head g = h / (hq / hk)), the
  * keys are the union of kv blocks lut[b][h][i][0 .. lut_count[b][h][i]); under
- * causal (s_q == s_k) only keys at positions <= t.  With s = scale * q_t . k_u,
+ * causal only the keys at index u <= t + key_offset (key_offset = 0 when
+ * queries and keys start at the same position; s_k - s_q when the queries
+ * are the last s_q positions of the keys' sequence, the causal dense pass of
+ * the speculative two-pass recipe, "Incremental_FlashAttention
+ * updating_log.md" Stage 5; -lo * 64 for a context-parallel rank whose keys
+ * start at position lo * 64; ignored without causal, |key_offset| <= 2^30).
+ * A row with no visible key is an empty row.  With s = scale * q_t . k_u,
  * O_t = sum_u e^(s_u - m) v_u / sum_u e^(s_u - m) and LSE_t = m + ln sum_u
  * e^(s_u - m) (natural log).  An empty key set gives O_t = 0, LSE_t = -inf.
  *
@@ -176,22 +182,23 @@ fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int 
  * dtype FBM_F16 / FBM_BF16; d = dv in {64, 128}; blkq = blkk = 64.
  * lut: device int32 [b, hq, nq, lut_stride] with nq = ceil(s_q / 64), entries in
  *   [0, ceil(s_k / 64)), strictly ascending; lut_count: device int32
- *   [b, hq, nq], in [0, min(nk, lut_stride)].  Every entry is checked on the
- *   device: one out of range is skipped and sets FBM_DEVERR_LUT_RANGE, one not
- *   above the entry before it in its row (a duplicate or a descending entry)
- *   is skipped and sets FBM_DEVERR_LUT_ORDER, and a count outside its range is
- *   clamped into it and sets FBM_DEVERR_LUT_RANGE.
+ *   [b, hq, nq], in [0, min(nk, lut_stride)].  The kernel checks each entry's
+ *   range (one outside is skipped and sets FBM_DEVERR_LUT_RANGE) and the count
+ *   (one outside its range is clamped into it and sets FBM_DEVERR_LUT_RANGE).
+ *   The order is the caller's contract and is not checked here (a duplicate
+ *   entry would be counted twice): lut_validate checks it on request.
  *   lut == NULL (and lut_count == NULL) selects dense attention: every kv
- *   block (every causally visible one under causal).
+ *   block (under causal, every block up to the one holding the q block's last
+ *   visible key).
  * pv_threshold: +inf turns the PV skip off.  A finite value >= 0 (natural log
  *   units of the scaled scores) enables the per-Q-tile PV skip (README, 'Not
  *   yet ported': pv_threshold per-Q-tile skip): the listed kv blocks are
  *   visited in LUT order with an exact running max m per row, and a block
  *   whose scores lie below m - pv_threshold in every row of the q block
  *   (rows past s_q do not count) is left out of O's P.V sum while its
- *   probabilities stay in the denominator and in the LSE.  Whole rows on the
- *   d = 128 kernel only (num_splits == 1, out given); otherwise
- *   FBM_ERR_UNSUPPORTED.  NaN or a negative value: FBM_ERR_INVALID_ARG.
+ *   probabilities stay in the denominator and in the LSE.  Whole rows only
+ *   (num_splits == 1, out given); otherwise FBM_ERR_UNSUPPORTED.  NaN or a
+ *   negative value: FBM_ERR_INVALID_ARG.
  * num_splits == 1: out = device [b, hq, s_q, dv] in dtype; lse = device fp32
  *   [b, hq, s_q] or NULL (return_lse off); o_partial / lse_partial unused.
  * num_splits == 1 with out == NULL (partial mode): the whole row's normalised
@@ -210,9 +217,9 @@ fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int 
 fbm_status sparse_fmha_fwd(const void *q, const void *k, const void *v, int dtype, int b,
                            int hq, int hk, int s_q, int s_k, int d, int dv, int blkq, int blkk,
                            const int32_t *lut, const int32_t *lut_count, int lut_stride,
-                           int num_splits, float scale, int causal, float pv_threshold,
-                           void *out, float *lse, float *o_partial, float *lse_partial,
-                           void *stream);
+                           int num_splits, float scale, int causal, int key_offset,
+                           float pv_threshold, void *out, float *lse, float *o_partial,
+                           float *lse_partial, void *stream);
 
 /*
  * attn_combine - merge split-KV partials over disjoint key sets
@@ -297,6 +304,29 @@ fbm_status lut_shard(const int32_t *lut, const int32_t *lut_count, int64_t rows,
                      void *stream);
 
 /*
+ * lut_validate - check a LUT against the contract sparse_fmha_fwd relies on,
+ * without changing it: per row a count and that many strictly ascending
+ * kv-block indices (the sparse_block_table / sparse_num_blocks pair of
+ * "Incremental_FlashAttention updating_log.md", 'Design decisions (locked)',
+ * whose contract the caller guarantees and the kernels do not assert).
+ *
+ * For each row r < rows: lut_count[r] outside [0, min(nk, lut_stride)], or an
+ * entry of lut[r][0 .. min(lut_count[r], ...)) outside [0, nk), sets
+ * FBM_DEVERR_LUT_RANGE; an entry not above the entry before it (a duplicate or
+ * a descending entry) sets FBM_DEVERR_LUT_ORDER.  Read the bits with
+ * fbm_get_error.  The attention kernels check ranges and counts themselves
+ * but not the order, which would cost the hot loop a dependent read per kv
+ * block: call this where LUTs come from outside sparge_block_map, whose rows
+ * are valid by construction.
+ *
+ * lut: device int32 [rows, lut_stride]; lut_count: device int32 [rows];
+ * rows, lut_stride, nk > 0, else FBM_ERR_INVALID_ARG before any launch.
+ * Asynchronous on `stream`.
+ */
+fbm_status lut_validate(const int32_t *lut, const int32_t *lut_count, int64_t rows,
+                        int lut_stride, int nk, void *stream);
+
+/*
  * sparse_decode_fwd - sparse decode over per-query token index lists through a
  * page table (ROCm/aiter pull 4919: sparse MLA decode with split-KV partials).
  *
@@ -333,8 +363,8 @@ fbm_status sparse_decode_fwd(const void *q, const void *kv_cache, int dtype, int
 fbm_status fbm_selftest_wait_timeout(uint64_t limit_ns, void *stream);
 
 /* Which sparse-FMHA kernel sparse_fmha_fwd launches for these arguments:
- * 1 = tcgen05 / TMA kernel, 2 = mma.sync kernel, 0 = none (the arguments
- * would be rejected).  Host-only; launches nothing. */
+ * 1 = the tcgen05 / TMA kernel (every supported shape: d = dv in {64, 128}),
+ * 0 = none (the arguments would be rejected).  Host-only; launches nothing. */
 int fbm_fmha_kernel_kind(int dtype, int d, int dv, int num_splits, int s_q, int s_k);
 
 #ifdef __cplusplus

@@ -89,13 +89,13 @@ def test_block_map_rejects(L, kw, code):
 
 def _fm(L, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=1, b=1, hq=4, hk=2, s_q=256, s_k=256, d=128, dv=128,
-             blkq=64, blkk=64, lut=FAKE, cnt=FAKE, stride=4, S=1, scale=0.1, causal=0,
+             blkq=64, blkk=64, lut=FAKE, cnt=FAKE, stride=4, S=1, scale=0.1, causal=0, koff=0,
              pv=float("inf"), out=FAKE, lse=None, op=None, lp=None)
     a.update(kw)
     return L.sparse_fmha_fwd(a["q"], a["k"], a["v"], a["dtype"], a["b"], a["hq"], a["hk"],
                              a["s_q"], a["s_k"], a["d"], a["dv"], a["blkq"], a["blkk"],
                              a["lut"], a["cnt"], a["stride"], a["S"], a["scale"], a["causal"],
-                             a["pv"], a["out"], a["lse"], a["op"], a["lp"], None)
+                             a["koff"], a["pv"], a["out"], a["lse"], a["op"], a["lp"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -104,7 +104,7 @@ def _fm(L, **kw):
     (dict(hk=3), fbm.FBM_ERR_INVALID_ARG),
     (dict(d=96, dv=96), fbm.FBM_ERR_UNSUPPORTED),
     (dict(dv=64), fbm.FBM_ERR_UNSUPPORTED),
-    (dict(causal=1, s_k=512), fbm.FBM_ERR_UNSUPPORTED),
+    (dict(causal=1, koff=(1 << 30) + 1), fbm.FBM_ERR_INVALID_ARG),
     (dict(S=2), fbm.FBM_ERR_INVALID_ARG),      # split without partial buffers
     (dict(S=0), fbm.FBM_ERR_INVALID_ARG),
     (dict(out=None), fbm.FBM_ERR_INVALID_ARG),
@@ -115,7 +115,6 @@ def _fm(L, **kw):
     (dict(pv=-1.0), fbm.FBM_ERR_INVALID_ARG),
     (dict(pv=4.0, S=2, out=None, op=FAKE, lp=FAKE), fbm.FBM_ERR_UNSUPPORTED),   # split
     (dict(pv=4.0, out=None, op=FAKE, lp=FAKE), fbm.FBM_ERR_UNSUPPORTED),        # partial
-    (dict(pv=4.0, d=64, dv=64), fbm.FBM_ERR_UNSUPPORTED),                      # mma.sync
 ])
 def test_fmha_rejects(L, kw, code):
     assert _fm(L, **kw) == code
@@ -136,6 +135,13 @@ def test_combine_and_decode_reject(L):
     bad = list(args)
     bad[9] = None  # page table
     assert L.sparse_decode_fwd(*bad) == fbm.FBM_ERR_INVALID_ARG
+
+
+def test_lut_validate_rejects(L):
+    assert L.lut_validate(None, FAKE, 4, 8, 8, None) == fbm.FBM_ERR_INVALID_ARG
+    assert L.lut_validate(FAKE, FAKE, 0, 8, 8, None) == fbm.FBM_ERR_INVALID_ARG
+    assert L.lut_validate(FAKE, FAKE, 4, 0, 8, None) == fbm.FBM_ERR_INVALID_ARG
+    assert L.lut_validate(FAKE, FAKE, 4, 8, 0, None) == fbm.FBM_ERR_INVALID_ARG
 
 
 def test_lut_shard_rejects(L):
@@ -174,7 +180,7 @@ def test_partial_mode_needs_both_partial_buffers(L):
 
 def test_kernel_kind_is_host_only(L):
     assert L.fbm_fmha_kernel_kind(0, 96, 96, 1, 128, 128) == 0
-    assert L.fbm_fmha_kernel_kind(1, 64, 64, 2, 128, 128) == 2
+    assert L.fbm_fmha_kernel_kind(1, 64, 64, 2, 128, 128) == 1
     assert L.fbm_fmha_kernel_kind(1, 128, 128, 1, 16384, 16384) in (1, 2)
 
 

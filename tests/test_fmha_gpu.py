@@ -239,64 +239,73 @@ def test_out_of_range_entry_is_skipped_and_flagged(fbm_gpu):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_lut_validation_skips_and_flags(fbm_gpu, d):
-    """Every entry is checked on the device: a duplicate or a descending entry
-    is skipped with FBM_DEVERR_LUT_ORDER, a count above min(nk, stride) is
-    clamped with FBM_DEVERR_LUT_RANGE, a negative count gives an empty row.
-    The result equals the oracle over the usable entries."""
+def test_count_out_of_range_is_clamped_and_flagged(fbm_gpu, d):
+    """A count above min(nk, stride) is clamped to it and a negative count
+    gives an empty row, each with FBM_DEVERR_LUT_RANGE; the result equals the
+    oracle over the clamped rows."""
     cfg = synth.C1.replace(b=1, hq=4, hk=2, s=512, d=d, dtype="f16")
     nq = cfg.nq
     x, (q, k, v) = prefill_on_gpu(cfg)
-
-    def run(lut, cnt):
-        out, lse = fbm_gpu.sparse_fmha_fwd(q, k, v, torch.from_numpy(lut).cuda(),
-                                           torch.from_numpy(cnt).cuda(), scale=cfg.scale,
-                                           return_lse=True)
-        return fbm_gpu.get_error(), out.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64)
-
-    def expect(o_np, l_np, good, good_cnt):
-        res = oracle.sparse_fmha(x["q"], x["k"], x["v"], good, good_cnt, cfg.scale, False,
-                                 dtype="f16")
-        for (b, h, i), (o_ref, l_ref) in res.items():
-            assert_close_o(o_np[b, h, i * 64:(i + 1) * 64], o_ref)
-            assert_close_lse(l_np[b, h, i * 64:(i + 1) * 64], l_ref)
-
-    base = np.full((1, 4, nq, nq), -1, dtype=np.int32)
-    # duplicates and descending entries
-    lut, cnt = base.copy(), np.zeros((1, 4, nq), dtype=np.int32)
-    good, gcnt = base.copy(), np.zeros_like(cnt)
-    rows = {0: ([1, 1, 3], [1, 3]), 1: ([5, 2], [5]), 2: ([0, 4, 4, 4, 6], [0, 4, 6]),
-            3: ([2, 7, 3, 1], [2, 7])}
-    for h, (row, ok) in rows.items():
-        for i in range(nq):
-            lut[0, h, i, :len(row)] = row
-            cnt[0, h, i] = len(row)
-            good[0, h, i, :len(ok)] = ok
-            gcnt[0, h, i] = len(ok)
-    bits, o_np, l_np = run(lut, cnt)
-    assert bits == fbm_gpu.FBM_DEVERR_LUT_ORDER
-    expect(o_np, l_np, good, gcnt)
-    # counts out of range: above nk (clamped to nk) and negative (empty row)
     lut = np.tile(np.arange(nq, dtype=np.int32), (1, 4, nq, 1))
     cnt = np.full((1, 4, nq), nq, dtype=np.int32)
     cnt[0, 1] = nq + 5
     cnt[0, 2] = -3
-    bits, o_np, l_np = run(lut, cnt)
-    assert bits == fbm_gpu.FBM_DEVERR_LUT_RANGE
-    gcnt = cnt.copy()
-    gcnt[0, 1] = nq
-    gcnt[0, 2] = 0
-    expect(o_np, l_np, lut, gcnt)
+    out, lse = fbm_gpu.sparse_fmha_fwd(q, k, v, torch.from_numpy(lut).cuda(),
+                                       torch.from_numpy(cnt).cuda(), scale=cfg.scale,
+                                       return_lse=True)
+    assert fbm_gpu.get_error() == fbm_gpu.FBM_DEVERR_LUT_RANGE
+    o_np, l_np = out.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64)
+    good = cnt.copy()
+    good[0, 1] = nq
+    good[0, 2] = 0
+    res = oracle.sparse_fmha(x["q"], x["k"], x["v"], lut, good, cfg.scale, False, dtype="f16")
+    for (b, h, i), (o_ref, l_ref) in res.items():
+        assert_close_o(o_np[b, h, i * 64:(i + 1) * 64], o_ref)
+        assert_close_lse(l_np[b, h, i * 64:(i + 1) * 64], l_ref)
     assert (o_np[0, 2] == 0).all() and np.isneginf(l_np[0, 2]).all()
     assert fbm_gpu.get_error() == 0
 
 
-def test_d128_runs_on_the_tcgen05_kernel(fbm_gpu):
-    """The hot shape must not fall back to the mma.sync kernel."""
+def test_lut_validate_finds_order_range_and_count_errors(fbm_gpu):
+    """lut_validate checks the sparse block table contract without changing
+    the LUT: duplicates and descending entries set FBM_DEVERR_LUT_ORDER,
+    entries outside [0, nk) and counts outside [0, min(nk, stride)] set
+    FBM_DEVERR_LUT_RANGE; the block map's own LUT at the headline shape is
+    valid."""
+    nk = 12
+    R, O = fbm_gpu.FBM_DEVERR_LUT_RANGE, fbm_gpu.FBM_DEVERR_LUT_ORDER
+    cases = [  # (row, count, expected bits)
+        ([0, 3, 7, 11], 4, 0), ([], 0, 0), (list(range(nk)), nk, 0),
+        ([1, 1, 3], 3, O), ([5, 2], 2, O), ([0, 4, 4, 9], 4, O),
+        ([0, nk], 2, R), ([-1, 2], 2, R), (list(range(nk)), nk + 1, R), ([0, 1], -2, R),
+        ([3, 2, nk + 4], 3, R | O),
+        # a long row whose only fault (index 32 not above index 31) straddles
+        # the 32-entry chunk boundary
+        (list(range(32)) + [31, 40], 34, O),
+    ]
+    for row, count, want in cases:
+        stride = max(nk, len(row), 40)
+        lut = torch.full((2, stride), -1, dtype=torch.int32)
+        lut[1, :len(row)] = torch.tensor(row, dtype=torch.int32)
+        lut[0, :3] = torch.tensor([0, 1, 2], dtype=torch.int32)
+        cnt = torch.tensor([3, count], dtype=torch.int32)
+        lut_d, cnt_d = lut.cuda(), cnt.cuda()
+        nk_case = 41 if len(row) > nk + 2 else nk
+        bits = fbm_gpu.lut_validate(lut_d, cnt_d, nk_case)
+        assert bits == want, (row, count, bits)
+        assert torch.equal(lut_d.cpu(), lut) and torch.equal(cnt_d.cpu(), cnt)
+    cfg = synth.C3
+    x, (q, k, v) = prefill_on_gpu(cfg)
+    lut, cnt, _ = fbm_gpu.sparge_block_map(q, k, topk=0.4, scale=cfg.scale)
+    assert fbm_gpu.lut_validate(lut, cnt, cfg.nq) == 0
+
+
+def test_every_shape_runs_on_the_tcgen05_kernel(fbm_gpu):
+    """Every supported shape runs the tcgen05 kernel (d = 64 and 128)."""
     for dt in (torch.float16, torch.bfloat16):
         assert fbm_gpu.fmha_kernel_kind(dt, 128, 128, 1, 16384, 16384) == 1
         assert fbm_gpu.fmha_kernel_kind(dt, 128, 128, 1, 1000, 1000) == 1
-    assert fbm_gpu.fmha_kernel_kind(torch.float16, 64, 64, 1, 512, 512) == 2
+    assert fbm_gpu.fmha_kernel_kind(torch.float16, 64, 64, 1, 512, 512) == 1
     assert fbm_gpu.fmha_kernel_kind(torch.float16, 128, 128, 4, 512, 512) == 1
 
 
@@ -335,9 +344,9 @@ def _pv_case(fbm, cfg, tau, lut, cnt):
     return skipped, changed
 
 
-@pytest.mark.parametrize("tau", [0.5, 2.0, 6.0])
-def test_pv_skip_full_rows_ragged(fbm_gpu, tau):
-    cfg = synth.C1.replace(hq=2, hk=1, s=1000, d=128, dtype="f16")
+@pytest.mark.parametrize("tau,d", [(0.5, 128), (2.0, 128), (6.0, 128), (0.5, 64), (2.0, 64)])
+def test_pv_skip_full_rows_ragged(fbm_gpu, tau, d):
+    cfg = synth.C1.replace(hq=2, hk=1, s=1000, d=d, dtype="f16")
     nq = cfg.nq
     lut = np.tile(np.arange(nq, dtype=np.int32), (1, 2, nq, 1))
     cnt = np.full((1, 2, nq), nq, dtype=np.int32)

@@ -114,3 +114,59 @@ def test_context_parallel_exchange_on_gloo_ranks(tmp_path, world):
         assert (g[4:] < 1e-10).all()
     with pytest.raises(ValueError):
         cp.kv_shard_bounds(2, 3)
+
+
+def _rs_worker(rank, world, port, out_dir):
+    """Causal context parallelism with the reduce-scatter exchange, on CPU:
+    the oracle stands in for this rank's GPU partial (keys of its kv range,
+    causal key offset -lo * 64) over every row; scatter_partials_to_owners
+    hands each rank the partials of the rows it owns, which it combines."""
+    import sys
+
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    from fmha_block_map_gb300 import cp
+
+    rng = np.random.default_rng(11)
+    s, nb = 1000, 16
+    q, k = rng.standard_normal((s, 32)), rng.standard_normal((s, 32))
+    v = rng.standard_normal((s, 16))
+    # a causal LUT: for q block i, a seeded subset of blocks <= i with the diagonal
+    luts = [sorted(set(rng.choice(i + 1, size=max(1, (i + 1) // 3), replace=False).tolist())
+                   | {i}) for i in range(nb)]
+    lo, hi = cp.kv_shard_bounds(nb, world)[rank]
+    r0, r1 = cp.shard_rows(s, lo, hi)
+    o = np.zeros((s, 16))
+    l = np.zeros(s)
+    for i in range(nb):
+        rows = slice(i * 64, min((i + 1) * 64, s))
+        o[rows], l[rows] = oracle.attention_unit(q, k[r0:r1], v[r0:r1],
+                                                 oracle.shard_lut_row(luts[i], lo, hi), i, 64,
+                                                 64, 0.3, True, key_offset=-lo * 64)
+    o_all, l_all, (a, b) = cp.scatter_partials_to_owners(torch.from_numpy(o),
+                                                         torch.from_numpy(l))
+    got_o, got_l = oracle.combine(o_all.numpy(), l_all.numpy())
+    ref_o = np.zeros((s, 16))
+    ref_l = np.zeros(s)
+    for i in range(nb):
+        rows = slice(i * 64, min((i + 1) * 64, s))
+        ref_o[rows], ref_l[rows] = oracle.attention_unit(q, k, v, luts[i], i, 64, 64, 0.3, True)
+    err = max(np.abs(got_o - ref_o[a:b]).max(), np.abs(got_l - ref_l[a:b]).max())
+    np.save(os.path.join(out_dir, f"rs{rank}.npy"), np.array([a, b, o_all.shape[0], err]))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_causal_context_parallel_reduce_scatter_on_gloo_ranks(tmp_path, world):
+    mp.start_processes(_rs_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       start_method="spawn", join=True)
+    got = [np.load(tmp_path / f"rs{r}.npy") for r in range(world)]
+    from fmha_block_map_gb300 import cp
+
+    # the owners' rows tile [0, s) in rank order; each rank combined only its own
+    assert [(int(g[0]), int(g[1])) for g in got] == cp.row_owner_bounds(1000, world)
+    for g in got:
+        assert int(g[2]) == world and g[3] < 1e-10
