@@ -57,6 +57,9 @@ def lib() -> ctypes.CDLL:
         L.attn_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
         L.lut_shard.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp]
         L.lut_validate.argtypes = [vp, vp, i64, i32, i32, vp]
+        L.lut_pair_union.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp]
+        L.sparse_fmha_fwd_pairs.argtypes = ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                             vp, vp, i32, f32, i32, i32, vp, vp, vp])
         L.quantize_e4m3_blocks.argtypes = [vp, i32, i64, i32, i32, vp, vp, vp]
         L.sparse_fmha_fwd_fp8.argtypes = ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                            i32, vp, vp, i32, f32, i32, vp, vp, vp])
@@ -68,6 +71,7 @@ def lib() -> ctypes.CDLL:
         L.fbm_fmha_kernel_kind.restype = i32
         for name in ("fbm_get_error", "sparge_block_map", "sparge_block_map_static",
                      "sparse_fmha_fwd", "attn_combine", "lut_shard", "lut_validate",
+                     "lut_pair_union", "sparse_fmha_fwd_pairs",
                      "sparse_decode_fwd",
                      "quantize_e4m3_blocks", "sparse_fmha_fwd_fp8"):
             getattr(L, name).restype = i32
@@ -360,6 +364,62 @@ def lut_validate(lut: torch.Tensor, lut_count: torch.Tensor, nk: int, *, stream=
     _check(lib().lut_validate(_ptr(lut), _ptr(lut_count), lut_count.numel(), lut.shape[-1], nk,
                               _stream(stream)))
     return get_error(stream)
+
+
+def lut_pair_union(lut: torch.Tensor, lut_count: torch.Tensor, nk: int, *,
+                   pair_lut: Optional[torch.Tensor] = None,
+                   pair_count: Optional[torch.Tensor] = None, stream=None):
+    """lut [b, hq, nq, stride] / lut_count [b, hq, nq] -> (pair_lut [b, hq,
+    ceil(nq / 2), nk], pair_count [b, hq, ceil(nq / 2)]): the union of the
+    LUT rows of q blocks 2p and 2p + 1, ascending, each entry
+    j | (in row 2p) << 29 | (in row 2p + 1) << 30."""
+    _cuda(lut, "lut"), _cuda(lut_count, "lut_count")
+    if lut.dtype != torch.int32 or lut_count.dtype != torch.int32:
+        raise TypeError("lut / lut_count must be int32")
+    *lead, nq, stride = lut.shape
+    bh = 1
+    for n in lead:
+        bh *= n
+    npq = (nq + 1) // 2
+    if pair_lut is None:
+        pair_lut = torch.empty(tuple(lead) + (npq, nk), dtype=torch.int32, device=lut.device)
+    if pair_count is None:
+        pair_count = torch.empty(tuple(lead) + (npq,), dtype=torch.int32, device=lut.device)
+    _check(lib().lut_pair_union(_ptr(lut), _ptr(lut_count), bh, nq, stride, nk, _ptr(pair_lut),
+                                _ptr(pair_count), pair_lut.shape[-1], _stream(stream)))
+    return pair_lut, pair_count
+
+
+def sparse_fmha_fwd_pairs(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                          pair_lut: Optional[torch.Tensor], pair_count: Optional[torch.Tensor], *,
+                          scale: Optional[float] = None, causal: bool = False,
+                          key_offset: int = 0, return_lse: bool = False,
+                          out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                          stream=None):
+    """sparse_fmha_fwd (whole rows) on 128-row tiles of q-block pairs:
+    pair_lut / pair_count from lut_pair_union (None: dense).  Returns
+    (out, lse or None)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _cuda(t, n)
+    b, hq, s_q, d = q.shape
+    hk, s_k, dv = k.shape[1], k.shape[2], v.shape[3]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    stride = 0
+    if pair_lut is not None:
+        _cuda(pair_lut, "pair_lut"), _cuda(pair_count, "pair_count")
+        if pair_lut.dtype != torch.int32 or pair_count.dtype != torch.int32:
+            raise TypeError("pair_lut / pair_count must be int32")
+        stride = pair_lut.shape[-1]
+    if out is None:
+        out = torch.empty((b, hq, s_q, dv), dtype=q.dtype, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty((b, hq, s_q), dtype=torch.float32, device=q.device)
+    _check(lib().sparse_fmha_fwd_pairs(
+        _ptr(q), _ptr(k), _ptr(v), _dt(q), b, hq, hk, s_q, s_k, d, dv, _ptr(pair_lut),
+        _ptr(pair_count), stride, float(scale), int(causal), int(key_offset), _ptr(out),
+        _ptr(lse), _stream(stream)))
+    return out, lse
 
 
 def sparse_decode_fwd(q: torch.Tensor, kv_cache: torch.Tensor, page_table: torch.Tensor,

@@ -353,6 +353,69 @@ fbm_status lut_validate(const int32_t *lut, const int32_t *lut_count, int64_t ro
                      "lut_validate launch");
 }
 
+fbm_status lut_pair_union(const int32_t *lut, const int32_t *lut_count, int64_t bh, int nq,
+                          int lut_stride, int nk, int32_t *pair_lut, int32_t *pair_count,
+                          int pair_stride, void *stream) {
+  if (!lut || !lut_count || !pair_lut || !pair_count)
+    return fail(FBM_ERR_INVALID_ARG, "lut_pair_union: null pointer");
+  if (bh <= 0 || nq <= 0 || lut_stride < 1 || nk < 1)
+    return fail(FBM_ERR_INVALID_ARG, "lut_pair_union: bh, nq, lut_stride and nk must be positive");
+  if (nk > 1024) return fail(FBM_ERR_UNSUPPORTED, "lut_pair_union: nk <= 1024");
+  if (pair_stride < nk)
+    return fail(FBM_ERR_INVALID_ARG, "lut_pair_union: pair_stride (%d) < nk (%d)", pair_stride, nk);
+  if (bh * ((nq + 1) / 2) > (int64_t)0x7fffffff * 8)
+    return fail(FBM_ERR_UNSUPPORTED, "lut_pair_union: too many rows");
+  fbm::PairUnionLaunch L{lut, lut_count, bh, nq, lut_stride, nk, pair_stride, pair_lut, pair_count,
+                         error_word()};
+  if (!L.err) return fail(FBM_ERR_CUDA, "lut_pair_union: error word lookup failed");
+  return cuda_status(fbm::launch_lut_pair_union(L, static_cast<cudaStream_t>(stream)),
+                     "lut_pair_union launch");
+}
+
+fbm_status sparse_fmha_fwd_pairs(const void *q, const void *k, const void *v, int dtype, int b,
+                                 int hq, int hk, int s_q, int s_k, int d, int dv,
+                                 const int32_t *pair_lut, const int32_t *pair_count,
+                                 int pair_stride, float scale, int causal, int key_offset,
+                                 void *out, float *lse, void *stream) {
+  if (!q || !k || !v || !out)
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_pairs: null q / k / v / out");
+  if ((pair_lut == nullptr) != (pair_count == nullptr))
+    return fail(FBM_ERR_INVALID_ARG,
+                "sparse_fmha_fwd_pairs: pair_lut and pair_count must both be set or both NULL");
+  if (b <= 0 || hq <= 0 || hk <= 0 || s_q <= 0 || s_k <= 0 || d <= 0 || dv <= 0)
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_pairs: sizes must be positive");
+  if (hq % hk != 0) return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_pairs: hq %% hk != 0");
+  if (dtype != FBM_F16 && dtype != FBM_BF16)
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_pairs: dtype must be f16 or bf16");
+  if (d != dv || (d != 64 && d != 128))
+    return fail(FBM_ERR_UNSUPPORTED, "sparse_fmha_fwd_pairs: d = dv in {64, 128}");
+  const int nq = (s_q + 63) / 64, nk = (s_k + 63) / 64;
+  if (pair_lut && pair_stride < 1)
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_pairs: pair_stride must be >= 1");
+  if (nk > (1 << 29)) return fail(FBM_ERR_UNSUPPORTED, "sparse_fmha_fwd_pairs: too many kv blocks");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_pairs: scale must be positive and finite");
+  if (causal && (key_offset < -(1 << 30) || key_offset > (1 << 30)))
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_pairs: |key_offset| must be at most 2^30");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(FBM_ERR_INVALID_ARG, "sparse_fmha_fwd_pairs: tensors must be 16-byte aligned");
+  if ((long long)b * hq * ((nq + 1) / 2) > 0x7fffffffLL)
+    return fail(FBM_ERR_UNSUPPORTED, "sparse_fmha_fwd_pairs: grid too large");
+  fbm::FmhaLaunch L{};
+  L.q = q; L.k = k; L.v = v;
+  L.bf16 = dtype == FBM_BF16;
+  L.b = b; L.hq = hq; L.hk = hk; L.s_q = s_q; L.s_k = s_k; L.d = d; L.nq = nq; L.nk = nk;
+  L.lut = pair_lut; L.cnt = pair_count; L.lut_stride = pair_lut ? pair_stride : nk;
+  L.num_splits = 1; L.causal = causal != 0; L.scale = scale;
+  L.key_offset = causal ? key_offset : 0;
+  L.pv_threshold = INFINITY;
+  L.out = out; L.lse = lse;
+  L.err = error_word();
+  if (!L.err) return fail(FBM_ERR_CUDA, "sparse_fmha_fwd_pairs: error word lookup failed");
+  return cuda_status(fbm::launch_fmha_pair(L, static_cast<cudaStream_t>(stream)),
+                     "sparse_fmha_fwd_pairs launch");
+}
+
 fbm_status sparse_decode_fwd(const void *q, const void *kv_cache, int dtype, int n_q, int hq,
                              int d, int dv, int page_size, int64_t n_pages,
                              const int32_t *page_table, int pages_per_query,

@@ -742,6 +742,9 @@ cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() { return get_encode(); }
+int device_sm_count() { return sm_count(); }
+
 bool fmha_tc_supported(int d, int dv, int num_splits, int s_q, int s_k) {
   return (d == 64 || d == 128) && dv == d && num_splits >= 1 && s_q > 0 && s_k > 0;
 }

@@ -90,6 +90,17 @@ struct LutValidateLaunch {
 };
 cudaError_t launch_lut_validate(const LutValidateLaunch &L, cudaStream_t st);
 
+struct PairUnionLaunch {
+  const int32_t *lut, *cnt;  // [bh, nq, lut_stride], [bh, nq]
+  int64_t bh;
+  int nq, lut_stride, nk, out_stride;
+  int32_t *out_lut, *out_cnt;  // [bh, ceil(nq / 2), out_stride], [bh, ceil(nq / 2)]
+  uint32_t *err;
+};
+cudaError_t launch_lut_pair_union(const PairUnionLaunch &L, cudaStream_t st);
+// the 128-row (q-block pair) attention kernel: whole rows, dtype output
+cudaError_t launch_fmha_pair(const FmhaLaunch &L, cudaStream_t st);
+
 struct DecodeLaunch {
   const void *q, *cache;
   int bf16, n_q, hq, d, dv, page;

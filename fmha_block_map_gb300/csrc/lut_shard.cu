@@ -103,3 +103,84 @@ cudaError_t launch_lut_validate(const LutValidateLaunch &L, cudaStream_t st) {
 }
 
 }  // namespace fbm
+
+// ---------------------------------------------------------------------------
+// q-block pair union
+// ---------------------------------------------------------------------------
+//
+// For the 128-row attention kernel: q blocks 2p and 2p + 1 of a (batch, head)
+// share one 128-row tile, which visits the union of their LUT rows.  One warp
+// per pair builds the union as a bitmask in shared memory (lane L owns the 32
+// kv blocks 32 L .. 32 L + 31), so the output is ascending and duplicate-free
+// whatever the input order, and emits every member j as
+// j | (in row 2p) << 29 | (in row 2p + 1) << 30, -1 padded, with the count.
+// Entries outside [0, nk) and counts outside [0, min(nk, lut_stride)] are
+// skipped (clamped) and set FBM_DEVERR_LUT_RANGE.
+
+namespace fbm {
+namespace {
+
+__global__ void __launch_bounds__(256) k_lut_pair_union(const PairUnionLaunch L) {
+  __shared__ uint32_t masks[8][2][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int npq = (L.nq + 1) / 2;
+  const int64_t unit = (int64_t)blockIdx.x * 8 + w;  // (bh, pair)
+  if (unit >= L.bh * npq) return;
+  const int64_t bh = unit / npq;
+  const int p = (int)(unit - bh * npq);
+  uint32_t *mA = masks[w][0], *mB = masks[w][1];
+  mA[lane] = 0u;
+  mB[lane] = 0u;
+  __syncwarp();
+  uint32_t bits = 0;
+  const int lim = min(L.nk, L.lut_stride);
+  for (int half = 0; half < 2; ++half) {
+    const int i = 2 * p + half;
+    if (i >= L.nq) break;
+    const int64_t row = bh * L.nq + i;
+    const int raw = L.cnt[row];
+    if (raw < 0 || raw > lim) bits |= FBM_DEVERR_LUT_RANGE;
+    const int n = min(max(raw, 0), lim);
+    const int32_t *src = L.lut + row * L.lut_stride;
+    uint32_t *m = half ? mB : mA;
+    for (int t = lane; t < n; t += 32) {
+      const int j = __ldg(src + t);
+      if (j < 0 || j >= L.nk) {
+        bits |= FBM_DEVERR_LUT_RANGE;
+        continue;
+      }
+      atomicOr(m + (j >> 5), 1u << (j & 31));
+    }
+  }
+  __syncwarp();
+  const uint32_t a = mA[lane], b = mB[lane], u = a | b;
+  const int mine = __popc(u);
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int up = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += up;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  int32_t *dst = L.out_lut + unit * L.out_stride;
+  int pos = incl - mine;
+  for (uint32_t rest = u; rest; rest &= rest - 1u) {
+    const int bit = __ffs(rest) - 1;
+    const int j = 32 * lane + bit;
+    dst[pos++] = j | (int)(((a >> bit) & 1u) << 29) | (int)(((b >> bit) & 1u) << 30);
+  }
+  for (int t = total + lane; t < L.out_stride; t += 32) dst[t] = -1;
+  if (lane == 0) L.out_cnt[unit] = total;
+  bits = __reduce_or_sync(0xffffffffu, bits);
+  if (lane == 0 && bits) atomicOr(L.err, bits);
+}
+
+}  // namespace
+
+cudaError_t launch_lut_pair_union(const PairUnionLaunch &L, cudaStream_t st) {
+  const int64_t units = L.bh * ((L.nq + 1) / 2);
+  k_lut_pair_union<<<(unsigned)((units + 7) / 8), 256, 0, st>>>(L);
+  return cudaGetLastError();
+}
+
+}  // namespace fbm

@@ -327,6 +327,56 @@ fbm_status lut_validate(const int32_t *lut, const int32_t *lut_count, int64_t ro
                         int lut_stride, int nk, void *stream);
 
 /*
+ * lut_pair_union - the LUT rows of q blocks 2p and 2p + 1 merged into one
+ * row, for sparse_fmha_fwd_pairs.  Not a step of the pages' method: it
+ * re-lays the block table ("Sparge Attention (Composable Kernel)" README: the
+ * per-q-block kv-block LUT) so that two q blocks can share 128-row tensor-core
+ * tiles.
+ *
+ * For each (bh < bh, p < ceil(nq / 2)): the union of the entries of
+ * lut[bh][2p][0 .. lut_count[bh][2p]) and lut[bh][2p + 1][...] (the second
+ * row absent when 2p + 1 == nq), ascending and without duplicates, each
+ * written as j | (j in row 2p) << 29 | (j in row 2p + 1) << 30 to
+ * pair_lut[bh][p][0 .. pair_count[bh][p]), -1 padded.  Entries outside
+ * [0, nk) are skipped and counts outside [0, min(nk, lut_stride)] clamped,
+ * each setting FBM_DEVERR_LUT_RANGE.
+ *
+ * lut: device int32 [bh, nq, lut_stride]; lut_count: device int32 [bh, nq];
+ * pair_lut: device int32 [bh, ceil(nq / 2), pair_stride], pair_stride >= nk;
+ * pair_count: device int32 [bh, ceil(nq / 2)].  nk <= 1024.  Invalid
+ * arguments return FBM_ERR_INVALID_ARG / FBM_ERR_UNSUPPORTED before any
+ * launch.  Asynchronous on `stream`.
+ */
+fbm_status lut_pair_union(const int32_t *lut, const int32_t *lut_count, int64_t bh, int nq,
+                          int lut_stride, int nk, int32_t *pair_lut, int32_t *pair_count,
+                          int pair_stride, void *stream);
+
+/*
+ * sparse_fmha_fwd_pairs - sparse_fmha_fwd (whole rows, dtype output) on
+ * 128-row tiles.  The result is that of sparse_fmha_fwd with the LUT the
+ * pairs were built from: each query row attends over its own q block's LUT
+ * row ("Sparge Attention (Composable Kernel)" README, the sparse FMHA stage),
+ * with the same causal rule and key_offset, O and LSE conventions and empty
+ * rows.  Rows 128 p .. 128 p + 127 (q blocks 2p and 2p + 1) share one tile
+ * that visits the union of the two LUT rows (pair_lut from lut_pair_union;
+ * each row masks the union members that are not its own), so every tensor-
+ * core MMA spans 128 query rows: |A u B| 128-row tiles instead of |A| + |B|
+ * 64-row ones.  pair_lut == NULL (with pair_count == NULL) is dense attention.
+ *
+ * q / k / v / out / lse / dtype / d / scale / causal / key_offset as in
+ * sparse_fmha_fwd (d = dv in {64, 128}); pair_lut: device int32
+ * [b, hq, ceil(nq / 2), pair_stride] and pair_count [b, hq, ceil(nq / 2)]
+ * with entries as lut_pair_union writes them (a range error is skipped and
+ * flagged as in sparse_fmha_fwd).  Argument errors return before any launch.
+ * Asynchronous on `stream`.
+ */
+fbm_status sparse_fmha_fwd_pairs(const void *q, const void *k, const void *v, int dtype, int b,
+                                 int hq, int hk, int s_q, int s_k, int d, int dv,
+                                 const int32_t *pair_lut, const int32_t *pair_count,
+                                 int pair_stride, float scale, int causal, int key_offset,
+                                 void *out, float *lse, void *stream);
+
+/*
  * sparse_decode_fwd - sparse decode over per-query token index lists through a
  * page table (ROCm/aiter pull 4919: sparse MLA decode with split-KV partials).
  *
