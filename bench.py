@@ -8,9 +8,11 @@ sparse_fmha_fwd over the selected tiles.  Inputs (Q, K, V: 805 MB) are larger
 than the 129 MB L2, so no flush is needed between steps.
 
 Metric: effective TFLOP/s = (selected tiles x 4 * 64 * 64 * d) / step time,
-plus the speedup over this library's own dense FMHA (the same kernel with no
-LUT) at the same shape.  `--topk` picks the step's topk (default 0.4); the
-sweep over {0.1, 0.2, 0.4, 0.6, 1.0} is reported alongside.
+plus the speedup over this library's own dense FMHA (no LUT, the 128-row
+tile kernel: the fastest dense attention this library has) at the same shape.  `--topk` picks the step's topk
+(default 0.4); the sweep over {0.1, 0.2, 0.4, 0.6, 1.0} is reported alongside,
+with the q-block pair path (lut_pair_union + sparse_fmha_fwd_pairs) next to
+the 64-row kernel the step uses.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs its own batch on its own GPU (no
@@ -40,7 +42,7 @@ TOPKS = (0.1, 0.2, 0.4, 0.6, 1.0)
 # headline workload, from one ncu capture, keyed by the sha256 prefix of the
 # kernel source the capture ran; a kernel edited since reports traffic = null.
 NCU_TRAFFIC = {
-    "43ae43e463ccc9fa": 1070770944,  # 814.14 MB read + 256.63 MB written
+    "0e10ad89e7b58dbd": 1070075648,  # 813.94 MB read + 256.14 MB written
 }
 
 
@@ -58,7 +60,14 @@ def parse():
                    help="skip the causal-GQA prefill and sparse-decode measurements")
     p.add_argument("--decode-only", action="store_true",
                    help="only the sparse-decode measurement (a small command for profiling it)")
-    return p.parse_args()
+    p.add_argument("--small", action="store_true",
+                   help="b1 h16 s16384 d128 (Q, K, V 201 MB: still larger than L2) with every "
+                        "leg but the step, the dense runs and the pair path off: a small case "
+                        "of the same kernels for profiler captures, not a bench number")
+    args = p.parse_args()
+    if args.small:
+        args.no_sweep = args.no_e2e = args.no_cpu = args.no_extra = True
+    return args
 
 
 def dist_env():
@@ -177,6 +186,8 @@ def run_ours(args):
     fbuild.build()
     fbm.lib()
     cfg = rank_config(synth.C3.replace(topk=args.topk), rank)
+    if args.small:
+        cfg = cfg.replace(b=1, hq=16, hk=16)
     x = synth.prefill(cfg)
     dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.float16).cuda()
     q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
@@ -202,6 +213,16 @@ def run_ours(args):
     def attn(dense=False):
         fbm.sparse_fmha_fwd(q, k, v, None if dense else lut, None if dense else cnt,
                             scale=cfg.scale, out=out)
+
+    # 128-row tiles over q-block pairs: the dense attention of this library at
+    # full tensor-core rate (the speedup denominator), and the sparse pair path
+    npq = (nq + 1) // 2
+    plut = torch.empty((cfg.b, cfg.hq, npq, nq), dtype=torch.int32, device="cuda")
+    pcnt = torch.empty((cfg.b, cfg.hq, npq), dtype=torch.int32, device="cuda")
+
+    def attn_pairs(dense=False):
+        fbm.sparse_fmha_fwd_pairs(q, k, v, None if dense else plut, None if dense else pcnt,
+                                  scale=cfg.scale, out=out)
 
     def timed(fn, steps, warm):
         for _ in range(warm):
@@ -262,21 +283,35 @@ def run_ours(args):
     # ---- the block map with K smoothing (one more K read), dense FMHA, topk sweep
     smooth_ms = timed(lambda: block_map(args.topk, smooth_k=True), 5, 1)
     block_map(args.topk)
-    dense_ms = timed(lambda: attn(dense=True), max(2, args.steps // 10), 1)
+    dense64_ms = timed(lambda: attn(dense=True), max(2, args.steps // 10), 1)
+    dense_ms = timed(lambda: attn_pairs(dense=True), max(2, args.steps // 10), 1)
+    if args.small:
+        # one sparse launch of the pair path at the step's topk, for profiler captures
+        fbm.lut_pair_union(lut, cnt, nq, pair_lut=plut, pair_count=pcnt)
+        attn_pairs()
     sweep = []
     if not args.no_sweep:
         for tk in TOPKS:
             block_map(tk)
+            fbm.lut_pair_union(lut, cnt, nq, pair_lut=plut, pair_count=pcnt)
             torch.cuda.synchronize()
             tl = int(cnt.sum().item())
+            ul = int(pcnt.sum().item())
             bm = timed(lambda: block_map(tk), 5, 1)
             a = timed(lambda: attn(), max(2, args.steps // 10), 1)
+            un = timed(lambda: fbm.lut_pair_union(lut, cnt, nq, pair_lut=plut, pair_count=pcnt),
+                       5, 1)
+            ap = timed(lambda: attn_pairs(), max(2, args.steps // 10), 1)
             sweep.append({"topk": tk, "selected_tiles": tl, "block_map_ms": round(bm, 4),
                           "attn_ms": round(a, 4),
                           "eff_tflops_attn": round(tl * FLOP_PER_TILE / (a * 1e-3) / 1e12, 1),
                           "eff_tflops_step": round(tl * FLOP_PER_TILE / ((a + bm) * 1e-3) / 1e12, 1),
                           "speedup_vs_dense_attn": round(dense_ms / a, 3),
-                          "speedup_vs_dense_step": round(dense_ms / (a + bm), 3)})
+                          "speedup_vs_dense_step": round(dense_ms / (a + bm), 3),
+                          # q-block pairs: (|A| + |B|) / |A u B| over adjacent q blocks
+                          "pair_union_gain": round(tl / ul, 3) if ul else None,
+                          "pairs_attn_ms": round(ap, 4), "pair_union_ms": round(un, 4),
+                          "pairs_eff_tflops_attn": round(tl * FLOP_PER_TILE / (ap * 1e-3) / 1e12, 1)})
         block_map(args.topk)
 
     # ---- context parallelism over kv-block ranges, two ranks emulated one after
@@ -425,11 +460,16 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded centroid-plus-noise blocks, 25% diffuse)",
-        "config": {"workload": "b2 h32 s16384 d128 fp16 non-causal, BLKQ=BLKK=64, "
-                               f"topk={args.topk}, simthreshd1=0.001",
-                   "b": 2, "h": 32, "s": 16384, "d": 128, "topk": args.topk,
-                   "l2": "inputs (805 MB) larger than L2; no flush"},
+        "config": {"workload": f"b{cfg.b} h{cfg.hq} s{cfg.s} d{cfg.d} fp16 non-causal, "
+                               f"BLKQ=BLKK=64, topk={args.topk}, simthreshd1=0.001"
+                               + (" (small profiling case)" if args.small else ""),
+                   "b": cfg.b, "h": cfg.hq, "s": cfg.s, "d": cfg.d, "topk": args.topk,
+                   "l2": f"inputs ({3 * q.numel() * 2 / 1e6:.0f} MB) larger than L2; no flush"},
         "speedup_vs_dense": {"dense_attn_ms": round(dense_ms, 4),
+                             "dense_kernel": "sparse_fmha_fwd_pairs, no LUT (128-row tiles)",
+                             "dense_eff_tflops": round(4 * cfg.b * cfg.hq * cfg.s * cfg.s * cfg.d
+                                                       / (dense_ms * 1e-3) / 1e12, 1),
+                             "dense_64row_attn_ms": round(dense64_ms, 4),
                              "vs_attn": round(dense_ms / at_ms, 3),
                              "vs_step": round(dense_ms / step_ms, 3)},
         "block_map": {"ms": round(bm_ms, 4), "algorithmic_bytes": bm_bytes,

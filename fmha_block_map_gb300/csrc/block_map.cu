@@ -13,11 +13,8 @@
 //                 summation order, so the result is deterministic); a second
 //                 pooling pass over K then subtracts it from every key row
 //                 before the norms and sums.
-//  k_pooled_scores one CTA per 32 q blocks of one (batch, head): the pooled
-//                 scores scale * qbar . kbar by an fp32 4x4 register-tiled
-//                 product (K-block means streamed through double-buffered shared
-//                 memory in 32-dimension chunks by cp.async, shared by the 32
-//                 rows), written as fp32 into the caller's LUT buffer, which has
+//  pooled scores  scale * qbar . kbar on tcgen05 (pooled_scores_tc.cu),
+//                 written as fp32 into the caller's LUT buffer, which has
 //                 exactly the size of the score matrix.
 //  k_select       one warp per q block: loads its score row, then the pooled
 //                 softmax, a radix (bitwise) threshold search for top-k / cdf,
@@ -184,13 +181,8 @@ __global__ void __launch_bounds__(256) k_key_mean(const float *__restrict__ kbar
 }
 
 // ---------------------------------------------------------------------------
-// k_pooled_scores, k_select
+// k_select
 // ---------------------------------------------------------------------------
-
-constexpr int kSelRows = 32;   // q blocks per CTA
-constexpr int kSelCols = 128;  // kv blocks per column tile
-constexpr int kSelDC = 32;     // dimensions per staged chunk
-constexpr int kSelLDK = kSelDC + 4;
 
 FBM_DEVICE uint32_t order_key(float f) {
   // order-preserving map of a finite float onto uint32 (finite values > 0x7FFFFF)
@@ -334,99 +326,6 @@ FBM_DEVICE uint32_t kth_largest_key(const uint32_t (&key)[NT], const float (&sc)
   return __reduce_min_sync(0xffffffffu, v);
 }
 
-template <int D>
-__global__ void __launch_bounds__(256) k_pooled_scores(SelectArgs a) {
-  extern __shared__ __align__(16) float smem[];
-  constexpr int LDQ = D + 4;
-  constexpr int NCH = D / kSelDC;                    // d chunks per column tile
-  float *q_s = smem;                                 // [32][LDQ]
-  float *k_s = q_s + kSelRows * LDQ;                 // [2][128][kSelLDK]
-  const int tid = threadIdx.x;
-  const int h = blockIdx.y, bi = blockIdx.z;
-  // scores of this (batch, head): [nq][nk] fp32 over the int32 LUT buffer
-  float *S = reinterpret_cast<float *>(a.lut) + (size_t)(bi * a.hq + h) * a.nq * a.nk;
-  const int ratio = a.hq / a.hk;
-  const int g = h / ratio;
-  const int i0 = blockIdx.x * kSelRows;
-  const float *qbar = a.qbar + ((size_t)(bi * a.hq + h) * a.nq) * D;
-  const float *kbar = a.kbar + ((size_t)(bi * a.hk + g) * a.nk) * D;
-
-  // chunk c of the whole sweep = (column tile c / NCH, d chunk c % NCH)
-  const int ntiles = (a.nk + kSelCols - 1) / kSelCols;
-  const int nchunks = ntiles * NCH;
-  auto stage = [&](int c, int buf) {
-    const int col0 = (c / NCH) * kSelCols, d0 = (c % NCH) * kSelDC;
-    float *dst = k_s + buf * kSelCols * kSelLDK;
-    for (int idx = tid; idx < kSelCols * (kSelDC / 4); idx += 256) {
-      const int r = idx / (kSelDC / 4), c4 = idx % (kSelDC / 4);
-      const bool ok = col0 + r < a.nk;
-      const float *src = kbar + (size_t)(ok ? col0 + r : 0) * D + d0 + c4 * 4;
-      cp_async16(smem_u32(dst + r * kSelLDK + c4 * 4), src, ok);
-    }
-  };
-  stage(0, 0);
-  cp_async_commit();
-  // the 32 pooled q rows
-  for (int idx = tid; idx < kSelRows * (D / 4); idx += 256) {
-    const int r = idx / (D / 4), c4 = idx % (D / 4);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i0 + r < a.nq) v = reinterpret_cast<const float4 *>(qbar + (size_t)(i0 + r) * D)[c4];
-    *reinterpret_cast<float4 *>(q_s + r * LDQ + c4 * 4) = v;
-  }
-  // 4 x 4 register tile: rows tr*4 .. +3, columns tc + 32 m
-  const int tr = tid >> 5, tc = tid & 31;
-  float acc[4][4];
-  for (int c = 0; c < nchunks; ++c) {
-    if (c % NCH == 0) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) acc[r][m] = 0.f;
-    }
-    if (c + 1 < nchunks) {
-      stage(c + 1, (c + 1) & 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const float *kc = k_s + (c & 1) * kSelCols * kSelLDK;
-    const int d0 = (c % NCH) * kSelDC;
-#pragma unroll
-    for (int kk = 0; kk < kSelDC; kk += 4) {
-      float4 qv[4], kv[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        qv[r] = *reinterpret_cast<const float4 *>(q_s + (tr * 4 + r) * LDQ + d0 + kk);
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        kv[m] = *reinterpret_cast<const float4 *>(kc + (tc + 32 * m) * kSelLDK + kk);
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          acc[r][m] = fmaf(qv[r].x, kv[m].x, acc[r][m]);
-          acc[r][m] = fmaf(qv[r].y, kv[m].y, acc[r][m]);
-          acc[r][m] = fmaf(qv[r].z, kv[m].z, acc[r][m]);
-          acc[r][m] = fmaf(qv[r].w, kv[m].w, acc[r][m]);
-        }
-    }
-    if (c % NCH == NCH - 1) {
-      const int col0 = (c / NCH) * kSelCols;
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int j = col0 + tc + 32 * m;
-          const int i = i0 + tr * 4 + r;
-          if (j < a.nk && i < a.nq) S[(size_t)i * a.nk + j] = a.scale * acc[r][m];
-        }
-    }
-    __syncthreads();
-  }
-}
-
 // one warp per q block (row): 8 warps per CTA
 template <int NT>
 __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
@@ -564,22 +463,6 @@ __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_const
 // host launchers
 // ---------------------------------------------------------------------------
 
-size_t block_map_smem_bytes(int d, int nt) {
-  (void)nt;
-  return sizeof(float) * ((size_t)kSelRows * (d + 4) + 2 * (size_t)kSelCols * kSelLDK);
-}
-
-template <int D>
-static cudaError_t launch_scores(const SelectArgs &a, cudaStream_t st) {
-  const size_t smem = block_map_smem_bytes(D, 0);
-  cudaError_t e = cudaFuncSetAttribute(k_pooled_scores<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((a.nq + kSelRows - 1) / kSelRows, a.hq, a.b);
-  k_pooled_scores<D><<<grid, 256, smem, st>>>(a);
-  return cudaGetLastError();
-}
-
 template <int NT>
 static cudaError_t launch_select(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {
   const int rows = a.b * a.hq * a.nq;
@@ -635,11 +518,7 @@ cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
   a.scale = L.scale; a.causal = L.causal; a.sink = L.sink; a.mode_cdf = L.mode_cdf;
   a.lut = L.lut; a.cnt = L.cnt; a.bmap = L.bmap;
   a.err = L.err;
-#ifdef FBM_SCORES_SIMT
-  e = L.d == 128 ? launch_scores<128>(a, st) : launch_scores<64>(a, st);
-#else
   e = launch_pooled_scores_tc(a, L.d, st);
-#endif
   if (e != cudaSuccess) return e;
   return launch_select_nt(a, L.hp, st);
 }

@@ -36,7 +36,6 @@ struct BlockMapLaunch {
   uint32_t *err;  // device error word
 };
 cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st);
-size_t block_map_smem_bytes(int d, int nt);
 
 struct FmhaLaunch {
   const void *q, *k, *v;
