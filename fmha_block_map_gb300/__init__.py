@@ -23,7 +23,7 @@ FBM_OK, FBM_ERR_INVALID_ARG, FBM_ERR_UNSUPPORTED, FBM_ERR_CUDA, FBM_ERR_DEVICE =
 FBM_F16, FBM_BF16, FBM_F32 = 0, 1, 2
 FBM_DEVERR_LUT_RANGE, FBM_DEVERR_TIMEOUT, FBM_DEVERR_LUT_ORDER = 0x1, 0x2, 0x4
 FBM_MAX_HEADS = 256
-FBM_STATIC_SCRATCH_BYTES = 24 << 20
+FBM_STATIC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
 

@@ -56,16 +56,16 @@ fbm_status cuda_status(cudaError_t e, const char *what) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t qbar, qsim, kbar, ksim, kmu, total;
+  size_t qpl, qsim, kpl, ksim, kmu, total;
 };
 
 WsLayout ws_layout(int b, int hq, int hk, int s, int d) {
   const size_t nq = (size_t)(s + 63) / 64, nk = nq;
   WsLayout w{};
   size_t off = 0;
-  w.qbar = off; off = align256(off + sizeof(float) * b * hq * nq * d);
+  w.qpl = off; off = align256(off + (size_t)b * hq * fbm::plane_head_bytes((int)nq, d));
   w.qsim = off; off = align256(off + sizeof(float) * b * hq * nq);
-  w.kbar = off; off = align256(off + sizeof(float) * b * hk * nk * d);
+  w.kpl = off; off = align256(off + (size_t)b * hk * fbm::plane_head_bytes((int)nk, d));
   w.ksim = off; off = align256(off + sizeof(float) * b * hk * nk);
   w.kmu = off; off = align256(off + sizeof(float) * b * hk * d);
   w.total = off;
@@ -166,9 +166,9 @@ fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int 
   L.mode_cdf = topk == nullptr;
   L.smooth_k = smooth_k != 0;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  L.qbar = reinterpret_cast<float *>(ws + w.qbar);
+  L.qpl = ws + w.qpl;
   L.qsim = reinterpret_cast<float *>(ws + w.qsim);
-  L.kbar = reinterpret_cast<float *>(ws + w.kbar);
+  L.kpl = ws + w.kpl;
   L.ksim = reinterpret_cast<float *>(ws + w.ksim);
   L.kmu = reinterpret_cast<float *>(ws + w.kmu);
   L.lut = lut; L.cnt = lut_count; L.bmap = block_map;

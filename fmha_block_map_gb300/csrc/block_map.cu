@@ -6,16 +6,18 @@
 //                 lane), row norms by a 3-level shuffle, fp32 row sums (the
 //                 pooled mean, two interleaved partial sums per element) and the
 //                 sum of unit rows (self-similarity = ||sum u||^2 / n^2).
-//                 HBM-bound: it reads Q and K once and writes (d + 1) floats
-//                 per block.
+//                 HBM-bound: it reads Q and K once and writes, per block, the
+//                 mean as three bf16 split planes (the operands of the pooled
+//                 scores' tensor-core product, in their shared-memory layout)
+//                 and one float.
 //  k_key_mean     K smoothing only: one CTA per (batch, KV head) forms the mean
-//                 key row from the block sums of the first pooling pass (fixed
+//                 key row from the block means of the first pooling pass (fixed
 //                 summation order, so the result is deterministic); a second
 //                 pooling pass over K then subtracts it from every key row
 //                 before the norms and sums.
-//  pooled scores  scale * qbar . kbar on tcgen05 (pooled_scores_tc.cu),
-//                 written as fp32 into the caller's LUT buffer, which has
-//                 exactly the size of the score matrix.
+//  pooled scores  scale * qbar . kbar on tcgen05 from the split planes
+//                 (pooled_scores_tc.cu), written as fp32 into the caller's LUT
+//                 buffer, which has exactly the size of the score matrix.
 //  k_select       one warp per q block: loads its score row, then the pooled
 //                 softmax, a radix (bitwise) threshold search for top-k / cdf,
 //                 and ballot-scan emission of the ascending LUT row over the
@@ -34,13 +36,31 @@ namespace fbm {
 
 struct PoolSide {
   const uint16_t *x;  // [bh, s, D] bit patterns
-  float *pooled;      // [bh * nb, D]
+  uint8_t *planes;    // pooled means as split planes (kernels.h)
   float *sim;         // [bh * nb]
   int s;              // rows per (batch, head)
   int nb;             // blocks per (batch, head)
   int nunits;         // bh * nb
   const float *mu;    // [bh, D] row subtracted before pooling (SMOOTH only)
 };
+
+// x = x0 + x1 + x2 in bf16, each difference exact in fp32: the three terms
+// carry the 24 significand bits of a normal fp32 value (the three-term bf16
+// scheme of Henry, Tang and Heinecke, "Leveraging the bfloat16 Artificial
+// Intelligence Datatype For Higher-Precision Computations", ARITH 2019)
+FBM_DEVICE void split3(float x, uint32_t &h0, uint32_t &h1, uint32_t &h2) {
+  const __nv_bfloat16 b0 = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(b0);
+  const __nv_bfloat16 b1 = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(b1);
+  h0 = __bfloat16_as_ushort(b0);
+  h1 = __bfloat16_as_ushort(b1);
+  h2 = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
+}
+
+FBM_DEVICE float plane_value(const uint8_t *p) {
+  return __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(p) << 16);
+}
 
 template <class E, int D, bool SMOOTH>
 __global__ void __launch_bounds__(256, SMOOTH ? 1 : 2) k_pool_sim(PoolSide qs, PoolSide ks) {
@@ -141,14 +161,47 @@ __global__ void __launch_bounds__(256, SMOOTH ? 1 : 2) k_pool_sim(PoolSide qs, P
   for (int e = 0; e < 16; ++e) su = fmaf(usum[e], usum[e], su);
 #pragma unroll
   for (int o = LPR / 2; o > 0; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
-  if (rgrp == 0) {
+  {
+    // the mean, split into three bf16 planes.  Every lane holds the sums of
+    // its sub's 16 values (pieces 2 sub and 2 sub + 1 of the block's row);
+    // row group rgrp splits 16 / RPI of them, so the RPI lanes of a sub fill
+    // the two pieces (a whole 32-byte sector) of each plane together
     const float fn = (float)n;
-    float4 *dst = reinterpret_cast<float4 *>(side.pooled + (size_t)unit * D) + sub * 4;
+    const int t = j / kPlaneRows, rr = j % kPlaneRows;
+    uint8_t *tile = side.planes + (size_t)bh * plane_head_bytes(side.nb, D) +
+                    (size_t)t * plane_tile_bytes(D);
+    constexpr int VPL = 16 / RPI;  // values per lane: 4 (d = 128) or 2 (d = 64)
+    const int e0 = rgrp * VPL;     // first of this lane's values within the 16
+    const int gp = 2 * sub + (e0 >> 3);
+    const int c = gp >> 3, c8 = gp & 7;  // 64-value chunk, piece within it
+    float val[VPL];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      dst[c] = make_float4(tot[4 * c] / fn, tot[4 * c + 1] / fn, tot[4 * c + 2] / fn,
-                           tot[4 * c + 3] / fn);
-    if (sub == 0) side.sim[unit] = su / (fn * fn);
+    for (int e = 0; e < VPL; ++e) val[e] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; q += VPL)  // constant indices into tot[]
+      if (q == e0) {
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) val[e] = tot[q + e];
+      }
+    uint32_t w[3][VPL / 2];
+#pragma unroll
+    for (int e = 0; e < VPL / 2; ++e) {
+      uint32_t a0, a1, a2, b0, b1, b2;
+      split3(val[2 * e] / fn, a0, a1, a2);
+      split3(val[2 * e + 1] / fn, b0, b1, b2);
+      w[0][e] = a0 | (b0 << 16);
+      w[1][e] = a1 | (b1 << 16);
+      w[2][e] = a2 | (b2 << 16);
+    }
+    uint8_t *dst = tile + c * plane_chunk_bytes() + rr * 128 + ((c8 ^ (rr & 7)) << 4) + (e0 & 7) * 2;
+#pragma unroll
+    for (int p = 0; p < 3; ++p) {
+      if constexpr (VPL == 4)
+        *reinterpret_cast<uint2 *>(dst + p * kPlaneBytes) = make_uint2(w[p][0], w[p][1]);
+      else
+        *reinterpret_cast<uint32_t *>(dst + p * kPlaneBytes) = w[p][0];
+    }
+    if (lane == 0) side.sim[unit] = su / (fn * fn);
   }
 }
 
@@ -157,19 +210,26 @@ __global__ void __launch_bounds__(256, SMOOTH ? 1 : 2) k_pool_sim(PoolSide qs, P
 // ---------------------------------------------------------------------------
 
 // mean key row of every (batch, KV head): sum_j n_j * kbar_j / s over the K
-// blocks, n_j the rows of block j.  256 threads = (256 / D) groups of D; group
-// g sums the blocks j = g mod (256 / D), then thread g = 0 adds the groups in
-// order.
+// blocks, n_j the rows of block j, kbar_j = x0 + x1 + x2 read back from the
+// split planes.  256 threads = (256 / D) groups of D; group g sums the blocks
+// j = g mod (256 / D), then thread g = 0 adds the groups in order.
 template <int D>
-__global__ void __launch_bounds__(256) k_key_mean(const float *__restrict__ kbar,
+__global__ void __launch_bounds__(256) k_key_mean(const uint8_t *__restrict__ kpl,
                                                   float *__restrict__ mu, int s, int nk) {
   constexpr int G = 256 / D;
   __shared__ float part[G][D];
   const int e = threadIdx.x % D, g = threadIdx.x / D;
-  const float *base = kbar + (size_t)blockIdx.x * nk * D + e;
+  const uint8_t *head = kpl + (size_t)blockIdx.x * plane_head_bytes(nk, D);
+  const int c = e >> 6, c8 = (e & 63) >> 3, w = e & 7;
   float acc = 0.f;
-#pragma unroll 8
-  for (int j = g; j < nk; j += G) acc = fmaf((float)min(kBlk, s - j * kBlk), base[(size_t)j * D], acc);
+#pragma unroll 4
+  for (int j = g; j < nk; j += G) {
+    const int t = j / kPlaneRows, rr = j % kPlaneRows;
+    const uint8_t *p = head + (size_t)t * plane_tile_bytes(D) + c * plane_chunk_bytes() +
+                       rr * 128 + ((c8 ^ (rr & 7)) << 4) + w * 2;
+    const float x = (plane_value(p) + plane_value(p + kPlaneBytes)) + plane_value(p + 2 * kPlaneBytes);
+    acc = fmaf((float)min(kBlk, s - j * kBlk), x, acc);
+  }
   part[g][e] = acc;
   __syncthreads();
   if (g == 0) {
@@ -326,14 +386,13 @@ FBM_DEVICE uint32_t kth_largest_key(const uint32_t (&key)[NT], const float (&sc)
   return __reduce_min_sync(0xffffffffu, v);
 }
 
-// one warp per q block (row): 8 warps per CTA
+// The selection of one q block (row), by one warp.  NT keys per lane cover
+// columns 0 .. 32 NT - 1; every eligible column of the row must lie below
+// 32 NT (the causal rows of a long sequence take a smaller NT than the
+// kernel's, so that they do work for their eligible prefix only).
 template <int NT>
-__global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
-  __shared__ __align__(16) int hist_all[8][256];  // radix-select counters, one set per warp
-  const int lane = threadIdx.x & 31;
-  int *hist = hist_all[threadIdx.x >> 5];
-  const int rowid = blockIdx.x * 8 + (threadIdx.x >> 5);  // (batch, head, q block)
-  if (rowid >= a.b * a.hq * a.nq) return;
+FBM_DEVICE void select_row(const SelectArgs &a, const HeadParams &hp, int rowid, int n_elig,
+                           int *hist, int lane) {
   const int i = rowid % a.nq;
   const int bh = rowid / a.nq;
   const int h = bh % a.hq, bi = bh / a.hq;
@@ -342,11 +401,10 @@ __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_const
   const float *ksim = a.ksim + (size_t)(bi * a.hk + g) * a.nk;
   const float *srow = reinterpret_cast<const float *>(a.lut) + (size_t)rowid * a.nk;
   const unsigned lt_mask = (1u << lane) - 1u;
+  const int ncols = min(a.nk, 32 * NT);
   {
     const float theta = hp.theta[h];
     const bool q_similar = qsim[i] > theta;
-    const int last_q = (i + 1) * a.blkq - 1;
-    const int n_elig = a.causal ? min(a.nk, last_q / a.blkk + 1) : a.nk;
     float sc[NT];
     uint32_t key[NT];
     bool elig[NT], ksim_ok[NT];
@@ -355,14 +413,14 @@ __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_const
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int j = lane + 32 * t;
-      const bool valid = j < a.nk;
-      elig[t] = valid && (!a.causal || j * a.blkk <= last_q);
-      ksim_ok[t] = valid && ksim[j] > theta;
+      const bool valid = j < ncols;
+      elig[t] = valid && j < n_elig;
+      ksim_ok[t] = elig[t] && ksim[j] > theta;
       const bool fin = elig[t] && ksim_ok[t];
       // a plain load (this kernel rewrites the row); adding +0 turns a -0
       // score into +0, so the float compares of the threshold search and the
       // integer keys order signed zeros alike
-      sc[t] = valid ? __fadd_rn(srow[j], 0.0f) : 0.f;
+      sc[t] = elig[t] ? __fadd_rn(srow[j], 0.0f) : 0.f;
       key[t] = fin ? order_key(sc[t]) : 0u;
       if (fin) mloc = fmaxf(mloc, sc[t]);
       nfin += fin ? 1 : 0;
@@ -451,12 +509,35 @@ __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_const
       const bool keep = elig[t] && (sel[t] || forced);
       const unsigned bal = __ballot_sync(0xffffffffu, keep);
       if (keep) lut[run + __popc(bal & lt_mask)] = j;
-      if (a.bmap && j < a.nk) a.bmap[row * a.nk + j] = keep ? 1 : 0;
+      if (a.bmap && j < ncols) a.bmap[row * a.nk + j] = keep ? 1 : 0;
       run += __popc(bal);
     }
     for (int p = run + lane; p < a.nk; p += 32) lut[p] = -1;
+    if (a.bmap)
+      for (int j = ncols + lane; j < a.nk; j += 32) a.bmap[row * a.nk + j] = 0;
     if (lane == 0) a.cnt[row] = run;
   }
+}
+
+
+// one warp per q block (row): 8 warps per CTA.  NT = ceil(nk / 32) keys per
+// lane; a causal row whose eligible prefix is shorter runs the body of a
+// smaller NT (the branch is uniform over the warp).
+template <int NT>
+__global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
+  __shared__ __align__(16) int hist_all[8][256];  // radix-select counters, one set per warp
+  const int lane = threadIdx.x & 31;
+  int *hist = hist_all[threadIdx.x >> 5];
+  const int rowid = blockIdx.x * 8 + (threadIdx.x >> 5);  // (batch, head, q block)
+  if (rowid >= a.b * a.hq * a.nq) return;
+  const int i = rowid % a.nq;
+  const int last_q = (i + 1) * a.blkq - 1;
+  const int n_elig = a.causal ? min(a.nk, last_q / a.blkk + 1) : a.nk;
+  constexpr int kQ = NT / 4;  // quarter steps (NT is a multiple of 4)
+  if (NT >= 8 && n_elig <= 32 * kQ) select_row<kQ>(a, hp, rowid, n_elig, hist, lane);
+  else if (NT >= 8 && n_elig <= 64 * kQ) select_row<2 * kQ>(a, hp, rowid, n_elig, hist, lane);
+  else if (NT >= 8 && n_elig <= 96 * kQ) select_row<3 * kQ>(a, hp, rowid, n_elig, hist, lane);
+  else select_row<NT>(a, hp, rowid, n_elig, hist, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -490,9 +571,9 @@ static void launch_pool(const BlockMapLaunch &L, const PoolSide &qs, const PoolS
 }
 
 cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
-  PoolSide qs{static_cast<const uint16_t *>(L.q), L.qbar, L.qsim, L.s, L.nq, L.b * L.hq * L.nq,
+  PoolSide qs{static_cast<const uint16_t *>(L.q), L.qpl, L.qsim, L.s, L.nq, L.b * L.hq * L.nq,
               nullptr};
-  PoolSide ks{static_cast<const uint16_t *>(L.k), L.kbar, L.ksim, L.s, L.nk, L.b * L.hk * L.nk,
+  PoolSide ks{static_cast<const uint16_t *>(L.k), L.kpl, L.ksim, L.s, L.nk, L.b * L.hk * L.nk,
               nullptr};
   launch_pool<false>(L, qs, ks, st);
   cudaError_t e = cudaGetLastError();
@@ -500,8 +581,8 @@ cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
   if (L.smooth_k) {
     // K smoothing: mean key row from the block means just written, then pool
     // and measure K again on the centred rows (Q results are kept)
-    if (L.d == 128) k_key_mean<128><<<L.b * L.hk, 256, 0, st>>>(L.kbar, L.kmu, L.s, L.nk);
-    else k_key_mean<64><<<L.b * L.hk, 256, 0, st>>>(L.kbar, L.kmu, L.s, L.nk);
+    if (L.d == 128) k_key_mean<128><<<L.b * L.hk, 256, 0, st>>>(L.kpl, L.kmu, L.s, L.nk);
+    else k_key_mean<64><<<L.b * L.hk, 256, 0, st>>>(L.kpl, L.kmu, L.s, L.nk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     PoolSide none = qs;
@@ -512,7 +593,7 @@ cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   SelectArgs a{};
-  a.qbar = L.qbar; a.qsim = L.qsim; a.kbar = L.kbar; a.ksim = L.ksim;
+  a.qpl = L.qpl; a.qsim = L.qsim; a.kpl = L.kpl; a.ksim = L.ksim;
   a.b = L.b; a.hq = L.hq; a.hk = L.hk; a.nq = L.nq; a.nk = L.nk;
   a.blkq = kBlk; a.blkk = kBlk;
   a.scale = L.scale; a.causal = L.causal; a.sink = L.sink; a.mode_cdf = L.mode_cdf;

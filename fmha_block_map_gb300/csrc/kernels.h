@@ -13,8 +13,25 @@ struct HeadParams {
   float sel[FBM_MAX_HEADS];    // topk or cdfthreshd per query head
 };
 
+// Pooled block means in the block-map workspace: each fp32 mean x is kept as
+// the three bf16 terms of x = x0 + x1 + x2 (x0 = bf16(x), x1 = bf16(x - x0),
+// x2 = bf16(x - x0 - x1)), laid out for the tensor-core product of the pooled
+// scores.  Per (batch, head): ceil(nb / 128) tiles of 128 blocks; per tile
+// d / 64 chunks of 64 values; per chunk the planes x0, x1, x2, each 128 rows
+// (blocks) of 128 bytes in the 128-byte-swizzled K-major layout (16-byte piece
+// c of row r at r * 128 + ((c ^ (r mod 8)) * 16)).  Rows past nb are never
+// written.
+constexpr int kPlaneRows = 128;
+constexpr size_t kPlaneBytes = 128 * 128;
+__host__ __device__ inline size_t plane_chunk_bytes() { return 3 * kPlaneBytes; }
+__host__ __device__ inline size_t plane_tile_bytes(int d) { return (size_t)(d / 64) * plane_chunk_bytes(); }
+__host__ __device__ inline size_t plane_head_bytes(int nb, int d) {
+  return (size_t)((nb + kPlaneRows - 1) / kPlaneRows) * plane_tile_bytes(d);
+}
+
 struct SelectArgs {
-  const float *qbar, *qsim, *kbar, *ksim;
+  const uint8_t *qpl, *kpl;  // pooled means as split planes (layout above)
+  const float *qsim, *ksim;
   int b, hq, hk, nq, nk, blkq, blkk;
   float scale;
   int causal, sink, mode_cdf;
@@ -30,7 +47,8 @@ struct BlockMapLaunch {
   float scale;
   int causal, sink, mode_cdf, smooth_k;
   HeadParams hp;
-  float *qbar, *qsim, *kbar, *ksim, *kmu;  // workspace carve-out
+  uint8_t *qpl, *kpl;                 // workspace carve-out: split planes,
+  float *qsim, *ksim, *kmu;           // self-similarities, mean key rows
   int32_t *lut, *cnt;
   uint8_t *bmap;
   uint32_t *err;  // device error word

@@ -106,6 +106,14 @@ FBM_DEVICE void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c
 FBM_DEVICE void prefetch_map(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// one contiguous global -> shared bulk copy, its bytes counted on an mbarrier
+// (both addresses 16-byte aligned, bytes a multiple of 16)
+FBM_DEVICE void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 FBM_DEVICE void bulk_store(void *gdst, uint32_t src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst),
                "r"(src), "r"(bytes)

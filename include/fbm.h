@@ -76,9 +76,11 @@ const char *fbm_last_error_message(void);
 fbm_status fbm_get_error(void *stream, uint32_t *detail);
 
 /*
- * Workspace (bytes) that sparge_block_map needs for the given shape: pooled
- * means (fp32) and self-similarities (fp32) of every Q and K block, and the
- * mean key row (fp32) of every (batch, KV head) for K smoothing.
+ * Workspace (bytes) that sparge_block_map needs for the given shape: the
+ * pooled mean of every Q and K block (fp32, kept as three bf16 terms in
+ * 128-block tiles: 6 d bytes per block, rounded up to whole tiles), the
+ * self-similarity (fp32) of every block, and the mean key row (fp32) of every
+ * (batch, KV head) for K smoothing.
  */
 size_t fbm_block_map_workspace_bytes(int b, int hq, int hk, int s, int d, int blkq,
                                      int blkk);
@@ -154,7 +156,7 @@ fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int 
  * All calls share the array, so calls that overlap on the GPU race; nothing
  * in it needs to start at zero.  The library allocates nothing.
  */
-#define FBM_STATIC_SCRATCH_BYTES (24u << 20)
+#define FBM_STATIC_SCRATCH_BYTES (32u << 20)
 fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int b, int hq, int hk,
                                    int s, int d, int blkq, int blkk, const float *topk,
                                    const float *cdfthreshd, const float *simthreshd1, float scale,
