@@ -25,8 +25,12 @@
 //                 Apart from the product (which keeps every SM's FMA pipe busy)
 //                 the selection is a chain of warp reductions; a kernel of its
 //                 own runs it at full occupancy.
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace fbm {
 
@@ -62,146 +66,223 @@ FBM_DEVICE float plane_value(const uint8_t *p) {
   return __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t *>(p) << 16);
 }
 
+// Persistent: one CTA per SM, 8 consumer warps and one producer warp.  The
+// rows of a 64-token block are contiguous in memory, so one bulk copy brings
+// a whole block into a stage of a shared-memory ring (kPoolStageBytes of
+// stages, kept full by the producer); consumer warp w reduces the CTA's
+// blocks k = w, w + 8, ... from shared memory.
+constexpr int kPoolConsumers = 8;
+constexpr int kPoolThreads = 32 * (kPoolConsumers + 1);
+constexpr int kPoolRingBytes = 192 * 1024;
+constexpr uint64_t kPoolWaitNs = 2000000000ull;
+
+template <int D>
+struct PoolRing {
+  static constexpr int kBlockBytes = kBlk * D * 2;  // one 64-row block of 16-bit values
+  static constexpr int kStages = kPoolRingBytes / kBlockBytes;
+  static constexpr int kBarOff = kPoolRingBytes;   // full[kStages], empty[kStages]
+  static constexpr int kFlagOff = kBarOff + 16 * kStages;
+  static constexpr int kSmem = kFlagOff + 16 + 128;  // + alignment slack
+};
+
 template <class E, int D, bool SMOOTH>
-__global__ void __launch_bounds__(256, SMOOTH ? 1 : 2) k_pool_sim(PoolSide qs, PoolSide ks) {
-  // (the centring row of the smoothing pass takes 16 more registers a thread:
-  // one CTA per SM then, instead of spilling)
-  // a lane owns 16 consecutive elements (32 bytes) of a row; a row spans LPR
-  // lanes and one warp-wide step covers RPI rows
+__global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolSide ks, uint32_t *err) {
+  using R = PoolRing<D>;
+  // a lane owns 16 elements of a row: 8 at sub * 8 and 8 at D / 2 + sub * 8,
+  // so the 8 lanes of a quarter warp read 128 contiguous bytes of shared
+  // memory; a row spans LPR lanes and one warp-wide step covers RPI rows
   constexpr int LPR = D / 16;
   constexpr int RPI = 32 / LPR;
   constexpr int STEPS = kBlk / RPI;
-  constexpr int UNR = 8;  // 16 loads (256 B) in flight per lane
-  const int lane = threadIdx.x & 31;
-  const int unit_all = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (unit_all >= qs.nunits + ks.nunits) return;
-  const PoolSide &side = unit_all < qs.nunits ? qs : ks;
-  const int unit = unit_all < qs.nunits ? unit_all : unit_all - qs.nunits;
-  const int bh = unit / side.nb;
-  const int j = unit - bh * side.nb;
-  const int row0 = j * kBlk;
-  const int n = min(kBlk, side.s - row0);
-  const uint16_t *base = side.x + ((size_t)bh * side.s + row0) * D;
+  constexpr int UNR = 4;  // shared-memory loads in flight per lane and step group
+  extern __shared__ uint8_t pool_smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(pool_smem_raw) + 127) &
+                                              ~uintptr_t(127));
+  const uint32_t sbase = smem_u32(smem);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + R::kFlagOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = qs.nunits + ks.nunits;
+  auto full = [&](int st) { return sbase + R::kBarOff + 8 * st; };
+  auto empty = [&](int st) { return sbase + R::kBarOff + 8 * (R::kStages + st); };
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < R::kStages; ++st) {
+      tc::mbar_init(full(st), 1);
+      tc::mbar_init(empty(st), 1);
+    }
+    tc::fence_mbar_init();
+    *abort_flag = 0;
+  }
+  __syncthreads();
+
+  if (warp == kPoolConsumers) {
+    // producer: one elected thread issues the bulk copies in order
+    if (lane == 0) {
+      int k = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x, ++k) {
+        const int st = k % R::kStages;
+        if (k >= R::kStages &&
+            !tc::mbar_wait(empty(st), ((k / R::kStages) - 1) & 1, abort_flag, kPoolWaitNs)) {
+          set_error(err, FBM_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        const PoolSide &side = u < qs.nunits ? qs : ks;
+        const int unit = u < qs.nunits ? u : u - qs.nunits;
+        const int bh = unit / side.nb, j = unit - bh * side.nb;
+        const int n = min(kBlk, side.s - j * kBlk);
+        const uint32_t bytes = (uint32_t)n * D * 2;
+        tc::mbar_arrive_tx(full(st), bytes);
+        tc::bulk_load(sbase + st * R::kBlockBytes, side.x + ((size_t)bh * side.s + (size_t)j * kBlk) * D,
+                      bytes, full(st));
+      }
+      // every copy this CTA issued has landed before it exits (bounded)
+      for (int kk = max(0, k - R::kStages); kk < k; ++kk)
+        tc::mbar_wait_for(full(kk % R::kStages), (kk / R::kStages) & 1, kPoolWaitNs);
+    }
+    return;
+  }
+
+  // consumers
   const int sub = lane % LPR;
   const int rgrp = lane / LPR;
-  float mu[16];
-  if constexpr (SMOOTH) {
-    const float4 *m4 = reinterpret_cast<const float4 *>(side.mu + (size_t)bh * D) + sub * 4;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float4 m = m4[c];
-      mu[4 * c] = m.x; mu[4 * c + 1] = m.y; mu[4 * c + 2] = m.z; mu[4 * c + 3] = m.w;
+  int k = warp;
+  for (int u = blockIdx.x + warp * gridDim.x; u < total; u += kPoolConsumers * gridDim.x,
+           k += kPoolConsumers) {
+    const int st = k % R::kStages;
+    if (!tc::mbar_wait(full(st), (k / R::kStages) & 1, abort_flag, kPoolWaitNs)) {
+      set_error(err, FBM_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+      break;
     }
-  }
-
-  // two interleaved partial sums per element keep the fp32 sums short
-  float msum[2][16], usum[16];
+    const PoolSide &side = u < qs.nunits ? qs : ks;
+    const int unit = u < qs.nunits ? u : u - qs.nunits;
+    const int bh = unit / side.nb;
+    const int j = unit - bh * side.nb;
+    const int n = min(kBlk, side.s - j * kBlk);
+    const uint8_t *blk = smem + st * R::kBlockBytes;
+    float mu[16];
+    if constexpr (SMOOTH) {
+      const float4 *m0 = reinterpret_cast<const float4 *>(side.mu + (size_t)bh * D + sub * 8);
+      const float4 *m1 = reinterpret_cast<const float4 *>(side.mu + (size_t)bh * D + D / 2 + sub * 8);
+      const float4 a0 = m0[0], a1 = m0[1], b0 = m1[0], b1 = m1[1];
+      const float mv[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
+                            b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-  for (int e = 0; e < 16; ++e) msum[0][e] = msum[1][e] = usum[e] = 0.f;
-
-#pragma unroll
-  for (int s0 = 0; s0 < STEPS; s0 += UNR) {
-    uint4 raw[UNR][2];
-#pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int r = (s0 + u) * RPI + rgrp;
-      if (r < n) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(base + (size_t)r * D) + sub * 2;
-        raw[u][0] = __ldg(src);
-        raw[u][1] = __ldg(src + 1);
-      } else {
-        raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
-      }
+      for (int e = 0; e < 16; ++e) mu[e] = mv[e];
     }
+
+    // two interleaved partial sums per element keep the fp32 sums short
+    float msum[2][16], usum[16];
 #pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      float x[16];
-      const uint32_t w[8] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
-                             raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
+    for (int e = 0; e < 16; ++e) msum[0][e] = msum[1][e] = usum[e] = 0.f;
 #pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        const float2 f = E::to_f2(w[p]);
-        x[2 * p] = f.x;
-        x[2 * p + 1] = f.y;
-      }
-      if constexpr (SMOOTH) {
-        // rows past the end stay zero: they add nothing to either sum
-        const int r = (s0 + u) * RPI + rgrp;
-        if (r < n) {
+    for (int s0 = 0; s0 < STEPS; s0 += UNR) {
+      uint4 raw[UNR][2];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) x[e] -= mu[e];
+      for (int uu = 0; uu < UNR; ++uu) {
+        const int r = (s0 + uu) * RPI + rgrp;
+        if (r < n) {  // rows past a partial block's end hold stale data
+          const uint8_t *row = blk + r * (2 * D);
+          raw[uu][0] = *reinterpret_cast<const uint4 *>(row + sub * 16);
+          raw[uu][1] = *reinterpret_cast<const uint4 *>(row + D + sub * 16);
+        } else {
+          raw[uu][0] = raw[uu][1] = make_uint4(0, 0, 0, 0);
         }
       }
-      float ss = 0.f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) ss = fmaf(x[e], x[e], ss);
+      for (int uu = 0; uu < UNR; ++uu) {
+        float x[16];
+        const uint32_t w[8] = {raw[uu][0].x, raw[uu][0].y, raw[uu][0].z, raw[uu][0].w,
+                               raw[uu][1].x, raw[uu][1].y, raw[uu][1].z, raw[uu][1].w};
 #pragma unroll
-      for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+        for (int p = 0; p < 8; ++p) {
+          const float2 f = E::to_f2(w[p]);
+          x[2 * p] = f.x;
+          x[2 * p + 1] = f.y;
+        }
+        if constexpr (SMOOTH) {
+          // rows past the end stay zero: they add nothing to either sum
+          const int r = (s0 + uu) * RPI + rgrp;
+          if (r < n) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] -= mu[e];
+          }
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          usum[e] = fmaf(x[e], inv, usum[e]);
+          msum[uu & 1][e] += x[e];
+        }
+      }
+    }
+    // the stage is free once every lane has read it
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(empty(st));
+
+    float tot[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) tot[e] = msum[0][e] + msum[1][e];
+#pragma unroll
+    for (int o = 16; o >= LPR; o >>= 1) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        usum[e] = fmaf(x[e], inv, usum[e]);
-        msum[u & 1][e] += x[e];
+        tot[e] += __shfl_xor_sync(0xffffffffu, tot[e], o);
+        usum[e] += __shfl_xor_sync(0xffffffffu, usum[e], o);
       }
     }
-  }
-  float tot[16];
+    float su = 0.f;
 #pragma unroll
-  for (int e = 0; e < 16; ++e) tot[e] = msum[0][e] + msum[1][e];
+    for (int e = 0; e < 16; ++e) su = fmaf(usum[e], usum[e], su);
 #pragma unroll
-  for (int o = 16; o >= LPR; o >>= 1) {
+    for (int o = LPR / 2; o > 0; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
+    {
+      // the mean, split into three bf16 planes.  Every lane holds the sums of
+      // its sub's 16 values (pieces sub and D / 16 + sub of the block's row);
+      // row group rgrp splits 16 / RPI of them, so the RPI lanes of a sub
+      // fill 16-byte pieces of each plane together
+      const float fn = (float)n;
+      const int t = j / kPlaneRows, rr = j % kPlaneRows;
+      uint8_t *tile = side.planes + (size_t)bh * plane_head_bytes(side.nb, D) +
+                      (size_t)t * plane_tile_bytes(D);
+      constexpr int VPL = 16 / RPI;  // values per lane: 4 (d = 128) or 2 (d = 64)
+      const int e0 = rgrp * VPL;     // first of this lane's values within the 16
+      const int gp = (e0 < 8 ? 0 : D / 16) + sub;
+      const int c = gp >> 3, c8 = gp & 7;  // 64-value chunk, piece within it
+      float val[VPL];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      tot[e] += __shfl_xor_sync(0xffffffffu, tot[e], o);
-      usum[e] += __shfl_xor_sync(0xffffffffu, usum[e], o);
-    }
-  }
-  float su = 0.f;
+      for (int e = 0; e < VPL; ++e) val[e] = 0.f;
 #pragma unroll
-  for (int e = 0; e < 16; ++e) su = fmaf(usum[e], usum[e], su);
+      for (int q = 0; q < 16; q += VPL)  // constant indices into tot[]
+        if (q == e0) {
 #pragma unroll
-  for (int o = LPR / 2; o > 0; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
-  {
-    // the mean, split into three bf16 planes.  Every lane holds the sums of
-    // its sub's 16 values (pieces 2 sub and 2 sub + 1 of the block's row);
-    // row group rgrp splits 16 / RPI of them, so the RPI lanes of a sub fill
-    // the two pieces (a whole 32-byte sector) of each plane together
-    const float fn = (float)n;
-    const int t = j / kPlaneRows, rr = j % kPlaneRows;
-    uint8_t *tile = side.planes + (size_t)bh * plane_head_bytes(side.nb, D) +
-                    (size_t)t * plane_tile_bytes(D);
-    constexpr int VPL = 16 / RPI;  // values per lane: 4 (d = 128) or 2 (d = 64)
-    const int e0 = rgrp * VPL;     // first of this lane's values within the 16
-    const int gp = 2 * sub + (e0 >> 3);
-    const int c = gp >> 3, c8 = gp & 7;  // 64-value chunk, piece within it
-    float val[VPL];
+          for (int e = 0; e < VPL; ++e) val[e] = tot[q + e];
+        }
+      uint32_t w[3][VPL / 2];
 #pragma unroll
-    for (int e = 0; e < VPL; ++e) val[e] = 0.f;
-#pragma unroll
-    for (int q = 0; q < 16; q += VPL)  // constant indices into tot[]
-      if (q == e0) {
-#pragma unroll
-        for (int e = 0; e < VPL; ++e) val[e] = tot[q + e];
+      for (int e = 0; e < VPL / 2; ++e) {
+        uint32_t a0, a1, a2, b0, b1, b2;
+        split3(val[2 * e] / fn, a0, a1, a2);
+        split3(val[2 * e + 1] / fn, b0, b1, b2);
+        w[0][e] = a0 | (b0 << 16);
+        w[1][e] = a1 | (b1 << 16);
+        w[2][e] = a2 | (b2 << 16);
       }
-    uint32_t w[3][VPL / 2];
+      uint8_t *dst = tile + c * plane_chunk_bytes() + rr * 128 + ((c8 ^ (rr & 7)) << 4) + (e0 & 7) * 2;
 #pragma unroll
-    for (int e = 0; e < VPL / 2; ++e) {
-      uint32_t a0, a1, a2, b0, b1, b2;
-      split3(val[2 * e] / fn, a0, a1, a2);
-      split3(val[2 * e + 1] / fn, b0, b1, b2);
-      w[0][e] = a0 | (b0 << 16);
-      w[1][e] = a1 | (b1 << 16);
-      w[2][e] = a2 | (b2 << 16);
+      for (int p = 0; p < 3; ++p) {
+        if constexpr (VPL == 4)
+          *reinterpret_cast<uint2 *>(dst + p * kPlaneBytes) = make_uint2(w[p][0], w[p][1]);
+        else
+          *reinterpret_cast<uint32_t *>(dst + p * kPlaneBytes) = w[p][0];
+      }
+      if (lane == 0) side.sim[unit] = su / (fn * fn);
     }
-    uint8_t *dst = tile + c * plane_chunk_bytes() + rr * 128 + ((c8 ^ (rr & 7)) << 4) + (e0 & 7) * 2;
-#pragma unroll
-    for (int p = 0; p < 3; ++p) {
-      if constexpr (VPL == 4)
-        *reinterpret_cast<uint2 *>(dst + p * kPlaneBytes) = make_uint2(w[p][0], w[p][1]);
-      else
-        *reinterpret_cast<uint32_t *>(dst + p * kPlaneBytes) = w[p][0];
-    }
-    if (lane == 0) side.sim[unit] = su / (fn * fn);
   }
 }
 
@@ -557,17 +638,39 @@ static cudaError_t launch_select_nt(const SelectArgs &a, const HeadParams &hp, c
   return launch_select<32>(a, hp, st);
 }
 
-template <bool SMOOTH>
-static void launch_pool(const BlockMapLaunch &L, const PoolSide &qs, const PoolSide &ks,
-                        cudaStream_t st) {
-  const int grid = (qs.nunits + ks.nunits + 7) / 8;
-  if (L.d == 128) {
-    if (L.bf16) k_pool_sim<BF16, 128, SMOOTH><<<grid, 256, 0, st>>>(qs, ks);
-    else k_pool_sim<F16, 128, SMOOTH><<<grid, 256, 0, st>>>(qs, ks);
-  } else {
-    if (L.bf16) k_pool_sim<BF16, 64, SMOOTH><<<grid, 256, 0, st>>>(qs, ks);
-    else k_pool_sim<F16, 64, SMOOTH><<<grid, 256, 0, st>>>(qs, ks);
+int device_sm_count();  // fmha_tc.cu
+
+constexpr int kMaxPoolDevices = 64;
+
+template <class E, int D, bool SMOOTH>
+static cudaError_t launch_pool_t(const PoolSide &qs, const PoolSide &ks, uint32_t *err,
+                                 cudaStream_t st) {
+  // the shared-memory attribute is per device: set it once on each
+  static std::atomic<bool> attr_done[kMaxPoolDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxPoolDevices || !attr_done[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(k_pool_sim<E, D, SMOOTH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PoolRing<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxPoolDevices) attr_done[dev].store(true, std::memory_order_release);
   }
+  const int total = qs.nunits + ks.nunits;
+  if (total == 0) return cudaSuccess;
+  const int grid = std::min(total, device_sm_count());
+  k_pool_sim<E, D, SMOOTH><<<grid, kPoolThreads, PoolRing<D>::kSmem, st>>>(qs, ks, err);
+  return cudaGetLastError();
+}
+
+template <bool SMOOTH>
+static cudaError_t launch_pool(const BlockMapLaunch &L, const PoolSide &qs, const PoolSide &ks,
+                               cudaStream_t st) {
+  if (L.d == 128)
+    return L.bf16 ? launch_pool_t<BF16, 128, SMOOTH>(qs, ks, L.err, st)
+                  : launch_pool_t<F16, 128, SMOOTH>(qs, ks, L.err, st);
+  return L.bf16 ? launch_pool_t<BF16, 64, SMOOTH>(qs, ks, L.err, st)
+                : launch_pool_t<F16, 64, SMOOTH>(qs, ks, L.err, st);
 }
 
 cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
@@ -575,8 +678,7 @@ cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
               nullptr};
   PoolSide ks{static_cast<const uint16_t *>(L.k), L.kpl, L.ksim, L.s, L.nk, L.b * L.hk * L.nk,
               nullptr};
-  launch_pool<false>(L, qs, ks, st);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pool<false>(L, qs, ks, st);
   if (e != cudaSuccess) return e;
   if (L.smooth_k) {
     // K smoothing: mean key row from the block means just written, then pool
@@ -588,8 +690,7 @@ cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
     PoolSide none = qs;
     none.nunits = 0;
     ks.mu = L.kmu;
-    launch_pool<true>(L, none, ks, st);
-    e = cudaGetLastError();
+    e = launch_pool<true>(L, none, ks, st);
     if (e != cudaSuccess) return e;
   }
   SelectArgs a{};
