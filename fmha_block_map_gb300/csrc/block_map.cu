@@ -117,6 +117,9 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolS
   if (warp == kPoolConsumers) {
     // producer: one elected thread issues the bulk copies in order
     if (lane == 0) {
+      // Q and K are read once: keep them from evicting the split planes,
+      // which the pooled-score kernel reads next
+      const uint64_t policy = tc::l2_evict_first();
       int k = 0;
       for (int u = blockIdx.x; u < total; u += gridDim.x, ++k) {
         const int st = k % R::kStages;
@@ -132,8 +135,9 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolS
         const int n = min(kBlk, side.s - j * kBlk);
         const uint32_t bytes = (uint32_t)n * D * 2;
         tc::mbar_arrive_tx(full(st), bytes);
-        tc::bulk_load(sbase + st * R::kBlockBytes, side.x + ((size_t)bh * side.s + (size_t)j * kBlk) * D,
-                      bytes, full(st));
+        tc::bulk_load_hint(sbase + st * R::kBlockBytes,
+                           side.x + ((size_t)bh * side.s + (size_t)j * kBlk) * D, bytes, full(st),
+                           policy);
       }
       // every copy this CTA issued has landed before it exits (bounded)
       for (int kk = max(0, k - R::kStages); kk < k; ++kk)
@@ -160,21 +164,24 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolS
     const int j = unit - bh * side.nb;
     const int n = min(kBlk, side.s - j * kBlk);
     const uint8_t *blk = smem + st * R::kBlockBytes;
-    float mu[16];
+    // element pairs (2 p, 2 p + 1) in one 64-bit register: packed f32x2
+    // arithmetic, each half an ordinary IEEE fp32 operation
+    uint64_t nmu[8];
     if constexpr (SMOOTH) {
       const float4 *m0 = reinterpret_cast<const float4 *>(side.mu + (size_t)bh * D + sub * 8);
       const float4 *m1 = reinterpret_cast<const float4 *>(side.mu + (size_t)bh * D + D / 2 + sub * 8);
       const float4 a0 = m0[0], a1 = m0[1], b0 = m1[0], b1 = m1[1];
-      const float mv[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
-                            b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int e = 0; e < 16; ++e) mu[e] = mv[e];
+      nmu[0] = tc::f2_pack(-a0.x, -a0.y); nmu[1] = tc::f2_pack(-a0.z, -a0.w);
+      nmu[2] = tc::f2_pack(-a1.x, -a1.y); nmu[3] = tc::f2_pack(-a1.z, -a1.w);
+      nmu[4] = tc::f2_pack(-b0.x, -b0.y); nmu[5] = tc::f2_pack(-b0.z, -b0.w);
+      nmu[6] = tc::f2_pack(-b1.x, -b1.y); nmu[7] = tc::f2_pack(-b1.z, -b1.w);
     }
 
     // two interleaved partial sums per element keep the fp32 sums short
-    float msum[2][16], usum[16];
+    uint64_t msum[2][8], usum[8];
+    const uint64_t zero2 = tc::f2_pack(0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) msum[0][e] = msum[1][e] = usum[e] = 0.f;
+    for (int p = 0; p < 8; ++p) msum[0][p] = msum[1][p] = usum[p] = zero2;
 #pragma unroll
     for (int s0 = 0; s0 < STEPS; s0 += UNR) {
       uint4 raw[UNR][2];
@@ -191,33 +198,35 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolS
       }
 #pragma unroll
       for (int uu = 0; uu < UNR; ++uu) {
-        float x[16];
+        uint64_t x[8];
         const uint32_t w[8] = {raw[uu][0].x, raw[uu][0].y, raw[uu][0].z, raw[uu][0].w,
                                raw[uu][1].x, raw[uu][1].y, raw[uu][1].z, raw[uu][1].w};
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
           const float2 f = E::to_f2(w[p]);
-          x[2 * p] = f.x;
-          x[2 * p + 1] = f.y;
+          x[p] = tc::f2_pack(f.x, f.y);
         }
         if constexpr (SMOOTH) {
           // rows past the end stay zero: they add nothing to either sum
           const int r = (s0 + uu) * RPI + rgrp;
           if (r < n) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] -= mu[e];
+            for (int p = 0; p < 8; ++p) x[p] = tc::f2_add(x[p], nmu[p]);
           }
         }
-        float ss = 0.f;
+        uint64_t ss2 = zero2;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ss = fmaf(x[e], x[e], ss);
+        for (int p = 0; p < 8; ++p) ss2 = tc::f2_fma(x[p], x[p], ss2);
+        const float2 ssp = tc::f2_unpack(ss2);
+        float ss = ssp.x + ssp.y;
 #pragma unroll
         for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+        const uint64_t inv2 = tc::f2_pack(inv, inv);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          usum[e] = fmaf(x[e], inv, usum[e]);
-          msum[uu & 1][e] += x[e];
+        for (int p = 0; p < 8; ++p) {
+          usum[p] = tc::f2_fma(x[p], inv2, usum[p]);
+          msum[uu & 1][p] = tc::f2_add(msum[uu & 1][p], x[p]);
         }
       }
     }
@@ -225,20 +234,27 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolS
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(empty(st));
 
-    float tot[16];
+    float tot[16], us[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) tot[e] = msum[0][e] + msum[1][e];
+    for (int p = 0; p < 8; ++p) {
+      const float2 a = tc::f2_unpack(msum[0][p]), b = tc::f2_unpack(msum[1][p]);
+      const float2 u2 = tc::f2_unpack(usum[p]);
+      tot[2 * p] = a.x + b.x;
+      tot[2 * p + 1] = a.y + b.y;
+      us[2 * p] = u2.x;
+      us[2 * p + 1] = u2.y;
+    }
 #pragma unroll
     for (int o = 16; o >= LPR; o >>= 1) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         tot[e] += __shfl_xor_sync(0xffffffffu, tot[e], o);
-        usum[e] += __shfl_xor_sync(0xffffffffu, usum[e], o);
+        us[e] += __shfl_xor_sync(0xffffffffu, us[e], o);
       }
     }
     float su = 0.f;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) su = fmaf(usum[e], usum[e], su);
+    for (int e = 0; e < 16; ++e) su = fmaf(us[e], us[e], su);
 #pragma unroll
     for (int o = LPR / 2; o > 0; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
     {
@@ -330,40 +346,30 @@ FBM_DEVICE uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-
-// The kcount-th largest key of a warp's row (NT keys per lane; key 0 = not
-// selectable; 1 <= kcount <= number of selectable keys), by radix selection:
-//  1. a coarse digit: each selectable score s maps to bin
-//     min(255, floor((s - lo) * 256 / (hi - lo))) over the row's range
-//     [lo, hi], a monotone map, so every key of a higher bin is larger than
-//     every key of a lower one;
-//  2. a 256-bin histogram of the digits (shared-memory counters of the warp)
-//     and a warp scan from the top bin down find the bin holding the
-//     kcount-th largest key and how many keys lie above it;
-//  3. that bin's keys are ranked exactly: when the bin is taken whole the
-//     answer is its smallest key; else, with at most 32 keys in the bin, each
-//     lane ranks one of them against the others; else (many scores within one
-//     bin) a bitwise search over the 32 key bits among the bin's keys.
-// Any monotone digit gives the exact result; this one spreads the pooled
-// scores of a row evenly over the bins, where the leading bits of the
-// order-preserving key (sign and exponent) would crowd them into a few.
-template <int NT>
-FBM_DEVICE uint32_t fin_mask(const uint32_t (&key)[NT]) {
-  uint32_t msk = 0;
-#pragma unroll
-  for (int t = 0; t < NT; ++t) msk |= (key[t] != 0u ? 1u : 0u) << t;
-  return msk;
+FBM_DEVICE float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// A row of scores held by one warp: NT per lane, column j = lane + 32 t; bit
+// t of a lane's word `fin` marks a selectable score (eligible and similar).
+// Scores carry no -0 (the loader adds +0), so comparing the floats orders
+// them exactly as their order-preserving keys do.
+FBM_DEVICE bool is_fin(uint32_t fin, int t) { return (fin >> t) & 1u; }
+
+// Largest T (a key) with #(selectable key >= T) >= kcount, by a bitwise
+// search over the 32 key bits among the candidates `cand` (bit t of this
+// lane's word).
 template <int NT>
-FBM_DEVICE uint32_t bitwise_kth(const uint32_t (&key)[NT], uint32_t cand, int kcount) {
-  // largest T with #(candidate key >= T) >= kcount
+FBM_DEVICE uint32_t bitwise_kth(const float (&sc)[NT], uint32_t cand, int kcount) {
+  uint32_t key[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) key[t] = ((cand >> t) & 1u) ? order_key(sc[t]) : 0u;
   uint32_t T = 0;
   for (int bit = 31; bit >= 0; --bit) {
     const uint32_t c = T | (1u << bit);
     int cnt = 0;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) cnt += ((cand >> t) & 1u) && key[t] >= c ? 1 : 0;
+    for (int t = 0; t < NT; ++t) cnt += key[t] >= c ? 1 : 0;
     const int tot = __reduce_add_sync(0xffffffffu, cnt);
     if (tot >= kcount) T = c;
     if (tot == kcount) break;  // exactly kcount keys >= T: no tie left to resolve
@@ -372,24 +378,51 @@ FBM_DEVICE uint32_t bitwise_kth(const uint32_t (&key)[NT], uint32_t cand, int kc
   uint32_t mn = 0xFFFFFFFFu;
 #pragma unroll
   for (int t = 0; t < NT; ++t)
-    if (((cand >> t) & 1u) && key[t] >= T) mn = min(mn, key[t]);
+    if (key[t] >= T && key[t] != 0u) mn = min(mn, key[t]);
   return __reduce_min_sync(0xffffffffu, mn);
 }
 
+// The kcount-th largest selectable score of a warp's row (1 <= kcount <=
+// number of selectable scores), by radix selection:
+//  1. a coarse digit: each selectable score s maps to bin
+//     min(255, floor((s - lo) * 256 / (hi - lo))) over the row's range
+//     [lo, hi], a monotone map, so every score of a higher bin is larger than
+//     every score of a lower one;
+//  2. a 256-bin histogram of the digits (shared-memory counters of the warp)
+//     and a warp scan from the top bin down find the bin holding the
+//     kcount-th largest score and how many scores lie above it;
+//  3. that bin's scores are ranked exactly: when the bin is taken whole the
+//     answer is its smallest score; else, with at most 32 scores in the bin,
+//     each lane ranks one of them against the others; else (many scores
+//     within one bin) a bitwise search over the 32 key bits of the bin.
+// Any monotone digit gives the exact result; this one spreads the pooled
+// scores of a row evenly over the bins, where the leading bits of the
+// order-preserving key (sign and exponent) would crowd them into a few.
+// `exact` is set when the scores >= the result number exactly kcount (no
+// tie at the threshold needs breaking).
 template <int NT>
-FBM_DEVICE uint32_t kth_largest_key(const uint32_t (&key)[NT], const float (&sc)[NT],
-                                    uint32_t fin, int kcount, float hi, int *hist, int lane) {
+FBM_DEVICE float kth_largest(const float (&sc)[NT], uint32_t finl, int kcount, float hi,
+                             int *hist, int lane, bool &exact) {
+  const unsigned lt = (1u << lane) - 1u;
   float lo_l = INFINITY;
 #pragma unroll
   for (int t = 0; t < NT; ++t)
-    if ((fin >> t) & 1u) lo_l = fminf(lo_l, sc[t]);
+    if (is_fin(finl, t)) lo_l = fminf(lo_l, sc[t]);
   float lo = lo_l;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
   const float range = hi - lo;
   const float inv = 256.0f / range;
-  if (!(range > 0.f) || !(inv < INFINITY) || !(inv > 0.f))
-    return bitwise_kth<NT>(key, fin, kcount);  // one value, or a range fp32 cannot split
+  if (!(range > 0.f) || !(inv < INFINITY) || !(inv > 0.f)) {
+    // one value, or a range fp32 cannot split
+    const uint32_t T = bitwise_kth<NT>(sc, finl, kcount);
+    const float tv = key_value(T);
+    int ge = 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) ge += ((finl >> t) & 1u) && sc[t] >= tv ? 1 : 0;
+    exact = __reduce_add_sync(0xffffffffu, ge) == kcount;
+    return tv;
+  }
   int dig[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) dig[t] = min(255, (int)((sc[t] - lo) * inv));
@@ -399,7 +432,7 @@ FBM_DEVICE uint32_t kth_largest_key(const uint32_t (&key)[NT], const float (&sc)
   __syncwarp();
 #pragma unroll
   for (int t = 0; t < NT; ++t)
-    if ((fin >> t) & 1u) atomicAdd(hist + dig[t], 1);
+    if ((finl >> t) & 1u) atomicAdd(hist + dig[t], 1);
   __syncwarp();
   // lane L owns bins 255 - 8 L down to 248 - 8 L
   int c[8];
@@ -411,7 +444,7 @@ FBM_DEVICE uint32_t kth_largest_key(const uint32_t (&key)[NT], const float (&sc)
   }
   int ssum = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) ssum += c[i];
+  for (int k = 0; k < 8; ++k) ssum += c[k];
   int incl = ssum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -420,13 +453,13 @@ FBM_DEVICE uint32_t kth_largest_key(const uint32_t (&key)[NT], const float (&sc)
   }
   int run = incl - ssum, found = -1, above = 0, binc = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (found < 0 && run + c[i] >= kcount) {
-      found = 255 - 8 * lane - i;
+  for (int k = 0; k < 8; ++k) {
+    if (found < 0 && run + c[k] >= kcount) {
+      found = 255 - 8 * lane - k;
       above = run;
-      binc = c[i];
+      binc = c[k];
     }
-    run += c[i];
+    run += c[k];
   }
   // the first crossing from the top (lanes after it cross at once)
   const unsigned bal = __ballot_sync(0xffffffffu, found >= 0);
@@ -436,176 +469,194 @@ FBM_DEVICE uint32_t kth_largest_key(const uint32_t (&key)[NT], const float (&sc)
   const int nbin = __shfl_sync(0xffffffffu, binc, src);
   uint32_t cand = 0;
 #pragma unroll
-  for (int t = 0; t < NT; ++t) cand |= (((fin >> t) & 1u) && dig[t] == dsel ? 1u : 0u) << t;
+  for (int t = 0; t < NT; ++t) cand |= (((finl >> t) & 1u) && dig[t] == dsel ? 1u : 0u) << t;
   if (need == nbin) {
-    // the bin is taken whole: its smallest key
-    uint32_t mn = 0xFFFFFFFFu;
+    // the bin is taken whole: its smallest score (every larger score is
+    // taken too, and every score equal to it lies in the bin)
+    float mn = INFINITY;
 #pragma unroll
     for (int t = 0; t < NT; ++t)
-      if ((cand >> t) & 1u) mn = min(mn, key[t]);
-    return __reduce_min_sync(0xffffffffu, mn);
+      if ((cand >> t) & 1u) mn = fminf(mn, sc[t]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    exact = true;
+    return mn;
   }
-  if (nbin > 32) return bitwise_kth<NT>(key, cand, need);
-  // compact the bin's keys, one per lane, in the warp's counters (done with)
+  if (nbin > 32) {
+    const uint32_t T = bitwise_kth<NT>(sc, cand, need);
+    const float tv = key_value(T);
+    int ge = 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) ge += ((cand >> t) & 1u) && sc[t] >= tv ? 1 : 0;
+    exact = __reduce_add_sync(0xffffffffu, ge) == need;
+    return tv;
+  }
+  // compact the bin's scores, one per lane, in the warp's counters (done with)
   __syncwarp();
-  uint32_t *slot = reinterpret_cast<uint32_t *>(hist);
-  const unsigned lt = (1u << lane) - 1u;
+  float *slot = reinterpret_cast<float *>(hist);
   int base = 0;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const bool cnd = (cand >> t) & 1u;
     const unsigned b = __ballot_sync(0xffffffffu, cnd);
-    if (cnd) slot[base + __popc(b & lt)] = key[t];
+    if (cnd) slot[base + __popc(b & lt)] = sc[t];
     base += __popc(b);
   }
   __syncwarp();
-  const uint32_t mine = lane < nbin ? slot[lane] : 0u;
+  const float mine = lane < nbin ? slot[lane] : -INFINITY;
   int gt = 0;
-  for (int i = 0; i < nbin; ++i) gt += slot[i] > mine ? 1 : 0;
-  // the need-th largest: the smallest key with fewer than `need` keys above it
-  const uint32_t v = (lane < nbin && gt < need) ? mine : 0xFFFFFFFFu;
-  return __reduce_min_sync(0xffffffffu, v);
+  for (int k = 0; k < nbin; ++k) gt += slot[k] > mine ? 1 : 0;
+  // the need-th largest: the smallest score with fewer than `need` above it
+  const float v = (lane < nbin && gt < need) ? mine : INFINITY;
+  float tv = v;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tv = fminf(tv, __shfl_xor_sync(0xffffffffu, tv, o));
+  exact = __popc(__ballot_sync(0xffffffffu, lane < nbin && mine >= tv)) == need;
+  return tv;
 }
 
-// The selection of one q block (row), by one warp.  NT keys per lane cover
+// The selection of one q block (row), by one warp.  NT scores per lane cover
 // columns 0 .. 32 NT - 1; every eligible column of the row must lie below
 // 32 NT (the causal rows of a long sequence take a smaller NT than the
 // kernel's, so that they do work for their eligible prefix only).
-template <int NT>
+template <int NT, bool CDF>
 FBM_DEVICE void select_row(const SelectArgs &a, const HeadParams &hp, int rowid, int n_elig,
                            int *hist, int lane) {
   const int i = rowid % a.nq;
   const int bh = rowid / a.nq;
   const int h = bh % a.hq, bi = bh / a.hq;
   const int g = h / (a.hq / a.hk);
-  const float *qsim = a.qsim + (size_t)(bi * a.hq + h) * a.nq;
   const float *ksim = a.ksim + (size_t)(bi * a.hk + g) * a.nk;
   const float *srow = reinterpret_cast<const float *>(a.lut) + (size_t)rowid * a.nk;
   const unsigned lt_mask = (1u << lane) - 1u;
   const int ncols = min(a.nk, 32 * NT);
-  {
-    const float theta = hp.theta[h];
-    const bool q_similar = qsim[i] > theta;
-    float sc[NT];
-    uint32_t key[NT];
-    bool elig[NT], ksim_ok[NT];
-    float mloc = -INFINITY;
-    int nfin = 0;
+  const float theta = hp.theta[h];
+  const bool q_similar = a.qsim[(size_t)(bi * a.hq + h) * a.nq + i] > theta;
+  float sc[NT];
+  uint32_t fin = 0;  // bit t: column lane + 32 t is selectable
+  float mloc = -INFINITY;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int j = lane + 32 * t;
-      const bool valid = j < ncols;
-      elig[t] = valid && j < n_elig;
-      ksim_ok[t] = elig[t] && ksim[j] > theta;
-      const bool fin = elig[t] && ksim_ok[t];
-      // a plain load (this kernel rewrites the row); adding +0 turns a -0
-      // score into +0, so the float compares of the threshold search and the
-      // integer keys order signed zeros alike
-      sc[t] = elig[t] ? __fadd_rn(srow[j], 0.0f) : 0.f;
-      key[t] = fin ? order_key(sc[t]) : 0u;
-      if (fin) mloc = fmaxf(mloc, sc[t]);
-      nfin += fin ? 1 : 0;
-    }
-    nfin = __reduce_add_sync(0xffffffffu, nfin);
-    bool sel[NT];
+  for (int t = 0; t < NT; ++t) {
+    const int j = lane + 32 * t;
+    const bool elig = j < n_elig;  // eligible columns form a prefix of the row
+    // a plain load (this kernel rewrites the row); adding +0 turns a -0
+    // score into +0, so float compares and integer keys order them alike
+    sc[t] = elig ? __fadd_rn(srow[j], 0.0f) : 0.f;
+    const bool f = elig && ksim[j] > theta;
+    fin |= (f ? 1u : 0u) << t;
+    if (f) mloc = fmaxf(mloc, sc[t]);
+  }
+  const int nfin = __reduce_add_sync(0xffffffffu, __popc(fin));
+  uint32_t sel = 0;  // this lane's selected scores, bit t
+  if (nfin > 0) {
+    const float m = warp_max(mloc);
+    if constexpr (!CDF) {
+      const float prod = __fmul_rn(hp.sel[h], (float)n_elig);
+      const int kcount = min((int)ceilf(prod), nfin);
+      bool exact = false;
+      const float tv = kth_largest<NT>(sc, fin, kcount, m, hist, lane, exact);
+      if (exact) {
 #pragma unroll
-    for (int t = 0; t < NT; ++t) sel[t] = false;
-    if (nfin > 0) {
-      const float m = warp_max(mloc);
-      if (!a.mode_cdf) {
-        const float prod = __fmul_rn(hp.sel[h], (float)n_elig);
-        const int kcount = min((int)ceilf(prod), nfin);
-        const uint32_t T = kth_largest_key<NT>(key, sc, fin_mask(key), kcount, m, hist, lane);
+        for (int t = 0; t < NT; ++t) sel |= (is_fin(fin, t) && sc[t] >= tv ? 1u : 0u) << t;
+      } else {
+        // ties at the threshold: the lower kv blocks first
         int cgt = 0;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) cgt += key[t] > T ? 1 : 0;
+        for (int t = 0; t < NT; ++t) cgt += is_fin(fin, t) && sc[t] > tv ? 1 : 0;
         const int need = kcount - __reduce_add_sync(0xffffffffu, cgt);
         int run = 0;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          const bool tie = key[t] == T && key[t] != 0u;
+          const bool tie = is_fin(fin, t) && sc[t] == tv;
           const unsigned bal = __ballot_sync(0xffffffffu, tie);
-          sel[t] = key[t] > T || (tie && run + __popc(bal & lt_mask) < need);
+          const bool s = (is_fin(fin, t) && sc[t] > tv) || (tie && run + __popc(bal & lt_mask) < need);
+          sel |= (s ? 1u : 0u) << t;
           run += __popc(bal);
         }
+      }
+    } else {
+      uint32_t key[NT];
+      float p[NT];
+      float ps = 0.f;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        key[t] = is_fin(fin, t) ? order_key(sc[t]) : 0u;
+        p[t] = key[t] ? expf(sc[t] - m) : 0.f;
+        ps += p[t];
+      }
+      const float inv = 1.0f / warp_sum(ps);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) p[t] *= inv;
+      const float tau = hp.sel[h];
+      float mass_all = 0.f;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) mass_all += p[t];
+      mass_all = warp_sum(mass_all);
+      if (mass_all < tau) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) sel |= (key[t] != 0u ? 1u : 0u) << t;
       } else {
-        float p[NT];
-        float ps = 0.f;
+        // largest T with mass(key >= T) >= tau
+        uint32_t T = 0;
+        for (int bit = 31; bit >= 0; --bit) {
+          const uint32_t cand = T | (1u << bit);
+          float ms = 0.f;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) ms += key[t] >= cand ? p[t] : 0.f;
+          if (warp_sum(ms) >= tau) T = cand;
+        }
+        float mgt = 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) mgt += key[t] > T ? p[t] : 0.f;
+        float carry = warp_sum(mgt);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          p[t] = key[t] ? expf(sc[t] - m) : 0.f;
-          ps += p[t];
-        }
-        const float inv = 1.0f / warp_sum(ps);
+          const bool tie = key[t] == T && key[t] != 0u;
+          float v = tie ? p[t] : 0.f;
+          float incl = v;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) p[t] *= inv;
-        const float tau = hp.sel[h];
-        float mass_all = 0.f;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) mass_all += p[t];
-        mass_all = warp_sum(mass_all);
-        if (mass_all < tau) {
-#pragma unroll
-          for (int t = 0; t < NT; ++t) sel[t] = key[t] != 0u;
-        } else {
-          // largest T with mass(key >= T) >= tau
-          uint32_t T = 0;
-          for (int bit = 31; bit >= 0; --bit) {
-            const uint32_t cand = T | (1u << bit);
-            float ms = 0.f;
-#pragma unroll
-            for (int t = 0; t < NT; ++t) ms += key[t] >= cand ? p[t] : 0.f;
-            if (warp_sum(ms) >= tau) T = cand;
+          for (int o = 1; o < 32; o <<= 1) {
+            const float up = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += up;
           }
-          float mgt = 0.f;
-#pragma unroll
-          for (int t = 0; t < NT; ++t) mgt += key[t] > T ? p[t] : 0.f;
-          float carry = warp_sum(mgt);
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const bool tie = key[t] == T && key[t] != 0u;
-            float v = tie ? p[t] : 0.f;
-            float incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const float up = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += up;
-            }
-            sel[t] = key[t] > T || (tie && carry + (incl - v) < tau);
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-          }
+          const bool s = key[t] > T || (tie && carry + (incl - v) < tau);
+          sel |= (s ? 1u : 0u) << t;
+          carry += __shfl_sync(0xffffffffu, incl, 31);
         }
       }
     }
-    // forced columns / rows, sink, causal; ascending emission by ballot scan
-    // (over the scores every lane has already read)
-    __syncwarp();
-    const size_t row = (size_t)rowid;
-    int32_t *lut = a.lut + row * a.nk;
-    int run = 0;
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int j = lane + 32 * t;
-      const bool forced = elig[t] && (!ksim_ok[t] || !q_similar || (a.sink && j == 0));
-      const bool keep = elig[t] && (sel[t] || forced);
-      const unsigned bal = __ballot_sync(0xffffffffu, keep);
-      if (keep) lut[run + __popc(bal & lt_mask)] = j;
-      if (a.bmap && j < ncols) a.bmap[row * a.nk + j] = keep ? 1 : 0;
-      run += __popc(bal);
-    }
-    for (int p = run + lane; p < a.nk; p += 32) lut[p] = -1;
-    if (a.bmap)
-      for (int j = ncols + lane; j < a.nk; j += 32) a.bmap[row * a.nk + j] = 0;
-    if (lane == 0) a.cnt[row] = run;
   }
+  // forced columns / rows, sink, causal; ascending emission by ballot scan
+  // (over the scores every lane has already read).  An eligible column is
+  // forced when its kv block is not similar (it is eligible but not
+  // selectable), when the q block is not similar, or for the sink.
+  __syncwarp();
+  const size_t row = (size_t)rowid;
+  int32_t *lut = a.lut + row * a.nk;
+  int run = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int j = lane + 32 * t;
+    const bool elig = j < n_elig;
+    const bool keep = elig && (((sel >> t) & 1u) || !is_fin(fin, t) || !q_similar ||
+                               (a.sink && j == 0));
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    if (keep) lut[run + __popc(bal & lt_mask)] = j;
+    if (a.bmap && j < ncols) a.bmap[row * a.nk + j] = keep ? 1 : 0;
+    run += __popc(bal);
+  }
+  for (int p = run + lane; p < a.nk; p += 32) lut[p] = -1;
+  if (a.bmap)
+    for (int j = ncols + lane; j < a.nk; j += 32) a.bmap[row * a.nk + j] = 0;
+  if (lane == 0) a.cnt[row] = run;
 }
 
-
-// one warp per q block (row): 8 warps per CTA.  NT = ceil(nk / 32) keys per
+// one warp per q block (row): 8 warps per CTA.  NT = ceil(nk / 32) scores per
 // lane; a causal row whose eligible prefix is shorter runs the body of a
 // smaller NT (the branch is uniform over the warp).
-template <int NT>
-__global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
+template <int NT, bool CDF>
+__global__ void __launch_bounds__(256, NT <= 8 ? 4 : (NT <= 16 ? 3 : 1))
+    k_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
   __shared__ __align__(16) int hist_all[8][256];  // radix-select counters, one set per warp
   const int lane = threadIdx.x & 31;
   int *hist = hist_all[threadIdx.x >> 5];
@@ -615,10 +666,10 @@ __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_const
   const int last_q = (i + 1) * a.blkq - 1;
   const int n_elig = a.causal ? min(a.nk, last_q / a.blkk + 1) : a.nk;
   constexpr int kQ = NT / 4;  // quarter steps (NT is a multiple of 4)
-  if (NT >= 8 && n_elig <= 32 * kQ) select_row<kQ>(a, hp, rowid, n_elig, hist, lane);
-  else if (NT >= 8 && n_elig <= 64 * kQ) select_row<2 * kQ>(a, hp, rowid, n_elig, hist, lane);
-  else if (NT >= 8 && n_elig <= 96 * kQ) select_row<3 * kQ>(a, hp, rowid, n_elig, hist, lane);
-  else select_row<NT>(a, hp, rowid, n_elig, hist, lane);
+  if (NT >= 8 && n_elig <= 32 * kQ) select_row<kQ, CDF>(a, hp, rowid, n_elig, hist, lane);
+  else if (NT >= 8 && n_elig <= 64 * kQ) select_row<2 * kQ, CDF>(a, hp, rowid, n_elig, hist, lane);
+  else if (NT >= 8 && n_elig <= 96 * kQ) select_row<3 * kQ, CDF>(a, hp, rowid, n_elig, hist, lane);
+  else select_row<NT, CDF>(a, hp, rowid, n_elig, hist, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -628,7 +679,8 @@ __global__ void __launch_bounds__(256) k_select(SelectArgs a, const __grid_const
 template <int NT>
 static cudaError_t launch_select(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {
   const int rows = a.b * a.hq * a.nq;
-  k_select<NT><<<(rows + 7) / 8, 256, 0, st>>>(a, hp);
+  if (a.mode_cdf) k_select<NT, true><<<(rows + 7) / 8, 256, 0, st>>>(a, hp);
+  else k_select<NT, false><<<(rows + 7) / 8, 256, 0, st>>>(a, hp);
   return cudaGetLastError();
 }
 

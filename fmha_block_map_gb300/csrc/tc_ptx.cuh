@@ -114,6 +114,21 @@ FBM_DEVICE void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// the same with an L2 eviction policy (e.g. from l2_evict_first())
+FBM_DEVICE void bulk_load_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+// an L2 policy for data read once: its lines are the first to be evicted
+FBM_DEVICE uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
 FBM_DEVICE void bulk_store(void *gdst, uint32_t src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst),
                "r"(src), "r"(bytes)
