@@ -60,6 +60,8 @@ def parse():
                    help="skip the causal-GQA prefill and sparse-decode measurements")
     p.add_argument("--decode-only", action="store_true",
                    help="only the sparse-decode measurement (a small command for profiling it)")
+    p.add_argument("--causal-gqa-only", action="store_true",
+                   help="only the causal GQA measurement (a small command for profiling it)")
     p.add_argument("--small", action="store_true",
                    help="b1 h16 s16384 d128 (Q, K, V 201 MB: still larger than L2) with every "
                         "leg but the step, the dense runs and the pair path off: a small case "
@@ -567,16 +569,18 @@ def measure_causal_gqa(hbm_gbs, peak):
             "attn_frac_peak": round(tiles * FLOP_PER_TILE / (at_ms * 1e-3) / 1e12 / peak, 4)}
 
 
-def measure_decode(hbm_gbs):
+def measure_decode(hbm_gbs, small=False):
     """64 queries x 16 heads on one 576-wide KV head, 2048 listed tokens each,
-    65536-page cache (4.8 GB bf16): split-KV decode + LSE combine."""
+    65536-page cache (4.8 GB bf16): split-KV decode + LSE combine.  small:
+    the same queries and list lengths over 128 pages per query (a 0.6 GB
+    cache, still larger than L2), for profiler captures."""
     import numpy as np
     import torch
 
     import fmha_block_map_gb300 as fbm
     import synth
 
-    cfg = synth.C5
+    cfg = synth.C5.replace(pages_per_query=128) if small else synth.C5
     inp = synth.decode(cfg)
     n_rows = cfg.n_pages * cfg.page
     cache = torch.empty((n_rows, cfg.d), dtype=torch.bfloat16, device="cuda")
@@ -610,8 +614,10 @@ def measure_decode(hbm_gbs):
     assert fbm.get_error() == 0
     del cache
     torch.cuda.empty_cache()
-    return {"workload": "64 queries x 16 heads, d=576 (V = first 512), 2048 tokens each, "
-                        "65536 pages of 64 rows, bf16", "by_splits": res}
+    return {"workload": f"{cfg.n_queries} queries x {cfg.hq} heads, d={cfg.d} (V = first "
+                        f"{cfg.dv}), {cfg.topk} tokens each, {cfg.n_pages} pages of {cfg.page} "
+                        "rows, bf16" + (" (small profiling case)" if small else ""),
+            "by_splits": res}
 
 
 # ----------------------------------------------------------------------------
@@ -756,7 +762,18 @@ def main():
         import torch
 
         torch.cuda.set_device(0)
-        print(json.dumps({"decode": measure_decode(load_peaks()[0]["hbm_gbs"])}))
+        print(json.dumps({"decode": measure_decode(load_peaks()[0]["hbm_gbs"], small=args.small)}))
+        return
+    if args.causal_gqa_only:
+        import torch
+
+        from fmha_block_map_gb300 import build as fbuild
+
+        torch.cuda.set_device(0)
+        fbuild.build()
+        peaks = load_peaks()[0]
+        print(json.dumps({"causal_gqa": measure_causal_gqa(peaks["hbm_gbs"],
+                                                           peaks.get("bf16_tflops", 1900.0))}))
         return
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:

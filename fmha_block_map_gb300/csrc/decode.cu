@@ -2,28 +2,35 @@
 // (ROCm/aiter pull 4919: sparse MLA decode; a K row holds 512 latent + 64
 // rotary values and V is its latent plane; split-KV partials).
 //
-// One CTA (4 warps) per (query, split).  Prologue: the CTA resolves every
-// listed token of its chunk to a physical cache row (index list, then page
-// table) into shared memory before any row is fetched, so the dependent
-// lookups are off the streaming loop.  Main loop over tiles of 32 tokens:
-//   - cp.async gathers the 32 rows (1152 B each) into a double-buffered,
-//     XOR-swizzled shared tile (a sentinel or invalid token is zero-filled and
-//     masked);
-//   - S = Q K^T [16 heads x 32 tokens] on mma.sync, the 576-wide contraction
-//     split over the 4 warps (each keeps its 144-column slice of Q in
-//     registers) and summed in a fixed order through shared memory;
+// One CTA (two groups of 4 warps) per (query, split).  Prologue: the CTA
+// resolves every listed token of its chunk to a physical cache row (index
+// list, then page table) into shared memory before any row is fetched, so the
+// dependent lookups are off the streaming loop, and stages Q.  The two warp
+// groups then work independently, group g on the 16-token tiles g, g + 2, ...
+// of the chunk, each with its own online-softmax state; per tile:
+//   - cp.async gathers the 16 rows (1152 B each) into the group's
+//     double-buffered, XOR-swizzled shared tile (a sentinel or invalid token
+//     is zero-filled and masked);
+//   - S = Q K^T [16 heads x 16 tokens] on mma.sync, the 576-wide contraction
+//     split over the group's 4 warps and summed in a fixed order through
+//     shared memory;
 //   - online softmax per head (base 2); P goes to shared memory as the A
 //     operand of O += P V, whose 512 output columns are split over the warps.
-// The 16 heads share each gathered row, so every selected row is read once
-// per query: the kernel is bound by HBM bandwidth.
+// At the end the two groups' states merge like two split-KV partials (the
+// Stage 1 combine of "Incremental_FlashAttention updating_log.md").  The 16
+// heads share each gathered row, so every selected row is read once per
+// query; two independent groups per CTA and two CTAs per SM keep 16 warps of
+// per-tile chains in flight on each SM.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace fbm {
 namespace {
 
-constexpr int kDTok = 32;     // tokens per tile
+constexpr int kDTok = 16;     // tokens per tile
 constexpr int kDHeads = 16;   // query heads (the MMA M dimension)
+constexpr int kDGroups = 2;   // independent 4-warp groups per CTA
+constexpr int kDThreads = 128 * kDGroups;
 
 template <class E>
 FBM_DEVICE void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -51,29 +58,51 @@ FBM_DEVICE void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
+// the 128 threads of one warp group (named barrier 1 + group)
+FBM_DEVICE void group_sync(int grp) {
+  asm volatile("bar.sync %0, 128;\n" ::"r"(1 + grp) : "memory");
+}
 
 template <int D>
 FBM_DEVICE uint32_t swz(int r, int ch) {
   return (uint32_t)(r * (D * 2) + ((ch ^ (r & 7)) << 4));
 }
 
-template <class E, int D, int DV>
-__global__ void __launch_bounds__(128) k_sparse_decode(const DecodeLaunch L) {
-  static_assert(D % 64 == 0 && DV % 64 == 0 && DV <= D, "shape");
-  constexpr int KS_PER_WARP = D / 64;          // 16-wide k-steps per warp for S
-  constexpr int TILE = kDTok * D * 2;
-  constexpr int P_LD = kDTok + 8;              // padded P row (elements)
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *p = smem;
-  const uint32_t sQ = smem_u32(p);               p += kDHeads * D * 2;
-  const uint32_t sKV = smem_u32(p);              p += 2 * TILE;
-  float *s_part = reinterpret_cast<float *>(p);  p += 4 * kDHeads * kDTok * sizeof(float);
-  uint16_t *s_p = reinterpret_cast<uint16_t *>(p); p += kDHeads * P_LD * 2;
-  float *s_alpha = reinterpret_cast<float *>(p); p += kDHeads * sizeof(float);
-  float *s_l = reinterpret_cast<float *>(p);     p += kDHeads * sizeof(float);
-  int32_t *s_rows = reinterpret_cast<int32_t *>(p);
+// shared memory of one warp group: two KV tiles, the warps' partial scores,
+// P and the per-head rescale factors
+template <int D>
+struct DecGroup {
+  static constexpr int kTile = kDTok * D * 2;
+  static constexpr int kPLd = kDTok + 8;  // padded P row (elements)
+  static constexpr int kPart = 2 * kTile;
+  static constexpr int kP = kPart + 4 * kDHeads * kDTok * 4;
+  static constexpr int kAlpha = kP + kDHeads * kPLd * 2;
+  static constexpr int kBytes = (kAlpha + kDHeads * 4 + 127) / 128 * 128;
+};
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+template <int D>
+constexpr size_t dec_fixed_bytes() {
+  return (size_t)kDHeads * D * 2 + (size_t)kDGroups * DecGroup<D>::kBytes + 4 * kDHeads * 4;
+}
+
+template <class E, int D, int DV>
+__global__ void __launch_bounds__(kDThreads, 2) k_sparse_decode(const DecodeLaunch L) {
+  static_assert(D % 64 == 0 && DV % 64 == 0 && DV <= D, "shape");
+  using G = DecGroup<D>;
+  constexpr int KS_PER_WARP = D / 64;  // 16-wide k-steps per warp for S
+  static_assert(4 * (DV / 4) * 16 * 4 <= 2 * G::kTile, "group 1's O fits in its KV tiles");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t sQ = smem_u32(smem);
+  const int tid = threadIdx.x, grp = tid >> 7, gtid = tid & 127;
+  const int warp = gtid >> 5, lane = tid & 31;
+  uint8_t *gb = smem + kDHeads * D * 2 + grp * G::kBytes;
+  const uint32_t sKV = smem_u32(gb);
+  float *s_part = reinterpret_cast<float *>(gb + G::kPart);
+  uint16_t *s_p = reinterpret_cast<uint16_t *>(gb + G::kP);
+  float *s_alpha = reinterpret_cast<float *>(gb + G::kAlpha);
+  float *s_ml = reinterpret_cast<float *>(smem + kDHeads * D * 2 + kDGroups * G::kBytes);
+  int32_t *s_rows = reinterpret_cast<int32_t *>(s_ml + 4 * kDHeads);
+
   const int split = blockIdx.x % L.num_splits;
   const int c = blockIdx.x / L.num_splits;
   const int base = L.topk / L.num_splits, extra = L.topk % L.num_splits;
@@ -82,8 +111,8 @@ __global__ void __launch_bounds__(128) k_sparse_decode(const DecodeLaunch L) {
   const uint16_t *cache = static_cast<const uint16_t *>(L.cache);
   const int max_pos = L.pages_per_query * L.page;
 
-  // prologue: token list -> physical rows (-1 = masked)
-  for (int t = tid; t < n; t += 128) {
+  // prologue: token list -> physical rows (-1 = masked), and Q [16][D]
+  for (int t = tid; t < n; t += kDThreads) {
     const int pos = __ldg(L.idx + (size_t)c * L.topk + lo + t);
     int row = -1;
     if (pos >= 0) {
@@ -97,91 +126,92 @@ __global__ void __launch_bounds__(128) k_sparse_decode(const DecodeLaunch L) {
     }
     s_rows[t] = row;
   }
-  // Q [16][D]
   {
     const uint16_t *qg = static_cast<const uint16_t *>(L.q) + (size_t)c * L.hq * D;
-    for (int ch = tid; ch < kDHeads * (D / 8); ch += 128) {
+    for (int ch = tid; ch < kDHeads * (D / 8); ch += kDThreads) {
       const int r = ch / (D / 8), cc = ch % (D / 8);
       cp_async16(sQ + swz<D>(r, cc), qg + (size_t)r * D + cc * 8, true);
     }
+    cp_async_commit();
+    cp_async_wait<0>();
   }
   __syncthreads();
+
+  // this group's tiles: grp, grp + 2, ...  Each thread gathers the 16-byte
+  // chunks ld_c, ld_c + 8, ... of row ld_r of a tile: one row lookup, then
+  // fixed strides (the swizzle only permutes the low three chunk bits)
+  static_assert(128 == kDTok * 8 && (D / 8) % 8 == 0, "8 threads per row");
+  const int ld_r = gtid >> 3, ld_c = gtid & 7;
+  const uint32_t ld_dst = (uint32_t)(ld_r * (D * 2) + ((ld_c ^ (ld_r & 7)) << 4));
   auto load_tile = [&](int tile, int stage) {
-    const uint32_t dst = sKV + stage * TILE;
-    for (int ch = tid; ch < kDTok * (D / 8); ch += 128) {
-      const int r = ch / (D / 8), cc = ch % (D / 8);
-      const int tok = tile * kDTok + r;
-      const int row = tok < n ? s_rows[tok] : -1;
-      const bool ok = row >= 0;
-      cp_async16(dst + swz<D>(r, cc), cache + (size_t)(ok ? row : 0) * D + cc * 8, ok);
-    }
+    const int tok = tile * kDTok + ld_r;
+    const int row = tok < n ? s_rows[tok] : -1;
+    const bool ok = row >= 0;
+    const uint16_t *src = cache + (size_t)(ok ? row : 0) * D + ld_c * 8;
+    const uint32_t dst = sKV + stage * G::kTile + ld_dst;
+#pragma unroll
+    for (int k = 0; k < D / 64; ++k) cp_async16(dst + k * 128, src + k * 64, ok);
   };
   const int ntiles = (n + kDTok - 1) / kDTok;
-  if (ntiles > 0) load_tile(0, 0);
+  const int mine = ntiles > grp ? (ntiles - grp + 1) / kDGroups : 0;
+  if (mine > 0) load_tile(grp, 0);
   cp_async_commit();
 
   float o[DV / 4 / 8][4];  // this warp's DV/4 columns: DV/32 n-tiles
 #pragma unroll
   for (int a = 0; a < DV / 32; ++a) o[a][0] = o[a][1] = o[a][2] = o[a][3] = 0.f;
-  // softmax role: thread -> head tid/8, tokens (tid%8)*4 .. +3
-  const int sm_head = tid >> 3, sm_tok = (tid & 7) * 4;
+  // softmax role: thread -> head gtid/8, tokens (gtid%8)*2 .. +1
+  const int sm_head = gtid >> 3, sm_tok = (gtid & 7) * 2;
   float m_run = -INFINITY, l_run = 0.f;
   const float sl2 = L.scale * 1.4426950408889634f;
-  uint32_t qf[KS_PER_WARP][4];
 
-  for (int t = 0; t < ntiles; ++t) {
-    const int stage = t & 1;
-    if (t + 1 < ntiles) {
-      load_tile(t + 1, stage ^ 1);
+  for (int j = 0; j < mine; ++j) {
+    const int tile = kDGroups * j + grp;
+    const int stage = j & 1;
+    if (j + 1 < mine) {
+      load_tile(tile + kDGroups, stage ^ 1);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
-    __syncthreads();
-    if (t == 0) {
-#pragma unroll
-      for (int ks = 0; ks < KS_PER_WARP; ++ks) {
-        const int ch = (warp * KS_PER_WARP + ks) * 2 + (lane >> 4);
-        ldsm_x4(sQ + swz<D>(lane & 15, ch), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
-      }
-    }
-    const uint32_t kv = sKV + stage * TILE;
+    group_sync(grp);
+    const uint32_t kv = sKV + stage * G::kTile;
     // partial S over this warp's slice of the contraction
-    float s[4][4];
+    float s[2][4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) s[a][0] = s[a][1] = s[a][2] = s[a][3] = 0.f;
+    for (int a = 0; a < 2; ++a) s[a][0] = s[a][1] = s[a][2] = s[a][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < KS_PER_WARP; ++ks) {
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        const int mi = lane >> 3;
-        const int tok = np * 16 + (mi >> 1) * 8 + (lane & 7);
-        const int ch = (warp * KS_PER_WARP + ks) * 2 + (mi & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kv + swz<D>(tok, ch), b0, b1, b2, b3);
-        mma16816<E>(s[2 * np], qf[ks], b0, b1);
-        mma16816<E>(s[2 * np + 1], qf[ks], b2, b3);
-      }
+      uint32_t qf[4];
+      const int qch = (warp * KS_PER_WARP + ks) * 2 + (lane >> 4);
+      ldsm_x4(sQ + swz<D>(lane & 15, qch), qf[0], qf[1], qf[2], qf[3]);
+      const int mi = lane >> 3;
+      const int tok = (mi >> 1) * 8 + (lane & 7);
+      const int ch = (warp * KS_PER_WARP + ks) * 2 + (mi & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kv + swz<D>(tok, ch), b0, b1, b2, b3);
+      mma16816<E>(s[0], qf, b0, b1);
+      mma16816<E>(s[1], qf, b2, b3);
     }
     float *sp = s_part + warp * kDHeads * kDTok;
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < 2; ++a)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const int head = (lane >> 2) + (cc >= 2 ? 8 : 0);
         const int tok = a * 8 + (lane & 3) * 2 + (cc & 1);
         sp[head * kDTok + tok] = s[a][cc];
       }
-    __syncthreads();
-    // online softmax for (sm_head, 4 tokens)
+    group_sync(grp);
+    // online softmax for (sm_head, 2 tokens)
     {
-      float x[4];
+      float x[2];
       float mx = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 2; ++u) {
         const int tok = sm_tok + u;
-        const int gtok = t * kDTok + tok;
+        const int gtok = tile * kDTok + tok;
         float v = s_part[sm_head * kDTok + tok] + s_part[kDHeads * kDTok + sm_head * kDTok + tok] +
                   s_part[2 * kDHeads * kDTok + sm_head * kDTok + tok] +
                   s_part[3 * kDHeads * kDTok + sm_head * kDTok + tok];
@@ -198,74 +228,100 @@ __global__ void __launch_bounds__(128) k_sparse_decode(const DecodeLaunch L) {
       m_run = m_new;
       float ls = 0.f;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 2; ++u) {
         x[u] = exp2f(fmaf(x[u], sl2, -b));
         ls += x[u];
       }
       l_run = l_run * alpha + ls;
-      uint2 pk = make_uint2(E::from_f2(x[0], x[1]), E::from_f2(x[2], x[3]));
-      *reinterpret_cast<uint2 *>(s_p + sm_head * P_LD + sm_tok) = pk;
-      if ((tid & 7) == 0) s_alpha[sm_head] = alpha;
+      *reinterpret_cast<uint32_t *>(s_p + sm_head * G::kPLd + sm_tok) = E::from_f2(x[0], x[1]);
+      if ((gtid & 7) == 0) s_alpha[sm_head] = alpha;
     }
-    __syncthreads();
+    group_sync(grp);
     // O = alpha * O + P V over this warp's DV/4 columns
     {
       const float a0 = s_alpha[lane >> 2], a1 = s_alpha[(lane >> 2) + 8];
+      // alpha is exactly 1 for a head whose running max did not move
+      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-      for (int a = 0; a < DV / 32; ++a) {
-        o[a][0] *= a0; o[a][1] *= a0; o[a][2] *= a1; o[a][3] *= a1;
-      }
-      const uint32_t sP = smem_u32(s_p);
-#pragma unroll
-      for (int kk = 0; kk < kDTok / 16; ++kk) {
-        uint32_t pa[4];
-        ldsm_x4(sP + (lane & 15) * (P_LD * 2) + (kk * 2 + (lane >> 4)) * 16, pa[0], pa[1], pa[2],
-                pa[3]);
-#pragma unroll
-        for (int dp = 0; dp < DV / 64; ++dp) {
-          const int mi = lane >> 3;
-          const int tok = kk * 16 + (mi & 1) * 8 + (lane & 7);
-          const int ch = (warp * (DV / 4) + dp * 16) / 8 + (mi >> 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(kv + swz<D>(tok, ch), b0, b1, b2, b3);
-          mma16816<E>(o[2 * dp], pa, b0, b1);
-          mma16816<E>(o[2 * dp + 1], pa, b2, b3);
+        for (int a = 0; a < DV / 32; ++a) {
+          o[a][0] *= a0; o[a][1] *= a0; o[a][2] *= a1; o[a][3] *= a1;
         }
       }
+      const uint32_t sP = smem_u32(s_p);
+      uint32_t pa[4];
+      ldsm_x4(sP + (lane & 15) * (G::kPLd * 2) + (lane >> 4) * 16, pa[0], pa[1], pa[2], pa[3]);
+#pragma unroll
+      for (int dp = 0; dp < DV / 64; ++dp) {
+        const int mi = lane >> 3;
+        const int tok = (mi & 1) * 8 + (lane & 7);
+        const int ch = (warp * (DV / 4) + dp * 16) / 8 + (mi >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(kv + swz<D>(tok, ch), b0, b1, b2, b3);
+        mma16816<E>(o[2 * dp], pa, b0, b1);
+        mma16816<E>(o[2 * dp + 1], pa, b2, b3);
+      }
     }
-    __syncthreads();
+    group_sync(grp);
   }
-  // epilogue
+
+  // merge the two groups' states (running max m in base 2, sum l, O) per head
   {
     float l = l_run;
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     l += __shfl_xor_sync(0xffffffffu, l, 4);
-    if ((tid & 7) == 0) {
-      s_l[sm_head] = l;
-      const bool live = l > 0.f;
-      L.lse_part[((size_t)split * L.n_q + c) * kDHeads + sm_head] =
-          live ? m_run * 0.6931471805599453f + logf(l) : -INFINITY;
+    if ((gtid & 7) == 0) {
+      s_ml[(2 * grp) * kDHeads + sm_head] = m_run;
+      s_ml[(2 * grp + 1) * kDHeads + sm_head] = l;
     }
   }
+  // group 1's O goes to its own (now idle) KV tiles, laid out by thread
+  float *s_o1 = reinterpret_cast<float *>(smem + kDHeads * D * 2 + G::kBytes);
+  if (grp == 1) {
+#pragma unroll
+    for (int a = 0; a < DV / 32; ++a)
+      *reinterpret_cast<float4 *>(s_o1 + ((size_t)a * 128 + gtid) * 4) =
+          make_float4(o[a][0], o[a][1], o[a][2], o[a][3]);
+  }
   __syncthreads();
-  const float l0 = s_l[lane >> 2], l1 = s_l[(lane >> 2) + 8];
-  const float i0 = l0 > 0.f ? 1.0f / l0 : 0.f, i1 = l1 > 0.f ? 1.0f / l1 : 0.f;
+  if (grp != 0) return;
+  float w0[2], w1[2], inv[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = (lane >> 2) + 8 * hh;
+    const float m0 = s_ml[h], l0 = s_ml[kDHeads + h];
+    const float m1 = s_ml[2 * kDHeads + h], l1 = s_ml[3 * kDHeads + h];
+    const float m = fmaxf(m0, m1);
+    w0[hh] = m == -INFINITY ? 0.f : exp2f(m0 - m);
+    w1[hh] = m == -INFINITY ? 0.f : exp2f(m1 - m);
+    const float l = w0[hh] * l0 + w1[hh] * l1;
+    inv[hh] = l > 0.f ? 1.0f / l : 0.f;
+  }
+  if ((gtid & 7) == 0) {
+    const int h = sm_head;
+    const float m0 = s_ml[h], l0 = s_ml[kDHeads + h];
+    const float m1 = s_ml[2 * kDHeads + h], l1 = s_ml[3 * kDHeads + h];
+    const float m = fmaxf(m0, m1);
+    const float l = m == -INFINITY ? 0.f : exp2f(m0 - m) * l0 + exp2f(m1 - m) * l1;
+    L.lse_part[((size_t)split * L.n_q + c) * kDHeads + h] =
+        l > 0.f ? m * 0.6931471805599453f + logf(l) : -INFINITY;
+  }
   float *dst = L.o_part + ((size_t)split * L.n_q + c) * kDHeads * DV;
 #pragma unroll
   for (int a = 0; a < DV / 32; ++a) {
+    const float4 p1 = *reinterpret_cast<const float4 *>(s_o1 + ((size_t)a * 128 + gtid) * 4);
     const int col = warp * (DV / 4) + a * 8 + (lane & 3) * 2;
     const int h0 = lane >> 2;
-    *reinterpret_cast<float2 *>(dst + (size_t)h0 * DV + col) = make_float2(o[a][0] * i0, o[a][1] * i0);
+    *reinterpret_cast<float2 *>(dst + (size_t)h0 * DV + col) =
+        make_float2((w0[0] * o[a][0] + w1[0] * p1.x) * inv[0], (w0[0] * o[a][1] + w1[0] * p1.y) * inv[0]);
     *reinterpret_cast<float2 *>(dst + (size_t)(h0 + 8) * DV + col) =
-        make_float2(o[a][2] * i1, o[a][3] * i1);
+        make_float2((w0[1] * o[a][2] + w1[1] * p1.z) * inv[1], (w0[1] * o[a][3] + w1[1] * p1.w) * inv[1]);
   }
 }
 
 template <class E, int D, int DV>
 size_t decode_smem(int chunk) {
-  return (size_t)kDHeads * D * 2 + 2 * (size_t)kDTok * D * 2 + 4 * kDHeads * kDTok * 4 +
-         kDHeads * (kDTok + 8) * 2 + 2 * kDHeads * 4 + (size_t)chunk * 4;
+  return dec_fixed_bytes<D>() + (size_t)chunk * 4;
 }
 
 template <class E>
@@ -275,7 +331,7 @@ cudaError_t launch_e(const DecodeLaunch &L, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k_sparse_decode<E, 576, 512>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_sparse_decode<E, 576, 512><<<L.n_q * L.num_splits, 128, smem, st>>>(L);
+  k_sparse_decode<E, 576, 512><<<L.n_q * L.num_splits, kDThreads, smem, st>>>(L);
   return cudaGetLastError();
 }
 
