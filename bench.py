@@ -226,6 +226,37 @@ def run_ours(args):
         fbm.sparse_fmha_fwd_pairs(q, k, v, None if dense else plut, None if dense else pcnt,
                                   scale=cfg.scale, out=out)
 
+    def overlap_pair_gain():
+        """(|A| + |B|) / |A u B| summed over q-block pairs chosen by LUT
+        overlap within each head: each q block in order takes its unmatched
+        partner of largest overlap (greedy; a statistic, not a kernel path)."""
+        m = torch.zeros((cfg.b * cfg.hq, nq, nq + 1), dtype=torch.float32, device="cuda")
+        ar = torch.arange(nq, device="cuda")
+        idx = torch.where(ar[None, None, :] < cnt.view(-1, nq, 1), lut.view(-1, nq, nq).long(),
+                          torch.full_like(lut.view(-1, nq, nq).long(), nq))
+        m.scatter_(2, idx, 1.0)
+        m = m[:, :, :nq]
+        ov = torch.bmm(m, m.transpose(1, 2)).cpu().numpy()
+        sizes = cnt.view(-1, nq).cpu().numpy().astype(np.int64)
+        tot = uni = 0
+        for hh in range(ov.shape[0]):
+            o = ov[hh]
+            free = np.ones(nq, dtype=bool)
+            for i in range(nq):
+                if not free[i]:
+                    continue
+                free[i] = False
+                cand = np.where(free, o[i], -1.0)
+                j = int(cand.argmax())
+                if cand[j] < 0:  # i is left alone (odd count)
+                    tot += sizes[hh, i]
+                    uni += sizes[hh, i]
+                    continue
+                free[j] = False
+                tot += sizes[hh, i] + sizes[hh, j]
+                uni += sizes[hh, i] + sizes[hh, j] - int(o[i, j])
+        return round(tot / uni, 3) if uni else None
+
     def timed(fn, steps, warm):
         for _ in range(warm):
             fn()
@@ -310,8 +341,10 @@ def run_ours(args):
                           "eff_tflops_step": round(tl * FLOP_PER_TILE / ((a + bm) * 1e-3) / 1e12, 1),
                           "speedup_vs_dense_attn": round(dense_ms / a, 3),
                           "speedup_vs_dense_step": round(dense_ms / (a + bm), 3),
-                          # q-block pairs: (|A| + |B|) / |A u B| over adjacent q blocks
+                          # q-block pairs: (|A| + |B|) / |A u B| over adjacent q blocks,
+                          # and over pairs chosen by LUT overlap within the head
                           "pair_union_gain": round(tl / ul, 3) if ul else None,
+                          "pair_union_gain_by_overlap": overlap_pair_gain(),
                           "pairs_attn_ms": round(ap, 4), "pair_union_ms": round(un, 4),
                           "pairs_eff_tflops_attn": round(tl * FLOP_PER_TILE / (ap * 1e-3) / 1e12, 1)})
         block_map(args.topk)
