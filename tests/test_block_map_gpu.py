@@ -185,3 +185,52 @@ def test_smooth_k_c3_sampled_heads(fbm_gpu):
     heads = [(0, 3), (1, 30)]
     run_case(fbm_gpu, synth.C3, "topk", 0.4, heads=heads, smooth_k=True)
 
+
+
+def _tied_case(fbm, cfg, period, mode, param):
+    """K blocks j set to copies of block j mod `period` (every block when
+    period = 1), so the pooled scores of a row take only `period` distinct
+    values, each many times over: the selection threshold falls inside a group
+    of exactly equal scores and the lower kv blocks must be taken first.  The
+    GPU scores of identical blocks are bitwise equal, so every row must match
+    the oracle exactly."""
+    x = dict(cached_prefill(cfg))
+    k = x["k"].copy()
+    nb = cfg.nq
+    for j in range(period, nb):
+        src = j % period
+        k[:, :, j * 64:(j + 1) * 64, :] = k[:, :, src * 64:(src + 1) * 64, :]
+    q_d, k_d = to_dev(x["q"], cfg.dtype), to_dev(k, cfg.dtype)
+    ph = synth.per_head(cfg, param)
+    th = synth.per_head(cfg, cfg.simthreshd1)
+    kw = {"topk": ph.tolist()} if mode == "topk" else {"cdfthreshd": ph.tolist()}
+    lut, cnt, _ = fbm.sparge_block_map(q_d, k_d, simthreshd1=th.tolist(), scale=cfg.scale,
+                                       causal=cfg.causal, attention_sink=cfg.attention_sink, **kw)
+    assert fbm.get_error() == 0
+    lut, cnt = lut.cpu().numpy(), cnt.cpu().numpy()
+    ora = oracle.sparge_block_map(x["q"], k, ph if mode == "topk" else None,
+                                  ph if mode == "cdf" else None, th, cfg.scale, cfg.causal,
+                                  cfg.attention_sink, dtype=cfg.dtype)
+    assert (cnt == ora["count"]).all()
+    assert (lut == ora["lut"]).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("period", [5, 1])
+def test_exact_ties_take_lower_blocks_first(fbm_gpu, causal, period):
+    # nq = 64: about 13 copies of each score (the in-bin ranking with ties),
+    # or a single value (a zero score range: the bitwise search)
+    cfg = synth.C1.replace(b=1, hq=2, hk=2, s=4096, d=128, dtype="f16", causal=causal)
+    _tied_case(fbm_gpu, cfg, period, "topk", 0.3)
+
+
+def test_exact_ties_in_a_crowded_bin(fbm_gpu):
+    # nq = 256: about 51 equal scores per value, more than a warp can rank
+    # pairwise, so the crossing bin goes through the bitwise search
+    cfg = synth.C1.replace(b=1, hq=2, hk=1, s=16384, d=128, dtype="bf16")
+    _tied_case(fbm_gpu, cfg, 5, "topk", 0.45)
+
+
+def test_exact_ties_cdf(fbm_gpu):
+    cfg = synth.C1.replace(b=1, hq=2, hk=2, s=4096, d=64, dtype="f16")
+    _tied_case(fbm_gpu, cfg, 7, "cdf", 0.6)

@@ -75,3 +75,11 @@ def test_full_decode_sampled(fbm_gpu):
     cache = gpu_cache(cfg)
     for S in (2, 4, 8):
         run(fbm_gpu, cfg, S, inp=inp, cache=cache, queries=[0, 13, 37, 63])
+
+
+@pytest.mark.parametrize("S", [17, 20, 32])
+def test_short_chunks(fbm_gpu, S):
+    # 300 tokens in 17 / 20 / 32 chunks: 17-18, 15 and 9-10 tokens each, so a
+    # chunk has two 16-token tiles, one full tile or one partial tile (the
+    # second warp group of the CTA then has one short tile or none)
+    run(fbm_gpu, SMALL, S)
