@@ -194,30 +194,37 @@ __global__ void __launch_bounds__(kDThreads, 2) k_sparse_decode(const DecodeLaun
       mma16816<E>(s[0], qf, b0, b1);
       mma16816<E>(s[1], qf, b2, b3);
     }
+    // the warp's partial scores, two adjacent tokens per 8-byte store (the
+    // softmax threads below read them back the same way, without conflicts)
     float *sp = s_part + warp * kDHeads * kDTok;
 #pragma unroll
     for (int a = 0; a < 2; ++a)
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int head = (lane >> 2) + (cc >= 2 ? 8 : 0);
-        const int tok = a * 8 + (lane & 3) * 2 + (cc & 1);
-        sp[head * kDTok + tok] = s[a][cc];
+      for (int hh = 0; hh < 2; ++hh) {
+        const int head = (lane >> 2) + 8 * hh;
+        const int tok = a * 8 + (lane & 3) * 2;
+        *reinterpret_cast<float2 *>(sp + head * kDTok + tok) =
+            make_float2(s[a][2 * hh], s[a][2 * hh + 1]);
       }
     group_sync(grp);
     // online softmax for (sm_head, 2 tokens)
     {
       float x[2];
       float mx = -INFINITY;
+      {
+        const float *pp = s_part + sm_head * kDTok + sm_tok;
+        const float2 p0 = *reinterpret_cast<const float2 *>(pp);
+        const float2 p1 = *reinterpret_cast<const float2 *>(pp + kDHeads * kDTok);
+        const float2 p2 = *reinterpret_cast<const float2 *>(pp + 2 * kDHeads * kDTok);
+        const float2 p3 = *reinterpret_cast<const float2 *>(pp + 3 * kDHeads * kDTok);
+        x[0] = p0.x + p1.x + p2.x + p3.x;
+        x[1] = p0.y + p1.y + p2.y + p3.y;
+      }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int tok = sm_tok + u;
-        const int gtok = tile * kDTok + tok;
-        float v = s_part[sm_head * kDTok + tok] + s_part[kDHeads * kDTok + sm_head * kDTok + tok] +
-                  s_part[2 * kDHeads * kDTok + sm_head * kDTok + tok] +
-                  s_part[3 * kDHeads * kDTok + sm_head * kDTok + tok];
-        if (gtok >= n || s_rows[gtok] < 0) v = -INFINITY;
-        x[u] = v;
-        mx = fmaxf(mx, v);
+        const int gtok = tile * kDTok + sm_tok + u;
+        if (gtok >= n || s_rows[gtok] < 0) x[u] = -INFINITY;
+        mx = fmaxf(mx, x[u]);
       }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
