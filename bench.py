@@ -72,6 +72,16 @@ def parse():
     return args
 
 
+def headline_config(cfg, topk, small=False):
+    """The `config` object of the JSON line (the same for both arms)."""
+    in_mb = cfg.b * (cfg.hq + 2 * cfg.hk) * cfg.s * cfg.d * 2 / 1e6
+    return {"workload": f"b{cfg.b} h{cfg.hq} s{cfg.s} d{cfg.d} fp16 non-causal, BLKQ=BLKK=64, "
+                        f"topk={topk}, simthreshd1=0.001"
+                        + (" (small profiling case)" if small else ""),
+            "b": cfg.b, "h": cfg.hq, "s": cfg.s, "d": cfg.d, "topk": topk,
+            "l2": f"inputs ({in_mb:.0f} MB) larger than L2; no flush"}
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -496,11 +506,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded centroid-plus-noise blocks, 25% diffuse)",
-        "config": {"workload": f"b{cfg.b} h{cfg.hq} s{cfg.s} d{cfg.d} fp16 non-causal, "
-                               f"BLKQ=BLKK=64, topk={args.topk}, simthreshd1=0.001"
-                               + (" (small profiling case)" if args.small else ""),
-                   "b": cfg.b, "h": cfg.hq, "s": cfg.s, "d": cfg.d, "topk": args.topk,
-                   "l2": f"inputs ({3 * q.numel() * 2 / 1e6:.0f} MB) larger than L2; no flush"},
+        "config": headline_config(cfg, args.topk, args.small),
         "speedup_vs_dense": {"dense_attn_ms": round(dense_ms, 4),
                              "dense_kernel": "sparse_fmha_fwd_pairs, no LUT (128-row tiles)",
                              "dense_eff_tflops": round(4 * cfg.b * cfg.hq * cfg.s * cfg.s * cfg.d
@@ -790,14 +796,13 @@ def run_reference(args):
     for _ in range(args.steps):
         vals.append(cpu_baseline(cfg, x, args.topk, qblocks=8, heads=1))
     t_all = time.perf_counter() - t_all
-    v = statistics.mean(r["value"] for r in vals)
+    v = round(statistics.mean(r["value"] for r in vals), 6)
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * t_all / args.steps, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded centroid-plus-noise blocks, 25% diffuse)",
-            "config": {"workload": "b2 h32 s16384 d128 fp16 non-causal, BLKQ=BLKK=64, "
-                                   f"topk={args.topk}, simthreshd1=0.001"},
+            "config": headline_config(synth.C3, args.topk),
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(),
                              "kind": "oracle", "sample": vals[0]["sample"]},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
