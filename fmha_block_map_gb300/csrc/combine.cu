@@ -1,12 +1,13 @@
 // LSE combine of split-KV partials (Incremental_FlashAttention updating_log,
 // Stage 1: the lse_max trick; ROCm/aiter pull 4919: the split-KV reduce).
 //
-// One warp per output row: lanes first read the S partial LSEs, form
-// m = max_s LSE_s and the weights w_s = exp(LSE_s - m), then stream the S
-// partial rows with 128-bit loads and write sum_s w_s O_s / sum_s w_s.  A row
-// whose partials are all -inf (empty) writes O = 0 and LSE = -inf.  The kernel
-// is bandwidth-bound: it reads S * (dv + 1) * 4 bytes and writes dv elements
-// (+ 4 bytes of LSE) per row.
+// One warp per output row: lanes read the S partial LSEs, form
+// m = max_s LSE_s and the weights w_s = exp(LSE_s - m), and stream the S
+// partial rows with 128-bit loads, up to 8 partials in flight per lane (the
+// first 8 issued before the weights are known), writing
+// sum_s w_s O_s / sum_s w_s.  A row whose partials are all -inf (empty) writes
+// O = 0 and LSE = -inf.  The kernel is bandwidth-bound: it reads
+// S * (dv + 1) * 4 bytes and writes dv elements (+ 4 bytes of LSE) per row.
 #include <type_traits>
 
 #include "common.cuh"
@@ -17,6 +18,8 @@ namespace {
 
 constexpr int kMaxSplits = 64;
 
+constexpr int kBatch = 8;  // partial rows loaded per lane before they are weighted
+
 template <int OUT>  // 0 = f16, 1 = bf16, 2 = f32
 __global__ void __launch_bounds__(256) k_attn_combine(const CombineLaunch L) {
   const int lane = threadIdx.x & 31;
@@ -26,6 +29,20 @@ __global__ void __launch_bounds__(256) k_attn_combine(const CombineLaunch L) {
   float l0 = -INFINITY, l1 = -INFINITY;
   if (lane < L.num_splits) l0 = L.lse_part[(int64_t)lane * L.rows + row];
   if (lane + 32 < L.num_splits) l1 = L.lse_part[(int64_t)(lane + 32) * L.rows + row];
+  // the partial rows of a batch are loaded before they are weighted, so their
+  // latency overlaps (for the first batch, the weights' own load and shuffles)
+  auto load_batch = [&](float4 (&x)[kBatch], int c, int s0) {
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int s = s0 + j;
+      x[j] = (s < L.num_splits && c < L.dv)
+                 ? __ldg(reinterpret_cast<const float4 *>(
+                       L.o_part + ((int64_t)s * L.rows + row) * L.dv + c))
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  float4 x[kBatch];
+  load_batch(x, lane * 4, 0);
   const float m = warp_max(fmaxf(l0, l1));
   const bool live = m != -INFINITY;
   const float w0 = live ? expf(l0 - m) : 0.f;
@@ -37,16 +54,19 @@ __global__ void __launch_bounds__(256) k_attn_combine(const CombineLaunch L) {
     const int c = c0 + lane * 4;
     const bool act = c < L.dv;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live) {
-      for (int s = 0; s < L.num_splits; ++s) {
+    for (int s0 = 0; s0 < L.num_splits; s0 += kBatch) {
+      if (c0 > 0 || s0 > 0) load_batch(x, c, s0);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int s = s0 + j;
         const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-        if (w == 0.f || !act) continue;  // an empty partial (weight 0) is skipped
-        const float4 x = __ldg(reinterpret_cast<const float4 *>(
-            L.o_part + ((int64_t)s * L.rows + row) * L.dv + c));
-        acc.x = fmaf(w, x.x, acc.x);
-        acc.y = fmaf(w, x.y, acc.y);
-        acc.z = fmaf(w, x.z, acc.z);
-        acc.w = fmaf(w, x.w, acc.w);
+        // an empty partial (weight 0) adds nothing, whatever its row holds
+        if (s < L.num_splits && w != 0.f) {
+          acc.x = fmaf(w, x[j].x, acc.x);
+          acc.y = fmaf(w, x[j].y, acc.y);
+          acc.z = fmaf(w, x[j].z, acc.z);
+          acc.w = fmaf(w, x[j].w, acc.w);
+        }
       }
     }
     if (!act) continue;
