@@ -82,9 +82,91 @@ __global__ void __launch_bounds__(256) k_attn_combine(const CombineLaunch L) {
   if (L.lse_out && lane == 0) L.lse_out[row] = live ? m + logf(wsum) : -INFINITY;
 }
 
+// Few splits (S <= 8): one thread per (row, CH chunks of 4 columns), unrolled
+// for at most SMAX splits.  Each thread reads the row's S LSEs itself (the
+// threads of a row share them through L1) and all of its S x CH partial
+// chunks at once, then weights them: no cross-lane reduction and no load
+// waiting on another, and with few registers many threads keep loads in
+// flight.  Same order of operations as the warp kernel above, so the results
+// are identical.
+constexpr int kSmallSplits = 8;
+
+template <int OUT, int SMAX, int CH>
+__global__ void __launch_bounds__(256) k_attn_combine_few(const CombineLaunch L) {
+  const int per_row = L.dv / (4 * CH);
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= L.rows * per_row) return;
+  const int64_t row = t / per_row;
+  const int c = (int)(t - row * per_row) * 4 * CH;
+  float l[SMAX];
+  float4 x[SMAX][CH];
+#pragma unroll
+  for (int s = 0; s < SMAX; ++s) {
+    const bool in = s < L.num_splits;
+    l[s] = in ? __ldg(L.lse_part + (int64_t)s * L.rows + row) : -INFINITY;
+    const float4 *src = reinterpret_cast<const float4 *>(L.o_part + ((int64_t)s * L.rows + row) * L.dv + c);
+#pragma unroll
+    for (int h = 0; h < CH; ++h) x[s][h] = in ? __ldg(src + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < SMAX; ++s) m = fmaxf(m, l[s]);
+  const bool live = m != -INFINITY;
+  float4 acc[CH];
+#pragma unroll
+  for (int h = 0; h < CH; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+#pragma unroll
+  for (int s = 0; s < SMAX; ++s) {
+    const float w = live ? expf(l[s] - m) : 0.f;
+    wsum += w;
+    // an empty partial (weight 0) adds nothing, whatever its row holds
+    if (w != 0.f) {
+#pragma unroll
+      for (int h = 0; h < CH; ++h) {
+        acc[h].x = fmaf(w, x[s][h].x, acc[h].x);
+        acc[h].y = fmaf(w, x[s][h].y, acc[h].y);
+        acc[h].z = fmaf(w, x[s][h].z, acc[h].z);
+        acc[h].w = fmaf(w, x[s][h].w, acc[h].w);
+      }
+    }
+  }
+  const float inv = live ? 1.0f / wsum : 0.f;
+#pragma unroll
+  for (int h = 0; h < CH; ++h) {
+    float4 a = acc[h];
+    a.x *= inv; a.y *= inv; a.z *= inv; a.w *= inv;
+    if constexpr (OUT == 2) {
+      reinterpret_cast<float4 *>(static_cast<float *>(L.out) + row * L.dv + c)[h] = a;
+    } else {
+      using E = typename std::conditional<OUT == 1, BF16, F16>::type;
+      reinterpret_cast<uint2 *>(static_cast<uint16_t *>(L.out) + row * L.dv + c)[h] =
+          make_uint2(E::from_f2(a.x, a.y), E::from_f2(a.z, a.w));
+    }
+  }
+  if (L.lse_out && c == 0) L.lse_out[row] = live ? m + logf(wsum) : -INFINITY;
+}
+
+template <int SMAX, int CH>
+cudaError_t launch_few(const CombineLaunch &L, cudaStream_t st) {
+  const int64_t threads = L.rows * (L.dv / (4 * CH));
+  const unsigned grid = (unsigned)((threads + 255) / 256);
+  if (L.out_dtype == FBM_F32) k_attn_combine_few<2, SMAX, CH><<<grid, 256, 0, st>>>(L);
+  else if (L.out_dtype == FBM_BF16) k_attn_combine_few<1, SMAX, CH><<<grid, 256, 0, st>>>(L);
+  else k_attn_combine_few<0, SMAX, CH><<<grid, 256, 0, st>>>(L);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const CombineLaunch &L, cudaStream_t st) {
+  // few splits: the per-thread kernel (its grid must fit one dimension)
+  if (L.num_splits <= kSmallSplits && L.rows * (L.dv / 4) / 256 < 0x7fffffff) {
+    const bool two = L.dv % 8 == 0;  // two chunks of 4 columns per thread
+    if (L.num_splits <= 2) return two ? launch_few<2, 2>(L, st) : launch_few<2, 1>(L, st);
+    if (L.num_splits <= 4) return two ? launch_few<4, 2>(L, st) : launch_few<4, 1>(L, st);
+    return launch_few<8, 1>(L, st);
+  }
   const int64_t threads = L.rows * 32;
   const unsigned grid = (unsigned)((threads + 255) / 256);
   if (L.out_dtype == FBM_F32) k_attn_combine<2><<<grid, 256, 0, st>>>(L);
