@@ -553,6 +553,31 @@ def run_ours(args):
 # ----------------------------------------------------------------------------
 
 
+def _graph_ms(fn, reps=20, warm=3):
+    """Device time of a short, launch-bound call: `reps` calls captured in one
+    CUDA graph, the graph replayed (after `warm` eager calls) and timed with
+    CUDA events, per call."""
+    import torch
+
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def _events_ms(fn, steps, warm):
     import torch
 
@@ -640,7 +665,9 @@ def measure_decode(hbm_gbs, small=False):
                                             num_splits=S, o_partial=op, lse_partial=lp)
         comb = lambda: fbm.attn_combine(op, lp, out=o, return_lse=False)
         d_ms = _events_ms(dec, 20, 3)
-        c_ms = _events_ms(comb, 20, 3)
+        # a few µs of device work: timed inside a CUDA graph, or the host's
+        # launch overhead would be measured instead
+        c_ms = _graph_ms(comb, 20, 3)
         rows_bytes = cfg.n_queries * cfg.topk * cfg.d * 2
         part_bytes = S * cfg.n_queries * cfg.hq * (cfg.dv + 1) * 4
         d_bytes = rows_bytes + q.numel() * 2 + ix.numel() * 4 + part_bytes \
