@@ -52,6 +52,9 @@ def lib() -> ctypes.CDLL:
                                         f32, i32, i32, i32, vp, vp, vp, vp, sz, vp])
         L.sparge_block_map_static.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp,
                                                vp, f32, i32, i32, i32, vp, vp, vp, vp])
+        L.sparge_block_map_e4m3.argtypes = ([vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp,
+                                             vp, f32, i32, i32, i32, vp, vp, vp, vp, sz, vp, vp, vp,
+                                             vp, vp])
         L.sparse_fmha_fwd.argtypes = ([vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                        vp, vp, i32, i32, f32, i32, i32, f32, vp, vp, vp, vp, vp])
         L.attn_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
@@ -173,6 +176,52 @@ def sparge_block_map(q: torch.Tensor, k: torch.Tensor, *, topk=None, cdfthreshd=
         _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return lut, lut_count, bmap
+
+
+def sparge_block_map_e4m3(q: torch.Tensor, k: torch.Tensor, *, topk=None, cdfthreshd=None,
+                          simthreshd1: Union[float, Sequence[float]] = 0.001,
+                          scale: Optional[float] = None, causal: bool = False,
+                          attention_sink: bool = False, return_block_map: bool = False,
+                          lut: Optional[torch.Tensor] = None,
+                          lut_count: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, smooth_k: bool = False,
+                          q8: Optional[torch.Tensor] = None, q_scale: Optional[torch.Tensor] = None,
+                          k8: Optional[torch.Tensor] = None, k_scale: Optional[torch.Tensor] = None,
+                          stream=None):
+    """sparge_block_map plus the e4m3 codes and per-block scales of q and k
+    (those of quantize_e4m3_blocks) from the same pass; d = 128.  Returns
+    (lut, lut_count, block_map or None, q8, q_scale, k8, k_scale)."""
+    _cuda(q, "q"), _cuda(k, "k")
+    b, hq, s, d = q.shape
+    hk = k.shape[1]
+    nq = (s + 63) // 64
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = q.device
+    if lut is None:
+        lut = torch.empty((b, hq, nq, nq), dtype=torch.int32, device=dev)
+    if lut_count is None:
+        lut_count = torch.empty((b, hq, nq), dtype=torch.int32, device=dev)
+    bmap = torch.empty((b, hq, nq, nq), dtype=torch.uint8, device=dev) if return_block_map else None
+    need = block_map_workspace_bytes(b, hq, hk, s, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if q8 is None:
+        q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
+    if k8 is None:
+        k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+    if q_scale is None:
+        q_scale = torch.empty((b, hq, nq), dtype=torch.float32, device=dev)
+    if k_scale is None:
+        k_scale = torch.empty((b, hk, nq), dtype=torch.float32, device=dev)
+    _check(lib().sparge_block_map_e4m3(
+        _ptr(q), _ptr(k), _dt(q), b, hq, hk, s, d, 64, 64,
+        _per_head(topk, hq, "topk"), _per_head(cdfthreshd, hq, "cdfthreshd"),
+        _per_head(simthreshd1, hq, "simthreshd1"), float(scale), int(causal),
+        int(attention_sink), int(smooth_k), _ptr(lut), _ptr(lut_count), _ptr(bmap),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(q8), _ptr(q_scale),
+        _ptr(k8), _ptr(k_scale), _stream(stream)))
+    return lut, lut_count, bmap, q8, q_scale, k8, k_scale
 
 
 def sparge_block_map_static(q: torch.Tensor, k: torch.Tensor, *, topk=None, cdfthreshd=None,

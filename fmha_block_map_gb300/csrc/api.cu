@@ -118,12 +118,15 @@ size_t fbm_workspace_bytes(int b, int hq, int hk, int s, int d) {
   return fbm_block_map_workspace_bytes(b, hq, hk, s, d, 64, 64);
 }
 
-fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int hq, int hk,
-                            int s, int d, int blkq, int blkk, const float *topk,
-                            const float *cdfthreshd, const float *simthreshd1, float scale,
-                            int causal, int attention_sink, int smooth_k, int32_t *lut,
-                            int32_t *lut_count, uint8_t *block_map, void *workspace,
-                            size_t workspace_bytes, void *stream) {
+namespace {
+
+// the block map, and (q8 != NULL) the e4m3 codes of Q and K from the same pass
+fbm_status block_map_impl(const void *q, const void *k, int dtype, int b, int hq, int hk, int s,
+                          int d, int blkq, int blkk, const float *topk, const float *cdfthreshd,
+                          const float *simthreshd1, float scale, int causal, int attention_sink,
+                          int smooth_k, int32_t *lut, int32_t *lut_count, uint8_t *block_map,
+                          void *workspace, size_t workspace_bytes, uint8_t *q8, float *q_scale,
+                          uint8_t *k8, float *k_scale, void *stream) {
   if (!q || !k || !lut || !lut_count || !workspace || !simthreshd1)
     return fail(FBM_ERR_INVALID_ARG, "sparge_block_map: null pointer argument");
   if (b <= 0 || hq <= 0 || hk <= 0 || s <= 0 || d <= 0)
@@ -172,10 +175,41 @@ fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int 
   L.ksim = reinterpret_cast<float *>(ws + w.ksim);
   L.kmu = reinterpret_cast<float *>(ws + w.kmu);
   L.lut = lut; L.cnt = lut_count; L.bmap = block_map;
+  L.q8 = q8; L.q_scale = q_scale; L.k8 = k8; L.k_scale = k_scale;
   L.err = error_word();
   if (!L.err) return fail(FBM_ERR_CUDA, "sparge_block_map: error word lookup failed");
   return cuda_status(fbm::launch_block_map(L, static_cast<cudaStream_t>(stream)),
                      "sparge_block_map launch");
+}
+
+}  // namespace
+
+fbm_status sparge_block_map(const void *q, const void *k, int dtype, int b, int hq, int hk,
+                            int s, int d, int blkq, int blkk, const float *topk,
+                            const float *cdfthreshd, const float *simthreshd1, float scale,
+                            int causal, int attention_sink, int smooth_k, int32_t *lut,
+                            int32_t *lut_count, uint8_t *block_map, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+  return block_map_impl(q, k, dtype, b, hq, hk, s, d, blkq, blkk, topk, cdfthreshd, simthreshd1,
+                        scale, causal, attention_sink, smooth_k, lut, lut_count, block_map,
+                        workspace, workspace_bytes, nullptr, nullptr, nullptr, nullptr, stream);
+}
+
+fbm_status sparge_block_map_e4m3(const void *q, const void *k, int dtype, int b, int hq, int hk,
+                                 int s, int d, int blkq, int blkk, const float *topk,
+                                 const float *cdfthreshd, const float *simthreshd1, float scale,
+                                 int causal, int attention_sink, int smooth_k, int32_t *lut,
+                                 int32_t *lut_count, uint8_t *block_map, void *workspace,
+                                 size_t workspace_bytes, uint8_t *q8, float *q_scale, uint8_t *k8,
+                                 float *k_scale, void *stream) {
+  if (!q8 || !q_scale || !k8 || !k_scale)
+    return fail(FBM_ERR_INVALID_ARG, "sparge_block_map_e4m3: null code or scale buffer");
+  if (d != 128) return fail(FBM_ERR_UNSUPPORTED, "sparge_block_map_e4m3: d = 128 only");
+  if (!aligned16(q8) || !aligned16(k8))
+    return fail(FBM_ERR_INVALID_ARG, "sparge_block_map_e4m3: code buffers must be 16-byte aligned");
+  return block_map_impl(q, k, dtype, b, hq, hk, s, d, blkq, blkk, topk, cdfthreshd, simthreshd1,
+                        scale, causal, attention_sink, smooth_k, lut, lut_count, block_map,
+                        workspace, workspace_bytes, q8, q_scale, k8, k_scale, stream);
 }
 
 int fbm_fmha_kernel_kind(int dtype, int d, int dv, int num_splits, int s_q, int s_k) {

@@ -28,6 +28,8 @@
 #include <algorithm>
 #include <atomic>
 
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -46,6 +48,8 @@ struct PoolSide {
   int nb;             // blocks per (batch, head)
   int nunits;         // bh * nb
   const float *mu;    // [bh, D] row subtracted before pooling (SMOOTH only)
+  uint8_t *codes;     // [bh, s, D] e4m3 codes of the raw rows (QUANT only)
+  float *scales;      // [bh * nb] one scale per block (QUANT only)
 };
 
 // x = x0 + x1 + x2 in bf16, each difference exact in fp32: the three terms
@@ -85,8 +89,9 @@ struct PoolRing {
   static constexpr int kSmem = kFlagOff + 16 + 128;  // + alignment slack
 };
 
-template <class E, int D, bool SMOOTH>
+template <class E, int D, bool SMOOTH, bool QUANT>
 __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolSide ks, uint32_t *err) {
+  static_assert(!QUANT || (D == 128 && !SMOOTH), "e4m3 codes: d = 128, raw rows");
   using R = PoolRing<D>;
   // a lane owns 16 elements of a row: 8 at sub * 8 and 8 at D / 2 + sub * 8,
   // so the 8 lanes of a quarter warp read 128 contiguous bytes of shared
@@ -180,6 +185,7 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolS
     // two interleaved partial sums per element keep the fp32 sums short
     uint64_t msum[2][8], usum[8];
     const uint64_t zero2 = tc::f2_pack(0.f, 0.f);
+    float amax = 0.f;  // max |x| over the block (QUANT; absent rows read as 0)
 #pragma unroll
     for (int p = 0; p < 8; ++p) msum[0][p] = msum[1][p] = usum[p] = zero2;
 #pragma unroll
@@ -205,6 +211,7 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolS
         for (int p = 0; p < 8; ++p) {
           const float2 f = E::to_f2(w[p]);
           x[p] = tc::f2_pack(f.x, f.y);
+          if constexpr (QUANT) amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
         }
         if constexpr (SMOOTH) {
           // rows past the end stay zero: they add nothing to either sum
@@ -228,6 +235,32 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolS
           usum[p] = tc::f2_fma(x[p], inv2, usum[p]);
           msum[uu & 1][p] = tc::f2_add(msum[uu & 1][p], x[p]);
         }
+      }
+    }
+    if constexpr (QUANT) {
+      // e4m3 codes of the block from the same shared-memory copy: one scale
+      // per block (amax / 448, IEEE), codes = e4m3(x * (448 / amax)) rounded
+      // to nearest even with saturation; an all-zero block has scale 1
+      amax = warp_max(amax);
+      const float qscale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+      const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+      if (lane == 0) side.scales[unit] = qscale;
+      uint8_t *dst = side.codes + ((size_t)bh * side.s + (size_t)j * kBlk) * D;
+      const int qsub = lane & 15, qsel = lane >> 4;  // 8 values of a row; even / odd row
+#pragma unroll 4
+      for (int r = qsel; r < n; r += 2) {
+        const uint4 wv = *reinterpret_cast<const uint4 *>(blk + r * (2 * D) + qsub * 16);
+        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t out[2];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float2 f = E::to_f2(ws[p]);
+          const float2 y = make_float2(__fmul_rn(f.x, inv), __fmul_rn(f.y, inv));
+          const uint32_t c2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);  // .x low
+          if (p & 1) out[p >> 1] |= c2 << 16;
+          else out[p >> 1] = c2;
+        }
+        *(reinterpret_cast<uint2 *>(dst + (size_t)r * D) + qsub) = make_uint2(out[0], out[1]);
       }
     }
     // the stage is free once every lane has read it
@@ -694,7 +727,7 @@ int device_sm_count();  // fmha_tc.cu
 
 constexpr int kMaxPoolDevices = 64;
 
-template <class E, int D, bool SMOOTH>
+template <class E, int D, bool SMOOTH, bool QUANT>
 static cudaError_t launch_pool_t(const PoolSide &qs, const PoolSide &ks, uint32_t *err,
                                  cudaStream_t st) {
   // the shared-memory attribute is per device: set it once on each
@@ -703,26 +736,32 @@ static cudaError_t launch_pool_t(const PoolSide &qs, const PoolSide &ks, uint32_
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxPoolDevices || !attr_done[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(k_pool_sim<E, D, SMOOTH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PoolRing<D>::kSmem);
+    e = cudaFuncSetAttribute(k_pool_sim<E, D, SMOOTH, QUANT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, PoolRing<D>::kSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxPoolDevices) attr_done[dev].store(true, std::memory_order_release);
   }
   const int total = qs.nunits + ks.nunits;
   if (total == 0) return cudaSuccess;
   const int grid = std::min(total, device_sm_count());
-  k_pool_sim<E, D, SMOOTH><<<grid, kPoolThreads, PoolRing<D>::kSmem, st>>>(qs, ks, err);
+  k_pool_sim<E, D, SMOOTH, QUANT><<<grid, kPoolThreads, PoolRing<D>::kSmem, st>>>(qs, ks, err);
   return cudaGetLastError();
 }
 
 template <bool SMOOTH>
 static cudaError_t launch_pool(const BlockMapLaunch &L, const PoolSide &qs, const PoolSide &ks,
                                cudaStream_t st) {
+  if constexpr (!SMOOTH) {
+    // e4m3 codes of Q and K requested (d = 128, checked by the caller)
+    if (qs.codes)
+      return L.bf16 ? launch_pool_t<BF16, 128, false, true>(qs, ks, L.err, st)
+                    : launch_pool_t<F16, 128, false, true>(qs, ks, L.err, st);
+  }
   if (L.d == 128)
-    return L.bf16 ? launch_pool_t<BF16, 128, SMOOTH>(qs, ks, L.err, st)
-                  : launch_pool_t<F16, 128, SMOOTH>(qs, ks, L.err, st);
-  return L.bf16 ? launch_pool_t<BF16, 64, SMOOTH>(qs, ks, L.err, st)
-                : launch_pool_t<F16, 64, SMOOTH>(qs, ks, L.err, st);
+    return L.bf16 ? launch_pool_t<BF16, 128, SMOOTH, false>(qs, ks, L.err, st)
+                  : launch_pool_t<F16, 128, SMOOTH, false>(qs, ks, L.err, st);
+  return L.bf16 ? launch_pool_t<BF16, 64, SMOOTH, false>(qs, ks, L.err, st)
+                : launch_pool_t<F16, 64, SMOOTH, false>(qs, ks, L.err, st);
 }
 
 cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
@@ -730,6 +769,8 @@ cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
               nullptr};
   PoolSide ks{static_cast<const uint16_t *>(L.k), L.kpl, L.ksim, L.s, L.nk, L.b * L.hk * L.nk,
               nullptr};
+  qs.codes = L.q8; qs.scales = L.q_scale;
+  ks.codes = L.k8; ks.scales = L.k_scale;
   cudaError_t e = launch_pool<false>(L, qs, ks, st);
   if (e != cudaSuccess) return e;
   if (L.smooth_k) {
@@ -741,7 +782,9 @@ cudaError_t launch_block_map(const BlockMapLaunch &L, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     PoolSide none = qs;
     none.nunits = 0;
+    none.codes = nullptr;
     ks.mu = L.kmu;
+    ks.codes = nullptr;
     e = launch_pool<true>(L, none, ks, st);
     if (e != cudaSuccess) return e;
   }

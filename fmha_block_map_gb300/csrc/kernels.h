@@ -49,6 +49,8 @@ struct BlockMapLaunch {
   HeadParams hp;
   uint8_t *qpl, *kpl;                 // workspace carve-out: split planes,
   float *qsim, *ksim, *kmu;           // self-similarities, mean key rows
+  uint8_t *q8, *k8;                   // e4m3 codes of Q and K, or null (d = 128)
+  float *q_scale, *k_scale;           // one scale per 64-row block
   int32_t *lut, *cnt;
   uint8_t *bmap;
   uint32_t *err;  // device error word

@@ -164,6 +164,31 @@ fbm_status sparge_block_map_static(const void *q, const void *k, int dtype, int 
                                    int32_t *lut_count, uint8_t *block_map, void *stream);
 
 /*
+ * sparge_block_map_e4m3 - sparge_block_map that also writes the e4m3 codes of
+ * Q and K from the same pass over them: the quantisation fused into the pool
+ * kernel that the "Sparge Attention (Composable Kernel)" README lists under
+ * 'Not yet ported' (it names int8; GB300's tensor cores take fp8).
+ *
+ * Same arguments, results and checks as sparge_block_map, plus:
+ * q8: device uint8 [b, hq, s, 128], q_scale: device fp32 [b, hq, ceil(s / 64)];
+ * k8: device uint8 [b, hk, s, 128], k_scale: device fp32 [b, hk, ceil(s / 64)].
+ * The codes and scales are those of quantize_e4m3_blocks (bit for bit): per
+ * 64-row block of the raw (unsmoothed) rows, amax = max |x| in fp32,
+ * scale = amax / 448 and code = e4m3(x * (448 / amax)) (IEEE rounding, round
+ * to nearest even, saturating; scale 1 for an all-zero block).  They feed
+ * sparse_fmha_fwd_fp8.  d = 128 only (FBM_ERR_UNSUPPORTED otherwise); the code
+ * buffers must be 16-byte aligned.  Caller-owned; the library allocates
+ * nothing.
+ */
+fbm_status sparge_block_map_e4m3(const void *q, const void *k, int dtype, int b, int hq, int hk,
+                                 int s, int d, int blkq, int blkk, const float *topk,
+                                 const float *cdfthreshd, const float *simthreshd1, float scale,
+                                 int causal, int attention_sink, int smooth_k, int32_t *lut,
+                                 int32_t *lut_count, uint8_t *block_map, void *workspace,
+                                 size_t workspace_bytes, uint8_t *q8, float *q_scale, uint8_t *k8,
+                                 float *k_scale, void *stream);
+
+/*
  * sparse_fmha_fwd - flash attention over the LUT-selected K/V tiles
  * ("Sparge Attention (Composable Kernel)" README: the sparse FMHA stage;
  * updating_log Stage 3 for the per-row-block loop over a block list).

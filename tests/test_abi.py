@@ -206,3 +206,18 @@ def test_static_block_map_holds_the_headline_shape(L):
 def test_selftest_checks_its_limit_on_the_host(L):
     assert L.fbm_selftest_wait_timeout(0, None) == fbm.FBM_ERR_INVALID_ARG
     assert L.fbm_selftest_wait_timeout(20_000_000_000, None) == fbm.FBM_ERR_INVALID_ARG
+
+
+def test_fused_e4m3_block_map_checks_on_the_host(L):
+    arr = (ctypes.c_float * 4)(*([0.1] * 4))
+    args = [FAKE, FAKE, 0, 1, 4, 4, 1024, 128, 64, 64, arr, None, arr, 0.08, 0, 0, 0, FAKE, FAKE,
+            None, FAKE, 1 << 30]
+    # d = 64 is not supported (the codes feed the d = 128 fp8 attention)
+    a = list(args)
+    a[7] = 64
+    assert L.sparge_block_map_e4m3(*a, FAKE, FAKE, FAKE, FAKE, None) == fbm.FBM_ERR_UNSUPPORTED
+    # every code and scale buffer is required, the code buffers 16-byte aligned
+    assert L.sparge_block_map_e4m3(*args, None, FAKE, FAKE, FAKE, None) == fbm.FBM_ERR_INVALID_ARG
+    assert L.sparge_block_map_e4m3(*args, FAKE, FAKE, FAKE, None, None) == fbm.FBM_ERR_INVALID_ARG
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert L.sparge_block_map_e4m3(*args, odd, FAKE, FAKE, FAKE, None) == fbm.FBM_ERR_INVALID_ARG

@@ -102,3 +102,45 @@ def test_fp8_attention_headline_sampled(fbm_gpu):
     cfg = synth.C3
     units = [(0, 3, 0), (0, 3, 255), (1, 20, 100), (1, 20, 255)]
     run_fp8(fbm_gpu, cfg, "topk", 0.4, units)
+
+
+@pytest.mark.parametrize("smooth_k", [False, True])
+def test_fused_block_map_codes_bit_exact(fbm_gpu, smooth_k):
+    # the e4m3 codes and scales written by the block map's pooling pass equal
+    # the oracle's quantisation of the raw rows (ragged s = 1000, an all-zero Q
+    # block, bf16 GQA), and the LUT is the one the plain block map writes
+    cfg = synth.C2.replace(b=1, hq=4, hk=2, s=1000, cs_range=None)
+    x = cached_prefill(cfg)
+    qb = x["q"].copy()
+    qb[0, 2, 128:192] = 0
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    q, k = dev(qb), dev(x["k"])
+    kw = dict(topk=0.5, scale=cfg.scale, causal=True, attention_sink=True, smooth_k=smooth_k)
+    lut, cnt, _, q8, qs, k8, ks = fbm_gpu.sparge_block_map_e4m3(q, k, **kw)
+    lut0, cnt0, _ = fbm_gpu.sparge_block_map(q, k, **kw)
+    assert fbm_gpu.get_error() == 0
+    assert torch.equal(lut, lut0) and torch.equal(cnt, cnt0)
+    for bits, codes, scales in ((qb, q8, qs), (x["k"], k8, ks)):
+        codes, scales = codes.cpu().numpy(), scales.cpu().numpy()
+        for h in range(bits.shape[1]):
+            vals, sc = oracle.quantize_blocks_e4m3(synth.bits_to_f64(bits[0, h], "bf16"), 64)
+            assert np.array_equal(scales[0, h].astype(np.float64), sc), h
+            assert np.array_equal(decode(codes[0, h]), vals), h
+    assert qs[0, 2, 2].item() == 1.0
+
+
+def test_fused_block_map_codes_headline_heads(fbm_gpu):
+    # headline shape: the fused codes equal the separate quantiser's, and two
+    # heads of them the oracle's
+    cfg = synth.C3
+    x, (q, k, v) = prefill_on_gpu(cfg)
+    lut, cnt, _, q8, qs, k8, ks = fbm_gpu.sparge_block_map_e4m3(q, k, topk=0.4, scale=cfg.scale)
+    q8b, qsb = fbm_gpu.quantize_e4m3_blocks(q)
+    k8b, ksb = fbm_gpu.quantize_e4m3_blocks(k)
+    assert fbm_gpu.get_error() == 0
+    assert torch.equal(q8, q8b) and torch.equal(qs, qsb)
+    assert torch.equal(k8, k8b) and torch.equal(ks, ksb)
+    for bi, h in ((0, 0), (1, 31)):
+        vals, sc = oracle.quantize_blocks_e4m3(synth.bits_to_f64(x["q"][bi, h], cfg.dtype), 64)
+        assert np.array_equal(qs[bi, h].cpu().numpy().astype(np.float64), sc)
+        assert np.array_equal(decode(q8[bi, h].cpu().numpy()), vals)
