@@ -16,8 +16,6 @@
 namespace fbm {
 namespace {
 
-constexpr int kMaxSplits = 64;
-
 constexpr int kBatch = 8;  // partial rows loaded per lane before they are weighted
 
 template <int OUT>  // 0 = f16, 1 = bf16, 2 = f32

@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for sm_100-family features used by the tcgen05
-// kernels: mbarriers (bounded waits), TMA tensor loads, bulk stores, TMEM
+// kernels: mbarriers (bounded waits), TMA tensor loads and stores, bulk copies, TMEM
 // allocation, tcgen05.mma / commit / ld / st and the UMMA shared-memory and
 // instruction descriptors.
 #pragma once
@@ -58,22 +58,6 @@ FBM_DEVICE bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abo
   }
 }
 
-// The bounded wait for roles that are not latency-critical: between polls the
-// thread sleeps about `sleep_ns`, which leaves the issue slots of its SM
-// sub-partition to the warps that issue MMAs and copies.
-FBM_DEVICE bool mbar_wait_backoff(uint32_t bar, uint32_t parity, const volatile int *abort,
-                                  uint64_t limit_ns, uint32_t sleep_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    __nanosleep(sleep_ns);
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0u) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > limit_ns) return false;
-    }
-  }
-}
 
 // The same wait without an abort flag (used for the final drain).
 FBM_DEVICE bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -129,11 +113,6 @@ FBM_DEVICE uint64_t l2_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
   return p;
 }
-FBM_DEVICE void bulk_store(void *gdst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst),
-               "r"(src), "r"(bytes)
-               : "memory");
-}
 FBM_DEVICE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 FBM_DEVICE void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
@@ -181,18 +160,9 @@ FBM_DEVICE void tc_fence_before() {
 FBM_DEVICE void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]
-FBM_DEVICE void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                        uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// The same MMA with the two descriptors given as their low words plus a shared
-// high word (see sdesc_lo / sdesc_hi_sw128), so that an issuing loop advances a
-// descriptor with one 32-bit add.
+// D[tmem] (+)= A[smem] * B[smem] (kind::f16), the two descriptors given as
+// their low words plus a shared high word (see sdesc_lo / sdesc_hi_sw128), so
+// that an issuing loop advances a descriptor with one 32-bit add.
 FBM_DEVICE void mma_f16_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -251,21 +221,6 @@ FBM_DEVICE void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       FBM_W8(0), FBM_W8(8), FBM_W8(16), FBM_W8(24)
       : "memory");
 }
-// 32 lanes x 16 consecutive 32-bit columns
-FBM_DEVICE void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];\n"
-      : FBM_R8(0), FBM_R8(8)
-      : "r"(taddr));
-}
-FBM_DEVICE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16};\n" ::"r"(taddr),
-      FBM_W8(0), FBM_W8(8)
-      : "memory");
-}
 #undef FBM_R8
 #undef FBM_W8
 // 16 lanes (a subpartition's rows of an M = 64 accumulator) x 64 columns: threads
@@ -299,14 +254,6 @@ FBM_DEVICE void tmem_ld_rowhalf32(uint32_t taddr, uint32_t (&r)[32]) {
       "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], 32;\n"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-}
-// 16 lanes x 32 columns: threads 0-15 write lane t, columns 0..15; threads
-// 16-31 write lane t - 16, columns 16..31
-FBM_DEVICE void tmem_st_rowhalf16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 16, {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
 }
 FBM_DEVICE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 FBM_DEVICE void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
