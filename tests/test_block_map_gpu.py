@@ -234,3 +234,13 @@ def test_exact_ties_in_a_crowded_bin(fbm_gpu):
 def test_exact_ties_cdf(fbm_gpu):
     cfg = synth.C1.replace(b=1, hq=2, hk=2, s=4096, d=64, dtype="f16")
     _tied_case(fbm_gpu, cfg, 7, "cdf", 0.6)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_longest_sequence(fbm_gpu, causal):
+    # s = 65536: nk = 1024, the most the block map takes.  The selection runs
+    # its 32-scores-per-lane kernel (causal rows its 8 / 16 / 24 / 32 bodies)
+    # and the scores kernel eight 128-block tiles per row of tiles
+    cfg = synth.C1.replace(b=1, hq=2, hk=1, s=65536, d=128, dtype="bf16", causal=causal,
+                           attention_sink=causal)
+    run_case(fbm_gpu, cfg, "topk", 0.1)

@@ -374,3 +374,14 @@ def test_pv_skip_infinite_threshold_is_bit_identical(fbm_gpu):
     a = fbm_gpu.sparse_fmha_fwd(*args, scale=cfg.scale, return_lse=True)
     b = fbm_gpu.sparse_fmha_fwd(*args, scale=cfg.scale, return_lse=True, pv_threshold=math.inf)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_longest_sequence_sampled(fbm_gpu):
+    # s = 65536 (LUT rows of up to 1024 kv blocks), causal GQA with a sink:
+    # whole rows and 3-way split partials on sampled q blocks, first and last
+    cfg = synth.C1.replace(b=1, hq=2, hk=1, s=65536, d=128, dtype="bf16", causal=True,
+                           attention_sink=True, topk=0.1)
+    lut, cnt = oracle_lut(cfg)
+    units = [(0, h, i) for h in range(2) for i in (0, 1, 511, 1022, 1023)]
+    check(fbm_gpu, cfg, lut, cnt, units=units)
+    check(fbm_gpu, cfg, lut, cnt, units=units, num_splits=3)
