@@ -83,3 +83,27 @@ def test_short_chunks(fbm_gpu, S):
     # chunk has two 16-token tiles, one full tile or one partial tile (the
     # second warp group of the CTA then has one short tile or none)
     run(fbm_gpu, SMALL, S)
+
+
+def test_f16_cache(fbm_gpu):
+    # the same decode with an f16 query and cache: the bf16 values of the
+    # generator are exactly representable in f16, so the oracle values are the same
+    cfg = SMALL
+    inp = synth.decode(cfg)
+    cache = gpu_cache(cfg).to(torch.float16)
+    qf = synth.bits_to_f64(inp["q"], "bf16")
+    assert np.abs(qf).max() < 60000 and np.abs(cache.float().cpu().numpy()).max() < 60000
+    q = torch.from_numpy(inp["q"].view(np.int16)).view(torch.bfloat16).cuda().to(torch.float16)
+    assert torch.equal(q.to(torch.float64).cpu(), torch.from_numpy(qf))
+    op, lp = fbm_gpu.sparse_decode_fwd(q, cache, torch.from_numpy(inp["page_table"]).cuda(),
+                                       torch.from_numpy(inp["idx"]).cuda(), dv=cfg.dv,
+                                       scale=cfg.sm_scale, num_splits=3)
+    out, lse = fbm_gpu.attn_combine(op, lp, out_dtype=torch.float16)
+    assert fbm_gpu.get_error() == 0
+    out, lse = out.double().cpu().numpy(), lse.double().cpu().numpy()
+    rows = decode_rows(inp["page_table"], inp["idx"], cfg.page)
+    for c in range(cfg.n_queries):
+        kv = synth.bits_to_f64(synth.cache_rows(cfg, rows[c]), "bf16")
+        ro, rl = oracle.decode_attention(qf[c], kv, cfg.dv, cfg.sm_scale)
+        assert_close_o(out[c], ro, f"O q{c}")
+        assert_close_lse(lse[c], rl, f"LSE q{c}")
