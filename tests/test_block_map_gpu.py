@@ -237,10 +237,18 @@ def test_exact_ties_cdf(fbm_gpu):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_longest_sequence(fbm_gpu, causal):
+@pytest.mark.parametrize("mode,param", [("topk", 0.1), ("cdf", 0.9)])
+def test_longest_sequence(fbm_gpu, causal, mode, param):
     # s = 65536: nk = 1024, the most the block map takes.  The selection runs
-    # its 32-scores-per-lane kernel (causal rows its 8 / 16 / 24 / 32 bodies)
-    # and the scores kernel eight 128-block tiles per row of tiles
+    # its 32-scores-per-lane kernels (causal rows their 8 / 16 / 24 / 32
+    # bodies) and the scores kernel eight 128-block tiles per row of tiles
     cfg = synth.C1.replace(b=1, hq=2, hk=1, s=65536, d=128, dtype="bf16", causal=causal,
                            attention_sink=causal)
-    run_case(fbm_gpu, cfg, "topk", 0.1)
+    run_case(fbm_gpu, cfg, mode, param)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_cdf_with_512_kv_blocks(fbm_gpu, causal):
+    # nk = 512: the 16-scores-per-lane cdf kernel
+    cfg = synth.C1.replace(b=1, hq=2, hk=2, s=32768, d=64, dtype="f16", causal=causal)
+    run_case(fbm_gpu, cfg, "cdf", 0.8)
