@@ -247,80 +247,78 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_pair(const __grid_constant
     }
   } else if (warp == kWarpS) {
     // ------------------------------------------------------------ S issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_f16(kBf16, false, false, 128, 128);
-      int pc = 0, uc = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-        bool bad;
-        const PUnit U = punit_of(P, u, &bad);
-        if (U.n == 0) continue;
-        const int npairs = (U.n + 1) >> 1;
-        const int qb = uc & 1;
-        if (!(ok = mbar_wait(bar(B_QF + qb), (uc >> 1) & 1, abort_flag, kWaitNs))) break;
+    // (the whole warp runs the loop; one elected lane issues each MMA)
+    constexpr uint32_t idS = idesc_f16(kBf16, false, false, 128, 128);
+    int pc = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+      bool bad;
+      const PUnit U = punit_of(P, u, &bad);
+      if (U.n == 0) continue;
+      const int npairs = (U.n + 1) >> 1;
+      const int qb = uc & 1;
+      if (!(ok = mbar_wait_w(bar(B_QF + qb), (uc >> 1) & 1, abort_flag, kWaitNs))) break;
+      tc_fence_after();
+      const uint32_t q_lo = sdesc_lo(sbase + OFF_Q + qb * kTile, 16);
+      for (int p = 0; p < npairs; ++p) {
+        const int g = pc + p, slot = g % kKSlots, ss = g % kSSlots;
+        if (!(ok = mbar_wait_w(bar(B_KF + slot), (g / kKSlots) & 1, abort_flag, kWaitNs))) break;
+        if (!(ok = mbar_wait_w(bar(B_SE + ss), ((g / kSSlots) & 1) ^ 1, abort_flag, kWaitNs))) break;
         tc_fence_after();
-        const uint32_t q_lo = sdesc_lo(sbase + OFF_Q + qb * kTile, 16);
-        for (int p = 0; p < npairs; ++p) {
-          const int g = pc + p, slot = g % kKSlots, ss = g % kSSlots;
-          if (!(ok = mbar_wait(bar(B_KF + slot), (g / kKSlots) & 1, abort_flag, kWaitNs))) break;
-          if (!(ok = mbar_wait(bar(B_SE + ss), ((g / kSSlots) & 1) ^ 1, abort_flag, kWaitNs))) break;
-          tc_fence_after();
-          const uint32_t k_lo = sdesc_lo(sbase + OFF_K + slot * kTile, 16);
-          const uint32_t dS = tbase + kTS + ss * 128;
+        const uint32_t k_lo = sdesc_lo(sbase + OFF_K + slot * kTile, 16);
+        const uint32_t dS = tbase + kTS + ss * 128;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
-            mma_f16_lo(dS, q_lo + off, k_lo + off, kDescHi, idS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(B_SF + ss));
-          mma_commit(bar(B_KE + slot));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+          mma_f16_lo_w(dS, q_lo + off, k_lo + off, kDescHi, idS, kk > 0 ? 1u : 0u);
         }
-        // Q's first release: every S of the unit is done (the epilogue, which
-        // stages the output tile in the slot, gives the second)
-        if (ok) mma_commit(bar(B_QE + qb));
-        pc += npairs;
-        uc += 1;
+        mma_commit_w(bar(B_SF + ss));
+        mma_commit_w(bar(B_KE + slot));
       }
-      if (!ok) fail(FBM_DEVERR_TIMEOUT);
-      mma_commit(bar(B_DRAIN));
-      if (!mbar_wait_for(bar(B_DRAIN), 0, kWaitNs)) set_error(P.err, FBM_DEVERR_TIMEOUT);
+      // Q's first release: every S of the unit is done (the epilogue, which
+      // stages the output tile in the slot, gives the second)
+      if (ok) mma_commit_w(bar(B_QE + qb));
+      pc += npairs;
+      uc += 1;
     }
+    if (!ok && lane == 0) fail(FBM_DEVERR_TIMEOUT);
+    mma_commit_w(bar(B_DRAIN));
+    if (!mbar_wait_for_w(bar(B_DRAIN), 0, kWaitNs) && lane == 0) set_error(P.err, FBM_DEVERR_TIMEOUT);
   } else if (warp == kWarpPV) {
     // ------------------------------------------------------------ PV issuer
-    if (lane == 0) {
-      // A = P (TMEM, K-major), B = V pair (MN-major: d contiguous)
-      constexpr uint32_t idO = idesc_f16(kBf16, false, true, 128, D);
-      const uint32_t tO = tbase + kTO;
-      int pc = 0, uc = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-        bool bad;
-        const PUnit U = punit_of(P, u, &bad);
-        if (U.n == 0) continue;
-        const int npairs = (U.n + 1) >> 1;
-        for (int p = 0; p < npairs; ++p) {
-          const int g = pc + p, slot = g % kVSlots, pb = g % kPBufs;
-          if (!(ok = mbar_wait(bar(B_PF + pb), (g / kPBufs) & 1, abort_flag, kWaitNs))) break;
-          if (!(ok = mbar_wait(bar(B_VF + slot), (g / kVSlots) & 1, abort_flag, kWaitNs))) break;
-          if (p == 0 && !(ok = mbar_wait(bar(B_OF), (uc & 1) ^ 1, abort_flag, kWaitNs))) break;
-          tc_fence_after();
-          const uint32_t v_lo = sdesc_lo(sbase + OFF_V + slot * kTile, kChunk);
-          const uint32_t tP = tbase + kTP + pb * 64;
-          const int steps = (2 * p + 1 >= U.n) ? 4 : 8;  // a half pair has 64 keys
+    // (the whole warp runs the loop; one elected lane issues each MMA)
+    // A = P (TMEM, K-major), B = V pair (MN-major: d contiguous)
+    constexpr uint32_t idO = idesc_f16(kBf16, false, true, 128, D);
+    const uint32_t tO = tbase + kTO;
+    int pc = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+      bool bad;
+      const PUnit U = punit_of(P, u, &bad);
+      if (U.n == 0) continue;
+      const int npairs = (U.n + 1) >> 1;
+      for (int p = 0; p < npairs; ++p) {
+        const int g = pc + p, slot = g % kVSlots, pb = g % kPBufs;
+        if (!(ok = mbar_wait_w(bar(B_PF + pb), (g / kPBufs) & 1, abort_flag, kWaitNs))) break;
+        if (!(ok = mbar_wait_w(bar(B_VF + slot), (g / kVSlots) & 1, abort_flag, kWaitNs))) break;
+        if (p == 0 && !(ok = mbar_wait_w(bar(B_OF), (uc & 1) ^ 1, abort_flag, kWaitNs))) break;
+        tc_fence_after();
+        const uint32_t v_lo = sdesc_lo(sbase + OFF_V + slot * kTile, kChunk);
+        const uint32_t tP = tbase + kTP + pb * 64;
+        const int steps = (2 * p + 1 >= U.n) ? 4 : 8;  // a half pair has 64 keys
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            if (kk < steps)
-              mma_f16_ta(tO, tP + kk * 8, v_lo + kk * 128, kDescHi, idO, (p > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(B_PV + pb));
-          mma_commit(bar(B_VE + slot));
-        }
-        pc += npairs;
-        uc += 1;
+        for (int kk = 0; kk < 8; ++kk)
+          if (kk < steps)
+            mma_f16_ta_w(tO, tP + kk * 8, v_lo + kk * 128, kDescHi, idO, (p > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_w(bar(B_PV + pb));
+        mma_commit_w(bar(B_VE + slot));
       }
-      if (!ok) fail(FBM_DEVERR_TIMEOUT);
-      mma_commit(bar(B_DRAIN2));
-      if (!mbar_wait_for(bar(B_DRAIN2), 0, kWaitNs)) set_error(P.err, FBM_DEVERR_TIMEOUT);
+      pc += npairs;
+      uc += 1;
     }
+    if (!ok && lane == 0) fail(FBM_DEVERR_TIMEOUT);
+    mma_commit_w(bar(B_DRAIN2));
+    if (!mbar_wait_for_w(bar(B_DRAIN2), 0, kWaitNs) && lane == 0) set_error(P.err, FBM_DEVERR_TIMEOUT);
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     using E = typename std::conditional<kBf16, BF16, F16>::type;

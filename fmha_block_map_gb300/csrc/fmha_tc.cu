@@ -308,97 +308,96 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     }
   } else if (warp == kWarpS) {
     // ------------------------------------------------------------ S issuer
-    if (lane == 0) {
-      // (kind::f8f6f4 with e4m3 A and B uses format code 0, as f16 does)
-      constexpr uint32_t idS = idesc_f16(kFp8 ? false : kBf16, false, false, 64, 128);
-      int pc = 0, uc = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-        const Unit U = unit_of<kPartial>(P, u);
-        if (U.n == 0) continue;
-        const int npairs = (U.n + 1) >> 1;
-        const int qb = uc & 1;
-        if (!(ok = mbar_wait(bar(B_QF + qb), (uc >> 1) & 1, abort_flag, kWaitNs))) break;
+    // (the whole warp runs the loop; one elected lane issues each MMA)
+    // (kind::f8f6f4 with e4m3 A and B uses format code 0, as f16 does)
+    constexpr uint32_t idS = idesc_f16(kFp8 ? false : kBf16, false, false, 64, 128);
+    int pc = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+      const Unit U = unit_of<kPartial>(P, u);
+      if (U.n == 0) continue;
+      const int npairs = (U.n + 1) >> 1;
+      const int qb = uc & 1;
+      if (!(ok = mbar_wait_w(bar(B_QF + qb), (uc >> 1) & 1, abort_flag, kWaitNs))) break;
+      tc_fence_after();
+      const uint32_t q_lo = sdesc_lo(sbase + OFF_Q + qb * kQBytes, 16);
+      for (int p = 0; p < npairs; ++p) {
+        const int g = pc + p, slot = g % kKSlots, ss = g % kSSlots;
+        if (!(ok = mbar_wait_w(bar(B_KF + slot), (g / kKSlots) & 1, abort_flag, kWaitNs))) break;
+        if (!(ok = mbar_wait_w(bar(B_SE + ss), ((g / kSSlots) & 1) ^ 1, abort_flag, kWaitNs))) break;
         tc_fence_after();
-        const uint32_t q_lo = sdesc_lo(sbase + OFF_Q + qb * kQBytes, 16);
-        for (int p = 0; p < npairs; ++p) {
-          const int g = pc + p, slot = g % kKSlots, ss = g % kSSlots;
-          if (!(ok = mbar_wait(bar(B_KF + slot), (g / kKSlots) & 1, abort_flag, kWaitNs))) break;
-          if (!(ok = mbar_wait(bar(B_SE + ss), ((g / kSSlots) & 1) ^ 1, abort_flag, kWaitNs))) break;
-          tc_fence_after();
-          const uint32_t k_lo = sdesc_lo(sbase + OFF_K + slot * kPairBytes, 16);
-          const uint32_t dS = tbase + kTS + ss * 128;
-          if constexpr (kFp8) {
-            // e4m3 rows are 128 bytes: one swizzle atom wide, 32 values of K per MMA
+        const uint32_t k_lo = sdesc_lo(sbase + OFF_K + slot * kPairBytes, 16);
+        const uint32_t dS = tbase + kTS + ss * 128;
+        if constexpr (kFp8) {
+          // e4m3 rows are 128 bytes: one swizzle atom wide, 32 values of K per MMA
 #pragma unroll
-            for (int kk = 0; kk < D / 32; ++kk)
-              mma_f8_lo(dS, q_lo + ((kk * 32) >> 4), k_lo + ((kk * 32) >> 4), kDescHi, idS,
+          for (int kk = 0; kk < D / 32; ++kk)
+            mma_f8_lo_w(dS, q_lo + ((kk * 32) >> 4), k_lo + ((kk * 32) >> 4), kDescHi, idS,
                         kk > 0 ? 1u : 0u);
-          } else {
+        } else {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_f16_lo(dS, q_lo + (((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4),
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_f16_lo_w(dS, q_lo + (((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4),
                          k_lo + (((kk >> 2) * kPairChunk + (kk & 3) * 32) >> 4), kDescHi, idS,
                          kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(B_SF + ss));
-          mma_commit(bar(B_KE + slot));
         }
-        if (ok) mma_commit(bar(B_QE + qb));  // Q free once every S of the row is done
-        pc += npairs;
-        uc += 1;
+        mma_commit_w(bar(B_SF + ss));
+        mma_commit_w(bar(B_KE + slot));
       }
-      if (!ok) fail(FBM_DEVERR_TIMEOUT);
-      // drain: every MMA this thread issued has completed before TMEM is freed
-      mma_commit(bar(B_DRAIN));
-      if (!mbar_wait_for(bar(B_DRAIN), 0, kWaitNs)) set_error(P.err, FBM_DEVERR_TIMEOUT);
+      if (ok) mma_commit_w(bar(B_QE + qb));  // Q free once every S of the row is done
+      pc += npairs;
+      uc += 1;
     }
+    if (!ok && lane == 0) fail(FBM_DEVERR_TIMEOUT);
+    // drain: every MMA this warp issued has completed before TMEM is freed
+    mma_commit_w(bar(B_DRAIN));
+    if (!mbar_wait_for_w(bar(B_DRAIN), 0, kWaitNs) && lane == 0) set_error(P.err, FBM_DEVERR_TIMEOUT);
   } else if (warp == kWarpPV) {
     // ------------------------------------------------------------ PV issuer
-    if (lane == 0) {
-      // A = P (TMEM, K-major), B = V pair (MN-major: d contiguous)
-      constexpr uint32_t idO = idesc_f16(kBf16, false, true, 64, D);
-      const uint32_t tO = tbase + kTO;
-      int pc = 0, uc = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-        const Unit U = unit_of<kPartial>(P, u);
-        if (U.n == 0) continue;
-        const int npairs = (U.n + 1) >> 1;
-        for (int p = 0; p < npairs; ++p) {
-          const int g = pc + p, slot = g % kVSlots, pb = g % kPBufs;
-          if (!(ok = mbar_wait(bar(B_PF + pb), (g / kPBufs) & 1, abort_flag, kWaitNs))) break;
-          if (!(ok = mbar_wait(bar(B_VF + slot), (g / kVSlots) & 1, abort_flag, kWaitNs))) break;
-          if (p == 0 && !(ok = mbar_wait(bar(B_OF), (uc & 1) ^ 1, abort_flag, kWaitNs))) break;
-          tc_fence_after();
-          const uint32_t v_lo = sdesc_lo(sbase + OFF_V + slot * kPairBytes, kPairChunk);
-          const uint32_t tP = tbase + kTP + pb * 64;
-          const bool half = 2 * p + 1 >= U.n;  // a half pair has 64 keys: 4 steps
-          bool skip_a = false, skip_b = false;
-          if constexpr (kPvSkip) {
-            // a block is skipped when all four softmax warps voted for it; the
-            // first block of a row never is (its running max is still -inf), so
-            // the first MMA below always starts the accumulator
-            const uint32_t vw = *reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC + 8 + pb * 4);
-            const uint32_t all4 = vw & (vw >> 8) & (vw >> 16) & (vw >> 24);
-            skip_a = (all4 & 1u) != 0;
-            skip_b = (all4 & 2u) != 0;
-          }
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            if (kk < 4 ? !skip_a : (!half && !skip_b))
-              mma_f16_ta(tO, tP + kk * 8, v_lo + kk * 128, kDescHi, idO,
-                         (p > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(B_PV + pb));
-          mma_commit(bar(B_VE + slot));
+    // (the whole warp runs the loop; one elected lane issues each MMA)
+    // A = P (TMEM, K-major), B = V pair (MN-major: d contiguous)
+    constexpr uint32_t idO = idesc_f16(kBf16, false, true, 64, D);
+    const uint32_t tO = tbase + kTO;
+    int pc = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+      const Unit U = unit_of<kPartial>(P, u);
+      if (U.n == 0) continue;
+      const int npairs = (U.n + 1) >> 1;
+      for (int p = 0; p < npairs; ++p) {
+        const int g = pc + p, slot = g % kVSlots, pb = g % kPBufs;
+        if (!(ok = mbar_wait_w(bar(B_PF + pb), (g / kPBufs) & 1, abort_flag, kWaitNs))) break;
+        if (!(ok = mbar_wait_w(bar(B_VF + slot), (g / kVSlots) & 1, abort_flag, kWaitNs))) break;
+        if (p == 0 && !(ok = mbar_wait_w(bar(B_OF), (uc & 1) ^ 1, abort_flag, kWaitNs))) break;
+        tc_fence_after();
+        const uint32_t v_lo = sdesc_lo(sbase + OFF_V + slot * kPairBytes, kPairChunk);
+        const uint32_t tP = tbase + kTP + pb * 64;
+        const bool half = 2 * p + 1 >= U.n;  // a half pair has 64 keys: 4 steps
+        bool skip_a = false, skip_b = false;
+        if constexpr (kPvSkip) {
+          // a block is skipped when all four softmax warps voted for it; the
+          // first block of a row never is (its running max is still -inf), so
+          // the first MMA below always starts the accumulator
+          const uint32_t vw = __shfl_sync(
+              0xffffffffu, *reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC + 8 + pb * 4), 0);
+          const uint32_t all4 = vw & (vw >> 8) & (vw >> 16) & (vw >> 24);
+          skip_a = (all4 & 1u) != 0;
+          skip_b = (all4 & 2u) != 0;
         }
-        pc += npairs;
-        uc += 1;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          if (kk < 4 ? !skip_a : (!half && !skip_b))
+            mma_f16_ta_w(tO, tP + kk * 8, v_lo + kk * 128, kDescHi, idO,
+                         (p > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_w(bar(B_PV + pb));
+        mma_commit_w(bar(B_VE + slot));
       }
-      if (!ok) fail(FBM_DEVERR_TIMEOUT);
-      mma_commit(bar(B_DRAIN2));
-      if (!mbar_wait_for(bar(B_DRAIN2), 0, kWaitNs)) set_error(P.err, FBM_DEVERR_TIMEOUT);
+      pc += npairs;
+      uc += 1;
     }
+    if (!ok && lane == 0) fail(FBM_DEVERR_TIMEOUT);
+    mma_commit_w(bar(B_DRAIN2));
+    if (!mbar_wait_for_w(bar(B_DRAIN2), 0, kWaitNs) && lane == 0) set_error(P.err, FBM_DEVERR_TIMEOUT);
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     using E = typename std::conditional<kBf16, BF16, F16>::type;
