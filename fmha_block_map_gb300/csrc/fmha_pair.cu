@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_pair(const __grid_constant
         const bool jvalid = e >= 0 && j < P.nk && ((e >> my_bit) & 1);
         const int kpos0 = (jvalid ? j : 0) * 64;
         const bool plain = jvalid && kpos0 + 64 <= P.s_k && (!P.causal || kpos0 + 63 <= qpos + P.koff);
-        ok = ok && mbar_wait(bar(B_SF + ss), (g / kSSlots) & 1, abort_flag, kWaitNs);
+        ok = mbar_wait_ok(ok, bar(B_SF + ss), (g / kSSlots) & 1, abort_flag, kWaitNs);
         tc_fence_after();
         uint32_t sv[64];
         {
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_pair(const __grid_constant
         // the S slot is free for S(g + kSSlots) as soon as it is in registers
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_SE + ss));
+        mbar_arrive_lane0(bar(B_SE + ss), lane);
         if (!plain) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_pair(const __grid_constant
           for (int i = 0; i < 4; ++i) l2[i] = f2_mul(l2[i], a2);
           if (p > 0) {
             const int gp = g - 1;
-            ok = ok && mbar_wait(bar(B_PV + gp % kPBufs), (gp / kPBufs) & 1, abort_flag, kWaitNs);
+            ok = mbar_wait_ok(ok, bar(B_PV + gp % kPBufs), (gp / kPBufs) & 1, abort_flag, kWaitNs);
             tc_fence_after();
 #pragma unroll
             for (int h = 0; h < kOC / 32; ++h) {
@@ -454,18 +454,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_pair(const __grid_constant
         }
         if (p >= kPBufs) {
           const int gp = g - kPBufs;
-          ok = ok && mbar_wait(bar(B_PV + pb), (gp / kPBufs) & 1, abort_flag, kWaitNs);
+          ok = mbar_wait_ok(ok, bar(B_PV + pb), (gp / kPBufs) & 1, abort_flag, kWaitNs);
         }
         tc_fence_after();
         tmem_st32(tl + kTP + pb * 64 + blk * 32, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PF + pb));
+        mbar_arrive_lane0(bar(B_PF + pb), lane);
       }
       // ---- epilogue: O = O / l, LSE = m ln 2 + ln l
       const int gl = pc + npairs - 1;
-      ok = ok && mbar_wait(bar(B_PV + gl % kPBufs), (gl / kPBufs) & 1, abort_flag, kWaitNs);
+      ok = mbar_wait_ok(ok, bar(B_PV + gl % kPBufs), (gl / kPBufs) & 1, abort_flag, kWaitNs);
       tc_fence_after();
       uint32_t o[kOC];
 #pragma unroll
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_pair(const __grid_constant
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_OF));  // O may take the next unit's first PV
+      mbar_arrive_lane0(bar(B_OF), lane);  // O may take the next unit's first PV
       float lt;
       {
         const float2 a = f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])));

@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         const int kpos0 = (jvalid ? j : 0) * 64;
         // every key of this thread's block visible to its row
         const bool plain = jvalid && kpos0 + 64 <= P.s_k && (!P.causal || kpos0 + 63 <= qpos + P.koff);
-        ok = ok && mbar_wait(bar(B_SF + ss), (g / kSSlots) & 1, abort_flag, kWaitNs);
+        ok = mbar_wait_ok(ok, bar(B_SF + ss), (g / kSSlots) & 1, abort_flag, kWaitNs);
         tc_fence_after();
         uint32_t sv[64];
         tmem_ld_rowhalf64(tl + kTS + ss * 128, sv);
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         // the S slot is free for S(g + kSSlots) as soon as it is in registers
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_SE + ss));
+        mbar_arrive_lane0(bar(B_SE + ss), lane);
         if (!plain) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           if (p > 0) {
             // O holds PV(0 .. p-1): wait for the last of them, then scale
             const int gp = g - 1;
-            ok = ok && mbar_wait(bar(B_PV + gp % kPBufs), (gp / kPBufs) & 1, abort_flag, kWaitNs);
+            ok = mbar_wait_ok(ok, bar(B_PV + gp % kPBufs), (gp / kPBufs) & 1, abort_flag, kWaitNs);
             tc_fence_after();
             uint32_t o[D / 2];
             ld_o<D>(tl + kTO, o);
@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         // previous row's epilogue has already waited for its last PV)
         if (p >= kPBufs) {
           const int gp = g - kPBufs;
-          ok = ok && mbar_wait(bar(B_PV + pb), (gp / kPBufs) & 1, abort_flag, kWaitNs);
+          ok = mbar_wait_ok(ok, bar(B_PV + pb), (gp / kPBufs) & 1, abort_flag, kWaitNs);
         }
         tc_fence_after();
         tmem_st_rowhalf32(tl + kTP + pb * 64, pk);
@@ -558,19 +558,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         __syncwarp();
         if (kPvSkip && lane == 0)  // read by the PV issuer once B_PF(pb) completes
           *reinterpret_cast<volatile uint8_t *>(smem + OFF_MISC + 8 + pb * 4 + sw) = (uint8_t)vote;
-        if (lane == 0) mbar_arrive(bar(B_PF + pb));
+        mbar_arrive_lane0(bar(B_PF + pb), lane);
       }
       // ---- epilogue: O = O / l, LSE = m ln 2 + ln l
       {
         const int gl = pc + npairs - 1;
-        ok = ok && mbar_wait(bar(B_PV + gl % kPBufs), (gl / kPBufs) & 1, abort_flag, kWaitNs);
+        ok = mbar_wait_ok(ok, bar(B_PV + gl % kPBufs), (gl / kPBufs) & 1, abort_flag, kWaitNs);
         tc_fence_after();
         uint32_t o[D / 2];
         ld_o<D>(tl + kTO, o);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_OF));  // O may take the next row's first PV
+        mbar_arrive_lane0(bar(B_OF), lane);  // O may take the next row's first PV
         float lt;
         {
           const float2 a = f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])));

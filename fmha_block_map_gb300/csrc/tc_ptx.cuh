@@ -59,6 +59,25 @@ FBM_DEVICE bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abo
 }
 
 
+// A bounded wait for code where every branch costs: when the phase is already
+// complete (the usual case on a steady pipeline) it takes one test and one
+// branch.  `ok` is passed through: once a wait has given up, later waits
+// return false without waiting.
+FBM_DEVICE bool mbar_wait_ok(bool ok, uint32_t bar, uint32_t parity, const volatile int *abort,
+                             uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return ok;
+  return ok && mbar_wait(bar, parity, abort, limit_ns);
+}
+
+// An arrive by lane 0 of the warp, predicated rather than branched around.
+FBM_DEVICE void mbar_arrive_lane0(uint32_t bar, int lane) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.eq.u32 p, %1, 0;\n"
+      " @p mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n" ::"r"(bar),
+      "r"(lane)
+      : "memory");
+}
+
 // The same wait without an abort flag (used for the final drain).
 FBM_DEVICE bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
