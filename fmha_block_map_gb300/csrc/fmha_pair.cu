@@ -452,10 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_pair(const __grid_constant
 #pragma unroll
           for (int i = 0; i < 32; ++i) pk[i] = 0u;
         }
-        if (p >= kPBufs) {
-          const int gp = g - kPBufs;
-          ok = mbar_wait_ok(ok, bar(B_PV + pb), (gp / kPBufs) & 1, abort_flag, kWaitNs);
-        }
+        // P buffer pb was last read by PV(g - kPBufs): wait for the previous
+        // completion of its barrier (on a fresh barrier the phase before the
+        // first counts as complete, so the first uses pass at once)
+        ok = mbar_wait_ok(ok, bar(B_PV + pb), ((g / kPBufs) & 1) ^ 1, abort_flag, kWaitNs);
         tc_fence_after();
         tmem_st32(tl + kTP + pb * 64 + blk * 32, pk);
         tmem_wait_st();
