@@ -111,21 +111,10 @@ __global__ void __launch_bounds__(kDThreads, 2) k_sparse_decode(const DecodeLaun
   const uint16_t *cache = static_cast<const uint16_t *>(L.cache);
   const int max_pos = L.pages_per_query * L.page;
 
-  // prologue: token list -> physical rows (-1 = masked), and Q [16][D]
-  for (int t = tid; t < n; t += kDThreads) {
-    const int pos = __ldg(L.idx + (size_t)c * L.topk + lo + t);
-    int row = -1;
-    if (pos >= 0) {
-      if (pos < max_pos) {
-        const int pg = __ldg(L.page_table + (size_t)c * L.pages_per_query + pos / L.page);
-        if (pg >= 0 && pg < L.n_pages) row = pg * L.page + pos % L.page;
-        else set_error(L.err, FBM_DEVERR_LUT_RANGE);
-      } else {
-        set_error(L.err, FBM_DEVERR_LUT_RANGE);
-      }
-    }
-    s_rows[t] = row;
-  }
+  // prologue: Q [16][D] first (its copy overlaps the lookups), then the token
+  // list -> physical rows (-1 = masked).  A thread issues the index loads of
+  // all its tokens before their page-table loads, so the prologue waits for
+  // two dependent loads rather than two per token.
   {
     const uint16_t *qg = static_cast<const uint16_t *>(L.q) + (size_t)c * L.hq * D;
     for (int ch = tid; ch < kDHeads * (D / 8); ch += kDThreads) {
@@ -133,8 +122,34 @@ __global__ void __launch_bounds__(kDThreads, 2) k_sparse_decode(const DecodeLaun
       cp_async16(sQ + swz<D>(r, cc), qg + (size_t)r * D + cc * 8, true);
     }
     cp_async_commit();
-    cp_async_wait<0>();
   }
+  constexpr int kLook = 4;  // tokens resolved per thread per round
+  for (int t0 = tid; t0 < n; t0 += kDThreads * kLook) {
+    int pos[kLook], pg[kLook];
+#pragma unroll
+    for (int u = 0; u < kLook; ++u) {
+      const int t = t0 + u * kDThreads;
+      pos[u] = t < n ? __ldg(L.idx + (size_t)c * L.topk + lo + t) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kLook; ++u)
+      pg[u] = (pos[u] >= 0 && pos[u] < max_pos)
+                  ? __ldg(L.page_table + (size_t)c * L.pages_per_query + pos[u] / L.page)
+                  : -1;
+#pragma unroll
+    for (int u = 0; u < kLook; ++u) {
+      const int t = t0 + u * kDThreads;
+      if (t < n) {
+        int row = -1;
+        if (pos[u] >= 0) {
+          if (pos[u] < max_pos && pg[u] >= 0 && pg[u] < L.n_pages) row = pg[u] * L.page + pos[u] % L.page;
+          else set_error(L.err, FBM_DEVERR_LUT_RANGE);
+        }
+        s_rows[t] = row;
+      }
+    }
+  }
+  cp_async_wait<0>();
   __syncthreads();
 
   // this group's tiles: grp, grp + 2, ...  Each thread gathers the 16-byte
