@@ -596,6 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         // staging: d half `half` of row `row` as D / 16 pieces of 16 bytes in
         // the 128-byte-swizzled [chunk][64 rows][128 B] tile (d = 128: the half
         // is chunk `half`; d = 64: pieces 4 half .. 4 half + 3 of the one chunk)
+        // the previous row's tensor store has long since read the staging tile:
+        // waiting for that here keeps the wait off the previous row's chain
+        if (tid == 0) bulk_wait_read0();
+        named_sync(kSoftmaxBar, kSoftmaxThreads);
         uint8_t *srow = smem + OFF_STAGE + (D == 128 ? half * kQChunk : 0) + row * 128;
 #pragma unroll
         for (int c = 0; c < D / 16; ++c) {
@@ -615,9 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           for (int c = 0; c < kNch; ++c)
             tma_store_3d(&P.to, sbase + OFF_STAGE + c * kQChunk, c * 64, q0, U.bh_q);
           bulk_commit();
-          bulk_wait_read0();
         }
-        named_sync(kSoftmaxBar, kSoftmaxThreads);  // the staging tile is free again
       }
       pc += npairs;
     }
