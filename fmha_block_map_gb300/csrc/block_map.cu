@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_sim(PoolSide qs, PoolS
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + R::kFlagOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = qs.nunits + ks.nunits;
+  pdl_trigger();  // the score kernel may launch now and wait for this grid
   auto full = [&](int st) { return sbase + R::kBarOff + 8 * st; };
   auto empty = [&](int st) { return sbase + R::kBarOff + 8 * (R::kStages + st); };
   if (threadIdx.x == 0) {
@@ -698,6 +699,7 @@ __global__ void __launch_bounds__(256, NT <= 8 ? 4 : (NT <= 16 ? 3 : 1))
   const int i = rowid % a.nq;
   const int last_q = (i + 1) * a.blkq - 1;
   const int n_elig = a.causal ? min(a.nk, last_q / a.blkk + 1) : a.nk;
+  pdl_wait();  // the scores kernel's output
   constexpr int kQ = NT / 4;  // quarter steps (NT is a multiple of 4)
   if (NT >= 8 && n_elig <= 32 * kQ) select_row<kQ, CDF>(a, hp, rowid, n_elig, hist, lane);
   else if (NT >= 8 && n_elig <= 64 * kQ) select_row<2 * kQ, CDF>(a, hp, rowid, n_elig, hist, lane);
@@ -712,9 +714,9 @@ __global__ void __launch_bounds__(256, NT <= 8 ? 4 : (NT <= 16 ? 3 : 1))
 template <int NT>
 static cudaError_t launch_select(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {
   const int rows = a.b * a.hq * a.nq;
-  if (a.mode_cdf) k_select<NT, true><<<(rows + 7) / 8, 256, 0, st>>>(a, hp);
-  else k_select<NT, false><<<(rows + 7) / 8, 256, 0, st>>>(a, hp);
-  return cudaGetLastError();
+  const dim3 grid((rows + 7) / 8);
+  if (a.mode_cdf) return launch_pdl(k_select<NT, true>, grid, dim3(256), 0, st, a, hp);
+  return launch_pdl(k_select<NT, false>, grid, dim3(256), 0, st, a, hp);
 }
 
 static cudaError_t launch_select_nt(const SelectArgs &a, const HeadParams &hp, cudaStream_t st) {

@@ -91,6 +91,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_pooled_scores_tc(const SelectAr
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the setup above overlaps the pooling kernel's tail; its planes are read
+  // (and this tile written) only after it completes
+  pdl_trigger();
+  pdl_wait();
   if (tid == 0) {
     constexpr uint32_t idesc = idesc_f16(true, false, false, kTM, kTN);
     constexpr uint32_t dhi = sdesc_hi_sw128(1024);  // 8-row atoms of 1024 bytes
@@ -191,8 +195,7 @@ cudaError_t launch_d(const SelectArgs &a, cudaStream_t st) {
     if (dev >= 0 && dev < kMaxDevices) attr_done[dev].store(true, std::memory_order_release);
   }
   dim3 grid(((a.nq + kTM - 1) / kTM) * ((a.nk + kTN - 1) / kTN), a.hq, a.b);
-  k_pooled_scores_tc<D><<<grid, kThreads, SMEM_ALLOC, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_pooled_scores_tc<D>, grid, dim3(kThreads), SMEM_ALLOC, st, a);
 }
 
 }  // namespace
