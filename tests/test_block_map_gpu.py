@@ -252,3 +252,63 @@ def test_cdf_with_512_kv_blocks(fbm_gpu, causal):
     # nk = 512: the 16-scores-per-lane cdf kernel
     cfg = synth.C1.replace(b=1, hq=2, hk=2, s=32768, d=64, dtype="f16", causal=causal)
     run_case(fbm_gpu, cfg, "cdf", 0.8)
+
+
+def _c4_small(seed):
+    """A causal GQA + sink case with 256 kv blocks (the chained launches of the
+    score and selection kernels, and the causal selection bodies)."""
+    return synth.C4.replace(s=16384, hq=8, hk=2, seed=seed)
+
+
+def test_back_to_back_calls_share_a_workspace(fbm_gpu):
+    """Two block maps on one stream, one workspace, no sync between them: each
+    LUT equals the one its inputs give alone (each kernel of the second call
+    starts only after the kernels of the first it could disturb)."""
+    fbm = fbm_gpu
+    outs, solo = [], []
+    cfgs = [_c4_small(11), _c4_small(12)]
+    ins = []
+    for cfg in cfgs:
+        x = synth.prefill(cfg)
+        ins.append((to_dev(x["q"], cfg.dtype), to_dev(x["k"], cfg.dtype)))
+    cfg = cfgs[0]
+    ws = torch.empty(fbm.block_map_workspace_bytes(cfg.b, cfg.hq, cfg.hk, cfg.s, cfg.d),
+                     dtype=torch.uint8, device="cuda")
+    kw = dict(topk=cfg.topk, simthreshd1=cfg.simthreshd1, scale=cfg.scale, causal=True,
+              attention_sink=True)
+    for q, k in ins:
+        solo.append(tuple(t.clone() for t in fbm.sparge_block_map(q, k, workspace=ws, **kw)[:2]))
+        torch.cuda.synchronize()
+    for q, k in ins:
+        outs.append(fbm.sparge_block_map(q, k, workspace=ws, **kw)[:2])
+    torch.cuda.synchronize()
+    assert fbm.get_error() == 0
+    for (lut, cnt), (slut, scnt) in zip(outs, solo):
+        assert torch.equal(lut, slut) and torch.equal(cnt, scnt)
+    assert not torch.equal(outs[0][0], outs[1][0])  # the two inputs select differently
+
+
+def test_graph_capture_matches_eager(fbm_gpu):
+    """The block map captured in a CUDA graph (its chained launches become graph
+    dependencies) and replayed gives the eager LUT."""
+    fbm = fbm_gpu
+    cfg = _c4_small(13)
+    x = synth.prefill(cfg)
+    q, k = to_dev(x["q"], cfg.dtype), to_dev(x["k"], cfg.dtype)
+    kw = dict(topk=cfg.topk, simthreshd1=cfg.simthreshd1, scale=cfg.scale, causal=True,
+              attention_sink=True)
+    ref_lut, ref_cnt = (t.clone() for t in fbm.sparge_block_map(q, k, **kw)[:2])
+    lut = torch.full_like(ref_lut, 7)
+    cnt = torch.full_like(ref_cnt, 7)
+    ws = torch.empty(fbm.block_map_workspace_bytes(cfg.b, cfg.hq, cfg.hk, cfg.s, cfg.d),
+                     dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        fbm.sparge_block_map(q, k, lut=lut, lut_count=cnt, workspace=ws, **kw)
+    g.replay()
+    torch.cuda.synchronize()
+    assert fbm.get_error() == 0
+    assert torch.equal(lut, ref_lut) and torch.equal(cnt, ref_cnt)
