@@ -676,6 +676,13 @@ def measure_decode(hbm_gbs, small=False):
         # a few µs of device work: timed inside a CUDA graph, or the host's
         # launch overhead would be measured instead
         c_ms = _graph_ms(comb, 20, 3)
+
+        def dec_comb():
+            dec()
+            comb()
+
+        # the pair as a decode step runs it (the combine a chained launch)
+        p_ms = _events_ms(dec_comb, 20, 3)
         rows_bytes = cfg.n_queries * cfg.topk * cfg.d * 2
         part_bytes = S * cfg.n_queries * cfg.hq * (cfg.dv + 1) * 4
         d_bytes = rows_bytes + q.numel() * 2 + ix.numel() * 4 + part_bytes \
@@ -685,7 +692,8 @@ def measure_decode(hbm_gbs, small=False):
                     "decode_GB_s": round(d_bytes / (d_ms * 1e-3) / 1e9, 1),
                     "decode_frac_hbm": round(d_bytes / (d_ms * 1e-3) / 1e9 / hbm_gbs, 3),
                     "combine_ms": round(c_ms, 4),
-                    "combine_GB_s": round(c_bytes / (c_ms * 1e-3) / 1e9, 1)})
+                    "combine_GB_s": round(c_bytes / (c_ms * 1e-3) / 1e9, 1),
+                    "decode_plus_combine_ms": round(p_ms, 4)})
     assert fbm.get_error() == 0
     del cache
     torch.cuda.empty_cache()

@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(256) k_attn_combine(const CombineLaunch L) {
   const int lane = threadIdx.x & 31;
   const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (row >= L.rows) return;
+  pdl_wait();  // the partials' writer (launched just before, on the same stream)
   // weights: lane s holds split s (and s + 32)
   float l0 = -INFINITY, l1 = -INFINITY;
   if (lane < L.num_splits) l0 = L.lse_part[(int64_t)lane * L.rows + row];
@@ -86,7 +87,8 @@ __global__ void __launch_bounds__(256) k_attn_combine(const CombineLaunch L) {
 // chunks at once, then weights them: no cross-lane reduction and no load
 // waiting on another, and with few registers many threads keep loads in
 // flight.  Same order of operations as the warp kernel above, so the results
-// are identical.
+// are identical.  Both kernels are chained launches (launch_pdl): they wait
+// for the kernel that wrote the partials before reading them.
 constexpr int kSmallSplits = 8;
 
 template <int OUT, int SMAX, int CH>
@@ -94,6 +96,7 @@ __global__ void __launch_bounds__(256) k_attn_combine_few(const CombineLaunch L)
   const int per_row = L.dv / (4 * CH);
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= L.rows * per_row) return;
+  pdl_wait();  // the partials' writer (launched just before, on the same stream)
   const int64_t row = t / per_row;
   const int c = (int)(t - row * per_row) * 4 * CH;
   float l[SMAX];
@@ -148,11 +151,10 @@ __global__ void __launch_bounds__(256) k_attn_combine_few(const CombineLaunch L)
 template <int SMAX, int CH>
 cudaError_t launch_few(const CombineLaunch &L, cudaStream_t st) {
   const int64_t threads = L.rows * (L.dv / (4 * CH));
-  const unsigned grid = (unsigned)((threads + 255) / 256);
-  if (L.out_dtype == FBM_F32) k_attn_combine_few<2, SMAX, CH><<<grid, 256, 0, st>>>(L);
-  else if (L.out_dtype == FBM_BF16) k_attn_combine_few<1, SMAX, CH><<<grid, 256, 0, st>>>(L);
-  else k_attn_combine_few<0, SMAX, CH><<<grid, 256, 0, st>>>(L);
-  return cudaGetLastError();
+  const dim3 grid((unsigned)((threads + 255) / 256));
+  if (L.out_dtype == FBM_F32) return launch_pdl(k_attn_combine_few<2, SMAX, CH>, grid, dim3(256), 0, st, L);
+  if (L.out_dtype == FBM_BF16) return launch_pdl(k_attn_combine_few<1, SMAX, CH>, grid, dim3(256), 0, st, L);
+  return launch_pdl(k_attn_combine_few<0, SMAX, CH>, grid, dim3(256), 0, st, L);
 }
 
 }  // namespace
@@ -166,11 +168,10 @@ cudaError_t launch_combine(const CombineLaunch &L, cudaStream_t st) {
     return launch_few<8, 1>(L, st);
   }
   const int64_t threads = L.rows * 32;
-  const unsigned grid = (unsigned)((threads + 255) / 256);
-  if (L.out_dtype == FBM_F32) k_attn_combine<2><<<grid, 256, 0, st>>>(L);
-  else if (L.out_dtype == FBM_BF16) k_attn_combine<1><<<grid, 256, 0, st>>>(L);
-  else k_attn_combine<0><<<grid, 256, 0, st>>>(L);
-  return cudaGetLastError();
+  const dim3 grid((unsigned)((threads + 255) / 256));
+  if (L.out_dtype == FBM_F32) return launch_pdl(k_attn_combine<2>, grid, dim3(256), 0, st, L);
+  if (L.out_dtype == FBM_BF16) return launch_pdl(k_attn_combine<1>, grid, dim3(256), 0, st, L);
+  return launch_pdl(k_attn_combine<0>, grid, dim3(256), 0, st, L);
 }
 
 }  // namespace fbm

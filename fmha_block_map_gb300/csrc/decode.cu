@@ -110,6 +110,10 @@ __global__ void __launch_bounds__(kDThreads, 2) k_sparse_decode(const DecodeLaun
   const int n = base + (split < extra ? 1 : 0);
   const uint16_t *cache = static_cast<const uint16_t *>(L.cache);
   const int max_pos = L.pages_per_query * L.page;
+  // a chained launch: it reads its inputs and writes its partials only once
+  // the kernel before it is done (no early trigger: a following decode's CTAs
+  // dispatched early would crowd onto the idle SMs and unbalance it)
+  pdl_wait();
 
   // prologue: Q [16][D] first (its copy overlaps the lookups), then the token
   // list -> physical rows (-1 = masked).  A thread issues the index loads of
@@ -353,8 +357,8 @@ cudaError_t launch_e(const DecodeLaunch &L, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k_sparse_decode<E, 576, 512>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_sparse_decode<E, 576, 512><<<L.n_q * L.num_splits, kDThreads, smem, st>>>(L);
-  return cudaGetLastError();
+  return launch_pdl(k_sparse_decode<E, 576, 512>, dim3(L.n_q * L.num_splits), dim3(kDThreads), smem,
+                    st, L);
 }
 
 }  // namespace
