@@ -107,3 +107,34 @@ def test_f16_cache(fbm_gpu):
         ro, rl = oracle.decode_attention(qf[c], kv, cfg.dv, cfg.sm_scale)
         assert_close_o(out[c], ro, f"O q{c}")
         assert_close_lse(lse[c], rl, f"LSE q{c}")
+
+
+def test_graph_capture_matches_eager(fbm_gpu):
+    """Decode + combine (chained launches) captured in a CUDA graph and replayed
+    give the eager partials and output, bit for bit."""
+    fbm = fbm_gpu
+    cfg = synth.C5.replace(n_queries=8, pages_per_query=16, topk=300)
+    inp = synth.decode(cfg)
+    cache = gpu_cache(cfg)
+    q = torch.from_numpy(inp["q"].view(np.int16)).view(torch.bfloat16).cuda()
+    pt = torch.from_numpy(inp["page_table"]).cuda()
+    ix = torch.from_numpy(inp["idx"]).cuda()
+    S = 3
+    kw = dict(dv=cfg.dv, scale=cfg.sm_scale, num_splits=S)
+    op0, lp0 = fbm.sparse_decode_fwd(q, cache, pt, ix, **kw)
+    out0, lse0 = fbm.attn_combine(op0, lp0, out_dtype=torch.bfloat16)
+    op = torch.full_like(op0, 7.0)
+    lp = torch.full_like(lp0, 7.0)
+    out = torch.zeros_like(out0)
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        fbm.sparse_decode_fwd(q, cache, pt, ix, o_partial=op, lse_partial=lp, **kw)
+        _, lse = fbm.attn_combine(op, lp, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    assert fbm.get_error() == 0
+    assert torch.equal(op, op0) and torch.equal(lp, lp0)
+    assert torch.equal(out, out0) and torch.equal(lse, lse0)
