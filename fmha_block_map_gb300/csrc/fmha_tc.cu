@@ -75,7 +75,7 @@ enum {
   B_QF = 0, B_QE = 2, B_KF = 4, B_KE = B_KF + kKSlots, B_VF = B_KE + kKSlots,
   B_VE = B_VF + kVSlots, B_SF = B_VE + kVSlots, B_SE = B_SF + kSSlots, B_PF = B_SE + kSSlots,
   B_PV = B_PF + kPBufs, B_OF = B_PV + kPBufs, B_DRAIN = B_OF + 1, B_DRAIN2 = B_DRAIN + 1,
-  NBAR = B_DRAIN2 + 1
+  B_PVI = B_DRAIN2 + 1, NBAR = B_PVI + 1
 };
 // Shared-memory layout for head dim D (64 or 128): a 64-row tile of D 16-bit
 // values is D / 64 chunks of 64 columns (128-byte rows, 128-byte swizzle).
@@ -321,6 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
       if (!(ok = mbar_wait_w(bar(B_QF + qb), (uc >> 1) & 1, abort_flag, kWaitNs))) break;
       tc_fence_after();
       const uint32_t q_lo = sdesc_lo(sbase + OFF_Q + qb * kQBytes, 16);
+      // the previous row's last PV goes into the tensor pipe before this row's
+      // first S, so the previous row's epilogue does not wait behind it
+      if (uc > 0 && !(ok = mbar_wait_w(bar(B_PVI), (uc - 1) & 1, abort_flag, kWaitNs))) break;
       for (int p = 0; p < npairs; ++p) {
         const int g = pc + p, slot = g % kKSlots, ss = g % kSSlots;
         if (!(ok = mbar_wait_w(bar(B_KF + slot), (g / kKSlots) & 1, abort_flag, kWaitNs))) break;
@@ -391,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
                          (p > 0 || kk > 0) ? 1u : 0u);
         mma_commit_w(bar(B_PV + pb));
         mma_commit_w(bar(B_VE + slot));
+        if (p == npairs - 1) mbar_arrive_lane0(bar(B_PVI), lane);  // the row's last PV is issued
       }
       pc += npairs;
       uc += 1;
