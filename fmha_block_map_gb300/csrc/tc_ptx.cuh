@@ -224,8 +224,10 @@ FBM_DEVICE void mma_commit(uint32_t bar) {
 // chosen by elect.sync issues the instruction.  The issuing loop then runs warp-
 // uniform, which keeps the descriptor arithmetic on uniform registers: a chain
 // of M = 64 MMAs issued this way measured 64-70 cycles per MMA, against ~90
-// from a single lane inside a divergent branch.  The same lane is elected each
-// time (the lowest active one), so a commit issued this way tracks the MMAs.
+// from a single lane inside a divergent branch.  With all 32 lanes active the
+// election is the same every time, so a commit issued this way comes from the
+// thread that issued the MMAs it tracks (a commit from another thread would
+// track none of them).
 FBM_DEVICE void mma_f16_lo_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
                              uint32_t idesc, uint32_t accumulate) {
   asm volatile(
