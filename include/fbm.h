@@ -24,7 +24,11 @@
  *    "host" arrays are read before the call returns.
  *  - All work is enqueued on `stream` (a cudaStream_t passed as void*, NULL =
  *    the legacy default stream) and runs asynchronously; outputs are valid
- *    once the stream reaches that point.
+ *    once the stream reaches that point.  The score and selection kernels of
+ *    the block map, the decode and the combine are programmatic dependent
+ *    launches: each may start while the kernel before it on the stream
+ *    finishes, but waits for it (griddepcontrol.wait) before reading any
+ *    input or writing any output, so stream order holds for all memory.
  *  - Argument checks run on the host before any launch.  A failed check
  *    returns FBM_ERR_INVALID_ARG or FBM_ERR_UNSUPPORTED and launches nothing;
  *    fbm_last_error_message() then describes it (per thread).
