@@ -95,19 +95,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_pooled_scores_tc(const SelectAr
   // (and this tile written) only after it completes
   pdl_trigger();
   pdl_wait();
-  if (tid == 0) {
+  if (warp == 0) {
+    // the whole warp runs the loop; one lane issues the copies, one elected
+    // lane each MMA (issued from a lone lane in a divergent branch, the 24 MMAs
+    // of a chunk took about twice their execution time)
     constexpr uint32_t idesc = idesc_f16(true, false, false, kTM, kTN);
     constexpr uint32_t dhi = sdesc_hi_sw128(1024);  // 8-row atoms of 1024 bytes
     constexpr uint32_t kChunk = (uint32_t)(3 * kPlaneBytes);
     bool ok = true;
     for (int c = 0; c < D / kKC; ++c) {
       // the chunk's planes of A and B: two bulk copies on one barrier
-      mbar_arrive_tx(full, 2 * kChunk);
-      bulk_load(sbase + OFF_A, pa + (size_t)c * kChunk, kChunk, full);
-      bulk_load(sbase + OFF_B, pb + (size_t)c * kChunk, kChunk, full);
-      if (!mbar_wait_for(full, c & 1, kWaitNs)) {
+      if (lane == 0) {
+        mbar_arrive_tx(full, 2 * kChunk);
+        bulk_load(sbase + OFF_A, pa + (size_t)c * kChunk, kChunk, full);
+        bulk_load(sbase + OFF_B, pb + (size_t)c * kChunk, kChunk, full);
+      }
+      __syncwarp();
+      if (!mbar_wait_for_w(full, c & 1, kWaitNs)) {
         ok = false;
-        mbar_wait_for(full, c & 1, kWaitNs);  // drain the copies in flight (bounded)
+        mbar_wait_for_w(full, c & 1, kWaitNs);  // drain the copies in flight (bounded)
         break;
       }
       tc_fence_after();
@@ -119,19 +125,19 @@ __global__ void __launch_bounds__(kThreads, 2) k_pooled_scores_tc(const SelectAr
         for (int t = 0; t < 6; ++t) {
           const int ta = t < 3 ? 2 - t : (t < 5 ? 4 - t : 0);
           const int tb = t < 3 ? t : (t < 5 ? t - 3 : 0);
-          mma_f16_lo(tmem, sdesc_lo(sbase + OFF_A + ta * (uint32_t)kPlaneBytes + ks * 32, 16),
-                     sdesc_lo(sbase + OFF_B + tb * (uint32_t)kPlaneBytes + ks * 32, 16), dhi, idesc,
-                     (c > 0 || ks > 0 || t > 0) ? 1u : 0u);
+          mma_f16_lo_w(tmem, sdesc_lo(sbase + OFF_A + ta * (uint32_t)kPlaneBytes + ks * 32, 16),
+                       sdesc_lo(sbase + OFF_B + tb * (uint32_t)kPlaneBytes + ks * 32, 16), dhi, idesc,
+                       (c > 0 || ks > 0 || t > 0) ? 1u : 0u);
         }
-      mma_commit(done);
+      mma_commit_w(done);
       // the planes are refilled (and TMEM read) only after the MMAs finish
-      if (!mbar_wait_for(done, c & 1, kWaitNs)) {
+      if (!mbar_wait_for_w(done, c & 1, kWaitNs)) {
         ok = false;
-        mbar_wait_for(done, c & 1, kWaitNs);  // drain the MMAs in flight (bounded)
+        mbar_wait_for_w(done, c & 1, kWaitNs);  // drain the MMAs in flight (bounded)
         break;
       }
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       set_error(a.err, FBM_DEVERR_TIMEOUT);
       *flag = 0;
     }
@@ -158,15 +164,23 @@ __global__ void __launch_bounds__(kThreads, 2) k_pooled_scores_tc(const SelectAr
                              a.scale * __uint_as_float(v[4 * e + 2]),
                              a.scale * __uint_as_float(v[4 * e + 3]));
     }
+    // whole rows of the tile.  Aligned full rows leave as bulk copies (one per
+    // row, issued by lanes 0-15 of every warp, asynchronous: the row loop of
+    // 16-byte stores took ~4000 cycles per tile); otherwise plain stores.
+    const bool bulk = ncol % 4 == 0 && (a.nk & 3) == 0 && (reinterpret_cast<uintptr_t>(S) & 15) == 0;
+    if (bulk) fence_proxy_async();  // this thread's staged values, for the async proxy
     __syncthreads();
-    // whole rows of the tile: 512 contiguous bytes per warp store
-    const bool vec = ncol == kTN && (a.nk & 3) == 0 && (reinterpret_cast<uintptr_t>(S) & 15) == 0;
-    for (int r = warp; r < nrow; r += kThreads / 32) {
-      float *grow = S + (size_t)(i0 + r) * a.nk + n0;
-      const float *srow = stage + r * kSPitch;
-      if (vec) {
-        reinterpret_cast<float4 *>(grow)[lane] = reinterpret_cast<const float4 *>(srow)[lane];
-      } else {
+    if (bulk) {
+      const int r = warp * 16 + lane;  // 8 warps x 16 lanes = the 128 rows of a full tile
+      if (lane < 16 && r < nrow) {
+        bulk_store(S + (size_t)(i0 + r) * a.nk + n0, smem_u32(stage + r * kSPitch), (uint32_t)ncol * 4);
+        bulk_commit();
+        bulk_wait_read0();  // the staged row is read before the CTA leaves
+      }
+    } else {
+      for (int r = warp; r < nrow; r += kThreads / 32) {
+        float *grow = S + (size_t)(i0 + r) * a.nk + n0;
+        const float *srow = stage + r * kSPitch;
         for (int c = lane; c < ncol; c += 32) grow[c] = srow[c];
       }
     }

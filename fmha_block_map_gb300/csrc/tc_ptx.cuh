@@ -132,6 +132,13 @@ FBM_DEVICE uint64_t l2_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
   return p;
 }
+// one contiguous shared -> global bulk copy (both addresses 16-byte aligned,
+// bytes a multiple of 16), tracked by the issuing thread's bulk groups
+FBM_DEVICE void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
 FBM_DEVICE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 FBM_DEVICE void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
