@@ -416,6 +416,58 @@ FBM_DEVICE uint32_t bitwise_kth(const float (&sc)[NT], uint32_t cand, int kcount
   return __reduce_min_sync(0xffffffffu, mn);
 }
 
+// A row's scores by value, for the out-of-line rare paths (the hot path keeps
+// them in registers).
+template <int NT>
+struct RowScores {
+  float v[NT];
+};
+struct KthResult {
+  float tv;
+  bool exact;
+};
+
+// The kcount-th largest score among `cand` by the bitwise key search, and
+// whether exactly kcount candidates lie at or above it.  Out of line: taken
+// only for a row whose range fp32 cannot split or whose crossing bin holds
+// more than 32 scores.
+template <int NT>
+__device__ __noinline__ KthResult kth_by_bits(const RowScores<NT> r, uint32_t cand, int kcount) {
+  const uint32_t T = bitwise_kth<NT>(r.v, cand, kcount);
+  const float tv = key_value(T);
+  int ge = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) ge += ((cand >> t) & 1u) && r.v[t] >= tv ? 1 : 0;
+  KthResult k;
+  k.tv = tv;
+  k.exact = __reduce_add_sync(0xffffffffu, ge) == kcount;
+  return k;
+}
+
+// Selection bits of a row whose threshold score tv is tied: every score above
+// tv, then the tied ones in ascending column order up to kcount.  Out of line
+// (rare for real-valued scores).
+template <int NT>
+__device__ __noinline__ uint32_t select_ties(const RowScores<NT> r, uint32_t fin, float tv, int kcount,
+                                             int lane) {
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int cgt = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) cgt += is_fin(fin, t) && r.v[t] > tv ? 1 : 0;
+  const int need = kcount - __reduce_add_sync(0xffffffffu, cgt);
+  int run = 0;
+  uint32_t sel = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const bool tie = is_fin(fin, t) && r.v[t] == tv;
+    const unsigned bal = __ballot_sync(0xffffffffu, tie);
+    const bool s = (is_fin(fin, t) && r.v[t] > tv) || (tie && run + __popc(bal & lt_mask) < need);
+    sel |= (s ? 1u : 0u) << t;
+    run += __popc(bal);
+  }
+  return sel;
+}
+
 // The kcount-th largest selectable score of a warp's row (1 <= kcount <=
 // number of selectable scores), by radix selection:
 //  1. a coarse digit: each selectable score s maps to bin
@@ -449,13 +501,12 @@ FBM_DEVICE float kth_largest(const float (&sc)[NT], uint32_t finl, int kcount, f
   const float inv = 256.0f / range;
   if (!(range > 0.f) || !(inv < INFINITY) || !(inv > 0.f)) {
     // one value, or a range fp32 cannot split
-    const uint32_t T = bitwise_kth<NT>(sc, finl, kcount);
-    const float tv = key_value(T);
-    int ge = 0;
+    RowScores<NT> r;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) ge += ((finl >> t) & 1u) && sc[t] >= tv ? 1 : 0;
-    exact = __reduce_add_sync(0xffffffffu, ge) == kcount;
-    return tv;
+    for (int t = 0; t < NT; ++t) r.v[t] = sc[t];
+    const KthResult k = kth_by_bits<NT>(r, finl, kcount);
+    exact = k.exact;
+    return k.tv;
   }
   int dig[NT];
 #pragma unroll
@@ -517,13 +568,12 @@ FBM_DEVICE float kth_largest(const float (&sc)[NT], uint32_t finl, int kcount, f
     return mn;
   }
   if (nbin > 32) {
-    const uint32_t T = bitwise_kth<NT>(sc, cand, need);
-    const float tv = key_value(T);
-    int ge = 0;
+    RowScores<NT> r;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) ge += ((cand >> t) & 1u) && sc[t] >= tv ? 1 : 0;
-    exact = __reduce_add_sync(0xffffffffu, ge) == need;
-    return tv;
+    for (int t = 0; t < NT; ++t) r.v[t] = sc[t];
+    const KthResult k = kth_by_bits<NT>(r, cand, need);
+    exact = k.exact;
+    return k.tv;
   }
   // compact the bin's scores, one per lane, in the warp's counters (done with)
   __syncwarp();
@@ -594,19 +644,10 @@ FBM_DEVICE void select_row(const SelectArgs &a, const HeadParams &hp, int rowid,
         for (int t = 0; t < NT; ++t) sel |= (is_fin(fin, t) && sc[t] >= tv ? 1u : 0u) << t;
       } else {
         // ties at the threshold: the lower kv blocks first
-        int cgt = 0;
+        RowScores<NT> r;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) cgt += is_fin(fin, t) && sc[t] > tv ? 1 : 0;
-        const int need = kcount - __reduce_add_sync(0xffffffffu, cgt);
-        int run = 0;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const bool tie = is_fin(fin, t) && sc[t] == tv;
-          const unsigned bal = __ballot_sync(0xffffffffu, tie);
-          const bool s = (is_fin(fin, t) && sc[t] > tv) || (tie && run + __popc(bal & lt_mask) < need);
-          sel |= (s ? 1u : 0u) << t;
-          run += __popc(bal);
-        }
+        for (int t = 0; t < NT; ++t) r.v[t] = sc[t];
+        sel = select_ties<NT>(r, fin, tv, kcount, lane);
       }
     } else {
       uint32_t key[NT];
@@ -668,6 +709,7 @@ FBM_DEVICE void select_row(const SelectArgs &a, const HeadParams &hp, int rowid,
   const size_t row = (size_t)rowid;
   int32_t *lut = a.lut + row * a.nk;
   int run = 0;
+  uint32_t keepm = 0;  // bit t: column lane + 32 t is kept
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const int j = lane + 32 * t;
@@ -676,12 +718,20 @@ FBM_DEVICE void select_row(const SelectArgs &a, const HeadParams &hp, int rowid,
                                (a.sink && j == 0));
     const unsigned bal = __ballot_sync(0xffffffffu, keep);
     if (keep) lut[run + __popc(bal & lt_mask)] = j;
-    if (a.bmap && j < ncols) a.bmap[row * a.nk + j] = keep ? 1 : 0;
+    keepm |= (keep ? 1u : 0u) << t;
     run += __popc(bal);
   }
   for (int p = run + lane; p < a.nk; p += 32) lut[p] = -1;
-  if (a.bmap)
-    for (int j = ncols + lane; j < a.nk; j += 32) a.bmap[row * a.nk + j] = 0;
+  if (a.bmap) {
+    // the optional 0/1 block map, kept out of the unrolled loops above
+    uint8_t *brow = a.bmap + row * a.nk;
+#pragma unroll 1
+    for (int t = 0; t < NT; ++t) {
+      const int j = lane + 32 * t;
+      if (j < ncols) brow[j] = (uint8_t)((keepm >> t) & 1u);
+    }
+    for (int j = ncols + lane; j < a.nk; j += 32) brow[j] = 0;
+  }
   if (lane == 0) a.cnt[row] = run;
 }
 
