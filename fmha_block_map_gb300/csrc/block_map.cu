@@ -737,9 +737,11 @@ FBM_DEVICE void select_row(const SelectArgs &a, const HeadParams &hp, int rowid,
 
 // one warp per q block (row): 8 warps per CTA.  NT = ceil(nk / 32) scores per
 // lane; a causal row whose eligible prefix is shorter runs the body of a
-// smaller NT (the branch is uniform over the warp).
+// smaller NT (the branch is uniform over the warp).  Up to NT = 16, four CTAs
+// per SM (64 registers): with a few spilled bytes this measured faster than
+// three CTAs at 80 registers, the rows waiting mostly on their loads.
 template <int NT, bool CDF>
-__global__ void __launch_bounds__(256, NT <= 8 ? 4 : (NT <= 16 ? 3 : 1))
+__global__ void __launch_bounds__(256, NT <= 16 ? 4 : 1)
     k_select(SelectArgs a, const __grid_constant__ HeadParams hp) {
   __shared__ __align__(16) int hist_all[8][256];  // radix-select counters, one set per warp
   const int lane = threadIdx.x & 31;
