@@ -325,6 +325,9 @@ def run_ours(args):
 
     # ---- the block map with K smoothing (one more K read), dense FMHA, topk sweep
     smooth_ms = timed(lambda: block_map(args.topk, smooth_k=True), 5, 1)
+    # the same call replayed from a CUDA graph (20 calls per replay): no host
+    # launch gaps between its three kernels or between calls
+    bm_graph_ms = _graph_ms(lambda: block_map(args.topk), reps=20, warm=3)
     block_map(args.topk)
     dense64_ms = timed(lambda: attn(dense=True), max(2, args.steps // 10), 1)
     dense_ms = timed(lambda: attn_pairs(dense=True), max(2, args.steps // 10), 1)
@@ -526,7 +529,9 @@ def run_ours(args):
                       "GB_s": round(bm_bytes / (bm_ms * 1e-3) / 1e9, 1),
                       "frac_hbm": round(bm_bytes / (bm_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
                       "share_of_step": round(bm_ms / step_ms, 3),
-                      "smooth_k_ms": round(smooth_ms, 4)},
+                      "smooth_k_ms": round(smooth_ms, 4),
+                      "graph_ms": round(bm_graph_ms, 4),
+                      "graph_frac_hbm": round(bm_bytes / (bm_graph_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)},
         "roofline": {"kernel": "sparse_fmha_fwd (k_fmha_tc, tcgen05)", "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} bf16 burst (fp16 tensor rate = bf16)",
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -632,6 +637,7 @@ def measure_causal_gqa(hbm_gbs, peak):
     # 30 back-to-back calls: the host's start-up before the first launch is
     # then a small share of the timed span
     bm_ms = _events_ms(bm, 30, 3)
+    bm_graph_ms = _graph_ms(bm, reps=20, warm=3)
     at_ms = _events_ms(at, 10, 3)
     bm_bytes = (q.numel() + k.numel()) * 2 + 2 * (32 * nq + 8 * nq) * 129 * 4 + lut.numel() * 4
     assert fbm.get_error() == 0
@@ -639,6 +645,8 @@ def measure_causal_gqa(hbm_gbs, peak):
             "selected_tiles": tiles, "block_map_ms": round(bm_ms, 4),
             "block_map_GB_s": round(bm_bytes / (bm_ms * 1e-3) / 1e9, 1),
             "block_map_frac_hbm": round(bm_bytes / (bm_ms * 1e-3) / 1e9 / hbm_gbs, 3),
+            "block_map_graph_ms": round(bm_graph_ms, 4),
+            "block_map_graph_frac_hbm": round(bm_bytes / (bm_graph_ms * 1e-3) / 1e9 / hbm_gbs, 3),
             "attn_ms": round(at_ms, 4),
             "attn_eff_tflops": round(tiles * FLOP_PER_TILE / (at_ms * 1e-3) / 1e12, 1),
             "attn_frac_peak": round(tiles * FLOP_PER_TILE / (at_ms * 1e-3) / 1e12 / peak, 4)}
