@@ -704,6 +704,29 @@ def measure_decode(hbm_gbs, small=False):
                     "combine_ms": round(c_ms, 4),
                     "combine_GB_s": round(c_bytes / (c_ms * 1e-3) / 1e9, 1),
                     "decode_plus_combine_ms": round(p_ms, 4)})
+    # the same calls replayed from CUDA graphs (20 per replay): no host launch
+    # gaps.  After the eager legs, so that their launch order is unchanged.
+    for r in res:
+        S = r["splits"]
+        op = torch.empty((S, cfg.n_queries, cfg.hq, cfg.dv), dtype=torch.float32, device="cuda")
+        lp = torch.empty((S, cfg.n_queries, cfg.hq), dtype=torch.float32, device="cuda")
+        o = torch.empty((cfg.n_queries, cfg.hq, cfg.dv), dtype=torch.bfloat16, device="cuda")
+
+        def dec_g(S=S, op=op, lp=lp):
+            fbm.sparse_decode_fwd(q, cache, pt, ix, dv=cfg.dv, scale=cfg.sm_scale, num_splits=S,
+                                  o_partial=op, lse_partial=lp)
+
+        def dec_comb_g(op=op, lp=lp, o=o):
+            dec_g()
+            fbm.attn_combine(op, lp, out=o, return_lse=False)
+
+        dg_ms = _graph_ms(dec_g, 20, 3)
+        pg_ms = _graph_ms(dec_comb_g, 20, 3)
+        d_bytes = (cfg.n_queries * cfg.topk * cfg.d * 2 + q.numel() * 2 + ix.numel() * 4
+                   + S * cfg.n_queries * cfg.hq * (cfg.dv + 1) * 4 + cfg.n_queries * cfg.topk * 4)
+        r["decode_graph_ms"] = round(dg_ms, 4)
+        r["decode_graph_frac_hbm"] = round(d_bytes / (dg_ms * 1e-3) / 1e9 / hbm_gbs, 3)
+        r["decode_plus_combine_graph_ms"] = round(pg_ms, 4)
     assert fbm.get_error() == 0
     del cache
     torch.cuda.empty_cache()
