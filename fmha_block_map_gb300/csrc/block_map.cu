@@ -1,15 +1,16 @@
 // Block-map prediction kernels ("Sparge Attention (Composable Kernel)" README:
 // mean-pool -> cosine sim -> pooled QK -> top-k / cdfthreshd LUT).
 //
-//  k_pool_sim     one warp per 64-token block of Q or K: each lane streams 32
-//                 bytes of a row per step (128-bit loads, 16 in flight per
-//                 lane), row norms by a 3-level shuffle, fp32 row sums (the
-//                 pooled mean, two interleaved partial sums per element) and the
-//                 sum of unit rows (self-similarity = ||sum u||^2 / n^2).
-//                 HBM-bound: it reads Q and K once and writes, per block, the
-//                 mean as three bf16 split planes (the operands of the pooled
-//                 scores' tensor-core product, in their shared-memory layout)
-//                 and one float.
+//  k_pool_sim     persistent, one CTA per SM: a producer lane bulk-copies
+//                 whole 64-token blocks of Q and K (contiguous rows) into a
+//                 192 KB shared-memory ring with an evict-first L2 hint; eight
+//                 consumer warps reduce them: row norms, fp32 row sums (the
+//                 pooled mean, two interleaved packed f32x2 partial sums per
+//                 element) and the sum of unit rows (self-similarity =
+//                 ||sum u||^2 / n^2).  HBM-bound: it reads Q and K once and
+//                 writes, per block, the mean as three bf16 split planes (the
+//                 operands of the pooled scores' tensor-core product, in their
+//                 shared-memory layout) and one float.
 //  k_key_mean     K smoothing only: one CTA per (batch, KV head) forms the mean
 //                 key row from the block means of the first pooling pass (fixed
 //                 summation order, so the result is deterministic); a second
@@ -18,13 +19,14 @@
 //  pooled scores  scale * qbar . kbar on tcgen05 from the split planes
 //                 (pooled_scores_tc.cu), written as fp32 into the caller's LUT
 //                 buffer, which has exactly the size of the score matrix.
-//  k_select       one warp per q block: loads its score row, then the pooled
-//                 softmax, a radix (bitwise) threshold search for top-k / cdf,
-//                 and ballot-scan emission of the ascending LUT row over the
-//                 scores it has read.  No atomics take part in slot assignment.
-//                 Apart from the product (which keeps every SM's FMA pipe busy)
-//                 the selection is a chain of warp reductions; a kernel of its
-//                 own runs it at full occupancy.
+//  k_select       one warp per q block: loads its score row, then (cdf mode) the
+//                 pooled softmax, a radix select of the threshold (a 256-bin
+//                 histogram of a linear digit, exact ranking inside the
+//                 crossing bin) and ballot-scan emission of the ascending LUT
+//                 row over the scores it has read.  No atomics take part in
+//                 slot assignment.  The paths real-valued rows rarely take run
+//                 out of line, so that the unrolled row bodies stay in the
+//                 instruction cache.
 #include <algorithm>
 #include <atomic>
 
