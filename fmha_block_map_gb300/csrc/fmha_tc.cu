@@ -33,12 +33,17 @@
 // score exceeds it by more than 2^8); both threads of a row agree on it through
 // one shuffle.
 //
-// Roles (one persistent CTA per SM, 8 warps):
+// Roles (one persistent CTA per SM; 12 warps for whole rows, 8 for fp32 partials):
 //   warp 0   TMA producer of Q (double buffer) and K pairs (3-slot ring)
 //   warp 1   TMA producer of V pairs (2-slot ring)
 //   warp 2   TMEM owner and S issuer
 //   warp 3   PV issuer
-//   warps 4-7 softmax and epilogue (TMEM subpartitions 0-3)
+//   warps 4-7 softmax (TMEM subpartitions 0-3); fp32 partials leave from here
+//   warps 8-11 epilogue of whole rows: a row's sum and max come from the
+//            softmax warps through shared memory, O from TMEM once the row's
+//            last PV is done, so the softmax warps go straight on to the next
+//            row.  setmaxnreg gives the softmax warpgroup 232 registers, the
+//            other two 80 and 128.
 // Pipeline: S(g) is issued once K(g) has landed and its TMEM slot is free (the
 // softmax releases a slot as soon as it holds the scores in registers), so the
 // S MMA of pair g + 1 runs during the softmax of pair g; PV(g) once P(g) is in
@@ -75,7 +80,10 @@ enum {
   B_QF = 0, B_QE = 2, B_KF = 4, B_KE = B_KF + kKSlots, B_VF = B_KE + kKSlots,
   B_VE = B_VF + kVSlots, B_SF = B_VE + kVSlots, B_SE = B_SF + kSSlots, B_PF = B_SE + kSSlots,
   B_PV = B_PF + kPBufs, B_OF = B_PV + kPBufs, B_DRAIN = B_OF + 1, B_DRAIN2 = B_DRAIN + 1,
-  B_PVI = B_DRAIN2 + 1, NBAR = B_PVI + 1
+  B_PVI = B_DRAIN2 + 1,
+  // whole rows: the softmax warps hand each row's sum and max to the epilogue
+  // warpgroup through two slots (full / free)
+  B_STF = B_PVI + 1, B_STE = B_STF + 2, NBAR = B_STE + 2
 };
 // Shared-memory layout for head dim D (64 or 128): a 64-row tile of D 16-bit
 // values is D / 64 chunks of 64 columns (128-byte rows, 128-byte swizzle).
@@ -91,7 +99,8 @@ struct Lay {
   static constexpr int OFF_BAR = OFF_STAGE + QBytes;
   // [0] tmem base, [1] abort flag, bytes 8 .. 15: PV-skip votes [P buffer][softmax warp]
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_STATS = OFF_MISC + 16;  // [slot][64 rows][max, sum] floats
+  static constexpr int SMEM_ALLOC = OFF_STATS + 2 * 64 * 2 * 4 + 1024;
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -106,7 +115,13 @@ constexpr int kWarpQK = 0, kWarpV = 1, kWarpS = 2, kWarpPV = 3, kWarpSm = 4;
 constexpr int kSoftmaxWarps = 4;
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kThreads = 32 * (kWarpSm + kSoftmaxWarps);
-constexpr int kSoftmaxBar = 1;  // named barrier of the softmax warps
+// whole rows: warps 8-11 are the epilogue warpgroup
+constexpr int kWarpEp = kWarpSm + kSoftmaxWarps;
+constexpr int kThreadsEp = kThreads + 32 * kSoftmaxWarps;
+constexpr int kSoftmaxBar = 1;  // named barrier of the warps that store O (4 warps)
+// register budgets of the three warpgroups with an epilogue warpgroup:
+// 128 x (80 + 232 + 128) = 56320, within the 384 x 168 the CTA is launched with
+constexpr uint32_t kRegsIo = 80, kRegsSoftmax = 232, kRegsEp = 128;
 
 struct TcParams {
   CUtensorMap tq, tk, tv, to;
@@ -190,7 +205,11 @@ FBM_DEVICE void st_o(uint32_t taddr, const uint32_t (&o)[D / 2]) {
 }
 
 template <int D, bool kBf16, bool kPartial, bool kPvSkip, bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__ TcParams P) {
+__global__ void __launch_bounds__(kPartial ? kThreads : kThreadsEp, 1)
+    k_fmha_tc(const __grid_constant__ TcParams P) {
+  // whole rows leave through the epilogue warpgroup; fp32 partials straight
+  // from the softmax warps' registers
+  constexpr bool kEpi = !kPartial;
   static_assert(!(kFp8 && (kPartial || kPvSkip)), "the fp8 variant runs whole rows");
   static_assert(!kFp8 || D == 128, "fp8 Q / K at d = 128");
   using Ly = Lay<D>;
@@ -209,8 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
   if (threadIdx.x == 0) {
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
-      if ((k >= B_SE && k < B_SE + kSSlots) || (k >= B_PF && k < B_PF + kPBufs) || k == B_OF)
-        cnt = kSoftmaxWarps;  // one elected arrive per softmax warp
+      if ((k >= B_SE && k < B_SE + kSSlots) || (k >= B_PF && k < B_PF + kPBufs) || k == B_OF ||
+          (k >= B_STF && k < B_STE + 2))
+        cnt = kSoftmaxWarps;  // one elected arrive per softmax (or epilogue) warp
       mbar_init(bar(k), cnt);
     }
     misc[1] = 0;
@@ -271,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
 
   if (warp == kWarpQK) {
     // ------------------------------------------------------------ Q and K producer
+    if constexpr (kEpi) regs_decrease<kRegsIo>();
     if (lane == 0) {
       int pc = 0, uc = 0;
       bool ok = true;
@@ -294,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     }
   } else if (warp == kWarpV) {
     // ------------------------------------------------------------ V producer
+    if constexpr (kEpi) regs_decrease<kRegsIo>();
     if (lane == 0) {
       int pc = 0;
       bool ok = true;
@@ -308,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     }
   } else if (warp == kWarpS) {
     // ------------------------------------------------------------ S issuer
+    if constexpr (kEpi) regs_decrease<kRegsIo>();
     // (the whole warp runs the loop; one elected lane issues each MMA)
     // (kind::f8f6f4 with e4m3 A and B uses format code 0, as f16 does)
     constexpr uint32_t idS = idesc_f16(kFp8 ? false : kBf16, false, false, 64, 128);
@@ -357,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     if (!mbar_wait_for_w(bar(B_DRAIN), 0, kWaitNs) && lane == 0) set_error(P.err, FBM_DEVERR_TIMEOUT);
   } else if (warp == kWarpPV) {
     // ------------------------------------------------------------ PV issuer
+    if constexpr (kEpi) regs_decrease<kRegsIo>();
     // (the whole warp runs the loop; one elected lane issues each MMA)
     // A = P (TMEM, K-major), B = V pair (MN-major: d contiguous)
     constexpr uint32_t idO = idesc_f16(kBf16, false, true, 64, D);
@@ -402,8 +426,87 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     if (!ok && lane == 0) fail(FBM_DEVERR_TIMEOUT);
     mma_commit_w(bar(B_DRAIN2));
     if (!mbar_wait_for_w(bar(B_DRAIN2), 0, kWaitNs) && lane == 0) set_error(P.err, FBM_DEVERR_TIMEOUT);
+  } else if (kEpi && warp >= kWarpEp) {
+    // ------------------------------------------------------------ epilogue warpgroup
+    // (whole rows) per row: the row's sum and max from the softmax warps, the
+    // row's last PV, O out of TMEM (then O is free for the next row's first
+    // PV), O / l through a swizzled staging tile and a tensor store, the LSE.
+    // The softmax warps meanwhile work on the next row.
+    regs_decrease<kRegsEp>();
+    using E = typename std::conditional<kBf16, BF16, F16>::type;
+    const int sw = warp - kWarpEp;            // TMEM subpartition
+    const int half = lane >> 4;               // d half of O
+    const int row = sw * 16 + (lane & 15);    // query row within the q block
+    const int tid = threadIdx.x - kWarpEp * 32;
+    const uint32_t tl = tbase + ((uint32_t)(sw * 32) << 16);
+    volatile float *stats = reinterpret_cast<volatile float *>(smem + Ly::OFF_STATS);
+    int pc = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
+      const Unit U = unit_of<false>(P, u);
+      const int q0 = U.i * 64;
+      const int rows = min(64, P.s_q - q0);
+      const size_t orow0 = (size_t)U.bh_q * P.s_q + q0;
+      if (U.n == 0) {
+        uint16_t *o = static_cast<uint16_t *>(P.out) + orow0 * D;
+        for (int e = tid * 8; e < rows * D; e += kSoftmaxThreads * 8)
+          *reinterpret_cast<uint4 *>(o + e) = make_uint4(0, 0, 0, 0);
+        if (P.lse && tid < rows) P.lse[orow0 + tid] = -INFINITY;
+        continue;
+      }
+      const int npairs = (U.n + 1) >> 1;
+      const int gl = pc + npairs - 1, rb = uc & 1;
+      ok = mbar_wait_ok(ok, bar(B_STF + rb), (uc >> 1) & 1, abort_flag, kWaitNs);
+      const float m = stats[(rb * 64 + row) * 2], lt = stats[(rb * 64 + row) * 2 + 1];
+      __syncwarp();
+      mbar_arrive_lane0(bar(B_STE + rb), lane);  // the slot may take row uc + 2
+      // the softmax warps waited for PV(gl - 2) before the row's last P, and
+      // before they handed the row over: the parity wait for PV(gl) is sound
+      ok = mbar_wait_ok(ok, bar(B_PV + gl % kPBufs), (gl / kPBufs) & 1, abort_flag, kWaitNs);
+      tc_fence_after();
+      uint32_t o[D / 2];
+      ld_o<D>(tl + kTO, o);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      mbar_arrive_lane0(bar(B_OF), lane);  // O may take the next row's first PV
+      const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+      if (P.lse && half == 0 && row < rows)
+        P.lse[orow0 + row] = lt > 0.f ? m * 0.6931471805599453f + logf(lt) : -INFINITY;
+      // staging: d half `half` of row `row` as D / 16 pieces of 16 bytes in
+      // the 128-byte-swizzled [chunk][64 rows][128 B] tile (d = 128: the half
+      // is chunk `half`; d = 64: pieces 4 half .. 4 half + 3 of the one chunk).
+      // The previous row's tensor store has long since read the tile.
+      if (tid == 0) bulk_wait_read0();
+      named_sync(kSoftmaxBar, kSoftmaxThreads);
+      uint8_t *srow = smem + OFF_STAGE + (D == 128 ? half * kQChunk : 0) + row * 128;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int z = 0; z < 4; ++z)
+          w[z] = E::from_f2(__uint_as_float(o[8 * c + 2 * z]) * inv,
+                            __uint_as_float(o[8 * c + 2 * z + 1]) * inv);
+        const int piece = D == 128 ? c : 4 * half + c;
+        *reinterpret_cast<uint4 *>(srow + ((piece ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async();
+      named_sync(kSoftmaxBar, kSoftmaxThreads);
+      if (tid == 0) {
+        // rows past the end of the sequence are clipped by the tensor map
+#pragma unroll
+        for (int c = 0; c < kNch; ++c)
+          tma_store_3d(&P.to, sbase + OFF_STAGE + c * kQChunk, c * 64, q0, U.bh_q);
+        bulk_commit();
+      }
+      pc += npairs;
+      uc += 1;
+    }
+    if (!ok) fail(FBM_DEVERR_TIMEOUT);
+    if (tid == 0) bulk_wait0();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    if constexpr (kEpi) regs_increase<kRegsSoftmax>();
     using E = typename std::conditional<kBf16, BF16, F16>::type;
     const int sw = warp - kWarpSm;            // == warp % 4: TMEM subpartition
     const int half = lane >> 4;               // block of the pair / d half of O
@@ -414,13 +517,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
     // Every softmax thread runs the same loop trip counts and barriers whatever
     // happens: a failed (timed-out) wait only clears `ok`, and later waits
     // return at once.
-    int pc = 0;
+    int pc = 0, uc = 0;
     bool ok = true;
+    volatile float *stats = reinterpret_cast<volatile float *>(smem + Ly::OFF_STATS);
     for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
       const Unit U = unit_of<kPartial>(P, u);
       const int q0 = U.i * 64;
       const int rows = min(64, P.s_q - q0);
       if (U.n == 0) {
+        if constexpr (kEpi) continue;  // the epilogue warpgroup writes the empty row
         const size_t orow0 = (kPartial ? (size_t)U.split * P.plane : 0) + (size_t)U.bh_q * P.s_q + q0;
         if constexpr (kPartial) {
           float *o = P.opart + orow0 * D;
@@ -563,7 +668,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
           *reinterpret_cast<volatile uint8_t *>(smem + OFF_MISC + 8 + pb * 4 + sw) = (uint8_t)vote;
         mbar_arrive_lane0(bar(B_PF + pb), lane);
       }
-      // ---- epilogue: O = O / l, LSE = m ln 2 + ln l
+      if constexpr (kEpi) {
+        // the row's sum and max go to the epilogue warpgroup, which waits for
+        // the row's last PV and stores O; this warp goes on to the next row
+        float lt;
+        {
+          const float2 a = f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])));
+          lt = a.x + a.y;
+        }
+        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+        const int rb = uc & 1;
+        // slot rb was last read for row uc - 2 (on a fresh barrier the phase
+        // before the first counts as complete)
+        ok = mbar_wait_ok(ok, bar(B_STE + rb), ((uc >> 1) & 1) ^ 1, abort_flag, kWaitNs);
+        if (half == 0) {
+          stats[(rb * 64 + row) * 2] = m;
+          stats[(rb * 64 + row) * 2 + 1] = lt;
+        }
+        __syncwarp();
+        mbar_arrive_lane0(bar(B_STF + rb), lane);
+        pc += npairs;
+        uc += 1;
+        continue;
+      }
+      // ---- fp32 partial (whole rows go to the epilogue warpgroup above):
+      // O / l straight from registers, LSE = m ln 2 + ln l
       {
         const int gl = pc + npairs - 1;
         ok = mbar_wait_ok(ok, bar(B_PV + gl % kPBufs), (gl / kPBufs) & 1, abort_flag, kWaitNs);
@@ -581,54 +710,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_fmha_tc(const __grid_constant__
         }
         lt += __shfl_xor_sync(0xffffffffu, lt, 16);
         const float inv = lt > 0.f ? 1.0f / lt : 0.f;
-        const size_t orow0 = (kPartial ? (size_t)U.split * P.plane : 0) + (size_t)U.bh_q * P.s_q + q0;
+        const size_t orow0 = (size_t)U.split * P.plane + (size_t)U.bh_q * P.s_q + q0;
         if (P.lse && half == 0 && row < rows)
           P.lse[orow0 + row] = lt > 0.f ? m * 0.6931471805599453f + logf(lt) : -INFINITY;
-        if constexpr (kPartial) {
-          // fp32 partial: this thread's D / 2 values of row `row`, d half `half`
-          if (row < rows) {
-            float4 *dst = reinterpret_cast<float4 *>(P.opart + (orow0 + row) * D + half * (D / 2));
+        // this thread's D / 2 values of row `row`, d half `half`
+        if (row < rows) {
+          float4 *dst = reinterpret_cast<float4 *>(P.opart + (orow0 + row) * D + half * (D / 2));
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c)
-              dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv, __uint_as_float(o[4 * c + 1]) * inv,
-                                   __uint_as_float(o[4 * c + 2]) * inv,
-                                   __uint_as_float(o[4 * c + 3]) * inv);
-          }
-          pc += npairs;
-          continue;
-        }
-        // staging: d half `half` of row `row` as D / 16 pieces of 16 bytes in
-        // the 128-byte-swizzled [chunk][64 rows][128 B] tile (d = 128: the half
-        // is chunk `half`; d = 64: pieces 4 half .. 4 half + 3 of the one chunk)
-        // the previous row's tensor store has long since read the staging tile:
-        // waiting for that here keeps the wait off the previous row's chain
-        if (tid == 0) bulk_wait_read0();
-        named_sync(kSoftmaxBar, kSoftmaxThreads);
-        uint8_t *srow = smem + OFF_STAGE + (D == 128 ? half * kQChunk : 0) + row * 128;
-#pragma unroll
-        for (int c = 0; c < D / 16; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int z = 0; z < 4; ++z)
-            w[z] = E::from_f2(__uint_as_float(o[8 * c + 2 * z]) * inv,
-                              __uint_as_float(o[8 * c + 2 * z + 1]) * inv);
-          const int piece = D == 128 ? c : 4 * half + c;
-          *reinterpret_cast<uint4 *>(srow + ((piece ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        fence_proxy_async();
-        named_sync(kSoftmaxBar, kSoftmaxThreads);
-        if (tid == 0) {
-          // rows past the end of the sequence are clipped by the tensor map
-#pragma unroll
-          for (int c = 0; c < kNch; ++c)
-            tma_store_3d(&P.to, sbase + OFF_STAGE + c * kQChunk, c * 64, q0, U.bh_q);
-          bulk_commit();
+          for (int c = 0; c < D / 8; ++c)
+            dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv, __uint_as_float(o[4 * c + 1]) * inv,
+                                 __uint_as_float(o[4 * c + 2]) * inv,
+                                 __uint_as_float(o[4 * c + 3]) * inv);
         }
       }
       pc += npairs;
     }
     if (!ok) fail(FBM_DEVERR_TIMEOUT);
-    if (tid == 0) bulk_wait0();
   }
 
   tc_fence_before();
@@ -740,7 +837,7 @@ cudaError_t launch_t(const FmhaLaunch &L, cudaStream_t st) {
   P.qscale = L.q_scale;
   P.kscale = L.k_scale;
   const int grid = std::min(P.units, sm_count());
-  k_fmha_tc<D, BF16, PARTIAL, PVSKIP, FP8><<<grid, kThreads, SMEM_ALLOC, st>>>(P);
+  k_fmha_tc<D, BF16, PARTIAL, PVSKIP, FP8><<<grid, PARTIAL ? kThreads : kThreadsEp, SMEM_ALLOC, st>>>(P);
   return cudaGetLastError();
 }
 

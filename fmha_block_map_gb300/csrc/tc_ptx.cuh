@@ -151,6 +151,17 @@ FBM_DEVICE void fence_proxy_async() {
 // ---------------------------------------------------------------------------
 // named barriers
 // ---------------------------------------------------------------------------
+// Per-warpgroup register budgets (every warp of a warpgroup executes the same
+// one; the budgets of all warpgroups together stay within what the CTA was
+// launched with, or the increase would wait for registers that never free)
+template <uint32_t R>
+FBM_DEVICE void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R));
+}
+template <uint32_t R>
+FBM_DEVICE void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R));
+}
 FBM_DEVICE void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
