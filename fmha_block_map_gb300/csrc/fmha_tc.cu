@@ -43,7 +43,7 @@
 //            softmax warps through shared memory, O from TMEM once the row's
 //            last PV is done, so the softmax warps go straight on to the next
 //            row.  setmaxnreg gives the softmax warpgroup 232 registers, the
-//            other two 80 and 128.
+//            other two 88 and 120.
 // Pipeline: S(g) is issued once K(g) has landed and its TMEM slot is free (the
 // softmax releases a slot as soon as it holds the scores in registers), so the
 // S MMA of pair g + 1 runs during the softmax of pair g; PV(g) once P(g) is in
@@ -120,8 +120,8 @@ constexpr int kWarpEp = kWarpSm + kSoftmaxWarps;
 constexpr int kThreadsEp = kThreads + 32 * kSoftmaxWarps;
 constexpr int kSoftmaxBar = 1;  // named barrier of the warps that store O (4 warps)
 // register budgets of the three warpgroups with an epilogue warpgroup:
-// 128 x (80 + 232 + 128) = 56320, within the 384 x 168 the CTA is launched with
-constexpr uint32_t kRegsIo = 80, kRegsSoftmax = 232, kRegsEp = 128;
+// 128 x (88 + 232 + 120) = 56320, within the 384 x 168 the CTA is launched with
+constexpr uint32_t kRegsIo = 88, kRegsSoftmax = 232, kRegsEp = 120;
 
 struct TcParams {
   CUtensorMap tq, tk, tv, to;
